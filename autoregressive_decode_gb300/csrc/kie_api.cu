@@ -1,0 +1,1008 @@
+// Host side of libkie: the C ABI declared in include/kie.h.
+//
+// The engine owns one device workspace (its own cudaMalloc, or a buffer the
+// caller passes), carved into: per-CTA weight streams, embedding table, norm
+// gains, KV cache, activations, plan tables and output staging.  All GPU work
+// runs on the stream given at creation.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "../../include/kie.h"
+#include "kie_internal.h"
+
+extern "C" void* kie_decode_kernel_ptr(int hd, int kv);
+extern "C" cudaError_t kie_launch_ctl(KieControl* c, int tok, int pos, int clear, cudaStream_t st);
+extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, const void* desc, int n,
+                                            cudaStream_t st);
+extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
+                                             int8_t* codes_i8, uint16_t* scales, cudaStream_t st);
+extern "C" cudaError_t kie_launch_quant_u8(const uint16_t* src, int n_seg, int64_t src_seg, int64_t src_row,
+                                           int rows, int row_elems, uint8_t* codes, int64_t dst_seg,
+                                           int64_t dst_row, float* scale, int32_t* zp, int64_t meta_stride,
+                                           cudaStream_t st);
+extern "C" cudaError_t kie_launch_e5m2(const uint16_t* x, size_t n, uint8_t* out, cudaStream_t st);
+extern "C" cudaError_t kie_launch_set_kv(const uint16_t* src, int n, int H, int hd, int max_ctx, int fmt,
+                                         uint8_t* dst, uint16_t* tail, int first_tail, cudaStream_t st);
+
+namespace {
+
+struct CopyDesc {
+    uint64_t dst, src;
+    uint32_t len, pad;
+};
+
+thread_local std::string g_last_error;
+
+constexpr int kLogitChunk = 64;      // steps per launch when logits are copied to the host
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kSmemLimit = 232448;   // 227 KB opt-in shared memory per block
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Plan of one GEMV phase type (host copy).
+struct HostPhase {
+    int K = 0, KC = 0, nK = 0, rpu = 1, wfmt = WF_F16, n_units = 0;
+    std::vector<int32_t> unit_begin;   // G+1
+    std::vector<uint32_t> bytes;       // G
+    std::vector<uint32_t> nslots;      // G
+    uint64_t unit_bytes() const {      // stream bytes of one unit (approximate, for balancing)
+        const uint64_t row = wfmt == WF_F16 ? uint64_t(K) * 2 : uint64_t(K) / 2 + uint64_t(K) / 64;
+        return row * rpu;
+    }
+};
+
+uint32_t slot_bytes_host(int wfmt, int rows_g, int kc) {
+    if (wfmt == WF_F16) return uint32_t(rows_g) * uint32_t(kc) * 2u;
+    uint32_t b = uint32_t(rows_g) * uint32_t(kc / 2) + uint32_t(rows_g) * uint32_t(kc / 64);
+    return (b + 15u) & ~15u;
+}
+
+struct Layout {  // byte offsets into the workspace
+    size_t wstream, wstream_bytes;
+    size_t emb, norms, inv_freq;
+    size_t kc, vc, kv_bytes, tail, seg_scale, seg_zp;
+    size_t x, q, o, a, att_part, head_cnt, amax_val, amax_idx, ctl;
+    size_t plan_i32, plan_u32, cta_base, cta_layer;
+    size_t out_tokens, out_logits, forced, step_token, step_logits;
+    size_t total;
+    int nseg;
+};
+
+struct Plan {
+    int G = 0;
+    HostPhase ph[PH_NTYPES];
+    std::vector<uint64_t> cta_base, cta_layer;
+    uint64_t stream_bytes = 0;
+    int nslot = 0, act_floats = 0, part_floats = 0;
+    size_t smem = 0;
+};
+
+bool valid_cfg(const kie_config* c, std::string& why) {
+    if (!c) { why = "config is NULL"; return false; }
+    if (c->n_layers < 1 || c->d_model < 8 || c->n_heads < 1 || c->ffn_dim < 8 || c->vocab < 2 || c->max_ctx < 1) {
+        why = "non-positive model dimension";
+        return false;
+    }
+    if (c->head_dim != 64 && c->head_dim != 128) { why = "head_dim must be 64 or 128"; return false; }
+    if (c->d_model % 8 || c->ffn_dim % 8 || (c->n_heads * c->head_dim) % 8) { why = "dims must be multiples of 8"; return false; }
+    if (c->kv_dtype < 0 || c->kv_dtype > 2) { why = "bad kv_dtype"; return false; }
+    if (c->ffn_wdtype < 0 || c->ffn_wdtype > 1) { why = "bad ffn_wdtype"; return false; }
+    if (c->ffn_wdtype == KIE_W_INT4_G128 && (c->d_model % 128 || c->ffn_dim % 128)) {
+        why = "INT4 FFN needs d_model and ffn_dim multiples of 128";
+        return false;
+    }
+    if (c->mode < 0 || c->mode > 1) { why = "bad mode"; return false; }
+    if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) { why = "bad rms_eps or rope_theta"; return false; }
+    return true;
+}
+
+// Partition every phase over G CTAs, balancing each CTA's cumulative stream bytes.
+void build_plan(const kie_config& c, int G, Plan& pl) {
+    pl.G = G;
+    const int d = c.d_model, H = c.n_heads, hd = c.head_dim, F = c.ffn_dim, V = c.vocab;
+    const bool i4 = c.ffn_wdtype == KIE_W_INT4_G128;
+    auto setp = [&](int t, int K, int rpu, int units, int wfmt) {
+        HostPhase& p = pl.ph[t];
+        p.K = K; p.rpu = rpu; p.n_units = units; p.wfmt = wfmt;
+        p.KC = std::min(K, wfmt == WF_F16 ? KIE_KC_F16 : KIE_KC_I4);
+        p.nK = (K + p.KC - 1) / p.KC;
+    };
+    setp(PH_QKV, d, 2, 3 * H * (hd / 2), WF_F16);
+    setp(PH_O, H * hd, 1, d, WF_F16);
+    setp(PH_GU, d, 2, F, i4 ? WF_I4 : WF_F16);
+    setp(PH_D, F, 1, d, i4 ? WF_I4 : WF_F16);
+    setp(PH_LM, d, 1, V, WF_F16);
+
+    std::vector<uint64_t> cum(G, 0);
+    auto assign = [&](int t, std::vector<uint64_t>& acc, uint64_t weight) {
+        HostPhase& p = pl.ph[t];
+        const int base = p.n_units / G, rem = p.n_units % G;
+        std::vector<int> order(G);
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return acc[a] < acc[b]; });
+        std::vector<int> cnt(G, base);
+        for (int k = 0; k < rem; ++k) cnt[order[k]] += 1;
+        p.unit_begin.assign(G + 1, 0);
+        for (int i = 0; i < G; ++i) p.unit_begin[i + 1] = p.unit_begin[i] + cnt[i];
+        p.bytes.assign(G, 0);
+        p.nslots.assign(G, 0);
+        for (int i = 0; i < G; ++i) {
+            const int rows = cnt[i] * p.rpu;
+            const int groups = (rows + KIE_R - 1) / KIE_R;
+            uint64_t b = 0;
+            for (int g = 0; g < groups; ++g) {
+                const int rg = std::min(KIE_R, rows - g * KIE_R);
+                for (int ch = 0; ch < p.nK; ++ch) {
+                    const int kc = std::min(p.KC, p.K - ch * p.KC);
+                    b += slot_bytes_host(p.wfmt, rg, kc);
+                }
+            }
+            p.bytes[i] = uint32_t(b);
+            p.nslots[i] = uint32_t(groups * p.nK);
+            acc[i] += b * weight;
+        }
+    };
+    for (int t : {PH_QKV, PH_O, PH_GU, PH_D}) assign(t, cum, 1);
+    for (auto& v : cum) v *= uint64_t(c.n_layers);
+    assign(PH_LM, cum, 1);
+
+    pl.cta_base.assign(G, 0);
+    pl.cta_layer.assign(G, 0);
+    uint64_t off = 0;
+    for (int i = 0; i < G; ++i) {
+        uint64_t lb = 0;
+        for (int t : {PH_QKV, PH_O, PH_GU, PH_D}) lb += pl.ph[t].bytes[i];
+        pl.cta_layer[i] = lb;
+        pl.cta_base[i] = off;
+        off += lb * uint64_t(c.n_layers) + pl.ph[PH_LM].bytes[i];
+    }
+    pl.stream_bytes = off;
+
+    // shared memory
+    int64_t part = 0;
+    for (int t = 0; t < PH_NTYPES; ++t) {
+        const HostPhase& p = pl.ph[t];
+        for (int i = 0; i < G; ++i) {
+            const int rows = (p.unit_begin[i + 1] - p.unit_begin[i]) * p.rpu;
+            part = std::max<int64_t>(part, ((rows + KIE_R - 1) / KIE_R) * KIE_R * p.nK);
+        }
+    }
+    // attention: head h gets floor((h+1)G/H) - floor(hG/H) >= floor(G/H) CTAs; a
+    // chunk holds at most ceil(max_ctx / floor(G/H)) rows (scores in the act
+    // buffer) and, for uint8 caches, meets at most rows/128 + 2 segments whose
+    // scale/zp (K and V) are staged in the partial buffer.
+    const int64_t min_heads_cta = std::max(1, G / H);
+    const int64_t max_seg = (int64_t(c.max_ctx) + min_heads_cta - 1) / min_heads_cta + 2;
+    part = std::max<int64_t>(part, 4 * (max_seg / KIE_SEG + 2));
+    part = std::max<int64_t>(part, G + H);   // O-phase combine: per-CTA weights and per-head 1/L
+    pl.part_floats = int(align_up(size_t(std::max<int64_t>(part, 4)), 4));
+    int act = std::max({d, F, H * hd, int(std::min<int64_t>(max_seg, 1 << 30))});
+    pl.act_floats = int(align_up(act, 8));
+    const KieSmemLayout l0 = kie_smem_layout(pl.part_floats, pl.act_floats, 0);
+    const long avail = long(kSmemLimit) - long(l0.total);
+    pl.nslot = int(std::max<long>(0, std::min<long>(KIE_MAX_SLOTS, avail / KIE_SLOT_BYTES)));
+    pl.smem = kie_smem_layout(pl.part_floats, pl.act_floats, pl.nslot).total;
+}
+
+void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
+    const int G = pl.G, d = c.d_model, H = c.n_heads, hd = c.head_dim, F = c.ffn_dim, V = c.vocab;
+    L.wstream = take(pl.stream_bytes);
+    L.wstream_bytes = pl.stream_bytes;
+    L.emb = take(size_t(V) * d * 2);
+    L.norms = take((size_t(c.n_layers) * 2 + 1) * d * 4);
+    L.inv_freq = take(size_t(hd / 2) * 4);
+    const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
+    L.kv_bytes = size_t(c.n_layers) * H * c.max_ctx * hd * esz;
+    L.kc = take(L.kv_bytes);
+    L.vc = take(L.kv_bytes);
+    L.nseg = (c.max_ctx + KIE_SEG - 1) / KIE_SEG;
+    const bool u8 = c.kv_dtype == KIE_KV_U8_ADAPTIVE;
+    L.tail = take(u8 ? size_t(c.n_layers) * 2 * H * KIE_SEG * hd * 2 : 0);
+    L.seg_scale = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
+    L.seg_zp = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
+    L.x = take(size_t(d) * 4);
+    L.q = take(size_t(H) * hd * 4);
+    L.a = take(size_t(F) * 4);
+    L.o = take(size_t(H) * hd * 4);
+    L.att_part = take(size_t(G) * (hd + 4) * 4);
+    L.head_cnt = take(size_t(H) * 4);
+    L.amax_val = take(size_t(G) * 4);
+    L.amax_idx = take(size_t(G) * 4);
+    L.ctl = take(sizeof(KieControl));
+    L.plan_i32 = take(size_t(PH_NTYPES) * (G + 1) * 4);
+    L.plan_u32 = take(size_t(PH_NTYPES) * 2 * G * 4);
+    L.cta_base = take(size_t(G) * 8);
+    L.cta_layer = take(size_t(G) * 8);
+    L.out_tokens = take(size_t(c.max_ctx) * 4);
+    L.out_logits = take(size_t(kLogitChunk) * V * 4);
+    L.forced = take(size_t(c.max_ctx) * 4);
+    L.step_token = take(4);
+    L.step_logits = take(size_t(V) * 4);
+    L.total = align_up(o, 256);
+}
+
+int query_grid(int device, std::string& why) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) { why = "cudaGetDeviceProperties failed"; return 0; }
+    return prop.multiProcessorCount;
+}
+
+}  // namespace
+
+struct kie_engine {
+    kie_config cfg{};
+    int G = 0;
+    cudaStream_t stream = nullptr;
+    void* ws = nullptr;
+    bool own_ws = false;
+    Layout lay{};
+    Plan plan;
+    KieParams P{};
+    void* kernel = nullptr;
+    bool loaded = false;
+    int pos = 0;
+    int sticky = 0;
+    uint64_t timeout_ns = kDefaultTimeoutNs;
+    cudaGraphExec_t graph = nullptr;
+    KieControl* h_ctl = nullptr;  // pinned staging
+    std::string err;
+
+    uint8_t* dev(size_t off) const { return static_cast<uint8_t*>(ws) + off; }
+};
+
+namespace {
+
+kie_status fail(kie_engine* e, kie_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    if (e) e->err = buf;
+    g_last_error = buf;
+    return st;
+}
+
+#define KIE_CUDA(e, call)                                                                        \
+    do {                                                                                         \
+        cudaError_t _r = (call);                                                                 \
+        if (_r != cudaSuccess) return fail((e), KIE_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(_r)); \
+    } while (0)
+
+kie_status check_tokens(kie_engine* e, const int32_t* t, int n) {
+    for (int i = 0; i < n; ++i)
+        if (t[i] < 0 || t[i] >= e->cfg.vocab) return fail(e, KIE_ERR_INVALID_ARG, "token id %d out of range", t[i]);
+    return KIE_OK;
+}
+
+kie_status ready(kie_engine* e, int n) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    if (!e->loaded) return fail(e, KIE_ERR_NOT_LOADED, "weights not loaded");
+    if (e->sticky) return fail(e, KIE_ERR_DEVICE_TIMEOUT, "engine poisoned by an earlier device error; call kie_reset");
+    if (n < 0) return fail(e, KIE_ERR_INVALID_ARG, "negative count");
+    if (int64_t(e->pos) + n > e->cfg.max_ctx) return fail(e, KIE_ERR_CTX_OVERFLOW, "pos %d + %d > max_ctx %d", e->pos, n, e->cfg.max_ctx);
+    return KIE_OK;
+}
+
+// Read the control block after a sync; a device error poisons the engine.
+kie_status check_device(kie_engine* e) {
+    KIE_CUDA(e, cudaMemcpyAsync(e->h_ctl, e->dev(e->lay.ctl), sizeof(KieControl), cudaMemcpyDeviceToHost, e->stream));
+    KIE_CUDA(e, cudaStreamSynchronize(e->stream));
+    if (e->h_ctl->err != KERR_NONE) {
+        e->sticky = e->h_ctl->err;
+        return fail(e, KIE_ERR_DEVICE_TIMEOUT, "device error %d (info %d)", e->h_ctl->err, e->h_ctl->err_info);
+    }
+    return KIE_OK;
+}
+
+kie_status set_ctl(kie_engine* e, int tok, int pos, bool clear) {
+    KIE_CUDA(e, kie_launch_ctl(reinterpret_cast<KieControl*>(e->dev(e->lay.ctl)), tok, pos, clear ? 1 : 0, e->stream));
+    return KIE_OK;
+}
+
+KieLaunch base_launch(kie_engine* e) {
+    KieLaunch l{};
+    l.n_steps = 1;
+    l.phase_begin = 0;
+    l.phase_end = 5 * e->cfg.n_layers + 1;
+    l.first_tok = -1;
+    l.pos0 = -1;
+    l.forced = nullptr;
+    l.lm_from_step = 0;
+    l.out_tokens = nullptr;
+    l.out_logits = nullptr;
+    l.timeout_ns = e->timeout_ns;
+    l.use_grid_barrier = 1;
+    return l;
+}
+
+kie_status launch_persistent(kie_engine* e, const KieLaunch& l) {
+    KIE_CUDA(e, cudaMemsetAsync(e->dev(e->lay.ctl) + offsetof(KieControl, bar), 0, 4, e->stream));
+    void* args[] = {(void*)&e->P, (void*)&l};
+    cudaError_t r = cudaLaunchCooperativeKernel(e->kernel, dim3(e->G), dim3(KIE_THREADS), args, e->plan.smem, e->stream);
+    if (r == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        return fail(e, KIE_ERR_LAUNCH, "persistent grid of %d CTAs cannot be co-resident", e->G);
+    }
+    if (r != cudaSuccess) return fail(e, KIE_ERR_CUDA, "cooperative launch: %s", cudaGetErrorString(r));
+    return KIE_OK;
+}
+
+// Graph mode: one captured graph = one decode step = 5L+1 single-phase launches.
+kie_status ensure_graph(kie_engine* e) {
+    if (e->graph) return KIE_OK;
+    cudaStream_t cap;
+    KIE_CUDA(e, cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+    cudaGraph_t g = nullptr;
+    cudaError_t r = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (r != cudaSuccess) { cudaStreamDestroy(cap); return fail(e, KIE_ERR_CUDA, "begin capture: %s", cudaGetErrorString(r)); }
+    const int P_ = 5 * e->cfg.n_layers + 1;
+    for (int phi = 0; phi < P_ && r == cudaSuccess; ++phi) {
+        KieLaunch l = base_launch(e);
+        l.phase_begin = phi;
+        l.phase_end = phi + 1;
+        l.use_grid_barrier = 0;
+        l.out_tokens = reinterpret_cast<int32_t*>(e->dev(e->lay.step_token));
+        l.out_logits = reinterpret_cast<float*>(e->dev(e->lay.step_logits));
+        void* args[] = {(void*)&e->P, (void*)&l};
+        r = cudaLaunchKernel(e->kernel, dim3(e->G), dim3(KIE_THREADS), args, e->plan.smem, cap);
+    }
+    cudaError_t r2 = cudaStreamEndCapture(cap, &g);
+    cudaStreamDestroy(cap);
+    if (r != cudaSuccess || r2 != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return fail(e, KIE_ERR_CUDA, "graph capture: %s", cudaGetErrorString(r != cudaSuccess ? r : r2));
+    }
+    r = cudaGraphInstantiate(&e->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (r != cudaSuccess) { e->graph = nullptr; return fail(e, KIE_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(r)); }
+    return KIE_OK;
+}
+
+// Run n steps.  Step 0 consumes first_tok (>= 0) or the forced/ctl token; the
+// step inputs after that are forced[t] (prefill) or the previous argmax.
+// d_tokens/d_logits: device outputs (may be null).  lm_from: LM head only from that step.
+kie_status run_steps(kie_engine* e, int n, int first_tok, const int32_t* d_forced, int lm_from, int32_t* d_tokens,
+                     float* d_logits) {
+    if (n <= 0) return KIE_OK;
+    kie_status st;
+    if (e->cfg.mode == KIE_MODE_PERSISTENT) {
+        KieLaunch l = base_launch(e);
+        l.n_steps = n;
+        l.first_tok = d_forced ? -1 : first_tok;
+        l.pos0 = e->pos;
+        l.forced = d_forced;
+        l.lm_from_step = lm_from;
+        l.out_tokens = d_tokens;
+        l.out_logits = d_logits;
+        if ((st = launch_persistent(e, l)) != KIE_OK) return st;
+    } else {
+        if ((st = ensure_graph(e)) != KIE_OK) return st;
+        if ((st = set_ctl(e, first_tok >= 0 ? first_tok : 0, e->pos, false)) != KIE_OK) return st;
+        int32_t* ctl_tok = reinterpret_cast<int32_t*>(e->dev(e->lay.ctl) + offsetof(KieControl, tok));
+        for (int t = 0; t < n; ++t) {
+            if (d_forced)
+                KIE_CUDA(e, cudaMemcpyAsync(ctl_tok, d_forced + t, 4, cudaMemcpyDeviceToDevice, e->stream));
+            KIE_CUDA(e, cudaGraphLaunch(e->graph, e->stream));
+            if (d_tokens)
+                KIE_CUDA(e, cudaMemcpyAsync(d_tokens + t, e->dev(e->lay.step_token), 4, cudaMemcpyDeviceToDevice, e->stream));
+            if (d_logits && t >= lm_from)
+                KIE_CUDA(e, cudaMemcpyAsync(d_logits + size_t(t - lm_from) * e->cfg.vocab, e->dev(e->lay.step_logits),
+                                            size_t(e->cfg.vocab) * 4, cudaMemcpyDeviceToDevice, e->stream));
+        }
+    }
+    e->pos += n;
+    return KIE_OK;
+}
+
+}  // namespace
+
+// =============================================================================================
+// C ABI
+// =============================================================================================
+extern "C" {
+
+size_t kie_workspace_bytes(const kie_config* cfg) {
+    std::string why;
+    if (!valid_cfg(cfg, why)) return 0;
+    const int G = query_grid(cfg->device, why);
+    if (G <= 0) return 0;
+    Plan pl;
+    build_plan(*cfg, G, pl);
+    Layout L;
+    compute_layout(*cfg, pl, L);
+    return L.total;
+}
+
+kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, void* cuda_stream, kie_engine** out) {
+    if (!out) return fail(nullptr, KIE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    std::string why;
+    if (!valid_cfg(cfg, why)) return fail(nullptr, KIE_ERR_INVALID_ARG, "invalid config: %s", why.c_str());
+    if (cudaSetDevice(cfg->device) != cudaSuccess) return fail(nullptr, KIE_ERR_CUDA, "cudaSetDevice(%d) failed", cfg->device);
+    const int G = query_grid(cfg->device, why);
+    if (G <= 0) return fail(nullptr, KIE_ERR_CUDA, "%s", why.c_str());
+    if (G < cfg->n_heads) return fail(nullptr, KIE_ERR_UNSUPPORTED, "need at least n_heads SMs");
+    if (G > KIE_MAX_GRID) return fail(nullptr, KIE_ERR_UNSUPPORTED, "more than %d SMs", KIE_MAX_GRID);
+    if (cfg->d_model > 4096) return fail(nullptr, KIE_ERR_UNSUPPORTED, "d_model above 4096");
+    if (uint64_t(cfg->n_heads) * uint64_t(cfg->max_ctx) * uint64_t(G) >= (1ull << 32))
+        return fail(nullptr, KIE_ERR_UNSUPPORTED, "n_heads * max_ctx too large for this grid");
+    kie_engine* e = new kie_engine();
+    e->cfg = *cfg;
+    e->G = G;
+    e->stream = static_cast<cudaStream_t>(cuda_stream);
+    build_plan(*cfg, G, e->plan);
+    // The ring protocol needs at least as many slots as consumer warps (see the
+    // full-barrier note in kie_decode.cu).
+    if (e->plan.nslot < KIE_NW) { delete e; return fail(nullptr, KIE_ERR_UNSUPPORTED, "shared memory too small for the weight ring"); }
+    compute_layout(*cfg, e->plan, e->lay);
+    if (workspace) {
+        if (ws_bytes < e->lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+            delete e;
+            return fail(nullptr, KIE_ERR_OOM, "workspace too small or misaligned (need %zu bytes)", e->lay.total);
+        }
+        e->ws = workspace;
+    } else {
+        if (cudaMalloc(&e->ws, e->lay.total) != cudaSuccess) {
+            cudaGetLastError();
+            delete e;
+            return fail(nullptr, KIE_ERR_OOM, "cudaMalloc of %zu bytes failed", e->lay.total);
+        }
+        e->own_ws = true;
+    }
+    if (cudaMallocHost(&e->h_ctl, sizeof(KieControl)) != cudaSuccess) {
+        kie_destroy(e);
+        return fail(nullptr, KIE_ERR_OOM, "cudaMallocHost failed");
+    }
+    e->kernel = kie_decode_kernel_ptr(cfg->head_dim, cfg->kv_dtype);
+    cudaError_t r = cudaFuncSetAttribute(e->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(e->plan.smem));
+    if (r != cudaSuccess) { kie_destroy(e); return fail(nullptr, KIE_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(r)); }
+    int per_sm = 0;
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, e->kernel, KIE_THREADS, e->plan.smem);
+    if (r != cudaSuccess || per_sm < 1) { kie_destroy(e); return fail(nullptr, KIE_ERR_LAUNCH, "decode kernel does not fit on an SM"); }
+
+    // plan tables and parameters
+    const Layout& L = e->lay;
+    const Plan& pl = e->plan;
+    std::vector<int32_t> pi32(size_t(PH_NTYPES) * (G + 1));
+    std::vector<uint32_t> pu32(size_t(PH_NTYPES) * 2 * G);
+    for (int t = 0; t < PH_NTYPES; ++t) {
+        std::copy(pl.ph[t].unit_begin.begin(), pl.ph[t].unit_begin.end(), pi32.begin() + size_t(t) * (G + 1));
+        std::copy(pl.ph[t].bytes.begin(), pl.ph[t].bytes.end(), pu32.begin() + size_t(t) * 2 * G);
+        std::copy(pl.ph[t].nslots.begin(), pl.ph[t].nslots.end(), pu32.begin() + size_t(t) * 2 * G + G);
+    }
+    std::vector<float> invf(cfg->head_dim / 2);
+    for (int i = 0; i < cfg->head_dim / 2; ++i)
+        invf[i] = float(std::pow(double(cfg->rope_theta), -(2.0 * i) / cfg->head_dim));
+    cudaStream_t st = e->stream;
+    bool ok = cudaMemcpyAsync(e->dev(L.plan_i32), pi32.data(), pi32.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(e->dev(L.plan_u32), pu32.data(), pu32.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(e->dev(L.cta_base), pl.cta_base.data(), G * 8, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(e->dev(L.cta_layer), pl.cta_layer.data(), G * 8, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemcpyAsync(e->dev(L.inv_freq), invf.data(), invf.size() * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+              cudaMemsetAsync(e->dev(L.x), 0, L.plan_i32 - L.x, st) == cudaSuccess &&
+              cudaStreamSynchronize(st) == cudaSuccess;
+    if (!ok) { kie_destroy(e); return fail(nullptr, KIE_ERR_CUDA, "initialising device tables failed"); }
+
+    KieParams& P = e->P;
+    P.L = cfg->n_layers; P.d = cfg->d_model; P.H = cfg->n_heads; P.hd = cfg->head_dim; P.F = cfg->ffn_dim;
+    P.V = cfg->vocab; P.max_ctx = cfg->max_ctx; P.G = G;
+    P.eps = cfg->rms_eps;
+    P.attn_scale = float(1.0 / std::sqrt(double(cfg->head_dim)));
+    P.kv = cfg->kv_dtype;
+    P.nseg = L.nseg;
+    P.wstream = e->dev(L.wstream);
+    P.cta_base = reinterpret_cast<const uint64_t*>(e->dev(L.cta_base));
+    P.cta_layer = reinterpret_cast<const uint64_t*>(e->dev(L.cta_layer));
+    for (int t = 0; t < PH_NTYPES; ++t) {
+        KiePhasePlan& q = P.ph[t];
+        const HostPhase& h = pl.ph[t];
+        q.K = h.K; q.KC = h.KC; q.nK = h.nK; q.rows_per_unit = h.rpu; q.wfmt = h.wfmt; q.n_units = h.n_units;
+        q.unit_begin = reinterpret_cast<const int32_t*>(e->dev(L.plan_i32)) + size_t(t) * (G + 1);
+        q.bytes = reinterpret_cast<const uint32_t*>(e->dev(L.plan_u32)) + size_t(t) * 2 * G;
+        q.nslots = q.bytes + G;
+    }
+    P.emb = reinterpret_cast<const uint16_t*>(e->dev(L.emb));
+    P.norms = reinterpret_cast<const float*>(e->dev(L.norms));
+    P.inv_freq = reinterpret_cast<const float*>(e->dev(L.inv_freq));
+    P.kc = e->dev(L.kc);
+    P.vc = e->dev(L.vc);
+    P.tail = reinterpret_cast<uint16_t*>(e->dev(L.tail));
+    P.seg_scale = reinterpret_cast<float*>(e->dev(L.seg_scale));
+    P.seg_zp = reinterpret_cast<int32_t*>(e->dev(L.seg_zp));
+    P.x = reinterpret_cast<float*>(e->dev(L.x));
+    P.q = reinterpret_cast<float*>(e->dev(L.q));
+    P.a = reinterpret_cast<float*>(e->dev(L.a));
+    P.o = reinterpret_cast<float*>(e->dev(L.o));
+    P.att_part = reinterpret_cast<float*>(e->dev(L.att_part));
+    P.head_cnt = reinterpret_cast<uint32_t*>(e->dev(L.head_cnt));
+    P.amax_val = reinterpret_cast<float*>(e->dev(L.amax_val));
+    P.amax_idx = reinterpret_cast<int32_t*>(e->dev(L.amax_idx));
+    P.ctl = reinterpret_cast<KieControl*>(e->dev(L.ctl));
+    P.nslot = pl.nslot;
+    P.act_floats = pl.act_floats;
+    P.part_floats = pl.part_floats;
+    *out = e;
+    return KIE_OK;
+}
+
+kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
+    if (!e || !w || !w->tok_emb || !w->final_norm || !w->lm_head || !w->layers)
+        return fail(e, KIE_ERR_INVALID_ARG, "NULL engine or weight pointer");
+    const kie_config& c = e->cfg;
+    const int d = c.d_model, H = c.n_heads, hd = c.head_dim, F = c.ffn_dim, V = c.vocab, G = e->G;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const kie_layer_weights& lw = w->layers[l];
+        if (!lw.attn_norm || !lw.wq || !lw.wk || !lw.wv || !lw.wo || !lw.ffn_norm || !lw.w_gate || !lw.w_up || !lw.w_down)
+            return fail(e, KIE_ERR_INVALID_ARG, "NULL weight pointer in layer %d", l);
+    }
+    cudaStream_t st = e->stream;
+    const Layout& L = e->lay;
+    const Plan& pl = e->plan;
+    const cudaMemcpyKind kind = w->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    e->loaded = false;
+    if (e->graph) { cudaGraphExecDestroy(e->graph); e->graph = nullptr; }
+
+    // embedding (as given) and norm gains (fp32)
+    KIE_CUDA(e, cudaMemcpyAsync(e->dev(L.emb), w->tok_emb, size_t(V) * d * 2, kind, st));
+    {
+        std::vector<uint16_t> g16(size_t(c.n_layers * 2 + 1) * d);
+        for (int l = 0; l < c.n_layers; ++l) {
+            KIE_CUDA(e, cudaMemcpy(g16.data() + size_t(2 * l) * d, w->layers[l].attn_norm, size_t(d) * 2, w->on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost));
+            KIE_CUDA(e, cudaMemcpy(g16.data() + size_t(2 * l + 1) * d, w->layers[l].ffn_norm, size_t(d) * 2, w->on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost));
+        }
+        KIE_CUDA(e, cudaMemcpy(g16.data() + size_t(2 * c.n_layers) * d, w->final_norm, size_t(d) * 2, w->on_device ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost));
+        std::vector<float> g32(g16.size());
+        for (size_t i = 0; i < g16.size(); ++i) {
+            // fp16 -> fp32, exact (IEEE half layout)
+            const uint16_t h = g16[i];
+            const uint32_t s = uint32_t(h >> 15) << 31, ex = (h >> 10) & 31, m = h & 1023;
+            float f;
+            if (ex == 0) f = std::ldexp(float(m), -24);
+            else if (ex == 31) f = m ? NAN : INFINITY;
+            else f = std::ldexp(float(m | 1024), int(ex) - 25);
+            uint32_t b;
+            std::memcpy(&b, &f, 4);
+            b |= s;
+            std::memcpy(&g32[i], &b, 4);
+        }
+        KIE_CUDA(e, cudaMemcpyAsync(e->dev(L.norms), g32.data(), g32.size() * 4, cudaMemcpyHostToDevice, st));
+        KIE_CUDA(e, cudaStreamSynchronize(st));
+    }
+
+    // staging buffer on the device for one source matrix (plus INT4 codes/scales)
+    const size_t max_mat = std::max({size_t(H) * hd * d, size_t(F) * d, size_t(V) * d}) * 2;
+    size_t i4_bytes = c.ffn_wdtype == KIE_W_INT4_G128 ? size_t(F) * d / 2 + size_t(F) * d / 128 * 2 + 256 : 0;
+    uint8_t* stage = nullptr;
+    uint8_t* i4 = nullptr;
+    CopyDesc* ddesc = nullptr;
+    size_t desc_cap = 0;
+    if (!w->on_device && cudaMalloc(&stage, max_mat) != cudaSuccess) return fail(e, KIE_ERR_OOM, "staging cudaMalloc failed");
+    if (i4_bytes && cudaMalloc(&i4, i4_bytes) != cudaSuccess) { cudaFree(stage); return fail(e, KIE_ERR_OOM, "INT4 staging cudaMalloc failed"); }
+    kie_status result = KIE_OK;
+    std::vector<CopyDesc> desc;
+
+    auto free_all = [&]() {
+        if (stage) cudaFree(stage);
+        if (i4) cudaFree(i4);
+        if (ddesc) cudaFree(ddesc);
+    };
+    auto flush = [&](const uint8_t* src_base) -> bool {
+        if (desc.empty()) return true;
+        if (desc.size() > desc_cap) {
+            if (ddesc) cudaFree(ddesc);
+            desc_cap = desc.size() * 2;
+            if (cudaMalloc(&ddesc, desc_cap * sizeof(CopyDesc)) != cudaSuccess) { ddesc = nullptr; return false; }
+        }
+        if (cudaMemcpyAsync(ddesc, desc.data(), desc.size() * sizeof(CopyDesc), cudaMemcpyHostToDevice, st) != cudaSuccess) return false;
+        if (kie_launch_copy_desc(e->dev(L.wstream), src_base, ddesc, int(desc.size()), st) != cudaSuccess) return false;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return false;
+        desc.clear();
+        return true;
+    };
+    // Emit copies of every row of phase `t` whose source is matrix `mat` (selector).
+    // row_of(unit, half) -> (matrix id, source row) ; base offset of the layer's phase in each CTA stream.
+    auto emit = [&](int t, int layer, int mat, auto row_of, bool int4, uint64_t codes_off, uint64_t scales_off) {
+        const HostPhase& p = pl.ph[t];
+        const int K = p.K;
+        for (int i = 0; i < G; ++i) {
+            uint64_t off = pl.cta_base[i];
+            if (t == PH_LM) off += uint64_t(c.n_layers) * pl.cta_layer[i];
+            else {
+                off += uint64_t(layer) * pl.cta_layer[i];
+                for (int tt = 0; tt < t; ++tt) off += pl.ph[tt].bytes[i];
+            }
+            const int u0 = p.unit_begin[i], nu = p.unit_begin[i + 1] - u0;
+            const int rows = nu * p.rpu;
+            const int groups = (rows + KIE_R - 1) / KIE_R;
+            for (int g = 0; g < groups; ++g) {
+                const int rg = std::min(KIE_R, rows - g * KIE_R);
+                for (int ch = 0; ch < p.nK; ++ch) {
+                    const int kc = std::min(p.KC, K - ch * p.KC);
+                    for (int r = 0; r < rg; ++r) {
+                        const int lr = g * KIE_R + r;
+                        int m, srow;
+                        row_of(u0 + lr / p.rpu, lr % p.rpu, m, srow);
+                        if (m != mat) continue;
+                        if (!int4) {
+                            desc.push_back({off + uint64_t(r) * kc * 2, uint64_t(srow) * K * 2 + uint64_t(ch) * p.KC * 2,
+                                            uint32_t(kc * 2), 0});
+                        } else {
+                            desc.push_back({off + uint64_t(r) * (kc / 2),
+                                            codes_off + uint64_t(srow) * (K / 2) + uint64_t(ch) * (p.KC / 2), uint32_t(kc / 2), 0});
+                            desc.push_back({off + uint64_t(rg) * (kc / 2) + uint64_t(r) * (kc / 64),
+                                            scales_off + uint64_t(srow) * (K / 128) * 2 + uint64_t(ch) * (p.KC / 128) * 2,
+                                            uint32_t(kc / 64), 0});
+                        }
+                    }
+                    off += slot_bytes_host(p.wfmt, rg, kc);
+                }
+            }
+        }
+    };
+    auto src_of = [&](const uint16_t* ptr, size_t bytes) -> const uint8_t* {
+        if (w->on_device) return reinterpret_cast<const uint8_t*>(ptr);
+        if (cudaMemcpyAsync(stage, ptr, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return nullptr;
+        return stage;
+    };
+    const int hh = hd / 2, per = H * hh;
+    auto qkv_row = [&](int U, int half, int& m, int& srow) {
+        const int which = U / per, rem = U % per, h = rem / hh, i = rem % hh;
+        m = which;
+        srow = h * hd + i + half * hh;
+    };
+    auto plain_row = [&](int U, int, int& m, int& srow) { m = 0; srow = U; };
+    auto gu_row = [&](int U, int half, int& m, int& srow) { m = half; srow = U; };
+
+    for (int l = 0; l < c.n_layers && result == KIE_OK; ++l) {
+        const kie_layer_weights& lw = w->layers[l];
+        const uint16_t* qkv[3] = {lw.wq, lw.wk, lw.wv};
+        for (int m = 0; m < 3 && result == KIE_OK; ++m) {
+            const uint8_t* s = src_of(qkv[m], size_t(H) * hd * d * 2);
+            if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
+            emit(PH_QKV, l, m, qkv_row, false, 0, 0);
+            if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+        }
+        if (result != KIE_OK) break;
+        {
+            const uint8_t* s = src_of(lw.wo, size_t(d) * H * hd * 2);
+            if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
+            emit(PH_O, l, 0, plain_row, false, 0, 0);
+            if (!flush(s)) { result = fail(e, KIE_ERR_CUDA, "repack failed"); break; }
+        }
+        const bool q4 = c.ffn_wdtype == KIE_W_INT4_G128;
+        const uint16_t* gu[2] = {lw.w_gate, lw.w_up};
+        for (int m = 0; m < 2 && result == KIE_OK; ++m) {
+            const uint8_t* s = src_of(gu[m], size_t(F) * d * 2);
+            if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
+            if (q4) {
+                const uint64_t sc_off = align_up(size_t(F) * d / 2, 256);
+                if (kie_launch_quant_int4(reinterpret_cast<const uint16_t*>(s), F, d, i4, nullptr,
+                                          reinterpret_cast<uint16_t*>(i4 + sc_off), st) != cudaSuccess) {
+                    result = fail(e, KIE_ERR_CUDA, "INT4 quantisation failed");
+                    break;
+                }
+                emit(PH_GU, l, m, gu_row, true, 0, sc_off);
+                if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            } else {
+                emit(PH_GU, l, m, gu_row, false, 0, 0);
+                if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            }
+        }
+        if (result != KIE_OK) break;
+        {
+            const uint8_t* s = src_of(lw.w_down, size_t(d) * F * 2);
+            if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
+            if (q4) {
+                const uint64_t sc_off = align_up(size_t(F) * d / 2, 256);
+                if (kie_launch_quant_int4(reinterpret_cast<const uint16_t*>(s), d, F, i4, nullptr,
+                                          reinterpret_cast<uint16_t*>(i4 + sc_off), st) != cudaSuccess) {
+                    result = fail(e, KIE_ERR_CUDA, "INT4 quantisation failed");
+                    break;
+                }
+                emit(PH_D, l, 0, plain_row, true, 0, sc_off);
+                if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            } else {
+                emit(PH_D, l, 0, plain_row, false, 0, 0);
+                if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            }
+        }
+    }
+    if (result == KIE_OK) {
+        const uint8_t* s = src_of(w->lm_head, size_t(V) * d * 2);
+        if (!s) result = fail(e, KIE_ERR_CUDA, "weight upload failed");
+        else {
+            emit(PH_LM, 0, 0, plain_row, false, 0, 0);
+            if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+        }
+    }
+    cudaStreamSynchronize(st);
+    free_all();
+    if (result != KIE_OK) return result;
+    e->loaded = true;
+    e->pos = 0;
+    e->sticky = 0;
+    return set_ctl(e, 0, 0, true);
+}
+
+kie_status kie_prefill(kie_engine* e, const int32_t* tokens, int32_t n, float* last_logits) {
+    kie_status st = ready(e, n);
+    if (st != KIE_OK) return st;
+    if (n == 0) return KIE_OK;
+    if (!tokens) return fail(e, KIE_ERR_INVALID_ARG, "tokens is NULL");
+    if ((st = check_tokens(e, tokens, n)) != KIE_OK) return st;
+    int32_t* d_forced = reinterpret_cast<int32_t*>(e->dev(e->lay.forced));
+    KIE_CUDA(e, cudaMemcpyAsync(d_forced, tokens, size_t(n) * 4, cudaMemcpyHostToDevice, e->stream));
+    float* d_log = reinterpret_cast<float*>(e->dev(e->lay.out_logits));
+    const int pos0 = e->pos;
+    if ((st = run_steps(e, n, -1, d_forced, n - 1, nullptr, d_log)) != KIE_OK) { e->pos = pos0; return st; }
+    if ((st = check_device(e)) != KIE_OK) return st;
+    if (last_logits)
+        KIE_CUDA(e, cudaMemcpy(last_logits, d_log, size_t(e->cfg.vocab) * 4, cudaMemcpyDeviceToHost));
+    return KIE_OK;
+}
+
+kie_status kie_generate_greedy_device(kie_engine* e, int32_t first_token, int32_t n, int32_t* d_out_tokens,
+                                      float* d_out_logits) {
+    kie_status st = ready(e, n);
+    if (st != KIE_OK) return st;
+    if (n == 0) return KIE_OK;
+    if (!d_out_tokens) return fail(e, KIE_ERR_INVALID_ARG, "d_out_tokens is NULL");
+    if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
+    return run_steps(e, n, first_token, nullptr, 0, d_out_tokens, d_out_logits);
+}
+
+kie_status kie_generate_greedy(kie_engine* e, int32_t first_token, int32_t n, int32_t* out_tokens, float* out_logits) {
+    kie_status st = ready(e, n);
+    if (st != KIE_OK) return st;
+    if (n == 0) return KIE_OK;
+    if (!out_tokens) return fail(e, KIE_ERR_INVALID_ARG, "out_tokens is NULL");
+    if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
+    int32_t* d_tok = reinterpret_cast<int32_t*>(e->dev(e->lay.out_tokens));
+    float* d_log = reinterpret_cast<float*>(e->dev(e->lay.out_logits));
+    if (!out_logits) {
+        if ((st = run_steps(e, n, first_token, nullptr, 0, d_tok, nullptr)) != KIE_OK) return st;
+    } else {
+        int done = 0, tok = first_token;
+        while (done < n) {
+            const int m = std::min(kLogitChunk, n - done);
+            if ((st = run_steps(e, m, tok, nullptr, 0, d_tok + done, d_log)) != KIE_OK) return st;
+            KIE_CUDA(e, cudaMemcpyAsync(out_logits + size_t(done) * e->cfg.vocab, d_log, size_t(m) * e->cfg.vocab * 4,
+                                        cudaMemcpyDeviceToHost, e->stream));
+            if ((st = check_device(e)) != KIE_OK) return st;
+            KIE_CUDA(e, cudaMemcpy(&tok, d_tok + done + m - 1, 4, cudaMemcpyDeviceToHost));
+            done += m;
+        }
+    }
+    KIE_CUDA(e, cudaMemcpyAsync(out_tokens, d_tok, size_t(n) * 4, cudaMemcpyDeviceToHost, e->stream));
+    return check_device(e);
+}
+
+kie_status kie_decode_step(kie_engine* e, int32_t token, int32_t* next_token, float* logits) {
+    if (!next_token) return fail(e, KIE_ERR_INVALID_ARG, "next_token is NULL");
+    return kie_generate_greedy(e, token, 1, next_token, logits);
+}
+
+kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint64_t* stamps, size_t cap) {
+    kie_status st = ready(e, n);
+    if (st != KIE_OK) return st;
+    if (e->cfg.mode != KIE_MODE_PERSISTENT) return fail(e, KIE_ERR_UNSUPPORTED, "tracing needs the persistent mode");
+    if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
+    const size_t nphase = size_t(n) * (5 * e->cfg.n_layers + 1) * KIE_PROF_EVENTS * e->G;
+    const size_t need = nphase + size_t(KIE_PROF_SLOTS) * 4;
+    if (!stamps || cap < need) return fail(e, KIE_ERR_INVALID_ARG, "stamp buffer needs %zu entries", need);
+    uint64_t* d = nullptr;
+    if (cudaMalloc(&d, need * 8) != cudaSuccess) return fail(e, KIE_ERR_OOM, "trace buffer cudaMalloc failed");
+    KieLaunch l = base_launch(e);
+    l.n_steps = n;
+    l.first_tok = first_token;
+    l.pos0 = e->pos;
+    l.out_tokens = reinterpret_cast<int32_t*>(e->dev(e->lay.out_tokens));
+    l.prof = d;
+    l.prof_slots = d + nphase;
+    cudaMemsetAsync(d, 0, need * 8, e->stream);
+    st = launch_persistent(e, l);
+    if (st == KIE_OK) {
+        e->pos += n;
+        st = check_device(e);
+    }
+    if (st == KIE_OK && cudaMemcpy(stamps, d, need * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(e, KIE_ERR_CUDA, "trace copy failed");
+    cudaFree(d);
+    return st;
+}
+
+kie_status kie_sync(kie_engine* e) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    return check_device(e);
+}
+
+kie_status kie_reset(kie_engine* e) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    cudaStreamSynchronize(e->stream);
+    e->sticky = 0;
+    e->pos = 0;
+    KIE_CUDA(e, cudaMemsetAsync(e->dev(e->lay.head_cnt), 0, size_t(e->cfg.n_heads) * 4, e->stream));
+    return set_ctl(e, 0, 0, true);
+}
+
+int32_t kie_get_pos(const kie_engine* e) { return e ? e->pos : -1; }
+
+kie_status kie_set_pos(kie_engine* e, int32_t pos) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    if (pos < 0 || pos > e->cfg.max_ctx) return fail(e, KIE_ERR_INVALID_ARG, "pos %d outside [0, %d]", pos, e->cfg.max_ctx);
+    e->pos = pos;
+    return set_ctl(e, 0, pos, false);
+}
+
+kie_status kie_set_timeout_ms(kie_engine* e, int32_t ms) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    if (ms <= 0) return fail(e, KIE_ERR_INVALID_ARG, "timeout must be positive");
+    e->timeout_ns = uint64_t(ms) * 1000000ull;
+    if (e->graph) { cudaGraphExecDestroy(e->graph); e->graph = nullptr; }
+    return KIE_OK;
+}
+
+void* kie_get_stream(const kie_engine* e) { return e ? static_cast<void*>(e->stream) : nullptr; }
+int32_t kie_grid_size(const kie_engine* e) { return e ? e->G : 0; }
+
+const char* kie_last_error(const kie_engine* e) { return e ? e->err.c_str() : g_last_error.c_str(); }
+
+void kie_destroy(kie_engine* e) {
+    if (!e) return;
+    if (e->stream) cudaStreamSynchronize(e->stream);
+    else cudaDeviceSynchronize();
+    if (e->graph) cudaGraphExecDestroy(e->graph);
+    if (e->own_ws && e->ws) cudaFree(e->ws);
+    if (e->h_ctl) cudaFreeHost(e->h_ctl);
+    delete e;
+}
+
+kie_status kie_set_kv(kie_engine* e, int32_t layer, const uint16_t* k_fp16, const uint16_t* v_fp16, int32_t n) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    const kie_config& c = e->cfg;
+    if (layer < 0 || layer >= c.n_layers) return fail(e, KIE_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!k_fp16 || !v_fp16) return fail(e, KIE_ERR_INVALID_ARG, "NULL K or V");
+    if (n < 0 || n > c.max_ctx) return fail(e, KIE_ERR_CTX_OVERFLOW, "n %d outside [0, max_ctx]", n);
+    if (n == 0) return KIE_OK;
+    const int H = c.n_heads, hd = c.head_dim;
+    const size_t elems = size_t(n) * H * hd;
+    uint16_t* stage = nullptr;
+    if (cudaMalloc(&stage, elems * 2) != cudaSuccess) return fail(e, KIE_ERR_OOM, "staging cudaMalloc failed");
+    kie_status result = KIE_OK;
+    cudaStream_t st = e->stream;
+    const Layout& L = e->lay;
+    for (int kv = 0; kv < 2 && result == KIE_OK; ++kv) {
+        const uint16_t* src = kv ? v_fp16 : k_fp16;
+        uint8_t* base = e->dev(kv ? L.vc : L.kc);
+        if (cudaMemcpyAsync(stage, src, elems * 2, cudaMemcpyHostToDevice, st) != cudaSuccess) { result = fail(e, KIE_ERR_CUDA, "upload failed"); break; }
+        const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
+        uint8_t* dst = base + size_t(layer) * H * c.max_ctx * hd * esz;
+        cudaError_t r;
+        if (c.kv_dtype != KIE_KV_U8_ADAPTIVE) {
+            r = kie_launch_set_kv(stage, n, H, hd, c.max_ctx, c.kv_dtype == KIE_KV_FP16 ? 0 : 1, dst, nullptr, 0, st);
+        } else {
+            const int full = n / KIE_SEG;
+            uint16_t* tail = reinterpret_cast<uint16_t*>(e->dev(L.tail)) + (size_t(layer) * 2 + kv) * H * KIE_SEG * hd;
+            float* sc = reinterpret_cast<float*>(e->dev(L.seg_scale)) + (size_t(layer) * 2 + kv) * H * L.nseg;
+            int32_t* zp = reinterpret_cast<int32_t*>(e->dev(L.seg_zp)) + (size_t(layer) * 2 + kv) * H * L.nseg;
+            r = cudaSuccess;
+            for (int h = 0; h < H && r == cudaSuccess; ++h) {
+                // segment s of head h: rows p = s*128 .. +127, row stride H*hd in the source
+                r = kie_launch_quant_u8(stage + size_t(h) * hd, full, int64_t(KIE_SEG) * H * hd, int64_t(H) * hd, KIE_SEG, hd,
+                                        dst + size_t(h) * c.max_ctx * hd, int64_t(KIE_SEG) * hd, hd, sc + size_t(h) * L.nseg,
+                                        zp + size_t(h) * L.nseg, 1, st);
+            }
+            if (r == cudaSuccess) r = kie_launch_set_kv(stage, n, H, hd, c.max_ctx, 2, nullptr, tail, full * KIE_SEG, st);
+        }
+        if (r != cudaSuccess) result = fail(e, KIE_ERR_CUDA, "set_kv kernel: %s", cudaGetErrorString(r));
+        if (cudaStreamSynchronize(st) != cudaSuccess) result = fail(e, KIE_ERR_CUDA, "set_kv sync failed");
+    }
+    cudaFree(stage);
+    return result;
+}
+
+kie_status kie_read_kv(kie_engine* e, int32_t layer, int32_t which, int32_t p0, int32_t n, void* out,
+                       uint16_t* tail_fp16, float* scale, int32_t* zp) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    const kie_config& c = e->cfg;
+    if (layer < 0 || layer >= c.n_layers || (which != 0 && which != 1)) return fail(e, KIE_ERR_INVALID_ARG, "bad layer/which");
+    if (p0 < 0 || n < 0 || int64_t(p0) + n > c.max_ctx) return fail(e, KIE_ERR_INVALID_ARG, "bad range");
+    if (!out) return fail(e, KIE_ERR_INVALID_ARG, "out is NULL");
+    KIE_CUDA(e, cudaStreamSynchronize(e->stream));
+    const Layout& L = e->lay;
+    const int H = c.n_heads, hd = c.head_dim;
+    const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
+    const uint8_t* base = e->dev(which ? L.vc : L.kc) + size_t(layer) * H * c.max_ctx * hd * esz;
+    for (int h = 0; h < H; ++h)
+        KIE_CUDA(e, cudaMemcpy(static_cast<uint8_t*>(out) + size_t(h) * n * hd * esz,
+                               base + (size_t(h) * c.max_ctx + p0) * hd * esz, size_t(n) * hd * esz, cudaMemcpyDeviceToHost));
+    if (c.kv_dtype == KIE_KV_U8_ADAPTIVE) {
+        const int s0 = p0 / KIE_SEG, s1 = (p0 + n + KIE_SEG - 1) / KIE_SEG;
+        for (int h = 0; h < H; ++h) {
+            const size_t mi = (size_t(layer) * 2 + which) * H * L.nseg + size_t(h) * L.nseg + s0;
+            if (scale && s1 > s0)
+                KIE_CUDA(e, cudaMemcpy(scale + size_t(h) * (s1 - s0), e->dev(L.seg_scale) + mi * 4, size_t(s1 - s0) * 4, cudaMemcpyDeviceToHost));
+            if (zp && s1 > s0)
+                KIE_CUDA(e, cudaMemcpy(zp + size_t(h) * (s1 - s0), e->dev(L.seg_zp) + mi * 4, size_t(s1 - s0) * 4, cudaMemcpyDeviceToHost));
+        }
+        if (tail_fp16) {
+            // positions of [p0, p0+n) in the open segment (the one holding pos)
+            const int open0 = (e->pos / KIE_SEG) * KIE_SEG;
+            std::vector<uint16_t> t(size_t(H) * KIE_SEG * hd);
+            KIE_CUDA(e, cudaMemcpy(t.data(), e->dev(L.tail) + (size_t(layer) * 2 + which) * H * KIE_SEG * hd * 2, t.size() * 2, cudaMemcpyDeviceToHost));
+            for (int h = 0; h < H; ++h)
+                for (int p = p0; p < p0 + n; ++p) {
+                    if (p < open0 || p >= open0 + KIE_SEG) continue;
+                    std::memcpy(tail_fp16 + (size_t(h) * n + (p - p0)) * hd, t.data() + (size_t(h) * KIE_SEG + (p - open0)) * hd, size_t(hd) * 2);
+                }
+        }
+    }
+    return KIE_OK;
+}
+
+// ---- stateless routines -----------------------------------------------------------------------
+kie_status kie_quantize_kv_u8(const uint16_t* x_fp16, int32_t n_seg, int32_t seg_elems, uint8_t* codes, float* scale,
+                              int32_t* zp) {
+    if (!x_fp16 || !codes || !scale || !zp || n_seg < 0 || seg_elems <= 0) return fail(nullptr, KIE_ERR_INVALID_ARG, "bad arguments");
+    if (n_seg == 0) return KIE_OK;
+    const size_t n = size_t(n_seg) * seg_elems;
+    uint8_t* buf = nullptr;
+    const size_t o_codes = align_up(n * 2, 256), o_sc = o_codes + align_up(n, 256), o_zp = o_sc + align_up(size_t(n_seg) * 4, 256);
+    if (cudaMalloc(&buf, o_zp + size_t(n_seg) * 4) != cudaSuccess) return fail(nullptr, KIE_ERR_OOM, "cudaMalloc failed");
+    kie_status st = KIE_OK;
+    if (cudaMemcpy(buf, x_fp16, n * 2, cudaMemcpyHostToDevice) != cudaSuccess ||
+        kie_launch_quant_u8(reinterpret_cast<uint16_t*>(buf), n_seg, seg_elems, seg_elems, 1, seg_elems, buf + o_codes,
+                            seg_elems, seg_elems, reinterpret_cast<float*>(buf + o_sc), reinterpret_cast<int32_t*>(buf + o_zp),
+                            1, nullptr) != cudaSuccess ||
+        cudaMemcpy(codes, buf + o_codes, n, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(scale, buf + o_sc, size_t(n_seg) * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(zp, buf + o_zp, size_t(n_seg) * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(nullptr, KIE_ERR_CUDA, "uint8 quantisation failed: %s", cudaGetErrorString(cudaGetLastError()));
+    cudaFree(buf);
+    return st;
+}
+
+kie_status kie_quantize_int4_g128(const uint16_t* w_fp16, int32_t rows, int32_t cols, int8_t* codes, uint16_t* scale_fp16) {
+    if (!w_fp16 || !codes || !scale_fp16 || rows <= 0 || cols <= 0 || cols % 128) return fail(nullptr, KIE_ERR_INVALID_ARG, "bad arguments");
+    const size_t n = size_t(rows) * cols;
+    uint8_t* buf = nullptr;
+    const size_t o_codes = align_up(n * 2, 256), o_sc = o_codes + align_up(n, 256);
+    if (cudaMalloc(&buf, o_sc + n / 128 * 2) != cudaSuccess) return fail(nullptr, KIE_ERR_OOM, "cudaMalloc failed");
+    kie_status st = KIE_OK;
+    if (cudaMemcpy(buf, w_fp16, n * 2, cudaMemcpyHostToDevice) != cudaSuccess ||
+        kie_launch_quant_int4(reinterpret_cast<uint16_t*>(buf), rows, cols, nullptr, reinterpret_cast<int8_t*>(buf + o_codes),
+                              reinterpret_cast<uint16_t*>(buf + o_sc), nullptr) != cudaSuccess ||
+        cudaMemcpy(codes, buf + o_codes, n, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(scale_fp16, buf + o_sc, n / 128 * 2, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(nullptr, KIE_ERR_CUDA, "INT4 quantisation failed: %s", cudaGetErrorString(cudaGetLastError()));
+    cudaFree(buf);
+    return st;
+}
+
+kie_status kie_convert_fp8_e5m2(const uint16_t* x_fp16, size_t n, uint8_t* out) {
+    if (!x_fp16 || !out) return fail(nullptr, KIE_ERR_INVALID_ARG, "bad arguments");
+    if (n == 0) return KIE_OK;
+    uint8_t* buf = nullptr;
+    const size_t o_out = align_up(n * 2, 256);
+    if (cudaMalloc(&buf, o_out + n) != cudaSuccess) return fail(nullptr, KIE_ERR_OOM, "cudaMalloc failed");
+    kie_status st = KIE_OK;
+    if (cudaMemcpy(buf, x_fp16, n * 2, cudaMemcpyHostToDevice) != cudaSuccess ||
+        kie_launch_e5m2(reinterpret_cast<uint16_t*>(buf), n, buf + o_out, nullptr) != cudaSuccess ||
+        cudaMemcpy(out, buf + o_out, n, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(nullptr, KIE_ERR_CUDA, "E5M2 conversion failed: %s", cudaGetErrorString(cudaGetLastError()));
+    cudaFree(buf);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,1259 @@
+// The decode program: one kernel that runs a range of phases of one or more
+// decode steps.  Persistent mode launches it once (cooperatively, one CTA per
+// SM) for all steps, with grid-wide barriers between phases; graph mode
+// launches it once per phase inside a CUDA graph.  Both run the same code with
+// the same partitioning, so they produce bit-identical results.
+//
+// Design (Kog page, table "Where standard inference stacks lose microseconds"):
+//  - row "kernel boundaries": one resident program for the whole decode path;
+//  - row "CPU scheduling and sampling": LM head and argmax on the GPU, the next
+//    token fed back without the host;
+//  - row "grid synchronization": grid barriers are a single gpu-scope counter
+//    with acquire/release, every wait bounded by %globaltimer;
+//  - rows "weight reloading" and "non-GEMM work": each CTA's weights for the
+//    whole step are one contiguous stream that a producer warp copies into a
+//    shared-memory ring with bulk async copies, independently of the
+//    activations, so HBM keeps streaming while consumers wait at barriers,
+//    normalise, do attention or reduce (beta == 1: every weight byte is read
+//    exactly once per token).
+#include "kie_device.cuh"
+#include "kie_internal.h"
+
+using namespace kie;
+
+namespace {
+
+constexpr int NW = KIE_NW;
+constexpr int NCT = NW * 32;  // consumer threads
+
+// Ring protocol.  Global slot index g lives in ring slot s = g % nslot as
+// generation q = g / nslot.  "full" barriers are doubled per slot: generation q
+// completes on full[2*s + (q & 1)] as that barrier's phase q/2, so a consumer
+// waiting for generation q can only meet that barrier in phase q/2 (data in
+// flight) or q/2 + 1 (data landed): generation q-2 was released before q-1 was
+// issued, and q+2 cannot be issued before this consumer releases q.  With a
+// single barrier per slot a consumer could arrive while generation q-1 is still
+// in flight, and the parity of q would then name an already completed phase.
+// Slot j of a phase goes to consumer warp j % NW, and every phase (and each
+// attention pass) starts after a consumer-wide barrier, so all slots of earlier
+// phases have landed.  The claim about q-2 then holds when nslot >= NW: for
+// j < NW, g - 2*nslot lies in an earlier phase; for j >= NW the warp's previous
+// slot g - NW landed, so every index <= g - NW was issued and every index
+// <= g - NW - nslot was released (landed), g - 2*nslot among them.
+// "empty[s]" completes once per release, in generation order (the producer
+// re-arms a slot only after its release), so one barrier suffices there.
+struct Smem {
+    uint64_t* full;
+    uint64_t* empty;
+    int32_t* flags;   // [0]: abort, [1]: last-arriver flag, [2]: token, [3]: contributor count
+    int32_t* plan;    // [PH_NTYPES][4]: first unit, units, slots, stream bytes of this CTA
+    uint64_t* cbase;  // [0]: this CTA's stream offset, [1]: bytes of one layer of it
+    int32_t* clist;   // attention: contributors (2*cta + segment) of the head being combined
+    float* red;       // reduction scratch: NW*(KIE_MAX_HEAD_DIM+2) + 64 floats
+    float* part;      // GEMV partial sums
+    float* act;       // activation (piece-split layout) / attention scores
+    uint8_t* ring;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* base, const KieParams& P) {
+    const KieSmemLayout l = kie_smem_layout(P.part_floats, P.act_floats, P.nslot);
+    Smem s;
+    s.full = reinterpret_cast<uint64_t*>(base + l.full);
+    s.empty = reinterpret_cast<uint64_t*>(base + l.empty);
+    s.cbase = reinterpret_cast<uint64_t*>(base + l.cbase);
+    s.flags = reinterpret_cast<int32_t*>(base + l.flags);
+    s.plan = reinterpret_cast<int32_t*>(base + l.plan);
+    s.clist = reinterpret_cast<int32_t*>(base + l.clist);
+    s.red = reinterpret_cast<float*>(base + l.red);
+    s.part = reinterpret_cast<float*>(base + l.part);
+    s.act = reinterpret_cast<float*>(base + l.act);
+    s.ring = base + l.ring;
+    return s;
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
+// Index of element k in the piece-split activation layout: pieces of 8
+// elements, first 4 of each piece in the low plane, last 4 in the high plane,
+// so that a lane reading "its" piece loads two conflict-free float4s.
+__device__ __forceinline__ int act_idx(int k, int half) {
+    return ((k & 4) ? half : 0) + (k >> 3) * 4 + (k & 3);
+}
+
+struct Cursor {  // geometry of one GEMV phase for this CTA
+    int K, KC, nK, rpu, wfmt;
+    int unit0, n_units, rows;
+    uint32_t nslots;
+};
+
+__device__ __forceinline__ Cursor cursor(const KieParams& P, const Smem& S, int type) {
+    const KiePhasePlan& pp = P.ph[type];
+    Cursor c;
+    c.K = pp.K; c.KC = pp.KC; c.nK = pp.nK; c.rpu = pp.rows_per_unit; c.wfmt = pp.wfmt;
+    c.unit0 = S.plan[type * 4 + 0];
+    c.n_units = S.plan[type * 4 + 1];
+    c.rows = c.n_units * c.rpu;
+    c.nslots = uint32_t(S.plan[type * 4 + 2]);
+    return c;
+}
+
+__device__ __forceinline__ uint32_t slot_bytes(int wfmt, int rows_g, int kc) {
+    if (wfmt == WF_F16) return uint32_t(rows_g) * uint32_t(kc) * 2u;
+    uint32_t b = uint32_t(rows_g) * uint32_t(kc / 2) + uint32_t(rows_g) * uint32_t(kc / 64);
+    return (b + 15u) & ~15u;
+}
+
+__device__ __forceinline__ void slot_geom(const Cursor& c, uint32_t j, int& g, int& ch, int& rows_g, int& kc) {
+    g = int(j / uint32_t(c.nK));
+    ch = int(j % uint32_t(c.nK));
+    rows_g = min(KIE_R, c.rows - g * KIE_R);
+    kc = min(c.KC, c.K - ch * c.KC);
+}
+
+// phase index within a step -> (layer, sub); sub: 0 QKV, 1 ATT, 2 O, 3 GU, 4 D, 5 LM
+__device__ __forceinline__ void phase_of(int phi, int L, int& layer, int& sub) {
+    if (phi >= 5 * L) { layer = L; sub = 5; }
+    else { layer = phi / 5; sub = phi % 5; }
+}
+__device__ __forceinline__ int gemv_type(int sub) {
+    return sub == 0 ? PH_QKV : sub == 2 ? PH_O : sub == 3 ? PH_GU : sub == 4 ? PH_D : sub == 5 ? PH_LM : -1;
+}
+__device__ __forceinline__ uint64_t stream_offset(const KieParams& P, const Smem& S, int layer, int type) {
+    uint64_t off = S.cbase[0];
+    if (type == PH_LM) return off + uint64_t(P.L) * S.cbase[1];
+    off += uint64_t(layer) * S.cbase[1];
+    for (int t = 0; t < type; ++t) off += uint32_t(S.plan[t * 4 + 3]);
+    return off;
+}
+
+__device__ __forceinline__ void slot_stamp(const KieLaunch& Lc, int cta, uint32_t g, int ev) {
+    if (Lc.prof_slots && cta == 0 && g < KIE_PROF_SLOTS) Lc.prof_slots[size_t(g) * 4 + ev] = globaltimer();
+}
+
+__device__ __forceinline__ void stamp(const KieParams& P, const KieLaunch& Lc, int t, int phi, int ev, int cta) {
+    if (Lc.prof) {
+        const size_t nph = size_t(5 * P.L + 1);
+        Lc.prof[((size_t(t) * nph + phi) * KIE_PROF_EVENTS + ev) * P.G + cta] = globaltimer();
+    }
+}
+
+__device__ void set_error(const KieParams& P, int code, int info) {
+    if (atomicCAS(&P.ctl->err, 0, code) == 0) P.ctl->err_info = info;
+}
+
+// ---------------------------------------------------------------------------------------------
+// KV cache access
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ size_t kv_elem_index(const KieParams& P, int layer, int h, int pos) {
+    return ((size_t(layer) * P.H + h) * P.max_ctx + pos) * P.hd;
+}
+__device__ __forceinline__ size_t tail_index(const KieParams& P, int layer, int kv, int h, int slot) {
+    return (((size_t(layer) * 2 + kv) * P.H + h) * KIE_SEG + slot) * P.hd;
+}
+__device__ __forceinline__ size_t meta_index(const KieParams& P, int layer, int kv, int h, int seg) {
+    return ((size_t(layer) * 2 + kv) * P.H + h) * P.nseg + seg;
+}
+
+// Attention work: head h owns CTAs [c0(h), c0(h+1)) with c0(h) = floor(h*G/H);
+// CTA k of them takes positions [floor(k*C/n_h), floor((k+1)*C/n_h)) of the C
+// attended ones.  Rows [j0, jt) were written in earlier steps and reach shared
+// memory through the weight ring (K slots, then V slots); rows [jt, j1) (the
+// current position, and for a uint8 cache the open segment kept in fp16) are
+// read directly after the grid barrier.
+struct AttChunk {
+    int h, c0, nh, j0, j1, jt;
+};
+__device__ __forceinline__ AttChunk att_chunk(const KieParams& P, int cta, int pos) {
+    AttChunk a;
+    const uint32_t H = uint32_t(P.H), G = uint32_t(P.G), C = uint32_t(pos) + 1u;
+    a.h = int(((uint32_t(cta) + 1u) * H - 1u) / G);
+    a.c0 = int(uint32_t(a.h) * G / H);
+    a.nh = int((uint32_t(a.h) + 1u) * G / H) - a.c0;
+    const uint32_t k = uint32_t(cta - a.c0);
+    a.j0 = int(k * C / uint32_t(a.nh));
+    a.j1 = int((k + 1u) * C / uint32_t(a.nh));
+    const int tma_end = (P.kv == KV_U8) ? (pos / KIE_SEG) * KIE_SEG : pos;
+    a.jt = max(a.j0, min(a.j1, tma_end));
+    return a;
+}
+__device__ __forceinline__ int att_row_bytes(const KieParams& P) { return P.hd * (P.kv == KV_F16 ? 2 : 1); }
+__device__ __forceinline__ int att_rows_per_slot(const KieParams& P) { return KIE_SLOT_BYTES / att_row_bytes(P); }
+__device__ __forceinline__ uint32_t att_kslots(const KieParams& P, const AttChunk& a) {
+    const int rps = att_rows_per_slot(P);
+    return uint32_t((a.jt - a.j0 + rps - 1) / rps);
+}
+
+// Producer: wait until global slot g's ring slot was released by its previous user.
+__device__ __forceinline__ bool producer_wait_empty(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                                    uint32_t g, int cta) {
+    const uint32_t nslot = uint32_t(P.nslot);
+    if (g < nslot) return true;
+    const uint32_t slot = g % nslot, par = ((g / nslot) - 1u) & 1u;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&S.empty[slot], par)) {
+        if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
+        if (globaltimer() - t0 > Lc.timeout_ns) {
+            set_error(P, KERR_TIMEOUT_EMPTY, cta);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Consumer warp: wait until global slot gidx has landed.  Every lane probes the
+// barrier (each lane needs the acquire of the bulk-copy data) but the decision
+// to continue or abort is warp-uniform, so no lane can leave the slot loop while
+// others go on to the warp's shuffles.
+__device__ __forceinline__ bool warp_wait_full(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                               uint32_t gidx, int cta, int lane) {
+    const uint32_t nslot = uint32_t(P.nslot);
+    const uint32_t slot = gidx % nslot, q = gidx / nslot;
+    uint64_t* fb = &S.full[2 * slot + (q & 1u)];
+    const uint32_t par = (q >> 1) & 1u;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        const bool done = mbar_try_wait(fb, par);
+        if (__all_sync(0xffffffffu, done)) return true;
+        int bad = 0;
+        if (lane == 0) {
+            if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) bad = 1;
+            else if (globaltimer() - t0 > Lc.timeout_ns) { set_error(P, KERR_TIMEOUT_FULL, cta); bad = 1; }
+        }
+        if (__shfl_sync(0xffffffffu, bad, 0)) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// producer warp: stream every slot of this CTA, in consumption order, into the ring
+// ---------------------------------------------------------------------------------------------
+__device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
+    const uint64_t pol = policy_evict_first();
+    const uint32_t nslot = uint32_t(P.nslot);
+    uint32_t g = 0;
+    bool abort = false;
+    const uint64_t pol_kv = policy_evict_first();
+    const int pos0 = Lc.pos0 >= 0 ? Lc.pos0 : ld_volatile_i32(&P.ctl->pos);
+    for (int t = 0; t < Lc.n_steps && !abort; ++t) {
+        for (int phi = Lc.phase_begin; phi < Lc.phase_end && !abort; ++phi) {
+            int layer, sub;
+            phase_of(phi, P.L, layer, sub);
+            const int type = gemv_type(sub);
+            if (sub == 1) {
+                // attention: this CTA's K rows then V rows written in earlier steps
+                const int pos = pos0 + t;
+                const AttChunk a = att_chunk(P, cta, pos);
+                const uint32_t nks = att_kslots(P, a);
+                const int rps = att_rows_per_slot(P), rb = att_row_bytes(P);
+                for (uint32_t j = 0; j < 2 * nks && !abort; ++j, ++g) {
+                    const uint32_t slot = g % nslot;
+                    if (!producer_wait_empty(P, Lc, S, g, cta)) { abort = true; break; }
+                    const int kv = j >= nks ? 1 : 0;
+                    const int r0 = int(j - uint32_t(kv) * nks) * rps;
+                    const int rows = min(rps, a.jt - a.j0 - r0);
+                    const uint8_t* base = kv ? P.vc : P.kc;
+                    const uint8_t* src = base + (kv_elem_index(P, layer, a.h, a.j0 + r0)) * size_t(rb / P.hd);
+                    const uint32_t bytes = uint32_t(rows * rb);
+                    uint64_t* fb = &S.full[2 * slot + ((g / nslot) & 1u)];
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(S.ring + size_t(slot) * KIE_SLOT_BYTES, src, bytes, fb, pol_kv);
+                    slot_stamp(Lc, cta, g, 0);
+                }
+                continue;
+            }
+            if (type < 0) continue;
+            if (type == PH_LM && t < Lc.lm_from_step) continue;
+            const Cursor c = cursor(P, S, type);
+            const uint8_t* src = P.wstream + stream_offset(P, S, layer, type);
+            for (uint32_t j = 0; j < c.nslots; ++j, ++g) {
+                const uint32_t slot = g % nslot;
+                if (!producer_wait_empty(P, Lc, S, g, cta)) { abort = true; break; }
+                int gg, ch, rows_g, kc;
+                slot_geom(c, j, gg, ch, rows_g, kc);
+                const uint32_t bytes = slot_bytes(c.wfmt, rows_g, kc);
+                uint64_t* fb = &S.full[2 * slot + ((g / nslot) & 1u)];
+                mbar_arrive_expect_tx(fb, bytes);
+                bulk_g2s(S.ring + size_t(slot) * KIE_SLOT_BYTES, src, bytes, fb, pol);
+                slot_stamp(Lc, cta, g, 0);
+                src += bytes;
+                if (j == 0) stamp(P, Lc, t, phi, 4, cta);
+                if (j + 1 == c.nslots) stamp(P, Lc, t, phi, 5, cta);
+            }
+        }
+    }
+    // Wait until every copy issued into the ring has landed before the CTA may exit.
+    const uint32_t issued = g;
+    const uint32_t first = issued > nslot ? issued - nslot : 0u;
+    for (uint32_t k = first; k < issued; ++k) {
+        const uint32_t slot = k % nslot, q = k / nslot;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&S.full[2 * slot + (q & 1u)], (q >> 1) & 1u)) {
+            if (globaltimer() - t0 > Lc.timeout_ns) { set_error(P, KERR_TIMEOUT_FULL, cta); break; }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// consumer helpers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float block_sum(float v, float* red, int tid) {
+    v = warp_sum(v);
+    if ((tid & 31) == 0) red[tid >> 5] = v;
+    consumer_sync(NCT);
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s += red[w];
+    consumer_sync(NCT);
+    return s;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red, int tid) {
+    v = warp_max(v);
+    if ((tid & 31) == 0) red[tid >> 5] = v;
+    consumer_sync(NCT);
+    float m = red[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) m = fmaxf(m, red[w]);
+    consumer_sync(NCT);
+    return m;
+}
+
+// act <- rmsnorm(src) * g, with src = x (fp32, global) or an embedding row (fp16).
+// Pass 1 stages the raw values in shared memory (4 loads in flight per thread)
+// while summing squares; pass 2 rescales each thread's own elements in place,
+// so no register array stays live across the block reduction.
+__device__ void act_rmsnorm(const KieParams& P, const Smem& S, const float* x, const uint16_t* emb_row,
+                            const float* g, int tid) {
+    const int d = P.d, half = P.act_floats / 2, ng = d >> 2;
+    float ss = 0.f;
+    for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int q = q0 + u * NCT;
+            if (q < ng) {
+                if (x) {
+                    v[u] = __ldcg(reinterpret_cast<const float4*>(x) + q);
+                } else {
+                    const uint2 hv = *reinterpret_cast<const uint2*>(emb_row + 4 * q);
+                    const float2 a = h2_to_f2(hv.x), b = h2_to_f2(hv.y);
+                    v[u] = make_float4(a.x, a.y, b.x, b.y);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int q = q0 + u * NCT;
+            if (q < ng) {
+                ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+                // 4 consecutive elements share one plane of one 8-element piece
+                *reinterpret_cast<float4*>(S.act + act_idx(4 * q, half)) = v[u];
+            }
+        }
+    }
+    const float tot = block_sum(ss, S.red, tid);
+    const float r = sqrtf(tot / float(d) + P.eps);
+    for (int q = tid; q < ng; q += NCT) {
+        float4* a = reinterpret_cast<float4*>(S.act + act_idx(4 * q, half));
+        const float4 v = *a;
+        const float4 gg = *reinterpret_cast<const float4*>(g + 4 * q);
+        *a = make_float4((v.x / r) * gg.x, (v.y / r) * gg.y, (v.z / r) * gg.z, (v.w / r) * gg.w);
+    }
+    consumer_sync(NCT);
+}
+
+__device__ void act_copy(const KieParams& P, const Smem& S, const float* src, int n, int tid) {
+    const int half = P.act_floats / 2, ng = n >> 2;
+    for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (q0 + u * NCT < ng) v[u] = __ldcg(reinterpret_cast<const float4*>(src) + q0 + u * NCT);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (q0 + u * NCT < ng) *reinterpret_cast<float4*>(S.act + act_idx(4 * (q0 + u * NCT), half)) = v[u];
+    }
+    consumer_sync(NCT);
+}
+
+// y-partials of one fp16 slot: rows_g rows x kc columns, row-major; columns start at k0.
+__device__ __forceinline__ void slot_f16(const uint8_t* slot, int rows_g, int kc, int k0, const float* act,
+                                         int half, int lane, float* acc) {
+    const int npc = kc >> 3;
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+    for (int p = lane; p < npc; p += 32) {
+        const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
+#pragma unroll
+        for (int r = 0; r < KIE_R; ++r) {
+            if (r < rows_g) {
+                const uint4 w = *reinterpret_cast<const uint4*>(slot + size_t(r) * kc * 2 + size_t(p) * 16);
+                const float2 a = h2_to_f2(w.x), b = h2_to_f2(w.y), c = h2_to_f2(w.z), e = h2_to_f2(w.w);
+                float s = acc[r];
+                s = fmaf(a.x, xl.x, s); s = fmaf(a.y, xl.y, s); s = fmaf(b.x, xl.z, s); s = fmaf(b.y, xl.w, s);
+                s = fmaf(c.x, xh.x, s); s = fmaf(c.y, xh.y, s); s = fmaf(e.x, xh.z, s); s = fmaf(e.y, xh.w, s);
+                acc[r] = s;
+            }
+        }
+    }
+}
+
+// The common full slot (KIE_R rows x KIE_KC_F16 columns) with compile-time
+// bounds, so the loads of all iterations can be in flight together.
+__device__ __forceinline__ void slot_f16_full(const uint8_t* slot, int k0, const float* act, int half, int lane,
+                                              float* acc) {
+    constexpr int NPC = KIE_KC_F16 / 8;
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+#pragma unroll
+    for (int it = 0; it < NPC / 32; ++it) {
+        const int p = lane + it * 32;
+        const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
+#pragma unroll
+        for (int r = 0; r < KIE_R; ++r) {
+            const uint4 w = *reinterpret_cast<const uint4*>(slot + size_t(r) * KIE_KC_F16 * 2 + size_t(p) * 16);
+            const float2 a = h2_to_f2(w.x), b = h2_to_f2(w.y), c = h2_to_f2(w.z), e = h2_to_f2(w.w);
+            float s = acc[r];
+            s = fmaf(a.x, xl.x, s); s = fmaf(a.y, xl.y, s); s = fmaf(b.x, xl.z, s); s = fmaf(b.y, xl.w, s);
+            s = fmaf(c.x, xh.x, s); s = fmaf(c.y, xh.y, s); s = fmaf(e.x, xh.z, s); s = fmaf(e.y, xh.w, s);
+            acc[r] = s;
+        }
+    }
+}
+
+// INT4 slot: codes [rows_g][kc/2] (element 2b in the low nibble of byte b, two's
+// complement), then fp16 scales [rows_g][kc/128].  Each lane takes 8-element
+// pieces; a piece lies inside one 128-column group.
+__device__ __forceinline__ void slot_i4(const uint8_t* slot, int rows_g, int kc, int k0, const float* act,
+                                        int half, int lane, float* acc) {
+    const int npc = kc >> 3;
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + size_t(rows_g) * (kc / 2));
+    const __half2 bias = __floats2half2_rn(1032.f, 1032.f);
+    for (int p = lane; p < npc; p += 32) {
+        const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
+        const float xlo[4] = {xl.x, xl.y, xl.z, xl.w};
+        const float xhi[4] = {xh.x, xh.y, xh.z, xh.w};
+        const int grp = p >> 4;
+#pragma unroll
+        for (int r = 0; r < KIE_R; ++r) {
+            if (r < rows_g) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(slot + size_t(r) * (kc / 2) + size_t(p) * 4);
+                const uint32_t u = w ^ 0x88888888u;  // nibble q -> q + 8 in [0, 15]
+                float t = 0.f;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    // (1024 + n) as fp16 for nibbles s and s+4, minus 1032 -> exact q
+                    uint32_t hbits = ((u >> (4 * s)) & 0x000F000Fu) | 0x64006400u;
+                    const __half2 q2 = __hsub2(*reinterpret_cast<__half2*>(&hbits), bias);
+                    const float2 f = __half22float2(q2);
+                    t = fmaf(f.x, xlo[s], t);
+                    t = fmaf(f.y, xhi[s], t);
+                }
+                const float scale = __half2float(__ushort_as_half(sc[r * (kc >> 7) + grp]));
+                acc[r] = fmaf(scale, t, acc[r]);
+            }
+        }
+    }
+}
+
+// Consume this phase's slots (those with global index == warp mod NW) and leave
+// per-(row, chunk) partial sums in S.part.  Returns false on abort.
+__device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c, uint32_t& gc,
+                         int warp, int lane, int cta) {
+    const uint32_t nslot = uint32_t(P.nslot);
+    const int half = P.act_floats / 2;
+    bool ok = true;
+    const uint32_t first = uint32_t(warp);   // slot j of a phase -> warp j % NW (mode independent)
+    for (uint32_t j = first; j < c.nslots; j += NW) {
+        const uint32_t gidx = gc + j;
+        const uint32_t slot = gidx % nslot;
+        if (!warp_wait_full(P, Lc, S, gidx, cta, lane)) { ok = false; break; }
+        if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
+        int g, ch, rows_g, kc;
+        slot_geom(c, j, g, ch, rows_g, kc);
+        float acc[KIE_R] = {0.f, 0.f, 0.f, 0.f};
+        const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
+        if (c.wfmt == WF_F16) {
+            if (rows_g == KIE_R && kc == KIE_KC_F16) slot_f16_full(sl, ch * c.KC, S.act, half, lane, acc);
+            else slot_f16(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+        }
+        else slot_i4(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+#pragma unroll
+        for (int r = 0; r < KIE_R; ++r) acc[r] = warp_sum(acc[r]);
+        if (lane == 0) {
+            for (int r = 0; r < rows_g; ++r) S.part[(g * KIE_R + r) * c.nK + ch] = acc[r];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            slot_stamp(Lc, cta, gidx, 2);
+            mbar_arrive(&S.empty[slot]);
+        }
+    }
+    gc += c.nslots;
+    if (!ok) S.flags[0] = 1;
+    consumer_sync(NCT);
+    return ld_volatile_i32(&S.flags[0]) == 0;
+}
+
+__device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) {
+    float y = 0.f;
+    for (int ch = 0; ch < c.nK; ++ch) y += S.part[r * c.nK + ch];
+    return y;
+}
+
+// store one element of the new K (kv=0) or V (kv=1) at position pos
+__device__ __forceinline__ void kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v) {
+    const __half hv = __float2half_rn(v);
+    if (P.kv == KV_F16) {
+        uint8_t* base = kv ? P.vc : P.kc;
+        reinterpret_cast<__half*>(base)[kv_elem_index(P, layer, h, pos) + dim] = hv;
+    } else if (P.kv == KV_E5M2) {
+        uint8_t* base = kv ? P.vc : P.kc;
+        base[kv_elem_index(P, layer, h, pos) + dim] = uint8_t(f16x2_to_e5m2x2(hv, hv) & 0xFFu);
+    } else {
+        reinterpret_cast<__half*>(P.tail)[tail_index(P, layer, kv, h, pos % KIE_SEG) + dim] = hv;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// phase epilogues
+// ---------------------------------------------------------------------------------------------
+__device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int layer, int pos, int tid) {
+    const int hh = P.hd / 2;
+    const int per = P.H * hh;  // units per matrix
+    for (int u = tid; u < c.n_units; u += NCT) {
+        const float ya = row_sum(S, c, 2 * u), yb = row_sum(S, c, 2 * u + 1);
+        const int U = c.unit0 + u;
+        const int which = U / per, rem = U % per, h = rem / hh, i = rem % hh;
+        if (which == 2) {
+            kv_store(P, layer, 1, h, pos, i, ya);
+            kv_store(P, layer, 1, h, pos, i + hh, yb);
+            continue;
+        }
+        float sn, cs;
+        sincosf(float(pos) * P.inv_freq[i], &sn, &cs);
+        const float ra = ya * cs - yb * sn, rb = yb * cs + ya * sn;
+        if (which == 0) {
+            P.q[h * P.hd + i] = ra;
+            P.q[h * P.hd + i + hh] = rb;
+        } else {
+            kv_store(P, layer, 0, h, pos, i, ra);
+            kv_store(P, layer, 0, h, pos, i + hh, rb);
+        }
+    }
+    // K/V written here are read in later steps by bulk copies (the async proxy).
+    fence_proxy_async_global();
+}
+
+__device__ void epi_residual(const KieParams& P, const Smem& S, const Cursor& c, int tid) {
+    for (int r = tid; r < c.rows; r += NCT) {
+        const int row = c.unit0 + r;
+        P.x[row] = __ldcg(P.x + row) + row_sum(S, c, r);
+    }
+}
+
+__device__ void epi_swiglu(const KieParams& P, const Smem& S, const Cursor& c, int tid) {
+    for (int u = tid; u < c.n_units; u += NCT) {
+        const float gt = row_sum(S, c, 2 * u), up = row_sum(S, c, 2 * u + 1);
+        P.a[c.unit0 + u] = (gt / (1.f + expf(-gt))) * up;
+    }
+}
+
+// LM head: logits, per-CTA argmax (lowest index on ties), last CTA reduces.
+// Returns the reduced token through S.flags[2] on the reducing CTA only.
+__device__ void epi_lm(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c, int cta, int tid,
+                       int step, int pos) {
+    float best = -INFINITY;
+    int bidx = 0x7fffffff;
+    for (int r = tid; r < c.rows; r += NCT) {
+        const float y = row_sum(S, c, r);
+        const int row = c.unit0 + r;
+        if (Lc.out_logits) Lc.out_logits[size_t(step - Lc.lm_from_step) * P.V + row] = y;
+        if (y > best || (y == best && row < bidx)) { best = y; bidx = row; }
+    }
+    // block argmax
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+        if (ov > best || (ov == best && oi < bidx)) { best = ov; bidx = oi; }
+    }
+    int* ridx = reinterpret_cast<int*>(S.red + 32);
+    if ((tid & 31) == 0) { S.red[tid >> 5] = best; ridx[tid >> 5] = bidx; }
+    consumer_sync(NCT);
+    if (tid == 0) {
+        for (int w = 1; w < NW; ++w) {
+            if (S.red[w] > best || (S.red[w] == best && ridx[w] < bidx)) { best = S.red[w]; bidx = ridx[w]; }
+        }
+        P.amax_val[cta] = best;
+        P.amax_idx[cta] = bidx;
+        __threadfence();
+        const uint32_t old = atomicAdd(&P.ctl->amax_cnt, 1u);
+        S.flags[1] = (old == uint32_t(P.G) - 1u) ? 1 : 0;
+    }
+    consumer_sync(NCT);
+    const int warp = tid >> 5, lane = tid & 31;
+    if (S.flags[1] && warp == 0) {
+        __threadfence();
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = lane; i < P.G; i += 32) {
+            const float v = __ldcg(P.amax_val + i);
+            const int ix = __ldcg(P.amax_idx + i);
+            if (v > bv || (v == bv && ix < bi)) { bv = v; bi = ix; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) {
+            if (bi < 0 || bi >= P.V) bi = 0;  // all logits NaN: keep a valid id
+            P.ctl->amax_cnt = 0u;
+            P.ctl->tok = bi;
+            P.ctl->pos = pos + 1;
+            if (Lc.out_tokens) Lc.out_tokens[step] = bi;
+            __threadfence();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// split-KV attention
+// ---------------------------------------------------------------------------------------------
+// One row's 16 dims [dim0, dim0+16) of K or V as raw storage (converted to fp32
+// only when used, so several rows can be in flight per lane).
+// mode: 0 = stored (fp16 / E5M2 / u8 codes with the segment's scale, zp),
+//       1 = u8 open segment, read from the fp16 tail,
+//       2 = u8 segment completed in this step (quantised now with fz's scale, zp).
+struct RawRow {
+    uint4 a, b;     // fp16: 32 bytes; 8-bit formats: a only
+    float sc;       // u8 mode 0
+    int zp;
+    int mode;
+};
+
+template <int KVF>
+__device__ __forceinline__ void load_raw(const KieParams& P, int layer, int kv, int h, int pos, int dim0, int mode,
+                                         RawRow& r) {
+    r.mode = mode;
+    if (KVF == KV_F16 || (KVF == KV_U8 && mode != 0)) {
+        const uint4* src;
+        if (KVF == KV_F16) {
+            const uint8_t* base = kv ? P.vc : P.kc;
+            src = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(base) +
+                                                 kv_elem_index(P, layer, h, pos) + dim0);
+        } else {
+            src = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(P.tail) +
+                                                 tail_index(P, layer, kv, h, pos % KIE_SEG) + dim0);
+        }
+        r.a = __ldcg(src);
+        r.b = __ldcg(src + 1);
+    } else {
+        const uint8_t* base = kv ? P.vc : P.kc;
+        r.a = __ldcg(reinterpret_cast<const uint4*>(base + kv_elem_index(P, layer, h, pos) + dim0));
+        if (KVF == KV_U8) {
+            const size_t mi = meta_index(P, layer, kv, h, pos / KIE_SEG);
+            r.sc = __ldcg(P.seg_scale + mi);
+            r.zp = __ldcg(P.seg_zp + mi);
+        }
+    }
+}
+
+template <int KVF>
+__device__ __forceinline__ void convert_row(const RawRow& r, const float* fz, float* f) {
+    if (KVF == KV_F16 || (KVF == KV_U8 && r.mode != 0)) {
+        const uint32_t w[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { const float2 t = h2_to_f2(w[i]); f[2 * i] = t.x; f[2 * i + 1] = t.y; }
+        if (KVF == KV_U8 && r.mode == 2) {
+            const float sc = fz[0];
+            const int zp = __float_as_int(fz[1]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int qv = min(max(__float2int_rn(f[i] / sc) + zp, 0), 255);
+                f[i] = float(qv - zp) * sc;
+            }
+        }
+    } else if (KVF == KV_E5M2) {
+        e5m2x4_to_f32(r.a.x, f); e5m2x4_to_f32(r.a.y, f + 4); e5m2x4_to_f32(r.a.z, f + 8); e5m2x4_to_f32(r.a.w, f + 12);
+    } else {
+        const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = float(int((w[i >> 2] >> (8 * (i & 3))) & 0xFFu) - r.zp) * r.sc;
+    }
+}
+
+// scale/zp of one (layer, kv, head) open segment, from its 128 fp16 tail rows.
+__device__ void u8_segment_params(const KieParams& P, const Smem& S, int layer, int kv, int h, int tid,
+                                  float* out /* [0]=scale, [1]=zp bits */) {
+    const __half* t = reinterpret_cast<const __half*>(P.tail) + tail_index(P, layer, kv, h, 0);
+    const int n = KIE_SEG * P.hd;
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = tid; i < n; i += NCT) {
+        const float v = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(t) + i)));
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+    }
+    mx = block_max(mx, S.red, tid);
+    mn = -block_max(-mn, S.red, tid);
+    if (tid == 0) {
+        float sc;
+        int zp;
+        if (mx == mn) { sc = 1.f; zp = __float2int_rn(-mn); }
+        else { sc = (mx - mn) / 255.f; zp = __float2int_rn(-mn / sc); }
+        out[0] = sc;
+        out[1] = __int_as_float(zp);
+    }
+    consumer_sync(NCT);
+}
+
+// Write codes + meta of a segment completed in this step (its owner CTA only).
+__device__ void u8_segment_commit(const KieParams& P, int layer, int kv, int h, int seg, const float* fz, int tid) {
+    const __half* t = reinterpret_cast<const __half*>(P.tail) + tail_index(P, layer, kv, h, 0);
+    uint8_t* dst = (kv ? P.vc : P.kc) + kv_elem_index(P, layer, h, seg * KIE_SEG);
+    const float sc = fz[0];
+    const int zp = __float_as_int(fz[1]);
+    const int n = KIE_SEG * P.hd;
+    for (int i = tid; i < n; i += NCT) {
+        const float v = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(t) + i)));
+        dst[i] = uint8_t(min(max(__float2int_rn(v / sc) + zp, 0), 255));
+    }
+    if (tid == 0) {
+        const size_t mi = meta_index(P, layer, kv, h, seg);
+        P.seg_scale[mi] = sc;
+        P.seg_zp[mi] = zp;
+    }
+}
+
+// 16 dims of a row held in shared memory (ring slot) -> fp32.
+template <int KVF>
+__device__ __forceinline__ void smem_row16(const uint8_t* row, int dim0, float sc, int zp, float* f) {
+    if (KVF == KV_F16) {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + dim0 * 2);
+        const uint4 b = *reinterpret_cast<const uint4*>(row + dim0 * 2 + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { const float2 t = h2_to_f2(w[i]); f[2 * i] = t.x; f[2 * i + 1] = t.y; }
+    } else if (KVF == KV_E5M2) {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + dim0);
+        e5m2x4_to_f32(a.x, f); e5m2x4_to_f32(a.y, f + 4); e5m2x4_to_f32(a.z, f + 8); e5m2x4_to_f32(a.w, f + 12);
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + dim0);
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = float(int((w[i >> 2] >> (8 * (i & 3))) & 0xFFu) - zp) * sc;
+    }
+}
+
+template <int HD, int KVF>
+__device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S, int layer, int pos, int cta,
+                          uint32_t& gc, int warp, int lane, int tid) {
+    constexpr int LPR = HD / 16;       // lanes per row (16 dims each)
+    constexpr int RPI = 32 / LPR;      // rows per warp instruction
+    constexpr int NRG = NW * RPI;      // row groups per CTA (direct rows)
+    constexpr int UR = 4;              // direct rows in flight per lane group
+    const AttChunk a = att_chunk(P, cta, pos);
+    const int h = a.h, j0 = a.j0, j1 = a.j1, jt = a.jt;
+    const int n = j1 - j0, nt = jt - j0;
+    const int lg = lane % LPR, rw = lane / LPR;
+    const int dim0 = lg * 16;
+    const int rps = att_rows_per_slot(P), rb = att_row_bytes(P);
+    const uint32_t nks = att_kslots(P, a), nslot = uint32_t(P.nslot);
+    float* scores = S.act;
+    float* fz = S.red + NW * (KIE_MAX_HEAD_DIM + 2);   // [0..1] K scale/zp, [2..3] V scale/zp (fresh segment)
+    float* segm = S.part;                              // uint8: per-segment scale/zp of this chunk [2][nseg][2]
+    const bool u8_fresh = (KVF == KV_U8) && (pos % KIE_SEG == KIE_SEG - 1);
+    const int open_seg = pos / KIE_SEG;
+    const int seg0 = j0 / KIE_SEG, nsegc = (KVF == KV_U8 && nt > 0) ? (jt - 1) / KIE_SEG - seg0 + 1 : 0;
+    if (KVF == KV_U8) {
+        for (int i = tid; i < 2 * nsegc; i += NCT) {
+            const int kv = i / nsegc, sg = seg0 + i % nsegc;
+            const size_t mi = meta_index(P, layer, kv, h, sg);
+            segm[2 * i] = __ldcg(P.seg_scale + mi);
+            segm[2 * i + 1] = __int_as_float(__ldcg(P.seg_zp + mi));
+        }
+        if (u8_fresh && j1 > open_seg * KIE_SEG) {
+            u8_segment_params(P, S, layer, 0, h, tid, fz);
+            u8_segment_params(P, S, layer, 1, h, tid, fz + 2);
+            if (j1 == pos + 1) {  // the CTA holding position pos stores the codes for later steps
+                u8_segment_commit(P, layer, 0, h, open_seg, fz, tid);
+                u8_segment_commit(P, layer, 1, h, open_seg, fz + 2, tid);
+                fence_proxy_async_global();
+            }
+        }
+        consumer_sync(NCT);
+    }
+    float qv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qv[i] = __ldcg(P.q + h * HD + dim0 + i);
+    // fp16 / E5M2: the only row not streamed through the ring is the current
+    // position, [jt, j1) = {pos} when this chunk ends at pos; warp 0's first
+    // row group fetches its K and V together with q (one round trip).
+    constexpr bool ONE_DIRECT = (KVF != KV_U8);
+    const bool has_pos = ONE_DIRECT && (j1 > jt);
+    RawRow kpos, vpos;
+    kpos.a = kpos.b = vpos.a = vpos.b = make_uint4(0, 0, 0, 0);
+    kpos.sc = vpos.sc = 0.f; kpos.zp = vpos.zp = 0; kpos.mode = vpos.mode = 0;
+    if (has_pos && warp == 0 && rw == 0) {
+        load_raw<KVF>(P, layer, 0, h, jt, dim0, 0, kpos);
+        load_raw<KVF>(P, layer, 1, h, jt, dim0, 0, vpos);
+    }
+
+    // ---- pass 1: scores, K rows from the ring
+    float mloc = -INFINITY;
+    bool ok = true;
+    const uint32_t first = uint32_t(warp);   // slot j of a phase -> warp j % NW (mode independent)
+    for (uint32_t j = first; j < nks; j += NW) {
+        const uint32_t gidx = gc + j, slot = gidx % nslot;
+        if (!warp_wait_full(P, Lc, S, gidx, cta, lane)) { ok = false; break; }
+        if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
+        const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
+        const int r0 = int(j) * rps, rs = min(rps, nt - r0);
+        constexpr int RU = 4;                           // rows per lane group per iteration
+        for (int ib = 0; ib < rs; ib += RPI * RU) {     // uniform over the warp
+            float dsum[RU];
+#pragma unroll
+            for (int u = 0; u < RU; ++u) {
+                const int rl = ib + rw + u * RPI;
+                float kf[16];
+                float sc = 0.f;
+                int zp = 0;
+                if (KVF == KV_U8 && rl < rs) {
+                    const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
+                    sc = segm[2 * sg];
+                    zp = __float_as_int(segm[2 * sg + 1]);
+                }
+                smem_row16<KVF>(sl + size_t(min(rl, rs - 1)) * rb, dim0, sc, zp, kf);
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) { d0 = fmaf(qv[i], kf[i], d0); d1 = fmaf(qv[i + 1], kf[i + 1], d1); }
+                dsum[u] = d0 + d1;
+            }
+#pragma unroll
+            for (int o = 1; o < LPR; o <<= 1) {
+#pragma unroll
+                for (int u = 0; u < RU; ++u) dsum[u] += __shfl_xor_sync(0xffffffffu, dsum[u], o);
+            }
+#pragma unroll
+            for (int u = 0; u < RU; ++u) {
+                const int rl = ib + rw + u * RPI;
+                if (rl < rs) {
+                    const float s = dsum[u] * P.attn_scale;
+                    if (lg == 0) scores[r0 + rl] = s;
+                    mloc = fmaxf(mloc, s);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            slot_stamp(Lc, cta, gidx, 2);
+            mbar_arrive(&S.empty[slot]);
+        }
+    }
+    // direct rows [jt, j1)
+    if (ONE_DIRECT) {
+        if (has_pos && warp == 0) {                     // uniform over warp 0
+            float kf[16];
+            convert_row<KVF>(kpos, fz, kf);
+            float dsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dsum = fmaf(qv[i], kf[i], dsum);
+#pragma unroll
+            for (int o = 1; o < LPR; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+            if (rw == 0) {
+                const float sc = dsum * P.attn_scale;
+                if (lg == 0) scores[nt] = sc;
+                mloc = fmaxf(mloc, sc);
+            }
+        }
+    } else
+    for (int base = nt + warp * RPI; base < n; base += NRG * UR) {
+        RawRow kr[UR];
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+            const int r = base + rw + u * NRG;
+            kr[u].a = kr[u].b = make_uint4(0, 0, 0, 0);
+            kr[u].sc = 0.f; kr[u].zp = 0; kr[u].mode = 0;
+            if (r < n) {
+                const int jj = j0 + r;
+                int mode = 0;
+                if (KVF == KV_U8) mode = u8_fresh ? 2 : 1;
+                load_raw<KVF>(P, layer, 0, h, jj, dim0, mode, kr[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+            const int r = base + rw + u * NRG;
+            float kf[16];
+            convert_row<KVF>(kr[u], fz, kf);
+            float dsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dsum = fmaf(qv[i], kf[i], dsum);
+#pragma unroll
+            for (int o = 1; o < LPR; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+            if (r < n) {
+                const float s = dsum * P.attn_scale;
+                if (lg == 0) scores[r] = s;
+                mloc = fmaxf(mloc, s);
+            }
+        }
+    }
+    gc += nks;
+    if (!ok) S.flags[0] = 1;
+    const float m = block_max(mloc, S.red, tid);
+    if (ld_volatile_i32(&S.flags[0]) != 0) return false;
+
+    // ---- pass 2: p = exp(s - m), l = sum p, o = sum p v
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float lsum = 0.f;
+    const uint32_t first2 = uint32_t(warp);
+    for (uint32_t j = first2; j < nks; j += NW) {
+        const uint32_t gidx = gc + j, slot = gidx % nslot;
+        if (!warp_wait_full(P, Lc, S, gidx, cta, lane)) { ok = false; break; }
+        if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
+        const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
+        const int r0 = int(j) * rps, rs = min(rps, nt - r0);
+        constexpr int RU2 = 2;
+        for (int ib = rw; ib < rs; ib += RPI * RU2) {    // no shuffles inside: lanes may diverge
+            float pr[RU2];
+            float vf[RU2][16];
+#pragma unroll
+            for (int u = 0; u < RU2; ++u) {
+                const int rl = ib + u * RPI;
+                float sc = 0.f;
+                int zp = 0;
+                if (KVF == KV_U8 && rl < rs) {
+                    const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
+                    sc = segm[2 * (nsegc + sg)];
+                    zp = __float_as_int(segm[2 * (nsegc + sg) + 1]);
+                }
+                smem_row16<KVF>(sl + size_t(min(rl, rs - 1)) * rb, dim0, sc, zp, vf[u]);
+                pr[u] = rl < rs ? expf(scores[r0 + rl] - m) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < RU2; ++u) {
+                lsum += pr[u];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = fmaf(pr[u], vf[u][i], acc[i]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            slot_stamp(Lc, cta, gidx, 2);
+            mbar_arrive(&S.empty[slot]);
+        }
+    }
+    if (ONE_DIRECT) {
+        if (has_pos && warp == 0 && rw == 0) {
+            float vf[16];
+            convert_row<KVF>(vpos, fz + 2, vf);
+            const float pr = expf(scores[nt] - m);
+            lsum += pr;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = fmaf(pr, vf[i], acc[i]);
+        }
+    } else
+    for (int base = nt + warp * RPI; base < n; base += NRG * UR) {
+        RawRow vr[UR];
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+            const int r = base + rw + u * NRG;
+            vr[u].a = vr[u].b = make_uint4(0, 0, 0, 0);
+            vr[u].sc = 0.f; vr[u].zp = 0; vr[u].mode = 0;
+            if (r < n) {
+                const int jj = j0 + r;
+                int mode = 0;
+                if (KVF == KV_U8) mode = u8_fresh ? 2 : 1;
+                load_raw<KVF>(P, layer, 1, h, jj, dim0, mode, vr[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+            const int r = base + rw + u * NRG;
+            if (r < n) {
+                float vf[16];
+                convert_row<KVF>(vr[u], fz + 2, vf);
+                const float pr = expf(scores[r] - m);
+                lsum += pr;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = fmaf(pr, vf[i], acc[i]);
+            }
+        }
+    }
+    gc += nks;
+    if (!ok) S.flags[0] = 1;
+    // reduce over the row groups of this warp (lanes with equal lg)
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1) {
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    }
+    float* wp = S.red + warp * (KIE_MAX_HEAD_DIM + 2);
+    consumer_sync(NCT);   // block_max's scratch (S.red[0..NW)) is free again
+    if (lane < LPR) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wp[2 + dim0 + i] = acc[i];
+        if (lane == 0) wp[0] = lsum;
+    }
+    consumer_sync(NCT);
+    if (ld_volatile_i32(&S.flags[0]) != 0) return false;
+    // partial (m, l, o[HD]) of this CTA's chunk
+    float* gp = P.att_part + size_t(cta) * (HD + 4);
+    if (tid < HD) {
+        float sacc = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) sacc += S.red[w * (KIE_MAX_HEAD_DIM + 2) + 2 + tid];
+        gp[4 + tid] = sacc;
+    } else if (tid == HD) {
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) l += S.red[w * (KIE_MAX_HEAD_DIM + 2)];
+        gp[0] = m;
+        gp[1] = l;
+    }
+    consumer_sync(NCT);
+    // The last of head h's CTAs to arrive combines the head's partials in CTA
+    // order.  The acq_rel add publishes this block's partial (ordered before it
+    // by the barrier above) and, for the last arriver, acquires the others'.
+    if (tid == 0) {
+        const uint32_t old = atom_add_acq_rel_gpu(P.head_cnt + h, 1u);
+        S.flags[1] = (old == uint32_t(a.nh) - 1u) ? 1 : 0;
+    }
+    consumer_sync(NCT);
+    if (S.flags[1]) {
+        if (tid < HD) {
+            // every contributor's (m, l, o[tid]) requested in one wave
+            constexpr int MAXC = 10;
+            const int cnt = a.nh;
+            float mk[MAXC], lk[MAXC], ok[MAXC];
+#pragma unroll
+            for (int k = 0; k < MAXC; ++k) {
+                if (k < cnt) {
+                    const float* pp = P.att_part + size_t(a.c0 + k) * (HD + 4);
+                    mk[k] = __ldcg(pp);
+                    lk[k] = __ldcg(pp + 1);
+                    ok[k] = __ldcg(pp + 4 + tid);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < MAXC; ++k) if (k < cnt) M = fmaxf(M, mk[k]);
+            for (int k = MAXC; k < cnt; ++k) M = fmaxf(M, __ldcg(P.att_part + size_t(a.c0 + k) * (HD + 4)));
+            float Ls = 0.f, Os = 0.f;
+#pragma unroll
+            for (int k = 0; k < MAXC; ++k) {
+                if (k < cnt) {
+                    const float w = (mk[k] == -INFINITY) ? 0.f : expf(mk[k] - M);   // empty chunk
+                    Ls = fmaf(w, lk[k], Ls);
+                    Os = fmaf(w, ok[k], Os);
+                }
+            }
+            for (int k = MAXC; k < cnt; ++k) {
+                const float* pp = P.att_part + size_t(a.c0 + k) * (HD + 4);
+                const float mm = __ldcg(pp);
+                const float w = (mm == -INFINITY) ? 0.f : expf(mm - M);
+                Ls = fmaf(w, __ldcg(pp + 1), Ls);
+                Os = fmaf(w, __ldcg(pp + 4 + tid), Os);
+            }
+            P.o[h * HD + tid] = Os / Ls;
+        }
+        if (tid == 0) P.head_cnt[h] = 0u;
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool grid_barrier(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                             uint32_t& nbar, int tid, int cta) {
+    consumer_sync(NCT);
+    if (tid == 0) {
+        // red.release is cumulative: the block's writes ordered before it by the
+        // consumer barrier above become visible to every acquirer of the count.
+        red_release_gpu_add(&P.ctl->bar, 1u);
+        const uint32_t target = (nbar + 1u) * uint32_t(P.G);
+        const uint64_t t0 = globaltimer();
+        int spins = 0;
+        while (int32_t(ld_acquire_gpu(&P.ctl->bar) - target) < 0) {
+            if ((++spins & 15) == 0) {
+                if (ld_volatile_i32(&P.ctl->err) != 0) { S.flags[0] = 1; break; }
+                if (globaltimer() - t0 > Lc.timeout_ns) {
+                    set_error(P, KERR_TIMEOUT_GRID, cta);
+                    S.flags[0] = 1;
+                    break;
+                }
+            }
+        }
+    }
+    ++nbar;
+    consumer_sync(NCT);
+    return ld_volatile_i32(&S.flags[0]) == 0;
+}
+
+template <int HD, int KVF>
+__device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta, int warp, int lane) {
+    const int tid = warp * 32 + lane;
+    uint32_t gc = 0, nbar = 0;
+    const int pos0 = Lc.pos0 >= 0 ? Lc.pos0 : ld_volatile_i32(&P.ctl->pos);
+    bool first_phase = true;
+    int tok = 0;
+    for (int t = 0; t < Lc.n_steps; ++t) {
+        const int pos = pos0 + t;
+        for (int phi = Lc.phase_begin; phi < Lc.phase_end; ++phi) {
+            int layer, sub;
+            phase_of(phi, P.L, layer, sub);
+            if (sub == 5 && t < Lc.lm_from_step) continue;
+            if (Lc.use_grid_barrier && !first_phase) {
+                if (!grid_barrier(P, Lc, S, nbar, tid, cta)) return;
+            }
+            first_phase = false;
+            if (tid == 0) stamp(P, Lc, t, phi, 0, cta);
+            const float* gains = P.norms + size_t(layer) * 2 * P.d;
+            if (sub == 0) {
+                const Cursor c = cursor(P, S, PH_QKV);
+                if (layer == 0) {
+                    if (tid == 0) {
+                        int tk = (t == 0 && Lc.first_tok >= 0) ? Lc.first_tok
+                                 : (Lc.forced ? Lc.forced[t] : __ldcg(&P.ctl->tok));
+                        if (tk < 0 || tk >= P.V) { set_error(P, KERR_BAD_TOKEN, tk); tk = 0; }
+                        S.flags[2] = tk;
+                    }
+                    consumer_sync(NCT);
+                    tok = S.flags[2];
+                    const uint16_t* row = P.emb + size_t(tok) * P.d;
+                    // the residual stream starts as the embedding row (each CTA writes a slice)
+                    const int s0 = int((int64_t(cta) * P.d) / P.G), s1 = int((int64_t(cta + 1) * P.d) / P.G);
+                    for (int k = s0 + tid; k < s1; k += NCT) P.x[k] = __half2float(__ushort_as_half(row[k]));
+                    act_rmsnorm(P, S, nullptr, row, gains, tid);
+                } else {
+                    act_rmsnorm(P, S, P.x, nullptr, gains, tid);
+                }
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+                epi_qkv(P, S, c, layer, pos, tid);
+            } else if (sub == 1) {
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!attention<HD, KVF>(P, Lc, S, layer, pos, cta, gc, warp, lane, tid)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+            } else if (sub == 2) {
+                const Cursor c = cursor(P, S, PH_O);
+                act_copy(P, S, P.o, P.H * P.hd, tid);
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+                epi_residual(P, S, c, tid);
+            } else if (sub == 3) {
+                const Cursor c = cursor(P, S, PH_GU);
+                act_rmsnorm(P, S, P.x, nullptr, gains + P.d, tid);
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+                epi_swiglu(P, S, c, tid);
+            } else if (sub == 4) {
+                const Cursor c = cursor(P, S, PH_D);
+                act_copy(P, S, P.a, P.F, tid);
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+                epi_residual(P, S, c, tid);
+            } else {
+                const Cursor c = cursor(P, S, PH_LM);
+                act_rmsnorm(P, S, P.x, nullptr, P.norms + size_t(P.L) * 2 * P.d, tid);
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+                epi_lm(P, Lc, S, c, cta, tid, t, pos);
+            }
+            if (tid == 0) stamp(P, Lc, t, phi, 3, cta);
+        }
+    }
+}
+
+}  // namespace
+
+template <int HD, int KVF>
+__global__ void __launch_bounds__(KIE_THREADS, 1) kie_decode_kernel(const KieParams P, const KieLaunch Lc) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    // Refuse to run if the launch gave less shared memory than the layout needs
+    // (uniform across the block, before any shared-memory access).
+    if (kie_smem_layout(P.part_floats, P.act_floats, P.nslot).total > dynamic_smem_size() ||
+        P.nslot < 1 || P.nslot > KIE_MAX_SLOTS || P.G > KIE_MAX_GRID) {
+        if (threadIdx.x == 0) set_error(P, KERR_SMEM, cta);
+        return;
+    }
+    const Smem S = carve(smem_raw, P);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P.nslot; ++i) {
+            mbar_init(&S.full[2 * i], 1);
+            mbar_init(&S.full[2 * i + 1], 1);
+            mbar_init(&S.empty[i], 1);
+        }
+        S.flags[0] = 0;
+        S.flags[1] = 0;
+        for (int t = 0; t < PH_NTYPES; ++t) {
+            S.plan[t * 4 + 0] = P.ph[t].unit_begin[cta];
+            S.plan[t * 4 + 1] = P.ph[t].unit_begin[cta + 1] - P.ph[t].unit_begin[cta];
+            S.plan[t * 4 + 2] = int32_t(P.ph[t].nslots[cta]);
+            S.plan[t * 4 + 3] = int32_t(P.ph[t].bytes[cta]);
+        }
+        S.cbase[0] = P.cta_base[cta];
+        S.cbase[1] = P.cta_layer[cta];
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (warp == NW) {
+        if (lane == 0) producer(P, Lc, S, cta);
+    } else {
+        consumer<HD, KVF>(P, Lc, S, cta, warp, lane);
+    }
+}
+
+// Set the control block from launch parameters (no host staging buffer involved).
+__global__ void kie_ctl_kernel(KieControl* c, int tok, int pos, int clear) {
+    c->tok = tok;
+    c->pos = pos;
+    if (clear) {
+        c->bar = 0u;
+        c->err = 0;
+        c->err_info = 0;
+        c->amax_cnt = 0u;
+    }
+}
+
+// host-visible launch helpers -----------------------------------------------------------------
+#include <cuda_runtime.h>
+
+extern "C" cudaError_t kie_launch_ctl(KieControl* c, int tok, int pos, int clear, cudaStream_t st) {
+    kie_ctl_kernel<<<1, 1, 0, st>>>(c, tok, pos, clear);
+    return cudaGetLastError();
+}
+
+typedef void (*kie_kernel_t)(const KieParams, const KieLaunch);
+
+extern "C" void* kie_decode_kernel_ptr(int hd, int kv) {
+    if (hd == 128) {
+        if (kv == KV_F16) return (void*)&kie_decode_kernel<128, KV_F16>;
+        if (kv == KV_E5M2) return (void*)&kie_decode_kernel<128, KV_E5M2>;
+        return (void*)&kie_decode_kernel<128, KV_U8>;
+    }
+    if (hd == 64) {
+        if (kv == KV_F16) return (void*)&kie_decode_kernel<64, KV_F16>;
+        if (kv == KV_E5M2) return (void*)&kie_decode_kernel<64, KV_E5M2>;
+        return (void*)&kie_decode_kernel<64, KV_U8>;
+    }
+    return nullptr;
+}

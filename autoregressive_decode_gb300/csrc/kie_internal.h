@@ -1,0 +1,157 @@
+// Internal structures shared by the host engine and the device program.
+//
+// The decode step is cut into phases; per layer:
+//   QKV  RMSNorm + fused q/k/v GEMV + RoPE + K/V append      (weights streamed)
+//   ATT  split-KV attention partials + per-head combine        (KV streamed)
+//   O    O-projection GEMV + residual                           (weights streamed)
+//   GU   RMSNorm + gate/up GEMV + SwiGLU                        (weights streamed)
+//   D    down GEMV + residual                                   (weights streamed)
+// and once per token LM (final RMSNorm + LM-head GEMV + argmax).
+//
+// Every GEMV phase partitions its output "units" (a row, or a pair of rows that
+// one epilogue needs together: the RoPE pair (i, i+h/2) of q or k, or the
+// matching gate/up rows) over the G CTAs of the grid.  Each CTA's weights for
+// all phases of all layers are laid out as ONE contiguous byte stream in HBM,
+// cut into slots of at most R rows x KC input columns; a producer warp copies
+// the stream slot by slot into a shared-memory ring with bulk async copies and
+// never waits for activations, so HBM streaming continues across grid barriers
+// and non-GEMM work.
+#pragma once
+#include <stdint.h>
+
+#define KIE_NW 7                 // consumer warps per CTA (with the producer: 2 warps per SM sub-partition, no register cap below 255)
+#define KIE_THREADS ((KIE_NW + 1) * 32)
+#define KIE_R 4                  // rows per slot
+#define KIE_KC_F16 2048          // input columns per slot, fp16 weights
+#define KIE_KC_I4 4096           // input columns per slot, INT4 weights
+#define KIE_SLOT_BYTES 16384     // slot capacity
+#define KIE_MAX_SLOTS 16
+#define KIE_SEG 128              // adaptive-range uint8 KV segment (tokens)
+#define KIE_MAX_HEAD_DIM 128
+#define KIE_MAX_GRID 256         // CTAs of the persistent grid (one per SM)
+#define KIE_PROF_EVENTS 6        // trace stamps per (step, phase, CTA)
+#define KIE_PROF_SLOTS 32768     // ring-slot trace entries (CTA 0)
+
+#if defined(__CUDACC__)
+#define KIE_HD __host__ __device__
+#else
+#define KIE_HD
+#endif
+
+// Dynamic shared-memory layout of the decode kernel; host (allocation size) and
+// device (carving) both use this one function.  Offsets are relative to the
+// dynamic shared-memory base; the ring starts on a 128-byte boundary.
+struct KieSmemLayout {
+    uint32_t full, empty, cbase, flags, plan, clist, red, part, act, ring, total;
+};
+KIE_HD inline uint32_t kie_align(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
+KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot) {
+    KieSmemLayout l;
+    uint32_t o = 0;
+    l.full = o;  o += KIE_MAX_SLOTS * 2 * 8;   // two per slot: even / odd generations
+    l.empty = o; o += KIE_MAX_SLOTS * 8;
+    l.cbase = o; o += 16;
+    l.flags = o; o += 64;
+    l.plan = o;  o += 5 * 4 * 4;
+    l.clist = o; o += KIE_MAX_GRID * 4;
+    l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64) * 4;
+    l.part = o;  o += uint32_t(part_floats) * 4;
+    l.act = kie_align(o, 16); o = l.act + uint32_t(act_floats) * 4;
+    l.ring = kie_align(o, 128);
+    l.total = l.ring + uint32_t(nslot) * KIE_SLOT_BYTES;
+    return l;
+}
+
+enum KiePhaseType { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3, PH_LM = 4, PH_NTYPES = 5 };
+enum KieWFmt { WF_F16 = 0, WF_I4 = 1 };
+enum KieKv { KV_F16 = 0, KV_E5M2 = 1, KV_U8 = 2 };
+
+enum KieErr {
+    KERR_NONE = 0,
+    KERR_TIMEOUT_GRID = 1,    // grid barrier wait expired
+    KERR_TIMEOUT_FULL = 2,    // consumer wait for a weight slot expired
+    KERR_TIMEOUT_EMPTY = 3,   // producer wait for a free slot expired
+    KERR_BAD_TOKEN = 4,       // input token id out of range
+    KERR_SMEM = 5,            // launched with less dynamic shared memory than the layout needs
+};
+
+// Partition of one GEMV phase type over the grid (identical for every layer).
+struct KiePhasePlan {
+    int32_t K;               // input columns
+    int32_t KC;              // columns per slot
+    int32_t nK;              // chunks per row = ceil(K / KC)
+    int32_t rows_per_unit;   // 1 or 2
+    int32_t wfmt;            // KieWFmt
+    int32_t n_units;         // units over the grid
+    const int32_t* unit_begin;   // [G+1] device: CTA i owns units [unit_begin[i], unit_begin[i+1])
+    const uint32_t* bytes;       // [G]   device: stream bytes of this phase for CTA i
+    const uint32_t* nslots;      // [G]   device: slots of this phase for CTA i
+};
+
+struct KieControl {
+    int32_t tok;             // input token of the next step
+    int32_t pos;             // its position
+    uint32_t bar;            // grid barrier counter (zeroed before each persistent launch)
+    int32_t err;             // KieErr of the first failure
+    int32_t err_info;        // CTA or phase of the first failure
+    uint32_t amax_cnt;       // arrivals at the LM argmax reduction
+    int32_t pad[2];
+};
+
+struct KieParams {
+    // model
+    int32_t L, d, H, hd, F, V, max_ctx, G;
+    float eps, attn_scale;
+    int32_t kv;              // KieKv
+    int32_t nseg;            // segments per (layer, kv, head) for uint8 caches
+    // weights
+    const uint8_t* wstream;
+    const uint64_t* cta_base;    // [G] byte offset of CTA i's stream
+    const uint64_t* cta_layer;   // [G] bytes of one layer of CTA i's stream
+    KiePhasePlan ph[PH_NTYPES];
+    const uint16_t* emb;         // [V][d] fp16
+    const float* norms;          // [L][2][d] then final [d], fp32
+    const float* inv_freq;       // [hd/2] fp32
+    // KV cache: [L][H][max_ctx][hd] of 2 (fp16) or 1 (E5M2, u8 codes) bytes
+    uint8_t* kc;
+    uint8_t* vc;
+    uint16_t* tail;              // u8: [L][2][H][SEG][hd] fp16, the open segment
+    float* seg_scale;            // u8: [L][2][H][nseg]
+    int32_t* seg_zp;             // u8: [L][2][H][nseg]
+    // activations and scratch
+    float* x;                    // [d] residual stream
+    float* q;                    // [H*hd] rotated query
+    float* a;                    // [F] SwiGLU output
+    float* o;                    // [H*hd] attention output
+    float* att_part;             // [G][hd+4] per-CTA attention partial: m, l, -, -, o[hd]
+    uint32_t* head_cnt;          // [H] arrivals of a head's CTAs at the combine
+    float* amax_val;             // [G]
+    int32_t* amax_idx;           // [G]
+    KieControl* ctl;
+    // shared-memory layout
+    int32_t nslot;               // ring slots
+    int32_t act_floats;          // activation buffer (floats)
+    int32_t part_floats;         // GEMV partial buffer (floats)
+};
+
+struct KieLaunch {
+    int32_t n_steps;             // tokens processed by this launch
+    int32_t phase_begin;         // phases [phase_begin, phase_end) of each step (5L+1 per step)
+    int32_t phase_end;
+    int32_t first_tok;           // >= 0: input token of step 0; < 0: read ctl->tok
+    int32_t pos0;                // >= 0: position of step 0; < 0: read ctl->pos
+    const int32_t* forced;       // device [n_steps] input tokens (prefill), or null
+    int32_t lm_from_step;        // LM head only for steps >= this
+    int32_t* out_tokens;         // device [n_steps] or null
+    float* out_logits;           // device [n_steps - lm_from_step][V] or null
+    uint64_t timeout_ns;
+    int32_t use_grid_barrier;    // 1 in the persistent (cooperative) launch
+    // Optional trace: %globaltimer stamps [n_steps][5L+1][KIE_PROF_EVENTS][G]:
+    // 0 phase start (after the grid barrier), 1 activation staged, 2 GEMV /
+    // attention done, 3 epilogue done, 4 producer issued the phase's first slot,
+    // 5 producer issued its last slot.  Null: no tracing.
+    uint64_t* prof;
+    // Optional ring trace of CTA 0: [KIE_PROF_SLOTS][4] stamps per slot index of
+    // the launch: 0 copy issued, 1 data seen by the consumer warp, 2 released.
+    uint64_t* prof_slots;
+};

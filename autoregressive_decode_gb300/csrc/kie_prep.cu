@@ -1,0 +1,207 @@
+// One-off preparation kernels: weight repacking into per-CTA streams, INT4
+// quantisation, adaptive-range uint8 segment quantisation, fp16 -> E5M2, and
+// writing a supplied context into the KV cache.  None of these is on the
+// per-token path.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kie_device.cuh"
+#include "kie_internal.h"
+
+using namespace kie;
+
+// ---- repack: byte copies described by (dst offset, src offset, length) ----------------------
+struct CopyDesc {
+    uint64_t dst;
+    uint64_t src;
+    uint32_t len;
+    uint32_t pad;
+};
+
+__global__ void kie_copy_desc_kernel(uint8_t* dst_base, const uint8_t* src_base, const CopyDesc* desc, int n) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int i = warp; i < n; i += nwarps) {
+        const CopyDesc d = desc[i];
+        uint8_t* dp = dst_base + d.dst;
+        const uint8_t* sp = src_base + d.src;
+        if (((d.dst | d.src | d.len) & 15u) == 0) {
+            const uint32_t nv = d.len >> 4;
+            for (uint32_t k = lane; k < nv; k += 32)
+                reinterpret_cast<uint4*>(dp)[k] = reinterpret_cast<const uint4*>(sp)[k];
+        } else {
+            for (uint32_t k = lane; k < d.len; k += 32) dp[k] = sp[k];
+        }
+    }
+}
+
+// ---- INT4 g128 symmetric quantisation -------------------------------------------------------
+// One warp per (row, group of 128 columns).  s = fp16_rne(absmax / 7) with the
+// division in fp32; q = clamp(rint_half_even(w / fp32(s)), -8, 7); q = 0 when s == 0.
+// packed: element 2b in the low nibble of byte b (two's complement); or, when
+// codes_i8 != null, one int8 per element.
+__global__ void kie_quant_int4_kernel(const uint16_t* w, int rows, int cols, uint8_t* packed, int8_t* codes_i8,
+                                      uint16_t* scales) {
+    const int ngrp = cols / 128;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= rows * ngrp) return;
+    const int r = warp / ngrp, g = warp % ngrp;
+    const uint16_t* src = w + size_t(r) * cols + size_t(g) * 128;
+    float v[4];
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = __half2float(__ushort_as_half(src[lane * 4 + i]));
+        am = fmaxf(am, fabsf(v[i]));
+    }
+    am = warp_max(am);
+    const __half s16 = __float2half_rn(am / 7.0f);
+    const float s = __half2float(s16);
+    int q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = (s > 0.f) ? min(max(__float2int_rn(v[i] / s), -8), 7) : 0;
+    if (codes_i8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) codes_i8[size_t(r) * cols + size_t(g) * 128 + lane * 4 + i] = int8_t(q[i]);
+    }
+    if (packed) {
+        uint8_t* dst = packed + size_t(r) * (cols / 2) + size_t(g) * 64 + lane * 2;
+        dst[0] = uint8_t((q[0] & 0xF) | ((q[1] & 0xF) << 4));
+        dst[1] = uint8_t((q[2] & 0xF) | ((q[3] & 0xF) << 4));
+    }
+    if (lane == 0) scales[size_t(r) * ngrp + g] = __half_as_ushort(s16);
+}
+
+// ---- adaptive-range uint8 quantisation ------------------------------------------------------
+// One CTA per segment.  A segment is `rows` rows of `row_elems` fp16 values;
+// element (r, k) of segment s is at src[s*src_seg + r*src_row + k] and its code
+// goes to codes[s*dst_seg + r*dst_row + k].  scale = (max-min)/255 and
+// zp = rint_half_even(-min/scale) in fp32 (IEEE division); constant segment:
+// scale 1, zp = rint(-min); code = clamp(rint(x/scale) + zp, 0, 255).
+__global__ void kie_quant_u8_kernel(const uint16_t* src, int64_t src_seg, int64_t src_row, int rows, int row_elems,
+                                    uint8_t* codes, int64_t dst_seg, int64_t dst_row, float* scale_out,
+                                    int32_t* zp_out, int64_t meta_stride) {
+    const int s = blockIdx.x;
+    const int n = rows * row_elems;
+    const uint16_t* sp = src + s * src_seg;
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int r = i / row_elems, k = i % row_elems;
+        const float v = __half2float(__ushort_as_half(sp[r * src_row + k]));
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+    }
+    __shared__ float smn[32], smx[32];
+    mn = -warp_max(-mn);
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) { smn[threadIdx.x >> 5] = mn; smx[threadIdx.x >> 5] = mx; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < int(blockDim.x >> 5); ++w) { mn = fminf(mn, smn[w]); mx = fmaxf(mx, smx[w]); }
+        smn[0] = mn;
+        smx[0] = mx;
+    }
+    __syncthreads();
+    mn = smn[0];
+    mx = smx[0];
+    float sc;
+    int zp;
+    if (mx == mn) { sc = 1.f; zp = __float2int_rn(-mn); }
+    else { sc = (mx - mn) / 255.f; zp = __float2int_rn(-mn / sc); }
+    uint8_t* dp = codes + s * dst_seg;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int r = i / row_elems, k = i % row_elems;
+        const float v = __half2float(__ushort_as_half(sp[r * src_row + k]));
+        dp[r * dst_row + k] = uint8_t(min(max(__float2int_rn(v / sc) + zp, 0), 255));
+    }
+    if (threadIdx.x == 0) {
+        scale_out[s * meta_stride] = sc;
+        zp_out[s * meta_stride] = zp;
+    }
+}
+
+// ---- fp16 -> E5M2 ----------------------------------------------------------------------------
+__global__ void kie_e5m2_kernel(const uint16_t* x, size_t n, uint8_t* out) {
+    for (size_t i = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2; i < n;
+         i += size_t(gridDim.x) * blockDim.x * 2) {
+        const __half a = __ushort_as_half(x[i]);
+        const __half b = (i + 1 < n) ? __ushort_as_half(x[i + 1]) : __ushort_as_half(0);
+        const uint16_t r = f16x2_to_e5m2x2(a, b);
+        out[i] = uint8_t(r & 0xFF);
+        if (i + 1 < n) out[i + 1] = uint8_t(r >> 8);
+    }
+}
+
+// ---- context loading: [n][H][hd] fp16 -> cache layout [H][max_ctx][hd] ----------------------
+// fmt 0: fp16 copy; 1: E5M2; 2: fp16 into the open-segment tail (positions >= first_tail).
+__global__ void kie_set_kv_kernel(const uint16_t* src, int n, int H, int hd, int max_ctx, int fmt, uint8_t* dst,
+                                  uint16_t* tail, int first_tail) {
+    const size_t total = size_t(n) * H * hd;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+        const int k = int(i % hd);
+        const int h = int((i / hd) % H);
+        const int p = int(i / (size_t(hd) * H));
+        const uint16_t v = src[i];
+        const size_t di = (size_t(h) * max_ctx + p) * hd + k;
+        if (fmt == 0) {
+            reinterpret_cast<uint16_t*>(dst)[di] = v;
+        } else if (fmt == 1) {
+            const __half hv = __ushort_as_half(v);
+            dst[di] = uint8_t(f16x2_to_e5m2x2(hv, hv) & 0xFF);
+        } else if (p >= first_tail) {
+            tail[(size_t(h) * KIE_SEG + (p - first_tail)) * hd + k] = v;
+        }
+    }
+}
+
+// ---- launch wrappers (host) --------------------------------------------------------------------
+#include <cuda_runtime.h>
+
+extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, const void* desc, int n,
+                                            cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int threads = 256;
+    int blocks = (n + 7) / 8;
+    if (blocks > 4096) blocks = 4096;
+    kie_copy_desc_kernel<<<blocks, threads, 0, st>>>(dst, src, reinterpret_cast<const CopyDesc*>(desc), n);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
+                                             int8_t* codes_i8, uint16_t* scales, cudaStream_t st) {
+    const long warps = long(rows) * (cols / 128);
+    const int threads = 256;
+    const long blocks = (warps * 32 + threads - 1) / threads;
+    kie_quant_int4_kernel<<<unsigned(blocks), threads, 0, st>>>(w, rows, cols, packed, codes_i8, scales);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_quant_u8(const uint16_t* src, int n_seg, int64_t src_seg, int64_t src_row,
+                                           int rows, int row_elems, uint8_t* codes, int64_t dst_seg,
+                                           int64_t dst_row, float* scale, int32_t* zp, int64_t meta_stride,
+                                           cudaStream_t st) {
+    if (n_seg <= 0) return cudaSuccess;
+    kie_quant_u8_kernel<<<n_seg, 256, 0, st>>>(src, src_seg, src_row, rows, row_elems, codes, dst_seg, dst_row,
+                                               scale, zp, meta_stride);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_e5m2(const uint16_t* x, size_t n, uint8_t* out, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    size_t blocks = (n / 2 + 255) / 256 + 1;
+    if (blocks > 8192) blocks = 8192;
+    kie_e5m2_kernel<<<unsigned(blocks), 256, 0, st>>>(x, n, out);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_set_kv(const uint16_t* src, int n, int H, int hd, int max_ctx, int fmt,
+                                         uint8_t* dst, uint16_t* tail, int first_tail, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    size_t total = size_t(n) * H * hd;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 16384) blocks = 16384;
+    kie_set_kv_kernel<<<unsigned(blocks), 256, 0, st>>>(src, n, H, hd, max_ctx, fmt, dst, tail, first_tail);
+    return cudaGetLastError();
+}

@@ -1,0 +1,308 @@
+"""Batch-1 decode benchmark.
+
+Workload (default): the ~1.8B dense decoder (25 layers, d 2048, 16 heads x 128,
+SwiGLU FFN 8192, vocab 32000, fp16 weights ~N(0, 0.02), RMSNorm gains 1), a
+2048-token uniform-random prompt prefilled on the GPU (untimed), then steps of
+256 greedy decode tokens at positions 2048..2303 (fp16 KV cache).  One bench
+step = one kie_generate_greedy of 256 tokens from position 2048.
+
+value   decode tokens/s with every input resident in HBM, timed with CUDA events
+        on the engine's stream (one persistent cooperative launch per step).
+e2e     the same metric through the host API (kie_generate_greedy with host
+        output buffers), wall clock, including the token copy back.
+roofline  achieved HBM GB/s of the decode kernel = algorithmic bytes per launch
+        (every weight once per token + K/V of all attended positions) / launch
+        time, against the measured copy bandwidth.
+cpu_baseline  the CPU oracle (numpy fp32) timed on this host's cores on a short
+        bounded sample of the same workload.
+
+Multi-GPU (torchrun): independent replicas, one engine per rank, no
+collective on the data path; value = tokens of all ranks / max rank time.
+
+`--impl reference` times the CPU oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "batch-1 decode tokens/s per request; achieved HBM GB/s (MBU) vs GB300 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="1p8b", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--mode", default="persistent", choices=["persistent", "graph"])
+    ap.add_argument("--decode-tokens", type=int, default=None,
+                    help="decode tokens per step (default: the workload's decode steps)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(w: S.Workload) -> str:
+    ctx = (f"{w.prompt_len}-token prompt" if w.kv_source == "prefill" else f"{w.context_len} synthetic KV positions")
+    ffn = "INT4 g128 FFN" if w.ffn_wdtype == "int4_g128" else "fp16 FFN"
+    return (f"{w.name}: {w.n_layers} layers, d {w.d_model}, {w.n_heads}x{w.head_dim} heads, FFN {w.ffn_dim}, "
+            f"vocab {w.vocab}, {ctx}, {w.decode_steps} greedy decode steps, {w.kv_dtype} KV, {ffn}")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def bytes_per_launch(w: S.Workload, p0: int, n: int) -> float:
+    import oracle as O  # the byte model lives with the bound it restates
+    return float(sum(O.decode_bytes_per_token(w, p + 1)["total"] for p in range(p0, p0 + n)))
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(w: S.Workload, weights: dict, p0: int, n_steps: int = 6):
+    """Time the oracle's decode on this host: a synthetic fp16 context of p0
+    positions (prefill cost excluded, as for the GPU metric), then n_steps
+    decode steps."""
+    import oracle as O
+    threads = len(os.sched_getaffinity(0))
+    dec = O.OracleDecoder(w, weights, max_ctx=p0 + n_steps)
+    for layer in range(w.n_layers):
+        k, v = S.gen_kv(w.with_(context_len=p0), layer)
+        dec.set_kv(layer, k, v)
+    dec.pos = p0
+    tok = S.gen_first_token(w)
+    dec.decode(tok)                      # warm-up step (page-in, BLAS threads)
+    t0 = time.perf_counter()
+    for _ in range(n_steps - 1):
+        tok = O.argmax_lowest(dec.decode(tok))
+    dt = time.perf_counter() - t0
+    return {"value": (n_steps - 1) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_steps - 1} timed decode steps (after 1 warm-up) at positions {p0 + 1}..{p0 + n_steps - 1} "
+                      f"of {w.name} over a synthetic {p0}-position KV context; numpy fp32 with OpenBLAS"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w: S.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    n_dec = args.decode_tokens or w.decode_steps
+    weights = S.gen_weights(w)
+    steps = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, weights, w.start_pos, n_steps=3)
+        if i >= args.warmup:
+            steps.append(cb)
+    val = statistics.median(s["value"] for s in steps)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": n_dec / val * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": workload_desc(w), "decode_tokens_per_step": n_dec},
+            "cpu_baseline": {**steps[-1], "value": val},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    import torch
+
+    from autoregressive_decode_gb300 import kie
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    n_dec = args.decode_tokens or w.decode_steps
+    p0 = w.start_pos
+    weights = S.gen_weights(w)
+    cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, p0 + n_dec,
+                          w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, args.mode, local)
+    stream = torch.cuda.Stream(device=local)
+    eng = kie.Engine(cfg, stream=stream)
+    eng.load_weights(weights)
+    # context: GPU prefill of the prompt (untimed), or synthetic KV
+    if w.kv_source == "prefill":
+        lg = eng.prefill(S.gen_prompt(w))
+        first = int(np.argmax(lg))
+    else:
+        for layer in range(w.n_layers):
+            k, v = S.gen_kv(w, layer)
+            eng.set_kv(layer, k, v)
+        eng.set_pos(p0)
+        first = S.gen_first_token(w)
+    d_tok = torch.empty(n_dec, dtype=torch.int32, device=f"cuda:{local}")
+
+    def step():
+        eng.set_pos(p0)
+        eng.generate_greedy_device(first, n_dec, d_tok)
+
+    for _ in range(args.warmup):
+        step()
+    eng.sync()
+    # device-timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ev0.record(stream)
+        for a, b in per:
+            eng.set_pos(p0)
+            a.record(stream)
+            eng.generate_greedy_device(first, n_dec, d_tok)
+            b.record(stream)
+        ev1.record(stream)
+        eng.sync()
+        torch.cuda.synchronize()
+    total_ms = ev0.elapsed_time(ev1)
+    launch_ms = [a.elapsed_time(b) for a, b in per]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    tokens_gpu = list(d_tok.cpu().numpy())
+
+    # end to end through the host API
+    e2e_ms = []
+    for i in range(max(2, args.steps // 2) + 1):
+        eng.set_pos(p0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        toks, _ = eng.generate_greedy(first, n_dec)
+        dt = (time.perf_counter() - t0) * 1e3
+        if i > 0:
+            e2e_ms.append(dt)
+    assert list(toks) == tokens_gpu, "host-API tokens differ from the device-timed run"
+    if ws > 1:
+        t = torch.tensor([max(e2e_ms)], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_max = float(t.item())
+    else:
+        e2e_max = statistics.median(e2e_ms)
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    ms_per_step = total_ms / args.steps
+    value = ws * n_dec / (ms_per_step / 1e3)
+    peak, peak_kind = peaks()
+    bpl = bytes_per_launch(w, p0, n_dec)
+    launch_avg = statistics.mean(launch_ms)
+    achieved = bpl / (launch_avg / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "storage": "fp16 weights, fp16 KV" if w.kv_dtype == "fp16" else w.kv_dtype,
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w), "decode_tokens_per_step": n_dec,
+                   "positions": f"{p0}..{p0 + n_dec - 1}", "mode": args.mode,
+                   "l2": "inputs larger than L2 (all weights streamed from HBM every token)",
+                   "replicas": ws},
+        # per step: the control-block kernel of set_pos, then one cooperative decode launch
+        # (persistent) or a control kernel plus (5L+1) phase kernels per token (graph)
+        "gpu_launches": args.steps * (2 if args.mode == "persistent" else 2 + (5 * w.n_layers + 1) * n_dec),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": peak_kind, "kernel": "kie_decode_kernel",
+                     "algorithmic_bytes_per_launch": bpl, "launch_ms": launch_avg},
+        "e2e": {"value": ws * n_dec / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4 * n_dec},
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and ws >= 1:
+        try:
+            line["cpu_baseline"] = cpu_baseline(w, weights, p0)
+        except Exception as ex:  # report, never hide
+            line["cpu_baseline"] = {"error": repr(ex)}
+    print(json.dumps(line), flush=True)
+    eng.close()
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

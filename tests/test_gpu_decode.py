@@ -1,0 +1,183 @@
+"""GPU decode parity against the CPU oracle on small models that still span
+several slots per CTA and ragged tails (vocab and FFN sizes that do not divide
+evenly over the grid), for every KV format, INT4 FFN weights, and both launch
+modes (persistent cooperative kernel, CUDA graph of per-phase launches)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+from _common import check_free_running, engine_for, teacher_forced, tol_for
+
+pytestmark = pytest.mark.gpu
+
+TINY = S.WORKLOADS["tiny"]
+# hd 128, d 512, ragged vocab (not a multiple of 4 rows x 152 CTAs), FFN 1536
+MEDIUM = S.Workload("medium", 5, 2, 512, 4, 128, 1536, 10007, prompt_len=100, decode_steps=24)
+
+
+def _prefill_both(w, weights, mode="persistent", max_ctx=None):
+    e = engine_for(w, weights, mode, max_ctx)
+    o = O.OracleDecoder(w, weights, max_ctx=max_ctx or w.max_ctx)
+    prompt = S.gen_prompt(w)
+    lg = e.prefill(prompt)
+    lo = o.prefill(prompt)
+    return e, o, lg, lo
+
+
+@pytest.mark.parametrize("w", [TINY, MEDIUM], ids=lambda w: w.name)
+@pytest.mark.parametrize("kv", ["fp16", "fp8_e5m2"])
+def test_prefill_then_teacher_forced_decode(w, kv):
+    w = w.with_(kv_dtype=kv)
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    tol = tol_for(w)
+    assert np.abs(lg - lo).max() <= tol
+    assert e.pos == o.pos == w.prompt_len
+    worst, _ = teacher_forced(e, o, O.argmax_lowest(lo), w.decode_steps, tol)
+    print(f"{w.name}/{kv}: max |dlogit| {worst:.3e}")
+
+
+def test_kv_cache_contents_after_prefill():
+    """Stored K/V equal the oracle's fp16 values up to fp16 rounding flips.
+    Layer 0's K/V depend on the current token only, so flips there come from
+    summation order alone (rare, one ulp); deeper layers also inherit earlier
+    positions' flips through attention, so they are held to a relative bound."""
+    w = TINY
+    weights = S.gen_weights(w)
+    e, o, _, _ = _prefill_both(w, weights)
+    for layer in range(w.n_layers):
+        for which in (0, 1):
+            data, _, _, _ = e.read_kv(layer, which, 0, w.prompt_len)
+            gpu = data.view(np.float16).astype(np.float32)
+            ref = (o.cache.k if which == 0 else o.cache.v)[layer][:, :w.prompt_len]
+            diff = gpu != ref
+            if layer == 0:
+                assert diff.mean() < 0.01
+                # one fp16 ulp, or fp32 summation noise (~1e-6 absolute) near zero
+                assert np.all(np.abs(gpu - ref)[diff] <= 2.0 ** -10 * np.abs(ref)[diff] + 1e-6)
+            else:
+                assert np.abs(gpu - ref).max() <= 1e-3 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("w", [TINY, MEDIUM], ids=lambda w: w.name)
+def test_free_running_greedy(w):
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    first = O.argmax_lowest(lo)
+    toks, logs = e.generate_greedy(first, w.decode_steps, want_logits=True)
+    check_free_running(o, first, toks, logs, tol_for(w))
+
+
+@pytest.mark.parametrize("w", [TINY, MEDIUM], ids=lambda w: w.name)
+def test_graph_mode_bit_identical_to_persistent(w):
+    weights = S.gen_weights(w)
+    prompt = S.gen_prompt(w)
+    res = {}
+    for mode in ("persistent", "graph"):
+        e = engine_for(w, weights, mode)
+        lg = e.prefill(prompt)
+        toks, logs = e.generate_greedy(int(np.argmax(lg)), 8, want_logits=True)
+        nxt, lg1 = e.decode_step(int(toks[-1]))
+        res[mode] = (lg, toks, logs, nxt, lg1)
+        e.close()
+    a, b = res["persistent"], res["graph"]
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    np.testing.assert_array_equal(a[2], b[2])
+    assert a[3] == b[3]
+    np.testing.assert_array_equal(a[4], b[4])
+
+
+def test_step_by_step_equals_generate():
+    """n chained decode_step calls == one generate_greedy of n steps (bit-exact)."""
+    w = TINY
+    weights = S.gen_weights(w)
+    prompt = S.gen_prompt(w)
+    e1 = engine_for(w, weights)
+    first = int(np.argmax(e1.prefill(prompt)))
+    toks, logs = e1.generate_greedy(first, 10, want_logits=True)
+    e2 = engine_for(w, weights)
+    e2.prefill(prompt)
+    t = first
+    for i in range(10):
+        t, lg = e2.decode_step(t)
+        assert t == toks[i]
+        np.testing.assert_array_equal(lg, logs[i])
+
+
+@pytest.mark.parametrize("ctx", [300, 383])
+def test_u8_synthetic_context_crossing_segment_completion(ctx):
+    """Synthetic N(0,1) K/V with 0.1% +-20 outliers; decoding fills the open
+    segment and completes it (position 383) inside the run, then starts the
+    next one."""
+    w = TINY.with_(kv_dtype="u8", kv_source="synthetic", prompt_len=0, context_len=ctx, decode_steps=100)
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights)
+    o = O.OracleDecoder(w, weights)
+    for layer in range(w.n_layers):
+        k, v = S.gen_kv(w, layer)
+        e.set_kv(layer, k, v)
+        o.set_kv(layer, k, v)
+    e.set_pos(ctx)
+    o.pos = ctx
+    # stored codes / scale / zp of the complete segments are bit-exact
+    full = (ctx // 128) * 128
+    data, _, sc, zp = e.read_kv(1, 0, 0, full)
+    np.testing.assert_array_equal(data, o.cache.codes[1][0][:, :full])
+    np.testing.assert_array_equal(sc, o.cache.scale[1][0][:, :full // 128])
+    np.testing.assert_array_equal(zp, o.cache.zp[1][0][:, :full // 128])
+    teacher_forced(e, o, S.gen_first_token(w), w.decode_steps, tol_for(w))
+    # the segment completed during decoding was stored with the same codes
+    seg = 383 // 128
+    data, _, sc, zp = e.read_kv(0, 1, seg * 128, 128)
+    np.testing.assert_array_equal(data, o.cache.codes[0][1][:, seg * 128:(seg + 1) * 128])
+    assert np.array_equal(sc[:, 0], o.cache.scale[0][1][:, seg])
+
+
+def test_int4_ffn_decode():
+    w = TINY.with_(ffn_wdtype="int4_g128")
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    assert np.abs(lg - lo).max() <= tol_for(w)
+    teacher_forced(e, o, O.argmax_lowest(lo), w.decode_steps, tol_for(w))
+
+
+def test_context_edges():
+    """Decode from position 0 (C = 1: attention returns V), fill the cache to
+    max_ctx exactly, and reject one more step without writing."""
+    w = TINY.with_(prompt_len=0, decode_steps=20)
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights, max_ctx=20)
+    o = O.OracleDecoder(w, weights, max_ctx=20)
+    teacher_forced(e, o, 7, 20, tol_for(w))
+    assert e.pos == 20
+    from autoregressive_decode_gb300.kie import KieError
+    with pytest.raises(KieError) as ei:
+        e.decode_step(3)
+    assert ei.value.status == -5
+    assert e.pos == 20
+
+
+def test_host_errors_on_gpu():
+    from autoregressive_decode_gb300 import kie
+    w = TINY
+    cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, 64)
+    e = kie.Engine(cfg)
+    with pytest.raises(kie.KieError) as ei:
+        e.decode_step(1)
+    assert ei.value.status == kie.KIE_ERR_NOT_LOADED
+    e.load_weights(S.gen_weights(w))
+    with pytest.raises(kie.KieError) as ei:
+        e.decode_step(w.vocab)
+    assert ei.value.status == kie.KIE_ERR_INVALID_ARG
+    with pytest.raises(kie.KieError) as ei:
+        e.prefill(np.array([1, -1], np.int32))
+    assert ei.value.status == kie.KIE_ERR_INVALID_ARG
+    assert e.pos == 0
+    with pytest.raises(kie.KieError) as ei:
+        e.generate_greedy(1, 65)
+    assert ei.value.status == kie.KIE_ERR_CTX_OVERFLOW
+    e.reset()
+    t, lg = e.decode_step(1)
+    assert 0 <= t < w.vocab and np.isfinite(lg).all()
