@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -20,6 +21,7 @@
 
 extern "C" void* kie_decode_kernel_ptr(int hd, int kv);
 extern "C" cudaError_t kie_launch_ctl(KieControl* c, int tok, int pos, int clear, cudaStream_t st);
+extern "C" cudaError_t kie_launch_err_merge(const KieControl* src, KieControl* dst, cudaStream_t st);
 extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, const void* desc, int n,
                                             cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
@@ -1003,6 +1005,120 @@ kie_status kie_convert_fp8_e5m2(const uint16_t* x_fp16, size_t n, uint8_t* out) 
         st = fail(nullptr, KIE_ERR_CUDA, "E5M2 conversion failed: %s", cudaGetErrorString(cudaGetLastError()));
     cudaFree(buf);
     return st;
+}
+
+// ---- decode step with scratch in a static device array (no allocation) -------------------------
+//
+// For callers that must not allocate device memory while decoding: code running
+// inside another framework's memory pool or allocator-less plugin host, a real-
+// time service that forbids allocation after start-up, or a process whose device
+// memory is already fully committed.  Together with an engine created on a
+// caller-provided workspace, this step performs no cudaMalloc, cudaFree or other
+// allocating call.  The decode kernel's scratch (residual stream, q, attention
+// output and partials, SwiGLU output, argmax partials, head counters, control
+// block) lives in the array below; weights and the KV cache stay in the engine.
+
+#define KIE_STATIC_SCRATCH_BYTES (256u * 1024u)
+
+// Every GPU that loads libkie holds this array until the process exits.  Host
+// code must not use its name as an address: the address comes from
+// cudaGetSymbolAddress, once per device, in static_scratch_ptr below.
+static __device__ __align__(256) uint8_t kie_static_scratch[KIE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+struct StaticScratchLayout {
+    size_t x, q, o, a, att_part, head_cnt, amax_val, amax_idx, ctl, total;
+};
+
+StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
+    StaticScratchLayout l;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
+    l.x = take(size_t(c.d_model) * 4);
+    l.q = take(size_t(c.n_heads) * c.head_dim * 4);
+    l.o = take(size_t(c.n_heads) * c.head_dim * 4);
+    l.a = take(size_t(c.ffn_dim) * 4);
+    l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
+    l.head_cnt = take(size_t(c.n_heads) * 4);
+    l.amax_val = take(size_t(G) * 4);
+    l.amax_idx = take(size_t(G) * 4);
+    l.ctl = take(sizeof(KieControl));
+    l.total = align_up(o, 256);
+    return l;
+}
+
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_dev[64] = {};
+
+// Device address of kie_static_scratch on `device` (looked up once per device,
+// with that device current).
+cudaError_t static_scratch_ptr(int device, void** out) {
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_dev[device]) {
+        int prev = 0;
+        cudaError_t r = cudaGetDevice(&prev);
+        if (r != cudaSuccess) return r;
+        if (prev != device && (r = cudaSetDevice(device)) != cudaSuccess) return r;
+        void* ptr = nullptr;
+        r = cudaGetSymbolAddress(&ptr, kie_static_scratch);
+        if (prev != device) cudaSetDevice(prev);
+        if (r != cudaSuccess) return r;
+        g_static_scratch_dev[device] = ptr;
+    }
+    *out = g_static_scratch_dev[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t token, int32_t* d_next_token,
+                                                     float* d_logits) {
+    kie_status st = ready(e, 1);
+    if (st != KIE_OK) return st;
+    if (!d_next_token) return fail(e, KIE_ERR_INVALID_ARG, "d_next_token is NULL");
+    if ((st = check_tokens(e, &token, 1)) != KIE_OK) return st;
+    if (e->cfg.mode != KIE_MODE_PERSISTENT) return fail(e, KIE_ERR_UNSUPPORTED, "static-scratch step needs the persistent mode");
+    const StaticScratchLayout sl = static_scratch_layout(e->cfg, e->G);
+    if (sl.total > KIE_STATIC_SCRATCH_BYTES)
+        return fail(e, KIE_ERR_UNSUPPORTED, "scratch of %zu bytes exceeds the static maximum of %u bytes", sl.total,
+                    KIE_STATIC_SCRATCH_BYTES);
+    void* base = nullptr;
+    cudaError_t r = static_scratch_ptr(e->cfg.device, &base);
+    if (r != cudaSuccess) return fail(e, KIE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(r));
+    uint8_t* b = static_cast<uint8_t*>(base);
+    // the control block (barrier count, error word, argmax arrivals) and the
+    // head counters must start at zero; everything else is written before read
+    KIE_CUDA(e, cudaMemsetAsync(b + sl.ctl, 0, sizeof(KieControl), e->stream));
+    KIE_CUDA(e, cudaMemsetAsync(b + sl.head_cnt, 0, size_t(e->cfg.n_heads) * 4, e->stream));
+    KieParams P = e->P;
+    P.x = reinterpret_cast<float*>(b + sl.x);
+    P.q = reinterpret_cast<float*>(b + sl.q);
+    P.o = reinterpret_cast<float*>(b + sl.o);
+    P.a = reinterpret_cast<float*>(b + sl.a);
+    P.att_part = reinterpret_cast<float*>(b + sl.att_part);
+    P.head_cnt = reinterpret_cast<uint32_t*>(b + sl.head_cnt);
+    P.amax_val = reinterpret_cast<float*>(b + sl.amax_val);
+    P.amax_idx = reinterpret_cast<int32_t*>(b + sl.amax_idx);
+    P.ctl = reinterpret_cast<KieControl*>(b + sl.ctl);
+    KieLaunch l = base_launch(e);
+    l.n_steps = 1;
+    l.first_tok = token;
+    l.pos0 = e->pos;
+    l.out_tokens = d_next_token;
+    l.out_logits = d_logits;
+    void* args[] = {(void*)&P, (void*)&l};
+    r = cudaLaunchCooperativeKernel(e->kernel, dim3(e->G), dim3(KIE_THREADS), args, e->plan.smem, e->stream);
+    if (r == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        return fail(e, KIE_ERR_LAUNCH, "persistent grid of %d CTAs cannot be co-resident", e->G);
+    }
+    if (r != cudaSuccess) return fail(e, KIE_ERR_CUDA, "cooperative launch: %s", cudaGetErrorString(r));
+    // a device error of this step is reported by the engine's next synchronising call
+    KIE_CUDA(e, kie_launch_err_merge(P.ctl, reinterpret_cast<KieControl*>(e->dev(e->lay.ctl)), e->stream));
+    e->pos += 1;
+    return KIE_OK;
 }
 
 }  // extern "C"

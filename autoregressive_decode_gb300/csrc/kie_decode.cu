@@ -1234,8 +1234,21 @@ __global__ void kie_ctl_kernel(KieControl* c, int tok, int pos, int clear) {
     }
 }
 
+// Copy a device error recorded in one control block into another (first error wins).
+__global__ void kie_err_merge_kernel(const KieControl* src, KieControl* dst) {
+    if (src->err != 0 && dst->err == 0) {
+        dst->err = src->err;
+        dst->err_info = src->err_info;
+    }
+}
+
 // host-visible launch helpers -----------------------------------------------------------------
 #include <cuda_runtime.h>
+
+extern "C" cudaError_t kie_launch_err_merge(const KieControl* src, KieControl* dst, cudaStream_t st) {
+    kie_err_merge_kernel<<<1, 1, 0, st>>>(src, dst);
+    return cudaGetLastError();
+}
 
 extern "C" cudaError_t kie_launch_ctl(KieControl* c, int tok, int pos, int clear, cudaStream_t st) {
     kie_ctl_kernel<<<1, 1, 0, st>>>(c, tok, pos, clear);

@@ -65,6 +65,7 @@ EXPORTS = {
     "kie_generate_greedy": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_generate_greedy_device": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_sync": (C.c_int, [C.c_void_p]),
+    "kie_decode_step_static_scratch": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_trace_decode": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t]),
     "kie_reset": (C.c_int, [C.c_void_p]),
     "kie_get_pos": (C.c_int32, [C.c_void_p]),
@@ -206,6 +207,10 @@ class Engine:
         buf = np.zeros(nph + 32768 * 4, np.uint64)
         _check(load().kie_trace_decode(self.h, int(first_token), int(n), _ptr(buf), buf.size), self.h)
         return buf[:nph].reshape(shape), buf[nph:].reshape(32768, 4)
+
+    def decode_step_static_scratch(self, token: int, d_next_token, d_logits=None):
+        """kie_decode_step_static_scratch: device outputs, no allocation, no sync."""
+        _check(load().kie_decode_step_static_scratch(self.h, int(token), _ptr(d_next_token), _ptr(d_logits)), self.h)
 
     def sync(self):
         _check(load().kie_sync(self.h), self.h)

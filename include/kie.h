@@ -181,6 +181,31 @@ void kie_destroy(kie_engine* e);
  * pos += n. */
 kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint64_t* stamps, size_t cap);
 
+/* ---- decode step without any allocation ------------------------------------------------------ */
+
+/* The pages have no counterpart to this call; it serves callers that may not
+ * allocate device memory while decoding (code hosted inside another
+ * framework's allocator, a plugin without allocation rights, a service that
+ * forbids allocation after start-up, or a device already fully committed).
+ * Together with an engine created on a caller-provided workspace it performs
+ * no cudaMalloc, cudaFree or other allocating call.
+ *
+ * One greedy step like kie_decode_step (consume `token` at pos, append its
+ * K/V, pos += 1) in persistent mode, enqueued on the engine's stream without
+ * synchronising.  d_next_token: DEVICE int32 receiving the argmax; d_logits:
+ * NULL or DEVICE fp32[vocab].  The step's scratch (activations, attention and
+ * argmax partials, control block) is a fixed 256 KiB array inside the library
+ * that every GPU loading the library keeps until the process exits; configs
+ * whose scratch would exceed it (roughly d_model + 2*n_heads*head_dim +
+ * ffn_dim + grid*(head_dim+4) floats) return KIE_ERR_UNSUPPORTED.  The first
+ * call on a device looks up the array's device address (once per device), so
+ * make that first call before any stream capture.  All calls on a device share
+ * the array and it keeps the last call's contents: calls that may overlap on
+ * the GPU (several engines, several streams) race and must be serialised by
+ * the caller.  A device error of the step is reported by the engine's next
+ * synchronising call (e.g. kie_sync). */
+kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t token, int32_t* d_next_token, float* d_logits);
+
 /* ---- context loading and inspection (synthetic contexts, tests) ---------------------------- */
 
 /* Write post-RoPE K and V for positions 0 .. n-1 of one layer through the
