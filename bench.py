@@ -72,6 +72,28 @@ def peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ["autoregressive_decode_gb300/csrc/kie_decode.cu", "autoregressive_decode_gb300/csrc/kie_device.cuh",
+                  "autoregressive_decode_gb300/csrc/kie_internal.h"]
+
+
+def measured_traffic(w: S.Workload, bpl: float):
+    """DRAM bytes per launch from the committed ncu capture, scaled from the
+    captured launch to this one by algorithmic bytes; None if the kernel sources
+    changed since the capture or the capture is for another workload."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"kie_decode_kernel_{w.name}_traffic.json")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256()
+        for p in rec["kernel_sources"]:
+            h.update(open(os.path.join(ROOT, p), "rb").read())
+        if h.hexdigest() != rec["kernel_sources_sha256"]:
+            return None
+        return (rec["dram_bytes_read"] + rec["dram_bytes_write"]) * bpl / rec["algorithmic_bytes"]
+    except Exception:
+        return None
+
+
 def bytes_per_launch(w: S.Workload, p0: int, n: int) -> float:
     import oracle as O  # the byte model lives with the bound it restates
     return float(sum(O.decode_bytes_per_token(w, p + 1)["total"] for p in range(p0, p0 + n)))
@@ -287,7 +309,7 @@ def main():
         # (persistent) or a control kernel plus (5L+1) phase kernels per token (graph)
         "gpu_launches": args.steps * (2 if args.mode == "persistent" else 2 + (5 * w.n_layers + 1) * n_dec),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_source": peak_kind, "kernel": "kie_decode_kernel",
+                     "traffic": measured_traffic(w, bpl), "peak_source": peak_kind, "kernel": "kie_decode_kernel",
                      "algorithmic_bytes_per_launch": bpl, "launch_ms": launch_avg},
         "e2e": {"value": ws * n_dec / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 4 * n_dec},
