@@ -38,6 +38,8 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """KIE_NVCC_EXTRA (environment) adds nvcc flags, e.g. -D overrides of the
+    tuning constants in csrc/kie_internal.h; set force=True when changing it."""
     if not force and not stale():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
@@ -46,7 +48,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for src in _sources():
         obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *os.environ.get("KIE_NVCC_EXTRA", "").split(), "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

@@ -45,10 +45,12 @@ constexpr int NCT = NW * 32;  // consumer threads
 struct Smem {
     uint64_t* full;
     uint64_t* empty;
-    int32_t* flags;   // [0]: abort, [1]: last-arriver flag, [2]: token, [3]: contributor count
+    int32_t* flags;   // [0]: abort, [1]: last-arriver flag, [2]: token, [3]: contributor count,
+                      // [4]: consumers' progress (index of the phase they started, within the launch)
     int32_t* plan;    // [PH_NTYPES][4]: first unit, units, slots, stream bytes of this CTA
     uint64_t* cbase;  // [0]: this CTA's stream offset, [1]: bytes of one layer of it
     int32_t* clist;   // attention: contributors (2*cta + segment) of the head being combined
+    float* rope;      // [2][hd/2] cos, sin of the current step's position
     float* red;       // reduction scratch: NW*(KIE_MAX_HEAD_DIM+2) + 64 floats
     float* part;      // GEMV partial sums
     float* act;       // activation (piece-split layout) / attention scores
@@ -64,6 +66,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const KieParams& P) {
     s.flags = reinterpret_cast<int32_t*>(base + l.flags);
     s.plan = reinterpret_cast<int32_t*>(base + l.plan);
     s.clist = reinterpret_cast<int32_t*>(base + l.clist);
+    s.rope = reinterpret_cast<float*>(base + l.rope);
     s.red = reinterpret_cast<float*>(base + l.red);
     s.part = reinterpret_cast<float*>(base + l.part);
     s.act = reinterpret_cast<float*>(base + l.act);
@@ -181,9 +184,15 @@ __device__ __forceinline__ AttChunk att_chunk(const KieParams& P, int cta, int p
     return a;
 }
 __device__ __forceinline__ int att_row_bytes(const KieParams& P) { return P.hd * (P.kv == KV_F16 ? 2 : 1); }
-__device__ __forceinline__ int att_rows_per_slot(const KieParams& P) { return KIE_SLOT_BYTES / att_row_bytes(P); }
+// Rows per K (or V) slot: the chunk's streamed rows spread over all consumer
+// warps (at least 8 rows, at most one full slot).
+__device__ __forceinline__ int att_rows_per_slot(const KieParams& P, const AttChunk& a) {
+    const int full = KIE_SLOT_BYTES / att_row_bytes(P);
+    const int spread = (a.jt - a.j0 + NW - 1) / NW;
+    return min(full, max(8, spread));
+}
 __device__ __forceinline__ uint32_t att_kslots(const KieParams& P, const AttChunk& a) {
-    const int rps = att_rows_per_slot(P);
+    const int rps = att_rows_per_slot(P, a);
     return uint32_t((a.jt - a.j0 + rps - 1) / rps);
 }
 
@@ -243,11 +252,28 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
             phase_of(phi, P.L, layer, sub);
             const int type = gemv_type(sub);
             if (sub == 1) {
-                // attention: this CTA's K rows then V rows written in earlier steps
+                // attention: this CTA's K rows then V rows written in earlier steps.
+                // Rows up to pos-1 were written by step t-1 (K/V at its QKV phase,
+                // uint8 codes of a completed segment during its attention), so the
+                // copies may start only once this block's consumers are past step
+                // t-1's attention of this layer, i.e. after the grid barrier that
+                // publishes those writes.  With a ring much smaller than one step's
+                // stream this never waits; it bounds the run-ahead of deep rings.
+                if (t >= 1) {
+                    const int32_t need = (t - 1) * (Lc.phase_end - Lc.phase_begin) + (phi - Lc.phase_begin) + 1;
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire_cta_shared(&S.flags[4]) < need) {
+                        if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) { abort = true; break; }
+                        if (globaltimer() - t0 > Lc.timeout_ns) { set_error(P, KERR_TIMEOUT_PROGRESS, cta); abort = true; break; }
+                        __nanosleep(64);
+                    }
+                    if (abort) break;
+                    fence_proxy_async_global();
+                }
                 const int pos = pos0 + t;
                 const AttChunk a = att_chunk(P, cta, pos);
                 const uint32_t nks = att_kslots(P, a);
-                const int rps = att_rows_per_slot(P), rb = att_row_bytes(P);
+                const int rps = att_rows_per_slot(P, a), rb = att_row_bytes(P);
                 for (uint32_t j = 0; j < 2 * nks && !abort; ++j, ++g) {
                     const uint32_t slot = g % nslot;
                     if (!producer_wait_empty(P, Lc, S, g, cta)) { abort = true; break; }
@@ -321,12 +347,14 @@ __device__ __forceinline__ float block_max(float v, float* red, int tid) {
     return m;
 }
 
-// act <- rmsnorm(src) * g, with src = x (fp32, global) or an embedding row (fp16).
-// Pass 1 stages the raw values in shared memory (4 loads in flight per thread)
-// while summing squares; pass 2 rescales each thread's own elements in place,
-// so no register array stays live across the block reduction.
-__device__ void act_rmsnorm(const KieParams& P, const Smem& S, const float* x, const uint16_t* emb_row,
-                            const float* g, int tid) {
+// RMSNorm folded into the GEMV: act <- src * g, and each warp leaves its part of
+// sum(src^2) in S.red[NORM_SLOT + warp]; the epilogue divides every output by
+// sqrt(mean(src^2) + eps) (norm_r).  W (x g / r) = (W (x g)) / r, so no
+// block-wide reduction sits between the barrier and the first slot.
+// src = x (fp32, global) or an embedding row (fp16).
+constexpr int NORM_SLOT = NW * (KIE_MAX_HEAD_DIM + 2) + 8;
+__device__ void act_scaled(const KieParams& P, const Smem& S, const float* x, const uint16_t* emb_row,
+                           const float* g, int tid) {
     const int d = P.d, half = P.act_floats / 2, ng = d >> 2;
     float ss = 0.f;
     for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
@@ -349,31 +377,49 @@ __device__ void act_rmsnorm(const KieParams& P, const Smem& S, const float* x, c
             const int q = q0 + u * NCT;
             if (q < ng) {
                 ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+                const float4 gg = *reinterpret_cast<const float4*>(g + 4 * q);
                 // 4 consecutive elements share one plane of one 8-element piece
-                *reinterpret_cast<float4*>(S.act + act_idx(4 * q, half)) = v[u];
+                *reinterpret_cast<float4*>(S.act + act_idx(4 * q, half)) =
+                    make_float4(v[u].x * gg.x, v[u].y * gg.y, v[u].z * gg.z, v[u].w * gg.w);
             }
         }
     }
-    const float tot = block_sum(ss, S.red, tid);
-    const float r = sqrtf(tot / float(d) + P.eps);
-    for (int q = tid; q < ng; q += NCT) {
-        float4* a = reinterpret_cast<float4*>(S.act + act_idx(4 * q, half));
-        const float4 v = *a;
-        const float4 gg = *reinterpret_cast<const float4*>(g + 4 * q);
-        *a = make_float4((v.x / r) * gg.x, (v.y / r) * gg.y, (v.z / r) * gg.z, (v.w / r) * gg.w);
-    }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) S.red[NORM_SLOT + (tid >> 5)] = ss;
     consumer_sync(NCT);
+}
+
+// sqrt(mean(src^2) + eps) of the phase's act_scaled input (after the phase's
+// final consumer barrier).
+__device__ __forceinline__ float norm_r(const KieParams& P, const Smem& S) {
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) ss += S.red[NORM_SLOT + w];
+    return sqrtf(ss / float(P.d) + P.eps);
+}
+
+// cos / sin of pos * inv_freq_i, i < hd/2, into S.rope (visible after the next
+// consumer barrier).
+__device__ __forceinline__ void rope_table(const KieParams& P, const Smem& S, int pos, int tid) {
+    const int hh = P.hd / 2;
+    if (tid < hh) {
+        float sn, cs;
+        sincosf(float(pos) * P.inv_freq[tid], &sn, &cs);
+        S.rope[tid] = cs;
+        S.rope[hh + tid] = sn;
+    }
 }
 
 __device__ void act_copy(const KieParams& P, const Smem& S, const float* src, int n, int tid) {
     const int half = P.act_floats / 2, ng = n >> 2;
-    for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
-        float4 v[4];
+    constexpr int U = 9;    // loads in flight per thread (9 x 224 covers most of an 8192-float vector)
+    for (int q0 = tid; q0 < ng; q0 += U * NCT) {
+        float4 v[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < U; ++u)
             if (q0 + u * NCT < ng) v[u] = __ldcg(reinterpret_cast<const float4*>(src) + q0 + u * NCT);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < U; ++u)
             if (q0 + u * NCT < ng) *reinterpret_cast<float4*>(S.act + act_idx(4 * (q0 + u * NCT), half)) = v[u];
     }
     consumer_sync(NCT);
@@ -529,8 +575,9 @@ __device__ __forceinline__ void kv_store(const KieParams& P, int layer, int kv, 
 __device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int layer, int pos, int tid) {
     const int hh = P.hd / 2;
     const int per = P.H * hh;  // units per matrix
+    const float r = norm_r(P, S);
     for (int u = tid; u < c.n_units; u += NCT) {
-        const float ya = row_sum(S, c, 2 * u), yb = row_sum(S, c, 2 * u + 1);
+        const float ya = row_sum(S, c, 2 * u) / r, yb = row_sum(S, c, 2 * u + 1) / r;
         const int U = c.unit0 + u;
         const int which = U / per, rem = U % per, h = rem / hh, i = rem % hh;
         if (which == 2) {
@@ -538,8 +585,7 @@ __device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int 
             kv_store(P, layer, 1, h, pos, i + hh, yb);
             continue;
         }
-        float sn, cs;
-        sincosf(float(pos) * P.inv_freq[i], &sn, &cs);
+        const float cs = S.rope[i], sn = S.rope[hh + i];
         const float ra = ya * cs - yb * sn, rb = yb * cs + ya * sn;
         if (which == 0) {
             P.q[h * P.hd + i] = ra;
@@ -561,8 +607,9 @@ __device__ void epi_residual(const KieParams& P, const Smem& S, const Cursor& c,
 }
 
 __device__ void epi_swiglu(const KieParams& P, const Smem& S, const Cursor& c, int tid) {
+    const float r = norm_r(P, S);
     for (int u = tid; u < c.n_units; u += NCT) {
-        const float gt = row_sum(S, c, 2 * u), up = row_sum(S, c, 2 * u + 1);
+        const float gt = row_sum(S, c, 2 * u) / r, up = row_sum(S, c, 2 * u + 1) / r;
         P.a[c.unit0 + u] = (gt / (1.f + expf(-gt))) * up;
     }
 }
@@ -573,8 +620,9 @@ __device__ void epi_lm(const KieParams& P, const KieLaunch& Lc, const Smem& S, c
                        int step, int pos) {
     float best = -INFINITY;
     int bidx = 0x7fffffff;
+    const float nr = norm_r(P, S);
     for (int r = tid; r < c.rows; r += NCT) {
-        const float y = row_sum(S, c, r);
+        const float y = row_sum(S, c, r) / nr;
         const int row = c.unit0 + r;
         if (Lc.out_logits) Lc.out_logits[size_t(step - Lc.lm_from_step) * P.V + row] = y;
         if (y > best || (y == best && row < bidx)) { best = y; bidx = row; }
@@ -767,7 +815,7 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     const int n = j1 - j0, nt = jt - j0;
     const int lg = lane % LPR, rw = lane / LPR;
     const int dim0 = lg * 16;
-    const int rps = att_rows_per_slot(P), rb = att_row_bytes(P);
+    const int rps = att_rows_per_slot(P, a), rb = att_row_bytes(P);
     const uint32_t nks = att_kslots(P, a), nslot = uint32_t(P.nslot);
     float* scores = S.act;
     float* fz = S.red + NW * (KIE_MAX_HEAD_DIM + 2);   // [0..1] K scale/zp, [2..3] V scale/zp (fresh segment)
@@ -1118,7 +1166,10 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 if (!grid_barrier(P, Lc, S, nbar, tid, cta)) return;
             }
             first_phase = false;
-            if (tid == 0) stamp(P, Lc, t, phi, 0, cta);
+            if (tid == 0) {
+                st_release_cta_shared(&S.flags[4], t * (Lc.phase_end - Lc.phase_begin) + (phi - Lc.phase_begin));
+                stamp(P, Lc, t, phi, 0, cta);
+            }
             const float* gains = P.norms + size_t(layer) * 2 * P.d;
             if (sub == 0) {
                 const Cursor c = cursor(P, S, PH_QKV);
@@ -1135,9 +1186,11 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                     // the residual stream starts as the embedding row (each CTA writes a slice)
                     const int s0 = int((int64_t(cta) * P.d) / P.G), s1 = int((int64_t(cta + 1) * P.d) / P.G);
                     for (int k = s0 + tid; k < s1; k += NCT) P.x[k] = __half2float(__ushort_as_half(row[k]));
-                    act_rmsnorm(P, S, nullptr, row, gains, tid);
+                    rope_table(P, S, pos, tid);
+                    act_scaled(P, S, nullptr, row, gains, tid);
                 } else {
-                    act_rmsnorm(P, S, P.x, nullptr, gains, tid);
+                    rope_table(P, S, pos, tid);
+                    act_scaled(P, S, P.x, nullptr, gains, tid);
                 }
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
                 if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
@@ -1156,7 +1209,7 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 epi_residual(P, S, c, tid);
             } else if (sub == 3) {
                 const Cursor c = cursor(P, S, PH_GU);
-                act_rmsnorm(P, S, P.x, nullptr, gains + P.d, tid);
+                act_scaled(P, S, P.x, nullptr, gains + P.d, tid);
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
                 if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
                 if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
@@ -1170,7 +1223,7 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 epi_residual(P, S, c, tid);
             } else {
                 const Cursor c = cursor(P, S, PH_LM);
-                act_rmsnorm(P, S, P.x, nullptr, P.norms + size_t(P.L) * 2 * P.d, tid);
+                act_scaled(P, S, P.x, nullptr, P.norms + size_t(P.L) * 2 * P.d, tid);
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
                 if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
                 if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
@@ -1204,6 +1257,7 @@ __global__ void __launch_bounds__(KIE_THREADS, 1) kie_decode_kernel(const KiePar
         }
         S.flags[0] = 0;
         S.flags[1] = 0;
+        S.flags[4] = -1;
         for (int t = 0; t < PH_NTYPES; ++t) {
             S.plan[t * 4 + 0] = P.ph[t].unit_begin[cta];
             S.plan[t * 4 + 1] = P.ph[t].unit_begin[cta + 1] - P.ph[t].unit_begin[cta];

@@ -78,6 +78,14 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+__device__ __forceinline__ void st_release_cta_shared(int32_t* p, int32_t v) {
+    asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_cta_shared(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
 __device__ __forceinline__ int32_t ld_volatile_i32(const int32_t* p) {
     return *reinterpret_cast<const volatile int32_t*>(p);
 }

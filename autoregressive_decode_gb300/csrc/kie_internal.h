@@ -22,9 +22,13 @@
 #define KIE_NW 7                 // consumer warps per CTA (with the producer: 2 warps per SM sub-partition, no register cap below 255)
 #define KIE_THREADS ((KIE_NW + 1) * 32)
 #define KIE_R 4                  // rows per slot
+#ifndef KIE_KC_F16
 #define KIE_KC_F16 2048          // input columns per slot, fp16 weights
-#define KIE_KC_I4 4096           // input columns per slot, INT4 weights
-#define KIE_SLOT_BYTES 16384     // slot capacity
+#endif
+#define KIE_KC_I4 (2 * KIE_KC_F16)  // input columns per slot, INT4 weights
+#ifndef KIE_SLOT_BYTES
+#define KIE_SLOT_BYTES 16384     // slot capacity (KIE_R rows x KIE_KC_F16 fp16); 8 KB slots measured slower
+#endif
 #define KIE_MAX_SLOTS 16
 #define KIE_SEG 128              // adaptive-range uint8 KV segment (tokens)
 #define KIE_MAX_HEAD_DIM 128
@@ -42,7 +46,7 @@
 // device (carving) both use this one function.  Offsets are relative to the
 // dynamic shared-memory base; the ring starts on a 128-byte boundary.
 struct KieSmemLayout {
-    uint32_t full, empty, cbase, flags, plan, clist, red, part, act, ring, total;
+    uint32_t full, empty, cbase, flags, plan, clist, rope, red, part, act, ring, total;
 };
 KIE_HD inline uint32_t kie_align(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot) {
@@ -54,6 +58,7 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
     l.flags = o; o += 64;
     l.plan = o;  o += 5 * 4 * 4;
     l.clist = o; o += KIE_MAX_GRID * 4;
+    l.rope = o;  o += KIE_MAX_HEAD_DIM * 4;     // cos/sin of the step's position, [2][hd/2]
     l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64) * 4;
     l.part = o;  o += uint32_t(part_floats) * 4;
     l.act = kie_align(o, 16); o = l.act + uint32_t(act_floats) * 4;
@@ -73,6 +78,7 @@ enum KieErr {
     KERR_TIMEOUT_EMPTY = 3,   // producer wait for a free slot expired
     KERR_BAD_TOKEN = 4,       // input token id out of range
     KERR_SMEM = 5,            // launched with less dynamic shared memory than the layout needs
+    KERR_TIMEOUT_PROGRESS = 6 // producer wait for the consumers' progress expired
 };
 
 // Partition of one GEMV phase type over the grid (identical for every layer).

@@ -12,8 +12,10 @@ from _common import check_free_running, engine_for, teacher_forced, tol_for
 pytestmark = pytest.mark.gpu
 
 TINY = S.WORKLOADS["tiny"]
-# hd 128, d 512, ragged vocab (not a multiple of 4 rows x 152 CTAs), FFN 1536
-MEDIUM = S.Workload("medium", 5, 2, 512, 4, 128, 1536, 10007, prompt_len=100, decode_steps=24)
+# hd 128; the down projection's FFN 4608 = two whole 2048-column weight chunks (the
+# GEMV fast path for full 4-row slots) plus a half chunk; ragged vocab (not a
+# multiple of 4 rows x 152 CTAs)
+MEDIUM = S.Workload("medium", 5, 2, 1024, 8, 128, 4608, 10007, prompt_len=100, decode_steps=24)
 
 
 def _prefill_both(w, weights, mode="persistent", max_ctx=None):
