@@ -455,7 +455,8 @@ __device__ __forceinline__ void slot_f16_full(const uint8_t* slot, int k0, const
     constexpr int NPC = KIE_KC_F16 / 8;
     const float* alo = act + (k0 >> 3) * 4;
     const float* ahi = alo + half;
-#pragma unroll
+    constexpr int kUnroll = KIE_F16_UNROLL;
+#pragma unroll kUnroll
     for (int it = 0; it < NPC / 32; ++it) {
         const int p = lane + it * 32;
         const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
@@ -1171,63 +1172,50 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 stamp(P, Lc, t, phi, 0, cta);
             }
             const float* gains = P.norms + size_t(layer) * 2 * P.d;
-            if (sub == 0) {
-                const Cursor c = cursor(P, S, PH_QKV);
-                if (layer == 0) {
-                    if (tid == 0) {
-                        int tk = (t == 0 && Lc.first_tok >= 0) ? Lc.first_tok
-                                 : (Lc.forced ? Lc.forced[t] : __ldcg(&P.ctl->tok));
-                        if (tk < 0 || tk >= P.V) { set_error(P, KERR_BAD_TOKEN, tk); tk = 0; }
-                        S.flags[2] = tk;
-                    }
-                    consumer_sync(NCT);
-                    tok = S.flags[2];
-                    const uint16_t* row = P.emb + size_t(tok) * P.d;
-                    // the residual stream starts as the embedding row (each CTA writes a slice)
-                    const int s0 = int((int64_t(cta) * P.d) / P.G), s1 = int((int64_t(cta + 1) * P.d) / P.G);
-                    for (int k = s0 + tid; k < s1; k += NCT) P.x[k] = __half2float(__ushort_as_half(row[k]));
-                    rope_table(P, S, pos, tid);
-                    act_scaled(P, S, nullptr, row, gains, tid);
+            if (sub == 1) {
+                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
+                if (!attention<HD, KVF>(P, Lc, S, layer, pos, cta, gc, warp, lane, tid)) return;
+                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
+            } else {
+                // One call site each for the activation staging, the GEMV and
+                // every epilogue: the phases share their instructions, which
+                // keeps the per-layer instruction working set small.
+                const int type = sub == 0 ? PH_QKV : sub == 2 ? PH_O : sub == 3 ? PH_GU : sub == 4 ? PH_D : PH_LM;
+                const Cursor c = cursor(P, S, type);
+                if (type == PH_O || type == PH_D) {
+                    act_copy(P, S, type == PH_O ? P.o : P.a, type == PH_O ? P.H * P.hd : P.F, tid);
                 } else {
-                    rope_table(P, S, pos, tid);
-                    act_scaled(P, S, P.x, nullptr, gains, tid);
+                    const float* xs = P.x;
+                    const uint16_t* erow = nullptr;
+                    const float* g = type == PH_QKV ? gains : type == PH_GU ? gains + P.d
+                                                                             : P.norms + size_t(P.L) * 2 * P.d;
+                    if (type == PH_QKV) {
+                        if (layer == 0) {
+                            if (tid == 0) {
+                                int tk = (t == 0 && Lc.first_tok >= 0) ? Lc.first_tok
+                                         : (Lc.forced ? Lc.forced[t] : __ldcg(&P.ctl->tok));
+                                if (tk < 0 || tk >= P.V) { set_error(P, KERR_BAD_TOKEN, tk); tk = 0; }
+                                S.flags[2] = tk;
+                            }
+                            consumer_sync(NCT);
+                            tok = S.flags[2];
+                            erow = P.emb + size_t(tok) * P.d;
+                            xs = nullptr;
+                            // the residual stream starts as the embedding row (each CTA writes a slice)
+                            const int s0 = int((int64_t(cta) * P.d) / P.G), s1 = int((int64_t(cta + 1) * P.d) / P.G);
+                            for (int k = s0 + tid; k < s1; k += NCT) P.x[k] = __half2float(__ushort_as_half(erow[k]));
+                        }
+                        rope_table(P, S, pos, tid);
+                    }
+                    act_scaled(P, S, xs, erow, g, tid);
                 }
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
                 if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
                 if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                epi_qkv(P, S, c, layer, pos, tid);
-            } else if (sub == 1) {
-                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!attention<HD, KVF>(P, Lc, S, layer, pos, cta, gc, warp, lane, tid)) return;
-                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-            } else if (sub == 2) {
-                const Cursor c = cursor(P, S, PH_O);
-                act_copy(P, S, P.o, P.H * P.hd, tid);
-                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
-                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                epi_residual(P, S, c, tid);
-            } else if (sub == 3) {
-                const Cursor c = cursor(P, S, PH_GU);
-                act_scaled(P, S, P.x, nullptr, gains + P.d, tid);
-                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
-                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                epi_swiglu(P, S, c, tid);
-            } else if (sub == 4) {
-                const Cursor c = cursor(P, S, PH_D);
-                act_copy(P, S, P.a, P.F, tid);
-                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
-                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                epi_residual(P, S, c, tid);
-            } else {
-                const Cursor c = cursor(P, S, PH_LM);
-                act_scaled(P, S, P.x, nullptr, P.norms + size_t(P.L) * 2 * P.d, tid);
-                if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
-                if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                epi_lm(P, Lc, S, c, cta, tid, t, pos);
+                if (type == PH_QKV) epi_qkv(P, S, c, layer, pos, tid);
+                else if (type == PH_GU) epi_swiglu(P, S, c, tid);
+                else if (type == PH_LM) epi_lm(P, Lc, S, c, cta, tid, t, pos);
+                else epi_residual(P, S, c, tid);
             }
             if (tid == 0) stamp(P, Lc, t, phi, 3, cta);
         }

@@ -26,6 +26,9 @@
 #define KIE_KC_F16 2048          // input columns per slot, fp16 weights
 #endif
 #define KIE_KC_I4 (2 * KIE_KC_F16)  // input columns per slot, INT4 weights
+#ifndef KIE_F16_UNROLL
+#define KIE_F16_UNROLL 8         // unroll of the full-slot fp16 GEMV loop (KIE_KC_F16 / 256 iterations)
+#endif
 #ifndef KIE_SLOT_BYTES
 #define KIE_SLOT_BYTES 16384     // slot capacity (KIE_R rows x KIE_KC_F16 fp16); 8 KB slots measured slower
 #endif
