@@ -71,7 +71,7 @@ struct Layout {  // byte offsets into the workspace
     size_t wstream, wstream_bytes;
     size_t emb, norms, inv_freq;
     size_t kc, vc, kv_bytes, tail, seg_scale, seg_zp;
-    size_t x, q, o, a, att_part, head_cnt, amax_val, amax_idx, ctl;
+    size_t x, kcur, vcur, head_cnt, zero_bytes, q, a, o, par_bytes, att_part, amax_val, amax_idx, ctl;
     size_t plan_i32, plan_u32, cta_base, cta_layer;
     size_t out_tokens, out_logits, forced, step_token, step_logits;
     size_t total;
@@ -212,12 +212,18 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.tail = take(u8 ? size_t(c.n_layers) * 2 * H * KIE_SEG * hd * 2 : 0);
     L.seg_scale = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
     L.seg_zp = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
+    // tagged activations and head counters, reset before each launch sequence
+    // (reset_tags): x .. head_cnt to zero, q .. o to one parity
     L.x = take(size_t(d) * 4);
+    L.kcur = take(size_t(H) * hd * 4);
+    L.vcur = take(size_t(H) * hd * 4);
+    L.head_cnt = take(size_t(H) * 4);
+    L.zero_bytes = L.head_cnt + size_t(H) * 4 - L.x;
     L.q = take(size_t(H) * hd * 4);
     L.a = take(size_t(F) * 4);
     L.o = take(size_t(H) * hd * 4);
+    L.par_bytes = L.o + size_t(H) * hd * 4 - L.q;
     L.att_part = take(size_t(G) * (hd + 4) * 4);
-    L.head_cnt = take(size_t(H) * 4);
     L.amax_val = take(size_t(G) * 4);
     L.amax_idx = take(size_t(G) * 4);
     L.ctl = take(sizeof(KieControl));
@@ -255,7 +261,7 @@ struct kie_engine {
     int pos = 0;
     int sticky = 0;
     uint64_t timeout_ns = kDefaultTimeoutNs;
-    cudaGraphExec_t graph = nullptr;
+    cudaGraphExec_t graph[2] = {nullptr, nullptr};   // graph mode, by tag_fill of the step's position
     KieControl* h_ctl = nullptr;  // pinned staging
     std::string err;
 
@@ -328,8 +334,24 @@ KieLaunch base_launch(kie_engine* e) {
     return l;
 }
 
+// Fill byte of q, a, o before a launch sequence starting at position pos: its
+// words carry the parity opposite to the first write's, (pos * L + 1) & 1.
+int tag_fill(const kie_config& c, int pos) {
+    return ((int64_t(pos) * c.n_layers + 1) & 1) ? 0x00 : 0x01;
+}
+
+// Reset the tagged activations before a launch sequence starting at pos.
+cudaError_t reset_tags(const kie_config& c, uint8_t* x, size_t zero_bytes, uint8_t* q, size_t par_bytes, int pos,
+                       cudaStream_t s) {
+    cudaError_t r = cudaMemsetAsync(x, 0, zero_bytes, s);
+    if (r == cudaSuccess) r = cudaMemsetAsync(q, tag_fill(c, pos), par_bytes, s);
+    return r;
+}
+
 kie_status launch_persistent(kie_engine* e, const KieLaunch& l) {
     KIE_CUDA(e, cudaMemsetAsync(e->dev(e->lay.ctl) + offsetof(KieControl, bar), 0, 4, e->stream));
+    KIE_CUDA(e, reset_tags(e->cfg, e->dev(e->lay.x), e->lay.zero_bytes, e->dev(e->lay.q), e->lay.par_bytes,
+                           l.pos0 >= 0 ? l.pos0 : e->pos, e->stream));
     void* args[] = {(void*)&e->P, (void*)&l};
     cudaError_t r = cudaLaunchCooperativeKernel(e->kernel, dim3(e->G), dim3(KIE_THREADS), args, e->plan.smem, e->stream);
     if (r == cudaErrorCooperativeLaunchTooLarge) {
@@ -340,15 +362,25 @@ kie_status launch_persistent(kie_engine* e, const KieLaunch& l) {
     return KIE_OK;
 }
 
-// Graph mode: one captured graph = one decode step = 5L+1 single-phase launches.
-kie_status ensure_graph(kie_engine* e) {
-    if (e->graph) return KIE_OK;
+void drop_graphs(kie_engine* e) {
+    for (auto& g : e->graph)
+        if (g) { cudaGraphExecDestroy(g); g = nullptr; }
+}
+
+// Graph mode: one captured graph = one decode step = the tag reset and 5L+1
+// single-phase launches.  The reset's fill byte depends on the step position's
+// parity, so there is one graph per fill byte.
+kie_status ensure_graph(kie_engine* e, int fill) {
+    if (e->graph[fill]) return KIE_OK;
     cudaStream_t cap;
     KIE_CUDA(e, cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
     cudaGraph_t g = nullptr;
     cudaError_t r = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
     if (r != cudaSuccess) { cudaStreamDestroy(cap); return fail(e, KIE_ERR_CUDA, "begin capture: %s", cudaGetErrorString(r)); }
     const int P_ = 5 * e->cfg.n_layers + 1;
+    // every step starts from reset activation tags and head counters
+    r = cudaMemsetAsync(e->dev(e->lay.x), 0, e->lay.zero_bytes, cap);
+    if (r == cudaSuccess) r = cudaMemsetAsync(e->dev(e->lay.q), fill, e->lay.par_bytes, cap);
     for (int phi = 0; phi < P_ && r == cudaSuccess; ++phi) {
         KieLaunch l = base_launch(e);
         l.phase_begin = phi;
@@ -365,9 +397,9 @@ kie_status ensure_graph(kie_engine* e) {
         if (g) cudaGraphDestroy(g);
         return fail(e, KIE_ERR_CUDA, "graph capture: %s", cudaGetErrorString(r != cudaSuccess ? r : r2));
     }
-    r = cudaGraphInstantiate(&e->graph, g, 0);
+    r = cudaGraphInstantiate(&e->graph[fill], g, 0);
     cudaGraphDestroy(g);
-    if (r != cudaSuccess) { e->graph = nullptr; return fail(e, KIE_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(r)); }
+    if (r != cudaSuccess) { e->graph[fill] = nullptr; return fail(e, KIE_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(r)); }
     return KIE_OK;
 }
 
@@ -389,13 +421,14 @@ kie_status run_steps(kie_engine* e, int n, int first_tok, const int32_t* d_force
         l.out_logits = d_logits;
         if ((st = launch_persistent(e, l)) != KIE_OK) return st;
     } else {
-        if ((st = ensure_graph(e)) != KIE_OK) return st;
+        for (int f = 0; f < 2; ++f)
+            if ((st = ensure_graph(e, f)) != KIE_OK) return st;
         if ((st = set_ctl(e, first_tok >= 0 ? first_tok : 0, e->pos, false)) != KIE_OK) return st;
         int32_t* ctl_tok = reinterpret_cast<int32_t*>(e->dev(e->lay.ctl) + offsetof(KieControl, tok));
         for (int t = 0; t < n; ++t) {
             if (d_forced)
                 KIE_CUDA(e, cudaMemcpyAsync(ctl_tok, d_forced + t, 4, cudaMemcpyDeviceToDevice, e->stream));
-            KIE_CUDA(e, cudaGraphLaunch(e->graph, e->stream));
+            KIE_CUDA(e, cudaGraphLaunch(e->graph[tag_fill(e->cfg, e->pos + t)], e->stream));
             if (d_tokens)
                 KIE_CUDA(e, cudaMemcpyAsync(d_tokens + t, e->dev(e->lay.step_token), 4, cudaMemcpyDeviceToDevice, e->stream));
             if (d_logits && t >= lm_from)
@@ -526,6 +559,8 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     P.q = reinterpret_cast<float*>(e->dev(L.q));
     P.a = reinterpret_cast<float*>(e->dev(L.a));
     P.o = reinterpret_cast<float*>(e->dev(L.o));
+    P.kcur = reinterpret_cast<uint32_t*>(e->dev(L.kcur));
+    P.vcur = reinterpret_cast<uint32_t*>(e->dev(L.vcur));
     P.att_part = reinterpret_cast<float*>(e->dev(L.att_part));
     P.head_cnt = reinterpret_cast<uint32_t*>(e->dev(L.head_cnt));
     P.amax_val = reinterpret_cast<float*>(e->dev(L.amax_val));
@@ -553,7 +588,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     const Plan& pl = e->plan;
     const cudaMemcpyKind kind = w->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
     e->loaded = false;
-    if (e->graph) { cudaGraphExecDestroy(e->graph); e->graph = nullptr; }
+    drop_graphs(e);
 
     // embedding (as given) and norm gains (fp32)
     KIE_CUDA(e, cudaMemcpyAsync(e->dev(L.emb), w->tok_emb, size_t(V) * d * 2, kind, st));
@@ -834,7 +869,8 @@ kie_status kie_reset(kie_engine* e) {
     cudaStreamSynchronize(e->stream);
     e->sticky = 0;
     e->pos = 0;
-    KIE_CUDA(e, cudaMemsetAsync(e->dev(e->lay.head_cnt), 0, size_t(e->cfg.n_heads) * 4, e->stream));
+    KIE_CUDA(e, reset_tags(e->cfg, e->dev(e->lay.x), e->lay.zero_bytes, e->dev(e->lay.q), e->lay.par_bytes, 0,
+                           e->stream));
     return set_ctl(e, 0, 0, true);
 }
 
@@ -851,7 +887,7 @@ kie_status kie_set_timeout_ms(kie_engine* e, int32_t ms) {
     if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
     if (ms <= 0) return fail(e, KIE_ERR_INVALID_ARG, "timeout must be positive");
     e->timeout_ns = uint64_t(ms) * 1000000ull;
-    if (e->graph) { cudaGraphExecDestroy(e->graph); e->graph = nullptr; }
+    drop_graphs(e);
     return KIE_OK;
 }
 
@@ -864,7 +900,7 @@ void kie_destroy(kie_engine* e) {
     if (!e) return;
     if (e->stream) cudaStreamSynchronize(e->stream);
     else cudaDeviceSynchronize();
-    if (e->graph) cudaGraphExecDestroy(e->graph);
+    drop_graphs(e);
     if (e->own_ws && e->ws) cudaFree(e->ws);
     if (e->h_ctl) cudaFreeHost(e->h_ctl);
     delete e;
@@ -1028,19 +1064,25 @@ static __device__ __align__(256) uint8_t kie_static_scratch[KIE_STATIC_SCRATCH_B
 namespace {
 
 struct StaticScratchLayout {
-    size_t x, q, o, a, att_part, head_cnt, amax_val, amax_idx, ctl, total;
+    size_t x, kcur, vcur, head_cnt, zero_bytes, q, a, o, par_bytes, att_part, amax_val, amax_idx, ctl, total;
 };
 
 StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
     StaticScratchLayout l;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
+    const size_t hq = size_t(c.n_heads) * c.head_dim * 4;
+    // tagged activations and head counters, reset per step as in the engine's workspace
     l.x = take(size_t(c.d_model) * 4);
-    l.q = take(size_t(c.n_heads) * c.head_dim * 4);
-    l.o = take(size_t(c.n_heads) * c.head_dim * 4);
-    l.a = take(size_t(c.ffn_dim) * 4);
-    l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
+    l.kcur = take(hq);
+    l.vcur = take(hq);
     l.head_cnt = take(size_t(c.n_heads) * 4);
+    l.zero_bytes = l.head_cnt + size_t(c.n_heads) * 4 - l.x;
+    l.q = take(hq);
+    l.a = take(size_t(c.ffn_dim) * 4);
+    l.o = take(hq);
+    l.par_bytes = l.o + hq - l.q;
+    l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
     l.amax_val = take(size_t(G) * 4);
     l.amax_idx = take(size_t(G) * 4);
     l.ctl = take(sizeof(KieControl));
@@ -1088,15 +1130,18 @@ extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t toke
     cudaError_t r = static_scratch_ptr(e->cfg.device, &base);
     if (r != cudaSuccess) return fail(e, KIE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(r));
     uint8_t* b = static_cast<uint8_t*>(base);
-    // the control block (barrier count, error word, argmax arrivals) and the
-    // head counters must start at zero; everything else is written before read
+    // the control block (barrier count, error word, argmax arrivals), the
+    // activation tags and the head counters must start at zero; everything
+    // else is written before it is read
     KIE_CUDA(e, cudaMemsetAsync(b + sl.ctl, 0, sizeof(KieControl), e->stream));
-    KIE_CUDA(e, cudaMemsetAsync(b + sl.head_cnt, 0, size_t(e->cfg.n_heads) * 4, e->stream));
+    KIE_CUDA(e, reset_tags(e->cfg, b + sl.x, sl.zero_bytes, b + sl.q, sl.par_bytes, e->pos, e->stream));
     KieParams P = e->P;
     P.x = reinterpret_cast<float*>(b + sl.x);
     P.q = reinterpret_cast<float*>(b + sl.q);
     P.o = reinterpret_cast<float*>(b + sl.o);
     P.a = reinterpret_cast<float*>(b + sl.a);
+    P.kcur = reinterpret_cast<uint32_t*>(b + sl.kcur);
+    P.vcur = reinterpret_cast<uint32_t*>(b + sl.vcur);
     P.att_part = reinterpret_cast<float*>(b + sl.att_part);
     P.head_cnt = reinterpret_cast<uint32_t*>(b + sl.head_cnt);
     P.amax_val = reinterpret_cast<float*>(b + sl.amax_val);

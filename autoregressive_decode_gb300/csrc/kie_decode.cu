@@ -149,6 +149,87 @@ __device__ void set_error(const KieParams& P, int code, int info) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// tagged activations
+// ---------------------------------------------------------------------------------------------
+// Inside a step no grid barrier separates the phases.  Every activation that
+// one CTA writes and others read carries a tag of the write that produced it,
+// and a reader polls until the tag it expects is there.  Writes are numbered
+// by n = pos * L + layer, the same in every launch mode:
+//  * q, a and o (fp32, written once per layer): the parity of n + 1 in the
+//    least significant mantissa bit (a relative change of at most 2^-23,
+//    applied identically in every mode);
+//  * x (fp32): parity 1 after an O epilogue, 0 after a D epilogue;
+//  * K and V of the current position: (storage bits << 16) | (n mod 65535) + 1.
+// Before every launch sequence the host sets x, K, V to tag 0 and q, a, o to
+// the parity opposite to the first write's, so the initial state never
+// matches.  One parity bit suffices because every reader of a write has read
+// the write before it at the same address (read-read coherence: what it sees
+// is that write or the one it waits for): every CTA stages all of x after each
+// epilogue that writes it, and reads its head's q and the whole of a and o
+// every layer.  No write can overtake a pending read: the next write of a
+// buffer needs the layer's whole data flow, which needs every reader of the
+// current value to be past it.
+__device__ __forceinline__ uint32_t tag_seq(const KieParams& P, int pos, int layer) {
+    return uint32_t(pos) * uint32_t(P.L) + uint32_t(layer);
+}
+__device__ __forceinline__ uint32_t tag_par(uint32_t n) { return (n + 1u) & 1u; }
+__device__ __forceinline__ uint32_t tag_ep16(uint32_t n) { return n % 65535u + 1u; }
+__device__ __forceinline__ float tag_f32(float v, uint32_t par) {
+    return __uint_as_float((__float_as_uint(v) & ~1u) | par);
+}
+__device__ __forceinline__ bool has_tag4(const float4& v, uint32_t par) {
+    return (((__float_as_uint(v.x) ^ par) | (__float_as_uint(v.y) ^ par) | (__float_as_uint(v.z) ^ par) |
+             (__float_as_uint(v.w) ^ par)) & 1u) == 0u;
+}
+__device__ __forceinline__ bool has_ep4(const uint4& v, uint32_t ep16) {
+    return ((v.x & 0xFFFFu) == ep16) & ((v.y & 0xFFFFu) == ep16) & ((v.z & 0xFFFFu) == ep16) & ((v.w & 0xFFFFu) == ep16);
+}
+
+// Bounded poll of one thread: false once the launch's timeout has passed
+// (recorded as KERR_TIMEOUT_DATA) or another thread or CTA has failed.
+struct TagWait {
+    uint64_t t0;
+    uint32_t spins;
+    __device__ TagWait() : t0(globaltimer()), spins(0) {}
+    __device__ __forceinline__ bool again(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
+        if ((++spins & 15u) != 0u) return true;
+        if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
+        if (globaltimer() - t0 > Lc.timeout_ns) {
+            set_error(P, KERR_TIMEOUT_DATA, cta);
+            S.flags[0] = 1;
+            return false;
+        }
+        return true;
+    }
+};
+
+// One tagged fp32 element (scalar poll).
+__device__ __forceinline__ float wait_f32(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* p,
+                                          uint32_t par, int cta) {
+    float v = ld_relaxed_f32(p);
+    if (((__float_as_uint(v) ^ par) & 1u) == 0u) return v;
+    TagWait w;
+    do {
+        v = ld_relaxed_f32(p);
+        if (((__float_as_uint(v) ^ par) & 1u) == 0u) break;
+    } while (w.again(P, Lc, S, cta));
+    return v;
+}
+// One tagged K/V word of the current position; returns its storage bits.
+__device__ __forceinline__ uint32_t wait_cur(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                             const uint32_t* p, uint32_t ep16, int cta) {
+    uint32_t v = ld_relaxed_u32(p);
+    if ((v & 0xFFFFu) != ep16) {
+        TagWait w;
+        do {
+            v = ld_relaxed_u32(p);
+            if ((v & 0xFFFFu) == ep16) break;
+        } while (w.again(P, Lc, S, cta));
+    }
+    return v >> 16;
+}
+
+// ---------------------------------------------------------------------------------------------
 // KV cache access
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ size_t kv_elem_index(const KieParams& P, int layer, int h, int pos) {
@@ -255,12 +336,12 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 // attention: this CTA's K rows then V rows written in earlier steps.
                 // Rows up to pos-1 were written by step t-1 (K/V at its QKV phase,
                 // uint8 codes of a completed segment during its attention), so the
-                // copies may start only once this block's consumers are past step
-                // t-1's attention of this layer, i.e. after the grid barrier that
-                // publishes those writes.  With a ring much smaller than one step's
-                // stream this never waits; it bounds the run-ahead of deep rings.
+                // copies may start only once this block's consumers have started
+                // step t, i.e. passed the grid barrier that publishes those writes.
+                // With a ring much smaller than one step's stream this never
+                // waits; it bounds the run-ahead of deep rings.
                 if (t >= 1) {
-                    const int32_t need = (t - 1) * (Lc.phase_end - Lc.phase_begin) + (phi - Lc.phase_begin) + 1;
+                    const int32_t need = t * (Lc.phase_end - Lc.phase_begin);
                     const uint64_t t0 = globaltimer();
                     while (ld_acquire_cta_shared(&S.flags[4]) < need) {
                         if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) { abort = true; break; }
@@ -353,24 +434,39 @@ __device__ __forceinline__ float block_max(float v, float* red, int tid) {
 // block-wide reduction sits between the barrier and the first slot.
 // src = x (fp32, global) or an embedding row (fp16).
 constexpr int NORM_SLOT = NW * (KIE_MAX_HEAD_DIM + 2) + 8;
-__device__ void act_scaled(const KieParams& P, const Smem& S, const float* x, const uint16_t* emb_row,
-                           const float* g, int tid) {
+// x is tagged with parity `par` (polled until every element carries it).
+__device__ void act_scaled(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* x,
+                           const uint16_t* emb_row, const float* g, uint32_t par, int tid, int cta) {
     const int d = P.d, half = P.act_floats / 2, ng = d >> 2;
     float ss = 0.f;
     for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
         float4 v[4];
+        uint32_t bad = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int q = q0 + u * NCT;
             if (q < ng) {
                 if (x) {
-                    v[u] = __ldcg(reinterpret_cast<const float4*>(x) + q);
+                    v[u] = ld_relaxed_f4(x + 4 * q);
+                    if (!has_tag4(v[u], par)) bad |= 1u << u;
                 } else {
                     const uint2 hv = *reinterpret_cast<const uint2*>(emb_row + 4 * q);
                     const float2 a = h2_to_f2(hv.x), b = h2_to_f2(hv.y);
                     v[u] = make_float4(a.x, a.y, b.x, b.y);
                 }
             }
+        }
+        if (bad) {
+            TagWait w;
+            do {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if ((bad >> u) & 1u) {
+                        v[u] = ld_relaxed_f4(x + 4 * (q0 + u * NCT));
+                        if (has_tag4(v[u], par)) bad &= ~(1u << u);
+                    }
+                }
+            } while (bad && w.again(P, Lc, S, cta));
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -410,14 +506,33 @@ __device__ __forceinline__ void rope_table(const KieParams& P, const Smem& S, in
     }
 }
 
-__device__ void act_copy(const KieParams& P, const Smem& S, const float* src, int n, int tid) {
+// src is tagged with parity `par` (polled until every element carries it).
+__device__ void act_copy(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* src, int n,
+                         uint32_t par, int tid, int cta) {
     const int half = P.act_floats / 2, ng = n >> 2;
     constexpr int U = 9;    // loads in flight per thread (9 x 224 covers most of an 8192-float vector)
     for (int q0 = tid; q0 < ng; q0 += U * NCT) {
         float4 v[U];
+        uint32_t bad = 0;
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (q0 + u * NCT < ng) v[u] = __ldcg(reinterpret_cast<const float4*>(src) + q0 + u * NCT);
+        for (int u = 0; u < U; ++u) {
+            if (q0 + u * NCT < ng) {
+                v[u] = ld_relaxed_f4(src + 4 * (q0 + u * NCT));
+                if (!has_tag4(v[u], par)) bad |= 1u << u;
+            }
+        }
+        if (bad) {
+            TagWait w;
+            do {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if ((bad >> u) & 1u) {
+                        v[u] = ld_relaxed_f4(src + 4 * (q0 + u * NCT));
+                        if (has_tag4(v[u], par)) bad &= ~(1u << u);
+                    }
+                }
+            } while (bad && w.again(P, Lc, S, cta));
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (q0 + u * NCT < ng) *reinterpret_cast<float4*>(S.act + act_idx(4 * (q0 + u * NCT), half)) = v[u];
@@ -556,62 +671,77 @@ __device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) 
     return y;
 }
 
-// store one element of the new K (kv=0) or V (kv=1) at position pos
-__device__ __forceinline__ void kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v) {
+// store one element of the new K (kv=0) or V (kv=1) at position pos; returns
+// the stored bits (fp16, or the E5M2 byte)
+__device__ __forceinline__ uint32_t kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v) {
     const __half hv = __float2half_rn(v);
     if (P.kv == KV_F16) {
         uint8_t* base = kv ? P.vc : P.kc;
         reinterpret_cast<__half*>(base)[kv_elem_index(P, layer, h, pos) + dim] = hv;
     } else if (P.kv == KV_E5M2) {
         uint8_t* base = kv ? P.vc : P.kc;
-        base[kv_elem_index(P, layer, h, pos) + dim] = uint8_t(f16x2_to_e5m2x2(hv, hv) & 0xFFu);
+        const uint32_t b = f16x2_to_e5m2x2(hv, hv) & 0xFFu;
+        base[kv_elem_index(P, layer, h, pos) + dim] = uint8_t(b);
+        return b;
     } else {
         reinterpret_cast<__half*>(P.tail)[tail_index(P, layer, kv, h, pos % KIE_SEG) + dim] = hv;
     }
+    return __half_as_ushort(hv);
 }
 
 // ---------------------------------------------------------------------------------------------
 // phase epilogues
 // ---------------------------------------------------------------------------------------------
-__device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int layer, int pos, int tid) {
+// q, K and V of this CTA's rows: the cache (for later steps) and the tagged
+// q / current-position K, V (for this step's attention), write number n.
+__device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int layer, int pos, uint32_t n,
+                        int tid) {
     const int hh = P.hd / 2;
     const int per = P.H * hh;  // units per matrix
+    const uint32_t par = tag_par(n), ep16 = tag_ep16(n);
     const float r = norm_r(P, S);
     for (int u = tid; u < c.n_units; u += NCT) {
         const float ya = row_sum(S, c, 2 * u) / r, yb = row_sum(S, c, 2 * u + 1) / r;
         const int U = c.unit0 + u;
         const int which = U / per, rem = U % per, h = rem / hh, i = rem % hh;
+        const int e0 = h * P.hd + i;
         if (which == 2) {
-            kv_store(P, layer, 1, h, pos, i, ya);
-            kv_store(P, layer, 1, h, pos, i + hh, yb);
+            const uint32_t b0 = kv_store(P, layer, 1, h, pos, i, ya), b1 = kv_store(P, layer, 1, h, pos, i + hh, yb);
+            st_relaxed_u32(P.vcur + e0, (b0 << 16) | ep16);
+            st_relaxed_u32(P.vcur + e0 + hh, (b1 << 16) | ep16);
             continue;
         }
         const float cs = S.rope[i], sn = S.rope[hh + i];
         const float ra = ya * cs - yb * sn, rb = yb * cs + ya * sn;
         if (which == 0) {
-            P.q[h * P.hd + i] = ra;
-            P.q[h * P.hd + i + hh] = rb;
+            st_relaxed_f32(P.q + e0, tag_f32(ra, par));
+            st_relaxed_f32(P.q + e0 + hh, tag_f32(rb, par));
         } else {
-            kv_store(P, layer, 0, h, pos, i, ra);
-            kv_store(P, layer, 0, h, pos, i + hh, rb);
+            const uint32_t b0 = kv_store(P, layer, 0, h, pos, i, ra), b1 = kv_store(P, layer, 0, h, pos, i + hh, rb);
+            st_relaxed_u32(P.kcur + e0, (b0 << 16) | ep16);
+            st_relaxed_u32(P.kcur + e0 + hh, (b1 << 16) | ep16);
         }
     }
     // K/V written here are read in later steps by bulk copies (the async proxy).
     fence_proxy_async_global();
 }
 
-__device__ void epi_residual(const KieParams& P, const Smem& S, const Cursor& c, int tid) {
+// x[row] += y[row]; x is read with parity par_in (or, in the first layer's O
+// phase, is the embedding row erow) and written with parity par_out.
+__device__ void epi_residual(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c,
+                             const uint16_t* erow, uint32_t par_in, uint32_t par_out, int tid, int cta) {
     for (int r = tid; r < c.rows; r += NCT) {
         const int row = c.unit0 + r;
-        P.x[row] = __ldcg(P.x + row) + row_sum(S, c, r);
+        const float xo = erow ? __half2float(__ushort_as_half(erow[row])) : wait_f32(P, Lc, S, P.x + row, par_in, cta);
+        st_relaxed_f32(P.x + row, tag_f32(xo + row_sum(S, c, r), par_out));
     }
 }
 
-__device__ void epi_swiglu(const KieParams& P, const Smem& S, const Cursor& c, int tid) {
+__device__ void epi_swiglu(const KieParams& P, const Smem& S, const Cursor& c, uint32_t par, int tid) {
     const float r = norm_r(P, S);
     for (int u = tid; u < c.n_units; u += NCT) {
         const float gt = row_sum(S, c, 2 * u) / r, up = row_sum(S, c, 2 * u + 1) / r;
-        P.a[c.unit0 + u] = (gt / (1.f + expf(-gt))) * up;
+        st_relaxed_f32(P.a + c.unit0 + u, tag_f32((gt / (1.f + expf(-gt))) * up, par));
     }
 }
 
@@ -742,14 +872,74 @@ __device__ __forceinline__ void convert_row(const RawRow& r, const float* fz, fl
     }
 }
 
+// The current position's 16 dims [dim0, dim0+16) of K (kv=0) or V, from the
+// tagged copy written in this step's QKV epilogue, as a RawRow of the stored
+// format (fp16 pairs; E5M2 bytes).  The uint8 cache keeps the open segment in
+// fp16, so its current row is fp16 too.
+template <int KVF>
+__device__ __forceinline__ void cur_row(const KieParams& P, const KieLaunch& Lc, const Smem& S, int kv, int h,
+                                        int dim0, uint32_t ep16, int cta, RawRow& r) {
+    const uint32_t* src = (kv ? P.vcur : P.kcur) + h * P.hd + dim0;
+    uint4 w[4];
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w[i] = ld_relaxed_u4(src + 4 * i);
+        if (!has_ep4(w[i], ep16)) bad |= 1u << i;
+    }
+    if (bad) {
+        TagWait tw;
+        do {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if ((bad >> i) & 1u) {
+                    w[i] = ld_relaxed_u4(src + 4 * i);
+                    if (has_ep4(w[i], ep16)) bad &= ~(1u << i);
+                }
+            }
+        } while (bad && tw.again(P, Lc, S, cta));
+    }
+    r.sc = 0.f;
+    r.zp = 0;
+    if (KVF == KV_E5M2) {
+        uint32_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            b[i] = ((w[i].x >> 16) & 0xFFu) | (((w[i].y >> 16) & 0xFFu) << 8) | (((w[i].z >> 16) & 0xFFu) << 16) |
+                   (((w[i].w >> 16) & 0xFFu) << 24);
+        r.a = make_uint4(b[0], b[1], b[2], b[3]);
+        r.b = make_uint4(0, 0, 0, 0);
+    } else {
+        uint32_t hp[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            hp[2 * i] = (w[i].x >> 16) | (w[i].y & 0xFFFF0000u);
+            hp[2 * i + 1] = (w[i].z >> 16) | (w[i].w & 0xFFFF0000u);
+        }
+        r.a = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+        r.b = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+    }
+}
+
+// Element i of a (layer, kv, head) open segment (row i / hd of the fp16 tail;
+// row prow is the current position, read from its tagged copy).
+__device__ __forceinline__ float seg_elem(const KieParams& P, const KieLaunch& Lc, const Smem& S, const __half* t,
+                                          int kv, int h, int i, int prow, uint32_t ep16, int cta) {
+    if (i / P.hd == prow) {
+        const uint32_t* cur = (kv ? P.vcur : P.kcur) + h * P.hd + i % P.hd;
+        return __half2float(__ushort_as_half((unsigned short)wait_cur(P, Lc, S, cur, ep16, cta)));
+    }
+    return __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(t) + i)));
+}
+
 // scale/zp of one (layer, kv, head) open segment, from its 128 fp16 tail rows.
-__device__ void u8_segment_params(const KieParams& P, const Smem& S, int layer, int kv, int h, int tid,
-                                  float* out /* [0]=scale, [1]=zp bits */) {
+__device__ void u8_segment_params(const KieParams& P, const KieLaunch& Lc, const Smem& S, int layer, int kv, int h,
+                                  int prow, uint32_t ep16, int tid, int cta, float* out /* [0]=scale, [1]=zp bits */) {
     const __half* t = reinterpret_cast<const __half*>(P.tail) + tail_index(P, layer, kv, h, 0);
     const int n = KIE_SEG * P.hd;
     float mn = INFINITY, mx = -INFINITY;
     for (int i = tid; i < n; i += NCT) {
-        const float v = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(t) + i)));
+        const float v = seg_elem(P, Lc, S, t, kv, h, i, prow, ep16, cta);
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
     }
@@ -767,14 +957,15 @@ __device__ void u8_segment_params(const KieParams& P, const Smem& S, int layer, 
 }
 
 // Write codes + meta of a segment completed in this step (its owner CTA only).
-__device__ void u8_segment_commit(const KieParams& P, int layer, int kv, int h, int seg, const float* fz, int tid) {
+__device__ void u8_segment_commit(const KieParams& P, const KieLaunch& Lc, const Smem& S, int layer, int kv, int h,
+                                  int seg, int prow, uint32_t ep16, const float* fz, int tid, int cta) {
     const __half* t = reinterpret_cast<const __half*>(P.tail) + tail_index(P, layer, kv, h, 0);
     uint8_t* dst = (kv ? P.vc : P.kc) + kv_elem_index(P, layer, h, seg * KIE_SEG);
     const float sc = fz[0];
     const int zp = __float_as_int(fz[1]);
     const int n = KIE_SEG * P.hd;
     for (int i = tid; i < n; i += NCT) {
-        const float v = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(t) + i)));
+        const float v = seg_elem(P, Lc, S, t, kv, h, i, prow, ep16, cta);
         dst[i] = uint8_t(min(max(__float2int_rn(v / sc) + zp, 0), 255));
     }
     if (tid == 0) {
@@ -805,8 +996,9 @@ __device__ __forceinline__ void smem_row16(const uint8_t* row, int dim0, float s
 }
 
 template <int HD, int KVF>
-__device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S, int layer, int pos, int cta,
-                          uint32_t& gc, int warp, int lane, int tid) {
+__device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S, int layer, int pos, uint32_t tn,
+                          int cta, uint32_t& gc, int warp, int lane, int tid) {
+    const uint32_t par = tag_par(tn), ep16 = tag_ep16(tn);   // tags of this layer's q, K, V (read) and o (written)
     constexpr int LPR = HD / 16;       // lanes per row (16 dims each)
     constexpr int RPI = 32 / LPR;      // rows per warp instruction
     constexpr int NRG = NW * RPI;      // row groups per CTA (direct rows)
@@ -832,19 +1024,44 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
             segm[2 * i + 1] = __int_as_float(__ldcg(P.seg_zp + mi));
         }
         if (u8_fresh && j1 > open_seg * KIE_SEG) {
-            u8_segment_params(P, S, layer, 0, h, tid, fz);
-            u8_segment_params(P, S, layer, 1, h, tid, fz + 2);
+            const int prow = pos % KIE_SEG;
+            u8_segment_params(P, Lc, S, layer, 0, h, prow, ep16, tid, cta, fz);
+            u8_segment_params(P, Lc, S, layer, 1, h, prow, ep16, tid, cta, fz + 2);
             if (j1 == pos + 1) {  // the CTA holding position pos stores the codes for later steps
-                u8_segment_commit(P, layer, 0, h, open_seg, fz, tid);
-                u8_segment_commit(P, layer, 1, h, open_seg, fz + 2, tid);
+                u8_segment_commit(P, Lc, S, layer, 0, h, open_seg, prow, ep16, fz, tid, cta);
+                u8_segment_commit(P, Lc, S, layer, 1, h, open_seg, prow, ep16, fz + 2, tid, cta);
                 fence_proxy_async_global();
             }
         }
         consumer_sync(NCT);
     }
     float qv[16];
+    {
+        const float* qp = P.q + h * HD + dim0;
+        float4 v4[4];
+        uint32_t bad = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) qv[i] = __ldcg(P.q + h * HD + dim0 + i);
+        for (int i = 0; i < 4; ++i) {
+            v4[i] = ld_relaxed_f4(qp + 4 * i);
+            if (!has_tag4(v4[i], par)) bad |= 1u << i;
+        }
+        if (bad) {
+            TagWait tw;
+            do {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if ((bad >> i) & 1u) {
+                        v4[i] = ld_relaxed_f4(qp + 4 * i);
+                        if (has_tag4(v4[i], par)) bad &= ~(1u << i);
+                    }
+                }
+            } while (bad && tw.again(P, Lc, S, cta));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qv[4 * i] = v4[i].x; qv[4 * i + 1] = v4[i].y; qv[4 * i + 2] = v4[i].z; qv[4 * i + 3] = v4[i].w;
+        }
+    }
     // fp16 / E5M2: the only row not streamed through the ring is the current
     // position, [jt, j1) = {pos} when this chunk ends at pos; warp 0's first
     // row group fetches its K and V together with q (one round trip).
@@ -854,8 +1071,8 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     kpos.a = kpos.b = vpos.a = vpos.b = make_uint4(0, 0, 0, 0);
     kpos.sc = vpos.sc = 0.f; kpos.zp = vpos.zp = 0; kpos.mode = vpos.mode = 0;
     if (has_pos && warp == 0 && rw == 0) {
-        load_raw<KVF>(P, layer, 0, h, jt, dim0, 0, kpos);
-        load_raw<KVF>(P, layer, 1, h, jt, dim0, 0, vpos);
+        cur_row<KVF>(P, Lc, S, 0, h, dim0, ep16, cta, kpos);
+        cur_row<KVF>(P, Lc, S, 1, h, dim0, ep16, cta, vpos);
     }
 
     // ---- pass 1: scores, K rows from the ring
@@ -937,7 +1154,8 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
                 const int jj = j0 + r;
                 int mode = 0;
                 if (KVF == KV_U8) mode = u8_fresh ? 2 : 1;
-                load_raw<KVF>(P, layer, 0, h, jj, dim0, mode, kr[u]);
+                if (jj == pos) { cur_row<KVF>(P, Lc, S, 0, h, dim0, ep16, cta, kr[u]); kr[u].mode = mode; }
+                else load_raw<KVF>(P, layer, 0, h, jj, dim0, mode, kr[u]);
             }
         }
 #pragma unroll
@@ -1025,7 +1243,8 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
                 const int jj = j0 + r;
                 int mode = 0;
                 if (KVF == KV_U8) mode = u8_fresh ? 2 : 1;
-                load_raw<KVF>(P, layer, 1, h, jj, dim0, mode, vr[u]);
+                if (jj == pos) { cur_row<KVF>(P, Lc, S, 1, h, dim0, ep16, cta, vr[u]); vr[u].mode = mode; }
+                else load_raw<KVF>(P, layer, 1, h, jj, dim0, mode, vr[u]);
             }
         }
 #pragma unroll
@@ -1078,8 +1297,10 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     // order.  The acq_rel add publishes this block's partial (ordered before it
     // by the barrier above) and, for the last arriver, acquires the others'.
     if (tid == 0) {
+        // the count only grows (zeroed per launch sequence): no reset can race
+        // with the next layer's arrivals
         const uint32_t old = atom_add_acq_rel_gpu(P.head_cnt + h, 1u);
-        S.flags[1] = (old == uint32_t(a.nh) - 1u) ? 1 : 0;
+        S.flags[1] = ((old + 1u) % uint32_t(a.nh) == 0u) ? 1 : 0;
     }
     consumer_sync(NCT);
     if (S.flags[1]) {
@@ -1117,9 +1338,8 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
                 Ls = fmaf(w, __ldcg(pp + 1), Ls);
                 Os = fmaf(w, __ldcg(pp + 4 + tid), Os);
             }
-            P.o[h * HD + tid] = Os / Ls;
+            st_relaxed_f32(P.o + h * HD + tid, tag_f32(Os / Ls, par));
         }
-        if (tid == 0) P.head_cnt[h] = 0u;
     }
     return true;
 }
@@ -1163,7 +1383,10 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
             int layer, sub;
             phase_of(phi, P.L, layer, sub);
             if (sub == 5 && t < Lc.lm_from_step) continue;
-            if (Lc.use_grid_barrier && !first_phase) {
+            // One grid barrier per step, before its first phase: it publishes
+            // the previous step's token and its K/V cache writes (read by this
+            // step's bulk copies).  Inside a step the tags order everything.
+            if (Lc.use_grid_barrier && !first_phase && layer == 0 && sub == 0) {
                 if (!grid_barrier(P, Lc, S, nbar, tid, cta)) return;
             }
             first_phase = false;
@@ -1171,10 +1394,11 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 st_release_cta_shared(&S.flags[4], t * (Lc.phase_end - Lc.phase_begin) + (phi - Lc.phase_begin));
                 stamp(P, Lc, t, phi, 0, cta);
             }
+            const uint32_t tn = tag_seq(P, pos, layer), par = tag_par(tn);
             const float* gains = P.norms + size_t(layer) * 2 * P.d;
             if (sub == 1) {
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!attention<HD, KVF>(P, Lc, S, layer, pos, cta, gc, warp, lane, tid)) return;
+                if (!attention<HD, KVF>(P, Lc, S, layer, pos, tn, cta, gc, warp, lane, tid)) return;
                 if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
             } else {
                 // One call site each for the activation staging, the GEMV and
@@ -1182,40 +1406,39 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 // keeps the per-layer instruction working set small.
                 const int type = sub == 0 ? PH_QKV : sub == 2 ? PH_O : sub == 3 ? PH_GU : sub == 4 ? PH_D : PH_LM;
                 const Cursor c = cursor(P, S, type);
+                // the step's input token: read by the first layer's QKV phase,
+                // and again by its O phase when that phase starts a launch
+                if (layer == 0 && (type == PH_QKV || (type == PH_O && phi == Lc.phase_begin))) {
+                    if (tid == 0) {
+                        int tk = (t == 0 && Lc.first_tok >= 0) ? Lc.first_tok
+                                 : (Lc.forced ? Lc.forced[t] : __ldcg(&P.ctl->tok));
+                        if (tk < 0 || tk >= P.V) { set_error(P, KERR_BAD_TOKEN, tk); tk = 0; }
+                        S.flags[2] = tk;
+                    }
+                    consumer_sync(NCT);
+                    tok = S.flags[2];
+                }
+                const uint16_t* erow = P.emb + size_t(tok) * P.d;   // the residual stream before layer 0
                 if (type == PH_O || type == PH_D) {
-                    act_copy(P, S, type == PH_O ? P.o : P.a, type == PH_O ? P.H * P.hd : P.F, tid);
+                    // o and a carry this layer's parity
+                    act_copy(P, Lc, S, type == PH_O ? P.o : P.a, type == PH_O ? P.H * P.hd : P.F, par, tid, cta);
                 } else {
-                    const float* xs = P.x;
-                    const uint16_t* erow = nullptr;
+                    // x: parity 0 after a D epilogue (QKV, LM), 1 after an O epilogue (GU)
+                    const bool from_emb = type == PH_QKV && layer == 0;
                     const float* g = type == PH_QKV ? gains : type == PH_GU ? gains + P.d
                                                                              : P.norms + size_t(P.L) * 2 * P.d;
-                    if (type == PH_QKV) {
-                        if (layer == 0) {
-                            if (tid == 0) {
-                                int tk = (t == 0 && Lc.first_tok >= 0) ? Lc.first_tok
-                                         : (Lc.forced ? Lc.forced[t] : __ldcg(&P.ctl->tok));
-                                if (tk < 0 || tk >= P.V) { set_error(P, KERR_BAD_TOKEN, tk); tk = 0; }
-                                S.flags[2] = tk;
-                            }
-                            consumer_sync(NCT);
-                            tok = S.flags[2];
-                            erow = P.emb + size_t(tok) * P.d;
-                            xs = nullptr;
-                            // the residual stream starts as the embedding row (each CTA writes a slice)
-                            const int s0 = int((int64_t(cta) * P.d) / P.G), s1 = int((int64_t(cta + 1) * P.d) / P.G);
-                            for (int k = s0 + tid; k < s1; k += NCT) P.x[k] = __half2float(__ushort_as_half(erow[k]));
-                        }
-                        rope_table(P, S, pos, tid);
-                    }
-                    act_scaled(P, S, xs, erow, g, tid);
+                    if (type == PH_QKV) rope_table(P, S, pos, tid);
+                    act_scaled(P, Lc, S, from_emb ? nullptr : P.x, from_emb ? erow : nullptr, g,
+                               type == PH_GU ? 1u : 0u, tid, cta);
                 }
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
                 if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
                 if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                if (type == PH_QKV) epi_qkv(P, S, c, layer, pos, tid);
-                else if (type == PH_GU) epi_swiglu(P, S, c, tid);
+                if (type == PH_QKV) epi_qkv(P, S, c, layer, pos, tn, tid);
+                else if (type == PH_GU) epi_swiglu(P, S, c, par, tid);
                 else if (type == PH_LM) epi_lm(P, Lc, S, c, cta, tid, t, pos);
-                else epi_residual(P, S, c, tid);
+                else if (type == PH_O) epi_residual(P, Lc, S, c, layer == 0 ? erow : nullptr, 0u, 1u, tid, cta);
+                else epi_residual(P, Lc, S, c, nullptr, 1u, 0u, tid, cta);
             }
             if (tid == 0) stamp(P, Lc, t, phi, 3, cta);
         }

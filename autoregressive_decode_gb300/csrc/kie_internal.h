@@ -81,7 +81,8 @@ enum KieErr {
     KERR_TIMEOUT_EMPTY = 3,   // producer wait for a free slot expired
     KERR_BAD_TOKEN = 4,       // input token id out of range
     KERR_SMEM = 5,            // launched with less dynamic shared memory than the layout needs
-    KERR_TIMEOUT_PROGRESS = 6 // producer wait for the consumers' progress expired
+    KERR_TIMEOUT_PROGRESS = 6, // producer wait for the consumers' progress expired
+    KERR_TIMEOUT_DATA = 7     // wait for another CTA's tagged activations expired
 };
 
 // Partition of one GEMV phase type over the grid (identical for every layer).
@@ -127,13 +128,20 @@ struct KieParams {
     uint16_t* tail;              // u8: [L][2][H][SEG][hd] fp16, the open segment
     float* seg_scale;            // u8: [L][2][H][nseg]
     int32_t* seg_zp;             // u8: [L][2][H][nseg]
-    // activations and scratch
+    // Activations passed between CTAs inside a step carry their own validity
+    // tag, so no grid barrier separates the phases of a layer: fp32 vectors
+    // hold a parity bit in the least significant mantissa bit; the current
+    // position's K and V hold (storage bits << 16 | 16-bit epoch).  All of
+    // x .. head_cnt is one contiguous range that is zeroed before every step
+    // sequence (tags 0, counters 0).
     float* x;                    // [d] residual stream
     float* q;                    // [H*hd] rotated query
     float* a;                    // [F] SwiGLU output
     float* o;                    // [H*hd] attention output
+    uint32_t* kcur;              // [H*hd] K of the current position, as stored, tagged
+    uint32_t* vcur;              // [H*hd] V of the current position, as stored, tagged
+    uint32_t* head_cnt;          // [H] arrivals of a head's CTAs at the combine (monotonic)
     float* att_part;             // [G][hd+4] per-CTA attention partial: m, l, -, -, o[hd]
-    uint32_t* head_cnt;          // [H] arrivals of a head's CTAs at the combine
     float* amax_val;             // [G]
     int32_t* amax_idx;           // [G]
     KieControl* ctl;
