@@ -71,7 +71,7 @@ struct Layout {  // byte offsets into the workspace
     size_t wstream, wstream_bytes;
     size_t emb, norms, inv_freq;
     size_t kc, vc, kv_bytes, tail, seg_scale, seg_zp;
-    size_t x, kcur, vcur, head_cnt, zero_bytes, q, a, o, par_bytes, att_part, amax_val, amax_idx, ctl;
+    size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl;
     size_t plan_i32, plan_u32, cta_base, cta_layer;
     size_t out_tokens, out_logits, forced, step_token, step_logits;
     size_t total;
@@ -212,18 +212,17 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.tail = take(u8 ? size_t(c.n_layers) * 2 * H * KIE_SEG * hd * 2 : 0);
     L.seg_scale = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
     L.seg_zp = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
-    // tagged activations and head counters, reset before each launch sequence
-    // (reset_tags): x .. head_cnt to zero, q .. o to one parity
+    // tagged activations, reset before each launch sequence (reset_tags):
+    // x .. vcur to zero, q .. att_part to one parity
     L.x = take(size_t(d) * 4);
     L.kcur = take(size_t(H) * hd * 4);
     L.vcur = take(size_t(H) * hd * 4);
-    L.head_cnt = take(size_t(H) * 4);
-    L.zero_bytes = L.head_cnt + size_t(H) * 4 - L.x;
+    L.zero_bytes = L.vcur + size_t(H) * hd * 4 - L.x;
     L.q = take(size_t(H) * hd * 4);
     L.a = take(size_t(F) * 4);
     L.o = take(size_t(H) * hd * 4);
-    L.par_bytes = L.o + size_t(H) * hd * 4 - L.q;
     L.att_part = take(size_t(G) * (hd + 4) * 4);
+    L.par_bytes = L.att_part + size_t(G) * (hd + 4) * 4 - L.q;
     L.amax_val = take(size_t(G) * 4);
     L.amax_idx = take(size_t(G) * 4);
     L.ctl = take(sizeof(KieControl));
@@ -340,7 +339,8 @@ int tag_fill(const kie_config& c, int pos) {
     return ((int64_t(pos) * c.n_layers + 1) & 1) ? 0x00 : 0x01;
 }
 
-// Reset the tagged activations before a launch sequence starting at pos.
+// Reset the tagged activations before a launch sequence starting at pos
+// (x, kcur, vcur to tag 0; q, a, o, att_part to the parity before the first write).
 cudaError_t reset_tags(const kie_config& c, uint8_t* x, size_t zero_bytes, uint8_t* q, size_t par_bytes, int pos,
                        cudaStream_t s) {
     cudaError_t r = cudaMemsetAsync(x, 0, zero_bytes, s);
@@ -378,7 +378,7 @@ kie_status ensure_graph(kie_engine* e, int fill) {
     cudaError_t r = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
     if (r != cudaSuccess) { cudaStreamDestroy(cap); return fail(e, KIE_ERR_CUDA, "begin capture: %s", cudaGetErrorString(r)); }
     const int P_ = 5 * e->cfg.n_layers + 1;
-    // every step starts from reset activation tags and head counters
+    // every step starts from reset activation tags
     r = cudaMemsetAsync(e->dev(e->lay.x), 0, e->lay.zero_bytes, cap);
     if (r == cudaSuccess) r = cudaMemsetAsync(e->dev(e->lay.q), fill, e->lay.par_bytes, cap);
     for (int phi = 0; phi < P_ && r == cudaSuccess; ++phi) {
@@ -562,7 +562,6 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     P.kcur = reinterpret_cast<uint32_t*>(e->dev(L.kcur));
     P.vcur = reinterpret_cast<uint32_t*>(e->dev(L.vcur));
     P.att_part = reinterpret_cast<float*>(e->dev(L.att_part));
-    P.head_cnt = reinterpret_cast<uint32_t*>(e->dev(L.head_cnt));
     P.amax_val = reinterpret_cast<float*>(e->dev(L.amax_val));
     P.amax_idx = reinterpret_cast<int32_t*>(e->dev(L.amax_idx));
     P.ctl = reinterpret_cast<KieControl*>(e->dev(L.ctl));
@@ -1064,7 +1063,7 @@ static __device__ __align__(256) uint8_t kie_static_scratch[KIE_STATIC_SCRATCH_B
 namespace {
 
 struct StaticScratchLayout {
-    size_t x, kcur, vcur, head_cnt, zero_bytes, q, a, o, par_bytes, att_part, amax_val, amax_idx, ctl, total;
+    size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl, total;
 };
 
 StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
@@ -1072,17 +1071,16 @@ StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
     const size_t hq = size_t(c.n_heads) * c.head_dim * 4;
-    // tagged activations and head counters, reset per step as in the engine's workspace
+    // tagged activations, reset per step as in the engine's workspace
     l.x = take(size_t(c.d_model) * 4);
     l.kcur = take(hq);
     l.vcur = take(hq);
-    l.head_cnt = take(size_t(c.n_heads) * 4);
-    l.zero_bytes = l.head_cnt + size_t(c.n_heads) * 4 - l.x;
+    l.zero_bytes = l.vcur + hq - l.x;
     l.q = take(hq);
     l.a = take(size_t(c.ffn_dim) * 4);
     l.o = take(hq);
-    l.par_bytes = l.o + hq - l.q;
     l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
+    l.par_bytes = l.att_part + size_t(G) * (c.head_dim + 4) * 4 - l.q;
     l.amax_val = take(size_t(G) * 4);
     l.amax_idx = take(size_t(G) * 4);
     l.ctl = take(sizeof(KieControl));
@@ -1130,9 +1128,9 @@ extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t toke
     cudaError_t r = static_scratch_ptr(e->cfg.device, &base);
     if (r != cudaSuccess) return fail(e, KIE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(r));
     uint8_t* b = static_cast<uint8_t*>(base);
-    // the control block (barrier count, error word, argmax arrivals), the
-    // activation tags and the head counters must start at zero; everything
-    // else is written before it is read
+    // the control block (barrier count, error word, argmax arrivals) starts at
+    // zero and the activation tags are reset; everything else is written
+    // before it is read
     KIE_CUDA(e, cudaMemsetAsync(b + sl.ctl, 0, sizeof(KieControl), e->stream));
     KIE_CUDA(e, reset_tags(e->cfg, b + sl.x, sl.zero_bytes, b + sl.q, sl.par_bytes, e->pos, e->stream));
     KieParams P = e->P;
@@ -1143,7 +1141,6 @@ extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t toke
     P.kcur = reinterpret_cast<uint32_t*>(b + sl.kcur);
     P.vcur = reinterpret_cast<uint32_t*>(b + sl.vcur);
     P.att_part = reinterpret_cast<float*>(b + sl.att_part);
-    P.head_cnt = reinterpret_cast<uint32_t*>(b + sl.head_cnt);
     P.amax_val = reinterpret_cast<float*>(b + sl.amax_val);
     P.amax_idx = reinterpret_cast<int32_t*>(b + sl.amax_idx);
     P.ctl = reinterpret_cast<KieControl*>(b + sl.ctl);

@@ -16,6 +16,8 @@
 //    activations, so HBM keeps streaming while consumers wait at barriers,
 //    normalise, do attention or reduce (beta == 1: every weight byte is read
 //    exactly once per token).
+#include <cfloat>
+
 #include "kie_device.cuh"
 #include "kie_internal.h"
 
@@ -34,14 +36,18 @@ constexpr int NCT = NW * 32;  // consumer threads
 // issued, and q+2 cannot be issued before this consumer releases q.  With a
 // single barrier per slot a consumer could arrive while generation q-1 is still
 // in flight, and the parity of q would then name an already completed phase.
-// Slot j of a phase goes to consumer warp j % NW, and every phase (and each
-// attention pass) starts after a consumer-wide barrier, so all slots of earlier
-// phases have landed.  The claim about q-2 then holds when nslot >= NW: for
-// j < NW, g - 2*nslot lies in an earlier phase; for j >= NW the warp's previous
-// slot g - NW landed, so every index <= g - NW was issued and every index
-// <= g - NW - nslot was released (landed), g - 2*nslot among them.
-// "empty[s]" completes once per release, in generation order (the producer
-// re-arms a slot only after its release), so one barrier suffices there.
+// Slot j of a phase goes to consumer warp j % NW, and every phase starts after
+// a consumer-wide barrier, so all slots of earlier phases have landed.  The
+// claim about q-2 then holds when nslot >= NW: for j < NW, g - 2*nslot lies in
+// an earlier phase; for j >= NW the warp's previous slot g - NW landed, so every
+// index <= g - NW was issued and every index <= g - NW - nslot was released
+// (landed), g - 2*nslot among them.  Attention's last partial round is shared
+// by all warps: before such a slot g a warp has waited for g - 1 (an earlier
+// shared slot) or for its own last slot, at most NW before g; either way
+// g - nslot was issued, so g - 2*nslot was released.
+// "empty[s]" completes once per release (NW arrivals: the slot's warp arrives
+// with count NW, each warp of a shared slot with 1), in generation order (the
+// producer re-arms a slot only after its release), so one barrier suffices.
 struct Smem {
     uint64_t* full;
     uint64_t* empty;
@@ -245,9 +251,9 @@ __device__ __forceinline__ size_t meta_index(const KieParams& P, int layer, int 
 // Attention work: head h owns CTAs [c0(h), c0(h+1)) with c0(h) = floor(h*G/H);
 // CTA k of them takes positions [floor(k*C/n_h), floor((k+1)*C/n_h)) of the C
 // attended ones.  Rows [j0, jt) were written in earlier steps and reach shared
-// memory through the weight ring (K slots, then V slots); rows [jt, j1) (the
-// current position, and for a uint8 cache the open segment kept in fp16) are
-// read directly after the grid barrier.
+// memory through the weight ring, K and V of the same rows in one slot; rows
+// [jt, j1) (the current position, and for a uint8 cache the open segment kept
+// in fp16) are read directly.
 struct AttChunk {
     int h, c0, nh, j0, j1, jt;
 };
@@ -265,14 +271,17 @@ __device__ __forceinline__ AttChunk att_chunk(const KieParams& P, int cta, int p
     return a;
 }
 __device__ __forceinline__ int att_row_bytes(const KieParams& P) { return P.hd * (P.kv == KV_F16 ? 2 : 1); }
-// Rows per K (or V) slot: the chunk's streamed rows spread over all consumer
-// warps (at least 8 rows, at most one full slot).
+// Rows per slot (its K rows, then the same rows of V at offset rows * row bytes):
+// a chunk that fits one slot per consumer warp is spread over them (at least 8
+// rows a slot); a longer one uses full slots (half a slot of K, half of V),
+// whole rounds of them one per warp and the last partial round shared by all.
 __device__ __forceinline__ int att_rows_per_slot(const KieParams& P, const AttChunk& a) {
-    const int full = KIE_SLOT_BYTES / att_row_bytes(P);
-    const int spread = (a.jt - a.j0 + NW - 1) / NW;
-    return min(full, max(8, spread));
+    const int full = KIE_SLOT_BYTES / (2 * att_row_bytes(P));
+    const int nt = a.jt - a.j0;
+    if (nt > NW * full) return full;
+    return min(full, max(8, (nt + NW - 1) / NW));
 }
-__device__ __forceinline__ uint32_t att_kslots(const KieParams& P, const AttChunk& a) {
+__device__ __forceinline__ uint32_t att_nslots(const KieParams& P, const AttChunk& a) {
     const int rps = att_rows_per_slot(P, a);
     return uint32_t((a.jt - a.j0 + rps - 1) / rps);
 }
@@ -353,20 +362,20 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 }
                 const int pos = pos0 + t;
                 const AttChunk a = att_chunk(P, cta, pos);
-                const uint32_t nks = att_kslots(P, a);
+                const uint32_t nsl = att_nslots(P, a);
                 const int rps = att_rows_per_slot(P, a), rb = att_row_bytes(P);
-                for (uint32_t j = 0; j < 2 * nks && !abort; ++j, ++g) {
+                for (uint32_t j = 0; j < nsl && !abort; ++j, ++g) {
                     const uint32_t slot = g % nslot;
                     if (!producer_wait_empty(P, Lc, S, g, cta)) { abort = true; break; }
-                    const int kv = j >= nks ? 1 : 0;
-                    const int r0 = int(j - uint32_t(kv) * nks) * rps;
+                    const int r0 = int(j) * rps;
                     const int rows = min(rps, a.jt - a.j0 - r0);
-                    const uint8_t* base = kv ? P.vc : P.kc;
-                    const uint8_t* src = base + (kv_elem_index(P, layer, a.h, a.j0 + r0)) * size_t(rb / P.hd);
+                    const size_t off = kv_elem_index(P, layer, a.h, a.j0 + r0) * size_t(rb / P.hd);
                     const uint32_t bytes = uint32_t(rows * rb);
                     uint64_t* fb = &S.full[2 * slot + ((g / nslot) & 1u)];
-                    mbar_arrive_expect_tx(fb, bytes);
-                    bulk_g2s(S.ring + size_t(slot) * KIE_SLOT_BYTES, src, bytes, fb, pol_kv);
+                    uint8_t* dst = S.ring + size_t(slot) * KIE_SLOT_BYTES;
+                    mbar_arrive_expect_tx(fb, 2u * bytes);
+                    bulk_g2s(dst, P.kc + off, bytes, fb, pol_kv);
+                    bulk_g2s(dst + size_t(rps) * rb, P.vc + off, bytes, fb, pol_kv);
                     slot_stamp(Lc, cta, g, 0);
                 }
                 continue;
@@ -656,7 +665,7 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
         __syncwarp();
         if (lane == 0) {
             slot_stamp(Lc, cta, gidx, 2);
-            mbar_arrive(&S.empty[slot]);
+            mbar_arrive_cnt(&S.empty[slot], NW);
         }
     }
     gc += c.nslots;
@@ -995,22 +1004,39 @@ __device__ __forceinline__ void smem_row16(const uint8_t* row, int dim0, float s
     }
 }
 
+// Online-softmax state of one lane: running max m, sum l and weighted V sum of
+// its 16 dims over the rows its row group has seen.
+struct SoftState {
+    float m, l, acc[16];
+};
+// Fold one row (score s, V dims v) into the state.
+__device__ __forceinline__ void soft_row(SoftState& st, float s, const float* v) {
+    const float mn = fmaxf(st.m, s);
+    const float cf = expf(st.m - mn), p = expf(s - mn);   // st.m = -inf: cf = 0
+    st.l = fmaf(st.l, cf, p);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(st.acc[i], cf, p * v[i]);
+    st.m = mn;
+}
+
 template <int HD, int KVF>
 __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S, int layer, int pos, uint32_t tn,
                           int cta, uint32_t& gc, int warp, int lane, int tid) {
     const uint32_t par = tag_par(tn), ep16 = tag_ep16(tn);   // tags of this layer's q, K, V (read) and o (written)
     constexpr int LPR = HD / 16;       // lanes per row (16 dims each)
-    constexpr int RPI = 32 / LPR;      // rows per warp instruction
+    constexpr int RPI = 32 / LPR;      // row groups of a warp (rows per warp instruction)
     constexpr int NRG = NW * RPI;      // row groups per CTA (direct rows)
     constexpr int UR = 4;              // direct rows in flight per lane group
+    constexpr int RB = HD * (KVF == KV_F16 ? 2 : 1);
+    constexpr int RMAX = KIE_SLOT_BYTES / (2 * RB * RPI);   // rows of one row group in a slot
+    constexpr int RU = 4;              // ring rows in flight per row group
     const AttChunk a = att_chunk(P, cta, pos);
     const int h = a.h, j0 = a.j0, j1 = a.j1, jt = a.jt;
     const int n = j1 - j0, nt = jt - j0;
     const int lg = lane % LPR, rw = lane / LPR;
     const int dim0 = lg * 16;
-    const int rps = att_rows_per_slot(P, a), rb = att_row_bytes(P);
-    const uint32_t nks = att_kslots(P, a), nslot = uint32_t(P.nslot);
-    float* scores = S.act;
+    const int rps = att_rows_per_slot(P, a);
+    const uint32_t nsl = att_nslots(P, a), nslot = uint32_t(P.nslot);
     float* fz = S.red + NW * (KIE_MAX_HEAD_DIM + 2);   // [0..1] K scale/zp, [2..3] V scale/zp (fresh segment)
     float* segm = S.part;                              // uint8: per-segment scale/zp of this chunk [2][nseg][2]
     const bool u8_fresh = (KVF == KV_U8) && (pos % KIE_SEG == KIE_SEG - 1);
@@ -1059,47 +1085,68 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            qv[4 * i] = v4[i].x; qv[4 * i + 1] = v4[i].y; qv[4 * i + 2] = v4[i].z; qv[4 * i + 3] = v4[i].w;
+            qv[4 * i] = v4[i].x * P.attn_scale; qv[4 * i + 1] = v4[i].y * P.attn_scale;
+            qv[4 * i + 2] = v4[i].z * P.attn_scale; qv[4 * i + 3] = v4[i].w * P.attn_scale;
         }
     }
-    // fp16 / E5M2: the only row not streamed through the ring is the current
-    // position, [jt, j1) = {pos} when this chunk ends at pos; warp 0's first
-    // row group fetches its K and V together with q (one round trip).
-    constexpr bool ONE_DIRECT = (KVF != KV_U8);
-    const bool has_pos = ONE_DIRECT && (j1 > jt);
+    // The current position is the last row of the head's last chunk; warp 0's
+    // first row group fetches its tagged K and V together with q.  fp16 / E5M2
+    // stream every other row through the ring; a uint8 cache reads the rest of
+    // its open segment directly (mode 1: fp16 tail; mode 2: the segment
+    // completes in this step and is quantised with its fresh scale / zp).
+    const int dmode = (KVF == KV_U8) ? (u8_fresh ? 2 : 1) : 0;
+    const bool has_pos = (j1 == pos + 1);
+    const int ndir = has_pos ? n - 1 : n;        // direct rows other than pos: [nt, ndir)
     RawRow kpos, vpos;
     kpos.a = kpos.b = vpos.a = vpos.b = make_uint4(0, 0, 0, 0);
-    kpos.sc = vpos.sc = 0.f; kpos.zp = vpos.zp = 0; kpos.mode = vpos.mode = 0;
+    kpos.sc = vpos.sc = 0.f; kpos.zp = vpos.zp = 0; kpos.mode = vpos.mode = dmode;
     if (has_pos && warp == 0 && rw == 0) {
         cur_row<KVF>(P, Lc, S, 0, h, dim0, ep16, cta, kpos);
         cur_row<KVF>(P, Lc, S, 1, h, dim0, ep16, cta, vpos);
+        kpos.mode = vpos.mode = dmode;
     }
 
-    // ---- pass 1: scores, K rows from the ring
-    float mloc = -INFINITY;
+    SoftState st;
+    st.m = -INFINITY;
+    st.l = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) st.acc[i] = 0.f;
+
+    // ---- ring slots: slot j holds rows [j*rps, j*rps + rs) of the chunk, K
+    // then V.  The first nrr (whole rounds) go to warp j % NW, whose row groups
+    // take rows rw, rw + RPI, ...; each slot of the last partial round is
+    // shared by all warps (row group rw of warp w takes rows w*RPI + rw + k*NRG).
+    // Each row group keeps its own online softmax.
     bool ok = true;
-    const uint32_t first = uint32_t(warp);   // slot j of a phase -> warp j % NW (mode independent)
-    for (uint32_t j = first; j < nks; j += NW) {
+    const uint32_t nrr = (nsl / NW) * NW, nmine = nrr / NW + (nsl - nrr);
+    for (uint32_t i = 0; i < nmine; ++i) {
+        const bool shared = i >= nrr / NW;
+        const uint32_t j = shared ? nrr + (i - nrr / NW) : uint32_t(warp) + i * NW;
+        const int rbase = shared ? warp * RPI : 0, rstr = shared ? NRG : RPI;
         const uint32_t gidx = gc + j, slot = gidx % nslot;
         if (!warp_wait_full(P, Lc, S, gidx, cta, lane)) { ok = false; break; }
         if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
-        const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
+        const uint8_t* ks = S.ring + size_t(slot) * KIE_SLOT_BYTES;
+        const uint8_t* vs = ks + size_t(rps) * RB;
         const int r0 = int(j) * rps, rs = min(rps, nt - r0);
-        constexpr int RU = 4;                           // rows per lane group per iteration
-        for (int ib = 0; ib < rs; ib += RPI * RU) {     // uniform over the warp
+        float sc[RMAX];
+        float mloc = -INFINITY;
+#pragma unroll
+        for (int k0 = 0; k0 < RMAX; k0 += RU) {
+            if (rbase + k0 * rstr >= rs) break;         // uniform over the warp
             float dsum[RU];
 #pragma unroll
             for (int u = 0; u < RU; ++u) {
-                const int rl = ib + rw + u * RPI;
+                const int rl = rbase + rw + (k0 + u) * rstr;
                 float kf[16];
-                float sc = 0.f;
+                float scl = 0.f;
                 int zp = 0;
                 if (KVF == KV_U8 && rl < rs) {
                     const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
-                    sc = segm[2 * sg];
+                    scl = segm[2 * sg];
                     zp = __float_as_int(segm[2 * sg + 1]);
                 }
-                smem_row16<KVF>(sl + size_t(min(rl, rs - 1)) * rb, dim0, sc, zp, kf);
+                smem_row16<KVF>(ks + size_t(min(rl, rs - 1)) * RB, dim0, scl, zp, kf);
                 float d0 = 0.f, d1 = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) { d0 = fmaf(qv[i], kf[i], d0); d1 = fmaf(qv[i + 1], kf[i + 1], d1); }
@@ -1112,50 +1159,78 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
             }
 #pragma unroll
             for (int u = 0; u < RU; ++u) {
-                const int rl = ib + rw + u * RPI;
-                if (rl < rs) {
-                    const float s = dsum[u] * P.attn_scale;
-                    if (lg == 0) scores[r0 + rl] = s;
-                    mloc = fmaxf(mloc, s);
+                const int rl = rbase + rw + (k0 + u) * rstr;
+                sc[k0 + u] = rl < rs ? dsum[u] : -INFINITY;
+                mloc = fmaxf(mloc, sc[k0 + u]);
+            }
+        }
+        // V rows of the same slot (no shuffles: row groups may diverge)
+        const float mn = fmaxf(st.m, mloc);
+        if (mn > -INFINITY) {
+            const float cf = expf(st.m - mn);
+            st.l *= cf;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) st.acc[i] *= cf;
+#pragma unroll
+            for (int k0 = 0; k0 < RMAX; k0 += RU) {
+                if (rbase + k0 * rstr >= rs) break;
+#pragma unroll
+                for (int u = 0; u < RU; ++u) {
+                    const int rl = rbase + rw + (k0 + u) * rstr;
+                    if (rl < rs) {
+                        float vf[16];
+                        float scl = 0.f;
+                        int zp = 0;
+                        if (KVF == KV_U8) {
+                            const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
+                            scl = segm[2 * (nsegc + sg)];
+                            zp = __float_as_int(segm[2 * (nsegc + sg) + 1]);
+                        }
+                        smem_row16<KVF>(vs + size_t(rl) * RB, dim0, scl, zp, vf);
+                        const float p = expf(sc[k0 + u] - mn);
+                        st.l += p;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(p, vf[i], st.acc[i]);
+                    }
                 }
             }
+            st.m = mn;
         }
         __syncwarp();
         if (lane == 0) {
             slot_stamp(Lc, cta, gidx, 2);
-            mbar_arrive(&S.empty[slot]);
+            mbar_arrive_cnt(&S.empty[slot], shared ? 1u : uint32_t(NW));
         }
     }
-    // direct rows [jt, j1)
-    if (ONE_DIRECT) {
-        if (has_pos && warp == 0) {                     // uniform over warp 0
-            float kf[16];
-            convert_row<KVF>(kpos, fz, kf);
-            float dsum = 0.f;
+    gc += nsl;
+    if (!ok) S.flags[0] = 1;
+
+    // ---- direct rows [jt, j1)
+    if (has_pos && warp == 0) {                         // uniform over warp 0
+        float kf[16];
+        convert_row<KVF>(kpos, fz, kf);
+        float dsum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dsum = fmaf(qv[i], kf[i], dsum);
+        for (int i = 0; i < 16; ++i) dsum = fmaf(qv[i], kf[i], dsum);
 #pragma unroll
-            for (int o = 1; o < LPR; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-            if (rw == 0) {
-                const float sc = dsum * P.attn_scale;
-                if (lg == 0) scores[nt] = sc;
-                mloc = fmaxf(mloc, sc);
-            }
+        for (int o = 1; o < LPR; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+        if (rw == 0) {
+            float vf[16];
+            convert_row<KVF>(vpos, fz + 2, vf);
+            soft_row(st, dsum, vf);
         }
-    } else
-    for (int base = nt + warp * RPI; base < n; base += NRG * UR) {
-        RawRow kr[UR];
+    }
+    if (KVF == KV_U8)
+    for (int base = nt + warp * RPI; base < ndir; base += NRG * UR) {
+        RawRow kr[UR], vr[UR];
 #pragma unroll
         for (int u = 0; u < UR; ++u) {
             const int r = base + rw + u * NRG;
-            kr[u].a = kr[u].b = make_uint4(0, 0, 0, 0);
-            kr[u].sc = 0.f; kr[u].zp = 0; kr[u].mode = 0;
-            if (r < n) {
-                const int jj = j0 + r;
-                int mode = 0;
-                if (KVF == KV_U8) mode = u8_fresh ? 2 : 1;
-                if (jj == pos) { cur_row<KVF>(P, Lc, S, 0, h, dim0, ep16, cta, kr[u]); kr[u].mode = mode; }
-                else load_raw<KVF>(P, layer, 0, h, jj, dim0, mode, kr[u]);
+            kr[u].a = kr[u].b = vr[u].a = vr[u].b = make_uint4(0, 0, 0, 0);
+            kr[u].sc = vr[u].sc = 0.f; kr[u].zp = vr[u].zp = 0; kr[u].mode = vr[u].mode = 0;
+            if (r < ndir) {
+                load_raw<KVF>(P, layer, 0, h, j0 + r, dim0, dmode, kr[u]);
+                load_raw<KVF>(P, layer, 1, h, j0 + r, dim0, dmode, vr[u]);
             }
         }
 #pragma unroll
@@ -1168,178 +1243,107 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
             for (int i = 0; i < 16; ++i) dsum = fmaf(qv[i], kf[i], dsum);
 #pragma unroll
             for (int o = 1; o < LPR; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-            if (r < n) {
-                const float s = dsum * P.attn_scale;
-                if (lg == 0) scores[r] = s;
-                mloc = fmaxf(mloc, s);
-            }
-        }
-    }
-    gc += nks;
-    if (!ok) S.flags[0] = 1;
-    const float m = block_max(mloc, S.red, tid);
-    if (ld_volatile_i32(&S.flags[0]) != 0) return false;
-
-    // ---- pass 2: p = exp(s - m), l = sum p, o = sum p v
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    float lsum = 0.f;
-    const uint32_t first2 = uint32_t(warp);
-    for (uint32_t j = first2; j < nks; j += NW) {
-        const uint32_t gidx = gc + j, slot = gidx % nslot;
-        if (!warp_wait_full(P, Lc, S, gidx, cta, lane)) { ok = false; break; }
-        if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
-        const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
-        const int r0 = int(j) * rps, rs = min(rps, nt - r0);
-        constexpr int RU2 = 2;
-        for (int ib = rw; ib < rs; ib += RPI * RU2) {    // no shuffles inside: lanes may diverge
-            float pr[RU2];
-            float vf[RU2][16];
-#pragma unroll
-            for (int u = 0; u < RU2; ++u) {
-                const int rl = ib + u * RPI;
-                float sc = 0.f;
-                int zp = 0;
-                if (KVF == KV_U8 && rl < rs) {
-                    const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
-                    sc = segm[2 * (nsegc + sg)];
-                    zp = __float_as_int(segm[2 * (nsegc + sg) + 1]);
-                }
-                smem_row16<KVF>(sl + size_t(min(rl, rs - 1)) * rb, dim0, sc, zp, vf[u]);
-                pr[u] = rl < rs ? expf(scores[r0 + rl] - m) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < RU2; ++u) {
-                lsum += pr[u];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = fmaf(pr[u], vf[u][i], acc[i]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) {
-            slot_stamp(Lc, cta, gidx, 2);
-            mbar_arrive(&S.empty[slot]);
-        }
-    }
-    if (ONE_DIRECT) {
-        if (has_pos && warp == 0 && rw == 0) {
-            float vf[16];
-            convert_row<KVF>(vpos, fz + 2, vf);
-            const float pr = expf(scores[nt] - m);
-            lsum += pr;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = fmaf(pr, vf[i], acc[i]);
-        }
-    } else
-    for (int base = nt + warp * RPI; base < n; base += NRG * UR) {
-        RawRow vr[UR];
-#pragma unroll
-        for (int u = 0; u < UR; ++u) {
-            const int r = base + rw + u * NRG;
-            vr[u].a = vr[u].b = make_uint4(0, 0, 0, 0);
-            vr[u].sc = 0.f; vr[u].zp = 0; vr[u].mode = 0;
-            if (r < n) {
-                const int jj = j0 + r;
-                int mode = 0;
-                if (KVF == KV_U8) mode = u8_fresh ? 2 : 1;
-                if (jj == pos) { cur_row<KVF>(P, Lc, S, 1, h, dim0, ep16, cta, vr[u]); vr[u].mode = mode; }
-                else load_raw<KVF>(P, layer, 1, h, jj, dim0, mode, vr[u]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < UR; ++u) {
-            const int r = base + rw + u * NRG;
-            if (r < n) {
+            if (r < ndir) {
                 float vf[16];
                 convert_row<KVF>(vr[u], fz + 2, vf);
-                const float pr = expf(scores[r] - m);
-                lsum += pr;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = fmaf(pr, vf[i], acc[i]);
+                soft_row(st, dsum, vf);
             }
         }
     }
-    gc += nks;
-    if (!ok) S.flags[0] = 1;
-    // reduce over the row groups of this warp (lanes with equal lg)
+
+    // ---- merge the row groups of this warp (lanes with equal lg), then the warps
 #pragma unroll
     for (int o = LPR; o < 32; o <<= 1) {
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        const float mo = __shfl_xor_sync(0xffffffffu, st.m, o), lo = __shfl_xor_sync(0xffffffffu, st.l, o);
+        const float mn = fmaxf(st.m, mo);
+        const float c1 = (st.m == -INFINITY) ? 0.f : expf(st.m - mn);
+        const float c2 = (mo == -INFINITY) ? 0.f : expf(mo - mn);
+        st.l = st.l * c1 + lo * c2;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+        for (int i = 0; i < 16; ++i) st.acc[i] = st.acc[i] * c1 + __shfl_xor_sync(0xffffffffu, st.acc[i], o) * c2;
+        st.m = mn;
     }
     float* wp = S.red + warp * (KIE_MAX_HEAD_DIM + 2);
-    consumer_sync(NCT);   // block_max's scratch (S.red[0..NW)) is free again
     if (lane < LPR) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) wp[2 + dim0 + i] = acc[i];
-        if (lane == 0) wp[0] = lsum;
+        for (int i = 0; i < 16; ++i) wp[2 + dim0 + i] = st.acc[i];
+        if (lane == 0) { wp[0] = st.m; wp[1] = st.l; }
     }
     consumer_sync(NCT);
     if (ld_volatile_i32(&S.flags[0]) != 0) return false;
-    // partial (m, l, o[HD]) of this CTA's chunk
+    // this CTA's partial (m, l, o[HD]), tagged with the layer's parity; an empty
+    // chunk stores m = -FLT_MAX (finite, so the tag bit cannot make it a NaN)
     float* gp = P.att_part + size_t(cta) * (HD + 4);
     if (tid < HD) {
-        float sacc = 0.f;
+        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) sacc += S.red[w * (KIE_MAX_HEAD_DIM + 2) + 2 + tid];
-        gp[4 + tid] = sacc;
-    } else if (tid == HD) {
-        float l = 0.f;
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, S.red[w * (KIE_MAX_HEAD_DIM + 2)]);
+        float ov = 0.f, lv = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) l += S.red[w * (KIE_MAX_HEAD_DIM + 2)];
-        gp[0] = m;
-        gp[1] = l;
+        for (int w = 0; w < NW; ++w) {
+            const float* ww = S.red + w * (KIE_MAX_HEAD_DIM + 2);
+            const float e = (ww[0] == -INFINITY) ? 0.f : expf(ww[0] - M);
+            ov = fmaf(e, ww[2 + tid], ov);
+            lv = fmaf(e, ww[1], lv);
+        }
+        st_relaxed_f32(gp + 4 + tid, tag_f32(ov, par));
+        if (tid == 0) {
+            st_relaxed_f32(gp, tag_f32(M == -INFINITY ? -FLT_MAX : M, par));
+            st_relaxed_f32(gp + 1, tag_f32(lv, par));
+        }
     }
-    consumer_sync(NCT);
-    // The last of head h's CTAs to arrive combines the head's partials in CTA
-    // order.  The acq_rel add publishes this block's partial (ordered before it
-    // by the barrier above) and, for the last arriver, acquires the others'.
-    if (tid == 0) {
-        // the count only grows (zeroed per launch sequence): no reset can race
-        // with the next layer's arrivals
-        const uint32_t old = atom_add_acq_rel_gpu(P.head_cnt + h, 1u);
-        S.flags[1] = ((old + 1u) % uint32_t(a.nh) == 0u) ? 1 : 0;
-    }
-    consumer_sync(NCT);
-    if (S.flags[1]) {
-        if (tid < HD) {
-            // every contributor's (m, l, o[tid]) requested in one wave
-            constexpr int MAXC = 10;
-            const int cnt = a.nh;
+    // The head's first CTA combines its CTAs' partials in CTA order (the same
+    // in every mode) and publishes o_h with the layer's parity.
+    if (cta == a.c0 && tid < HD) {
+        constexpr int MAXC = 10;
+        float M = -INFINITY, Ls = 0.f, Os = 0.f;
+        for (int k0 = 0; k0 < a.nh; k0 += MAXC) {
             float mk[MAXC], lk[MAXC], ok[MAXC];
+            uint32_t bad = 0;
 #pragma unroll
             for (int k = 0; k < MAXC; ++k) {
-                if (k < cnt) {
-                    const float* pp = P.att_part + size_t(a.c0 + k) * (HD + 4);
-                    mk[k] = __ldcg(pp);
-                    lk[k] = __ldcg(pp + 1);
-                    ok[k] = __ldcg(pp + 4 + tid);
+                if (k0 + k < a.nh) {
+                    const float* pp = P.att_part + size_t(a.c0 + k0 + k) * (HD + 4);
+                    mk[k] = ld_relaxed_f32(pp);
+                    lk[k] = ld_relaxed_f32(pp + 1);
+                    ok[k] = ld_relaxed_f32(pp + 4 + tid);
+                    if (((__float_as_uint(mk[k]) ^ par) | (__float_as_uint(lk[k]) ^ par) |
+                         (__float_as_uint(ok[k]) ^ par)) & 1u) bad |= 1u << k;
                 }
             }
-            float M = -INFINITY;
+            if (bad) {
+                TagWait tw;
+                do {
 #pragma unroll
-            for (int k = 0; k < MAXC; ++k) if (k < cnt) M = fmaxf(M, mk[k]);
-            for (int k = MAXC; k < cnt; ++k) M = fmaxf(M, __ldcg(P.att_part + size_t(a.c0 + k) * (HD + 4)));
-            float Ls = 0.f, Os = 0.f;
+                    for (int k = 0; k < MAXC; ++k) {
+                        if ((bad >> k) & 1u) {
+                            const float* pp = P.att_part + size_t(a.c0 + k0 + k) * (HD + 4);
+                            mk[k] = ld_relaxed_f32(pp);
+                            lk[k] = ld_relaxed_f32(pp + 1);
+                            ok[k] = ld_relaxed_f32(pp + 4 + tid);
+                            if ((((__float_as_uint(mk[k]) ^ par) | (__float_as_uint(lk[k]) ^ par) |
+                                  (__float_as_uint(ok[k]) ^ par)) & 1u) == 0u) bad &= ~(1u << k);
+                        }
+                    }
+                } while (bad && tw.again(P, Lc, S, cta));
+            }
+            float Mb = M;
+#pragma unroll
+            for (int k = 0; k < MAXC; ++k) if (k0 + k < a.nh) Mb = fmaxf(Mb, mk[k]);
+            const float cf = (M == -INFINITY) ? 0.f : expf(M - Mb);
+            Ls *= cf;
+            Os *= cf;
 #pragma unroll
             for (int k = 0; k < MAXC; ++k) {
-                if (k < cnt) {
-                    const float w = (mk[k] == -INFINITY) ? 0.f : expf(mk[k] - M);   // empty chunk
+                if (k0 + k < a.nh) {
+                    const float w = expf(mk[k] - Mb);          // -FLT_MAX (empty chunk): 0
                     Ls = fmaf(w, lk[k], Ls);
                     Os = fmaf(w, ok[k], Os);
                 }
             }
-            for (int k = MAXC; k < cnt; ++k) {
-                const float* pp = P.att_part + size_t(a.c0 + k) * (HD + 4);
-                const float mm = __ldcg(pp);
-                const float w = (mm == -INFINITY) ? 0.f : expf(mm - M);
-                Ls = fmaf(w, __ldcg(pp + 1), Ls);
-                Os = fmaf(w, __ldcg(pp + 4 + tid), Os);
-            }
-            st_relaxed_f32(P.o + h * HD + tid, tag_f32(Os / Ls, par));
+            M = Mb;
         }
+        st_relaxed_f32(P.o + h * HD + tid, tag_f32(Os / Ls, par));
     }
     return true;
 }
@@ -1464,7 +1468,7 @@ __global__ void __launch_bounds__(KIE_THREADS, 1) kie_decode_kernel(const KiePar
         for (int i = 0; i < P.nslot; ++i) {
             mbar_init(&S.full[2 * i], 1);
             mbar_init(&S.full[2 * i + 1], 1);
-            mbar_init(&S.empty[i], 1);
+            mbar_init(&S.empty[i], NW);   // a slot's user arrives with NW, or each warp of a shared slot with 1
         }
         S.flags[0] = 0;
         S.flags[1] = 0;

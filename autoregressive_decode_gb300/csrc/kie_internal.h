@@ -131,16 +131,15 @@ struct KieParams {
     // Activations passed between CTAs inside a step carry their own validity
     // tag, so no grid barrier separates the phases of a layer: fp32 vectors
     // hold a parity bit in the least significant mantissa bit; the current
-    // position's K and V hold (storage bits << 16 | 16-bit epoch).  All of
-    // x .. head_cnt is one contiguous range that is zeroed before every step
-    // sequence (tags 0, counters 0).
+    // position's K and V hold (storage bits << 16 | 16-bit epoch).  The host
+    // resets x, kcur, vcur (to zero) and q, a, o, att_part (to one parity)
+    // before every launch sequence.
     float* x;                    // [d] residual stream
+    uint32_t* kcur;              // [H*hd] K of the current position, as stored, tagged
+    uint32_t* vcur;              // [H*hd] V of the current position, as stored, tagged
     float* q;                    // [H*hd] rotated query
     float* a;                    // [F] SwiGLU output
     float* o;                    // [H*hd] attention output
-    uint32_t* kcur;              // [H*hd] K of the current position, as stored, tagged
-    uint32_t* vcur;              // [H*hd] V of the current position, as stored, tagged
-    uint32_t* head_cnt;          // [H] arrivals of a head's CTAs at the combine (monotonic)
     float* att_part;             // [G][hd+4] per-CTA attention partial: m, l, -, -, o[hd]
     float* amax_val;             // [G]
     int32_t* amax_idx;           // [G]
