@@ -19,7 +19,9 @@
 #pragma once
 #include <stdint.h>
 
+#ifndef KIE_NW
 #define KIE_NW 7                 // consumer warps per CTA (with the producer: 2 warps per SM sub-partition, no register cap below 255)
+#endif
 #define KIE_THREADS ((KIE_NW + 1) * 32)
 #define KIE_R 4                  // rows per slot
 #ifndef KIE_KC_F16

@@ -16,6 +16,10 @@ TINY = S.WORKLOADS["tiny"]
 # GEMV fast path for full 4-row slots) plus a half chunk; ragged vocab (not a
 # multiple of 4 rows x 152 CTAs)
 MEDIUM = S.Workload("medium", 5, 2, 1024, 8, 128, 4608, 10007, prompt_len=100, decode_steps=24)
+# d_model 2048: the fp16 GEMV phases run through the TMEM stage (whole 4-row x
+# 2048-column slots); vocab 8002 leaves a 2-row tail slot in the LM phase,
+# which goes through the shared-memory path of the same phase
+WIDE = S.Workload("wide", 6, 2, 2048, 16, 128, 4096, 8002, prompt_len=40, decode_steps=16)
 
 
 def _prefill_both(w, weights, mode="persistent", max_ctx=None):
@@ -27,7 +31,7 @@ def _prefill_both(w, weights, mode="persistent", max_ctx=None):
     return e, o, lg, lo
 
 
-@pytest.mark.parametrize("w", [TINY, MEDIUM], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [TINY, MEDIUM, WIDE], ids=lambda w: w.name)
 @pytest.mark.parametrize("kv", ["fp16", "fp8_e5m2"])
 def test_prefill_then_teacher_forced_decode(w, kv):
     w = w.with_(kv_dtype=kv)
@@ -71,7 +75,7 @@ def test_free_running_greedy(w):
     check_free_running(o, first, toks, logs, tol_for(w))
 
 
-@pytest.mark.parametrize("w", [TINY, MEDIUM], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [TINY, MEDIUM, WIDE], ids=lambda w: w.name)
 def test_graph_mode_bit_identical_to_persistent(w):
     weights = S.gen_weights(w)
     prompt = S.gen_prompt(w)
@@ -91,9 +95,9 @@ def test_graph_mode_bit_identical_to_persistent(w):
     np.testing.assert_array_equal(a[4], b[4])
 
 
-def test_step_by_step_equals_generate():
+@pytest.mark.parametrize("w", [TINY, WIDE], ids=lambda w: w.name)
+def test_step_by_step_equals_generate(w):
     """n chained decode_step calls == one generate_greedy of n steps (bit-exact)."""
-    w = TINY
     weights = S.gen_weights(w)
     prompt = S.gen_prompt(w)
     e1 = engine_for(w, weights)
@@ -106,6 +110,24 @@ def test_step_by_step_equals_generate():
         t, lg = e2.decode_step(t)
         assert t == toks[i]
         np.testing.assert_array_equal(lg, logs[i])
+
+
+@pytest.mark.parametrize("kv", ["fp16", "fp8_e5m2"])
+def test_long_chunks_synthetic_context(kv):
+    """2,300 context positions over 9-10 CTAs per head: chunks of ~240 rows need
+    more than one ring slot per consumer warp, so the last partial round of K/V
+    slots is shared by all warps."""
+    w = WIDE.with_(kv_dtype=kv, kv_source="synthetic", context_len=2300, prompt_len=0, decode_steps=4)
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights)
+    o = O.OracleDecoder(w, weights, max_ctx=w.max_ctx)
+    for layer in range(w.n_layers):
+        k, v = S.gen_kv(w, layer)
+        e.set_kv(layer, k, v)
+        o.set_kv(layer, k, v)
+    e.set_pos(w.context_len)
+    o.pos = w.context_len
+    teacher_forced(e, o, S.gen_first_token(w), w.decode_steps, tol_for(w))
 
 
 @pytest.mark.parametrize("ctx", [300, 383])
