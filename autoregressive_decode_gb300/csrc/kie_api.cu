@@ -5,6 +5,7 @@
 // gains, KV cache, activations, plan tables and output staging.  All GPU work
 // runs on the stream given at creation.
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cmath>
@@ -24,6 +25,26 @@ extern "C" cudaError_t kie_launch_ctl(KieControl* c, int tok, int pos, int clear
 extern "C" cudaError_t kie_launch_err_merge(const KieControl* src, KieControl* dst, cudaStream_t st);
 extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, const void* desc, int n,
                                             cudaStream_t st);
+// tensor-core prefill (kie_prefill.cu)
+extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const __half* W, float* C, int ldc,
+                                   int M_pad, int N_pad, int K, int m_valid, uint64_t timeout_ns, int* err,
+                                   cudaStream_t st);
+extern "C" cudaError_t kie_pf_pack(const __half* src, int n, int K, int row0, __half* dst, cudaStream_t st);
+extern "C" cudaError_t kie_pf_embed(const int32_t* tokens, int T, const uint16_t* emb, int d, float* x,
+                                    cudaStream_t st);
+extern "C" cudaError_t kie_pf_norm_split(const float* x, int ld, const float* g, float eps, int T, int T_pad, int d,
+                                         __half* hi, __half* lo, cudaStream_t st);
+extern "C" cudaError_t kie_pf_split(const float* src, int ld, int T, int T_pad, int K, __half* hi, __half* lo,
+                                    cudaStream_t st);
+extern "C" cudaError_t kie_pf_swiglu_split(const float* C, int ldc, int T, int T_pad, int F, __half* hi, __half* lo,
+                                           cudaStream_t st);
+extern "C" cudaError_t kie_pf_residual(float* x, const float* C, int ldc, int T, int d, cudaStream_t st);
+extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0, int H, int hd, const float* inv_freq,
+                                       int kvfmt, uint8_t* kc, uint8_t* vc, int layer, int max_ctx, float* Q,
+                                       cudaStream_t st);
+extern "C" cudaError_t kie_pf_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H,
+                                        int hd, int kvfmt, int max_ctx, int pos0, int T, float scale, float* O,
+                                        cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
                                              int8_t* codes_i8, uint16_t* scales, cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_u8(const uint16_t* src, int n_seg, int64_t src_seg, int64_t src_row,
@@ -74,9 +95,24 @@ struct Layout {  // byte offsets into the workspace
     size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl;
     size_t plan_i32, plan_u32, cta_base, cta_layer;
     size_t out_tokens, out_logits, forced, step_token, step_logits;
+    // tensor-core prefill: weight tiles (per layer: Wqkv, Wo, Wgu, Wd; then Wlm) and scratch
+    bool pf = false;
+    int pf_tc = 0;                    // prompt rows per prefill chunk (a multiple of 128)
+    size_t pf_w, pf_layer_elems, pf_qkv, pf_o, pf_gu, pf_d, pf_lm;   // element offsets within a layer / of Wlm
+    size_t pf_x, pf_ahi, pf_alo, pf_c, pf_q, pf_att, pf_err;
     size_t total;
     int nseg;
 };
+
+int pad256(int n) { return (n + 255) / 256 * 256; }
+
+// The tensor-core prefill covers fp16 FFN weights with an fp16 or E5M2 cache
+// (the uint8 cache changes stored values when a segment completes, and INT4
+// weights have no fp16 copy); every GEMM K must be a multiple of 64.
+bool prefill_tc_ok(const kie_config& c) {
+    return c.ffn_wdtype == KIE_W_FP16 && c.kv_dtype != KIE_KV_U8_ADAPTIVE && c.d_model % 64 == 0 &&
+           (c.n_heads * c.head_dim) % 64 == 0 && c.ffn_dim % 64 == 0;
+}
 
 struct Plan {
     int G = 0;
@@ -235,6 +271,28 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.forced = take(size_t(c.max_ctx) * 4);
     L.step_token = take(4);
     L.step_logits = take(size_t(V) * 4);
+    L.pf = prefill_tc_ok(c);
+    if (L.pf) {
+        const int HD = H * hd;
+        L.pf_qkv = 0;
+        L.pf_o = L.pf_qkv + size_t(pad256(3 * HD)) * d;
+        L.pf_gu = L.pf_o + size_t(pad256(d)) * HD;
+        L.pf_d = L.pf_gu + size_t(pad256(2 * F)) * d;
+        L.pf_layer_elems = L.pf_d + size_t(pad256(d)) * F;
+        L.pf_lm = L.pf_layer_elems * c.n_layers;
+        L.pf_w = take((L.pf_lm + size_t(pad256(V)) * d) * 2);
+        L.pf_tc = std::min(1024, (c.max_ctx + 127) / 128 * 128);
+        const size_t kmax = std::max({d, HD, F});
+        const size_t nmax = std::max<size_t>(size_t(L.pf_tc) * std::max({pad256(3 * HD), pad256(2 * F), pad256(d)}),
+                                             size_t(128) * pad256(V));
+        L.pf_x = take(size_t(L.pf_tc) * d * 4);
+        L.pf_ahi = take(size_t(L.pf_tc) * kmax * 2);
+        L.pf_alo = take(size_t(L.pf_tc) * kmax * 2);
+        L.pf_c = take(nmax * 4);
+        L.pf_q = take(size_t(L.pf_tc) * HD * 4);
+        L.pf_att = take(size_t(L.pf_tc) * HD * 4);
+        L.pf_err = take(16);
+    }
     L.total = align_up(o, 256);
 }
 
@@ -438,6 +496,70 @@ kie_status run_steps(kie_engine* e, int n, int first_tok, const int32_t* d_force
     }
     e->pos += n;
     return KIE_OK;
+}
+
+// Prompt prefill through the tensor-core path (kie_prefill.cu): chunks of up
+// to pf_tc prompt rows, each through all layers; the last row's logits.
+kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, float* last_logits) {
+    const kie_config& c = e->cfg;
+    const Layout& L = e->lay;
+    cudaStream_t st = e->stream;
+    const int d = c.d_model, H = c.n_heads, hd = c.head_dim, HD = H * hd, F = c.ffn_dim, V = c.vocab;
+    const __half* pfw = reinterpret_cast<const __half*>(e->dev(L.pf_w));
+    float* x = reinterpret_cast<float*>(e->dev(L.pf_x));
+    __half* ahi = reinterpret_cast<__half*>(e->dev(L.pf_ahi));
+    __half* alo = reinterpret_cast<__half*>(e->dev(L.pf_alo));
+    float* C = reinterpret_cast<float*>(e->dev(L.pf_c));
+    float* Q = reinterpret_cast<float*>(e->dev(L.pf_q));
+    float* O = reinterpret_cast<float*>(e->dev(L.pf_att));
+    int* err = reinterpret_cast<int*>(e->dev(L.pf_err));
+    const float* norms = reinterpret_cast<const float*>(e->dev(L.norms));
+    const float* inv_freq = reinterpret_cast<const float*>(e->dev(L.inv_freq));
+    const uint16_t* emb = reinterpret_cast<const uint16_t*>(e->dev(L.emb));
+    int32_t* d_tok = reinterpret_cast<int32_t*>(e->dev(L.forced));
+    const int kvf = c.kv_dtype == KIE_KV_FP16 ? KV_F16 : KV_E5M2;
+    const float scale = 1.0f / std::sqrt(float(hd));
+    const int nqkv = pad256(3 * HD), ngu = pad256(2 * F), nd = pad256(d), nv = pad256(V);
+    const uint64_t to = e->timeout_ns;
+    KIE_CUDA(e, cudaMemsetAsync(err, 0, 4, st));
+    KIE_CUDA(e, cudaMemcpyAsync(d_tok, tokens, size_t(n) * 4, cudaMemcpyHostToDevice, st));
+    const int pos_start = e->pos;
+    int Tn = 0;
+    for (int c0 = 0; c0 < n; c0 += L.pf_tc) {
+        Tn = std::min(L.pf_tc, n - c0);
+        const int Tp = (Tn + 127) / 128 * 128, pos = pos_start + c0;
+        KIE_CUDA(e, kie_pf_embed(d_tok + c0, Tn, emb, d, x, st));
+        for (int l = 0; l < c.n_layers; ++l) {
+            const __half* W = pfw + L.pf_layer_elems * l;
+            const float* g1 = norms + size_t(2 * l) * d;
+            const float* g2 = g1 + d;
+            KIE_CUDA(e, kie_pf_norm_split(x, d, g1, c.rms_eps, Tn, Tp, d, ahi, alo, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_qkv_post(C, nqkv, Tn, pos, H, hd, inv_freq, kvf, e->dev(L.kc), e->dev(L.vc), l,
+                                        c.max_ctx, Q, st));
+            KIE_CUDA(e, kie_pf_attention(Q, e->dev(L.kc), e->dev(L.vc), l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O,
+                                         st));
+            KIE_CUDA(e, kie_pf_split(O, HD, Tn, Tp, HD, ahi, alo, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));
+            KIE_CUDA(e, kie_pf_norm_split(x, d, g2, c.rms_eps, Tn, Tp, d, ahi, alo, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_gu, C, ngu, Tp, ngu, d, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_swiglu_split(C, ngu, Tn, Tp, F, ahi, alo, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_d, C, nd, Tp, nd, F, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));
+        }
+    }
+    // logits of the last prompt row
+    KIE_CUDA(e, kie_pf_norm_split(x + size_t(Tn - 1) * d, d, norms + size_t(2 * c.n_layers) * d, c.rms_eps, 1, 128, d,
+                                  ahi, alo, st));
+    KIE_CUDA(e, kie_pf_gemm(ahi, alo, pfw + L.pf_lm, C, nv, 128, nv, d, 1, to, err, st));
+    int herr = 0;
+    KIE_CUDA(e, cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
+    KIE_CUDA(e, cudaStreamSynchronize(st));
+    if (herr) return fail(e, KIE_ERR_DEVICE_TIMEOUT, "prefill GEMM wait expired");
+    if (last_logits) KIE_CUDA(e, cudaMemcpy(last_logits, C, size_t(V) * 4, cudaMemcpyDeviceToHost));
+    e->pos = pos_start + n;
+    return set_ctl(e, 0, e->pos, false);
 }
 
 }  // namespace
@@ -700,12 +822,22 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     auto plain_row = [&](int U, int, int& m, int& srow) { m = 0; srow = U; };
     auto gu_row = [&](int U, int half, int& m, int& srow) { m = half; srow = U; };
 
+    // tensor-core prefill copy of the weights (tiles; padding rows stay zero)
+    __half* pfw = reinterpret_cast<__half*>(e->dev(L.pf_w));
+    if (L.pf && cudaMemsetAsync(pfw, 0, (L.pf_lm + size_t(pad256(V)) * d) * 2, st) != cudaSuccess)
+        result = fail(e, KIE_ERR_CUDA, "prefill weight clear failed");
+    auto pf_pack = [&](const uint8_t* src, int n, int K, int row0, size_t off) -> bool {
+        return !L.pf || kie_pf_pack(reinterpret_cast<const __half*>(src), n, K, row0, pfw + off, st) == cudaSuccess;
+    };
+    const int HDm = H * hd;
     for (int l = 0; l < c.n_layers && result == KIE_OK; ++l) {
         const kie_layer_weights& lw = w->layers[l];
         const uint16_t* qkv[3] = {lw.wq, lw.wk, lw.wv};
+        const size_t lb = L.pf_layer_elems * l;
         for (int m = 0; m < 3 && result == KIE_OK; ++m) {
             const uint8_t* s = src_of(qkv[m], size_t(H) * hd * d * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
+            if (!pf_pack(s, HDm, d, m * HDm, lb + L.pf_qkv)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
             emit(PH_QKV, l, m, qkv_row, false, 0, 0);
             if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
         }
@@ -713,6 +845,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
         {
             const uint8_t* s = src_of(lw.wo, size_t(d) * H * hd * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
+            if (!pf_pack(s, d, HDm, 0, lb + L.pf_o)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
             emit(PH_O, l, 0, plain_row, false, 0, 0);
             if (!flush(s)) { result = fail(e, KIE_ERR_CUDA, "repack failed"); break; }
         }
@@ -731,6 +864,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
                 emit(PH_GU, l, m, gu_row, true, 0, sc_off);
                 if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
             } else {
+                if (!pf_pack(s, F, d, m * F, lb + L.pf_gu)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
                 emit(PH_GU, l, m, gu_row, false, 0, 0);
                 if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
             }
@@ -749,6 +883,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
                 emit(PH_D, l, 0, plain_row, true, 0, sc_off);
                 if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
             } else {
+                if (!pf_pack(s, d, F, 0, lb + L.pf_d)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
                 emit(PH_D, l, 0, plain_row, false, 0, 0);
                 if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
             }
@@ -757,6 +892,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     if (result == KIE_OK) {
         const uint8_t* s = src_of(w->lm_head, size_t(V) * d * 2);
         if (!s) result = fail(e, KIE_ERR_CUDA, "weight upload failed");
+        else if (!pf_pack(s, V, d, 0, L.pf_lm)) result = fail(e, KIE_ERR_CUDA, "prefill pack failed");
         else {
             emit(PH_LM, 0, 0, plain_row, false, 0, 0);
             if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
@@ -777,6 +913,7 @@ kie_status kie_prefill(kie_engine* e, const int32_t* tokens, int32_t n, float* l
     if (n == 0) return KIE_OK;
     if (!tokens) return fail(e, KIE_ERR_INVALID_ARG, "tokens is NULL");
     if ((st = check_tokens(e, tokens, n)) != KIE_OK) return st;
+    if (e->lay.pf) return prefill_tensor_cores(e, tokens, n, last_logits);
     int32_t* d_forced = reinterpret_cast<int32_t*>(e->dev(e->lay.forced));
     KIE_CUDA(e, cudaMemcpyAsync(d_forced, tokens, size_t(n) * 4, cudaMemcpyHostToDevice, e->stream));
     float* d_log = reinterpret_cast<float*>(e->dev(e->lay.out_logits));

@@ -1,0 +1,446 @@
+// Prompt prefill on the tensor cores: the whole prompt goes
+// through each layer as [T x K] GEMMs instead of T single-token decode steps.
+//
+//   per layer:  u = RMSNorm(x) g1             kie_pf_norm_split   (fp32 -> fp16 hi + lo tiles)
+//               [q k v] = u Wqkv^T            kie_pf_gemm         (tcgen05, fp32 accumulate in TMEM)
+//               RoPE q, k; store k, v         kie_pf_qkv_post     (cache in its storage format)
+//               o = causal softmax(q k^T) v   kie_pf_attention    (reads the stored K/V, as decode does)
+//               x += o Wo^T                   kie_pf_split, kie_pf_gemm, kie_pf_residual
+//               u = RMSNorm(x) g2             kie_pf_norm_split
+//               [g u] = u Wgu^T               kie_pf_gemm
+//               x += (silu(g) u) Wd^T         kie_pf_swiglu_split, kie_pf_gemm, kie_pf_residual
+//   last row:   logits = RMSNorm(x) gf Wlm^T  kie_pf_norm_split (one row), kie_pf_gemm
+//
+// Operands.  The MMA takes fp16; activations are fp32 in this path (as in the
+// decode kernel), so every activation a is split into hi = fp16(a) and
+// lo = fp16(a - hi) and each K step issues two MMAs, A_hi W^T + A_lo W^T, into
+// the same fp32 accumulator: the product then carries a's full precision up to
+// 2^-22 relative, well inside the fp32 reference's tolerance.  Weights are fp16
+// as given.
+//
+// Tile layout.  Both operands are stored in global memory already in the
+// tensor cores' canonical no-swizzle K-major layout, tile by tile (tiles of
+// 128 rows for activations, 256 rows for weights, 64 columns of K), so one
+// plain bulk copy moves a tile into shared memory: element (r, k) of a tile
+// sits at byte (r/8)*1024 + (k/8)*128 + (r%8)*16 + (k%8)*2, i.e. 8-row x
+// 16-byte core matrices, 128 bytes apart along K and 1024 bytes apart along
+// rows; tile (rb, kb) starts at element (rb * KB + kb) * rows * 64.
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "kie_device.cuh"
+#include "kie_internal.h"
+
+using namespace kie;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
+constexpr uint32_t A_BYTES = BM * BK * 2;                 // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;                 // 32 KB
+constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + B_BYTES;   // A hi, A lo, B
+constexpr uint32_t GEMM_SMEM = STAGES * STAGE_BYTES + 256;
+
+__device__ __forceinline__ size_t tile_idx(int r, int k, int rows, int KB) {
+    return (size_t(r / rows) * KB + (k >> 6)) * size_t(rows) * 64 + size_t((r % rows) >> 3) * 512 +
+           size_t((k & 63) >> 3) * 64 + size_t(r & 7) * 8 + size_t(k & 7);
+}
+
+__device__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* err) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (ld_volatile_i32(err) != 0) return false;
+        if (globaltimer() - t0 > timeout_ns) { atomicExch(err, 1); return false; }
+    }
+    return true;
+}
+
+// C[m, n] = sum_k (Ahi + Alo)[m, k] W[n, k] for one 128 x 256 tile of C.
+// Thread 0 streams the K tiles (3-stage ring), thread 32 issues the MMAs, all
+// four warps then move their 32 TMEM lanes (rows) to C.  Rows >= m_valid are
+// not stored.  Every wait is bounded; a timeout sets *err.
+__global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __restrict__ Ahi,
+                                                             const __half* __restrict__ Alo,
+                                                             const __half* __restrict__ W, float* __restrict__ C,
+                                                             int ldc, int KB, int m_valid, uint64_t timeout_ns,
+                                                             int* err) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* done = empty + STAGES;
+    uint32_t* taddr = reinterpret_cast<uint32_t*>(done + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = blockIdx.x, mb = blockIdx.y;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(done, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(taddr, BN);   // 128 lanes x 256 fp32 columns
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tacc = *taddr;
+    const size_t a_off = size_t(mb) * KB * (BM * BK), w_off = size_t(nb) * KB * (BN * BK);
+    if (threadIdx.x == 0) {
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % STAGES;
+            if (kb >= STAGES && !wait_bounded(&empty[s], uint32_t((kb / STAGES) - 1) & 1u, timeout_ns, err)) break;
+            uint8_t* dst = sm + s * STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+            bulk_g2s_keep(dst, Ahi + a_off + size_t(kb) * (BM * BK), A_BYTES, &full[s]);
+            bulk_g2s_keep(dst + A_BYTES, Alo + a_off + size_t(kb) * (BM * BK), A_BYTES, &full[s]);
+            bulk_g2s_keep(dst + 2 * A_BYTES, W + w_off + size_t(kb) * (BN * BK), B_BYTES, &full[s]);
+        }
+    } else if (threadIdx.x == 32) {
+        // kind::f16 instruction descriptor: fp32 D (bit 4), fp16 A and B, both
+        // K-major, N / 8 in bits 17..22, M / 16 in bits 24..28
+        const uint32_t idesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % STAGES;
+            if (!wait_bounded(&full[s], uint32_t(kb / STAGES) & 1u, timeout_ns, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint8_t* st = sm + s * STAGE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {   // K = 16 per MMA: two core matrices, 256 bytes
+                const uint64_t bd = smem_desc_noswz(st + 2 * A_BYTES + kk * 256, 128, 1024);
+                tc_mma_f16(tacc, smem_desc_noswz(st + kk * 256, 128, 1024), bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                tc_mma_f16(tacc, smem_desc_noswz(st + A_BYTES + kk * 256, 128, 1024), bd, idesc, 1u);
+            }
+            tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(done);
+    }
+    __syncwarp();
+    const bool ok = wait_bounded(done, 0u, timeout_ns, err);
+    tc_fence_after();
+    __syncwarp();
+    if (ok) {
+        const int row = mb * BM + warp * 32 + lane;
+        float* crow = C + size_t(row) * ldc + size_t(nb) * BN;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tacc + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+            if (row < m_valid) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(crow + c0 + i) =
+                        make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                    __uint_as_float(v[i + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tacc, BN);
+}
+
+// Repack rows [0, n) of a row-major fp16 matrix [n x K] into rows [row0, row0 + n)
+// of a weight tile array (256-row tiles).  One thread per 8-element group.
+__global__ void kie_pf_pack_kernel(const __half* __restrict__ src, int n, int K, int row0, __half* __restrict__ dst) {
+    const int KB = K / 64, g8 = K / 8;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < size_t(n) * g8; i += size_t(gridDim.x) * blockDim.x) {
+        const int r = int(i / g8), k = int(i % g8) * 8;
+        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) =
+            *reinterpret_cast<const uint4*>(src + size_t(r) * K + k);
+    }
+}
+
+__device__ __forceinline__ void put_split(__half* hi, __half* lo, size_t idx, float v) {
+    const __half h = __float2half_rn(v);
+    hi[idx] = h;
+    lo[idx] = __float2half_rn(v - __half2float(h));
+}
+
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += red[w];
+    __syncthreads();
+    return s;
+}
+
+// x[t] = fp32(E[tokens[t]])
+__global__ void kie_pf_embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ emb, int d,
+                                    float* __restrict__ x) {
+    const int t = blockIdx.x;
+    const uint16_t* row = emb + size_t(tokens[t]) * d;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) x[size_t(t) * d + k] = __half2float(__ushort_as_half(row[k]));
+}
+
+// Rows [0, T) of x (row stride ld): u = x / sqrt(mean(x^2) + eps) * g split into
+// hi / lo tiles of 128 rows; rows [T, T_pad) are written as zeros.  256 threads per row.
+__global__ void kie_pf_norm_split_kernel(const float* __restrict__ x, int ld, const float* __restrict__ g, float eps,
+                                         int T, int d, __half* __restrict__ hi, __half* __restrict__ lo) {
+    __shared__ float red[8];
+    const int t = blockIdx.x, KB = d / 64;
+    if (t >= T) {
+        for (int k = threadIdx.x; k < d; k += blockDim.x) {
+            const size_t idx = tile_idx(t, k, BM, KB);
+            hi[idx] = __float2half_rn(0.f);
+            lo[idx] = __float2half_rn(0.f);
+        }
+        return;
+    }
+    const float* xr = x + size_t(t) * ld;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) ss += xr[k] * xr[k];
+    ss = block_sum256(ss, red);
+    const float r = sqrtf(ss / float(d) + eps);
+    for (int k = threadIdx.x; k < d; k += blockDim.x) put_split(hi, lo, tile_idx(t, k, BM, KB), xr[k] / r * g[k]);
+}
+
+// Rows [0, T) of src (row stride ld, K columns) split into hi / lo tiles; rows [T, T_pad) zero.
+__global__ void kie_pf_split_kernel(const float* __restrict__ src, int ld, int T, int K, __half* __restrict__ hi,
+                                    __half* __restrict__ lo) {
+    const int t = blockIdx.x, KB = K / 64;
+    for (int k = threadIdx.x; k < K; k += blockDim.x)
+        put_split(hi, lo, tile_idx(t, k, BM, KB), t < T ? src[size_t(t) * ld + k] : 0.f);
+}
+
+// a = silu(C[:, i]) * C[:, F + i], split into hi / lo tiles; rows [T, T_pad) zero.
+__global__ void kie_pf_swiglu_split_kernel(const float* __restrict__ C, int ldc, int T, int F, __half* __restrict__ hi,
+                                           __half* __restrict__ lo) {
+    const int t = blockIdx.x, KB = F / 64;
+    for (int i = threadIdx.x; i < F; i += blockDim.x) {
+        float a = 0.f;
+        if (t < T) {
+            const float gt = C[size_t(t) * ldc + i], up = C[size_t(t) * ldc + F + i];
+            a = (gt / (1.f + expf(-gt))) * up;
+        }
+        put_split(hi, lo, tile_idx(t, i, BM, KB), a);
+    }
+}
+
+// x[t, :] += C[t, :d]
+__global__ void kie_pf_residual_kernel(float* __restrict__ x, const float* __restrict__ C, int ldc, int d) {
+    const int t = blockIdx.x;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) x[size_t(t) * d + k] += C[size_t(t) * ldc + k];
+}
+
+// Rotate q and k of row t (position pos0 + t) by RoPE (half-split pairs), store
+// k and v into the cache in its storage format (fp16 round to nearest even;
+// E5M2 from that fp16), and q (fp32) into Q[t][H*hd].
+__global__ void kie_pf_qkv_post_kernel(const float* __restrict__ C, int ldc, int pos0, int H, int hd,
+                                       const float* __restrict__ inv_freq, int kvfmt, uint8_t* __restrict__ kc,
+                                       uint8_t* __restrict__ vc, int layer, int max_ctx, float* __restrict__ Q) {
+    const int t = blockIdx.x, pos = pos0 + t, hh = hd / 2, HD = H * hd;
+    const float* row = C + size_t(t) * ldc;
+    for (int u = threadIdx.x; u < H * hh; u += blockDim.x) {
+        const int h = u / hh, i = u % hh;
+        float sn, cs;
+        sincosf(float(pos) * inv_freq[i], &sn, &cs);
+        const int e0 = h * hd + i;
+        const float qa = row[e0], qb = row[e0 + hh];
+        Q[size_t(t) * HD + e0] = qa * cs - qb * sn;
+        Q[size_t(t) * HD + e0 + hh] = qb * cs + qa * sn;
+        const float ka = row[HD + e0], kb = row[HD + e0 + hh];
+        const float kv[4] = {ka * cs - kb * sn, kb * cs + ka * sn, row[2 * HD + e0], row[2 * HD + e0 + hh]};
+        const size_t base = ((size_t(layer) * H + h) * max_ctx + pos) * hd + i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint8_t* cache = j < 2 ? kc : vc;
+            const size_t at = base + ((j & 1) ? hh : 0);
+            const __half hv = __float2half_rn(kv[j]);
+            if (kvfmt == KV_F16) reinterpret_cast<__half*>(cache)[at] = hv;
+            else cache[at] = uint8_t(f16x2_to_e5m2x2(hv, hv) & 0xFFu);
+        }
+    }
+}
+
+// Causal attention of T query rows (positions pos0 + t) of head blockIdx.y over
+// the stored cache positions 0 .. pos0 + t.  A block takes 64 query rows; its
+// 256 threads are (row r = tid / 4, part c = tid % 4): part c scores keys
+// c + 4i of each 64-key tile and accumulates the output dims 16j + 4c .. +3.
+// Online softmax per row; the 4 parts of a row share the running max.
+template <int HD, int KVF>
+__global__ void __launch_bounds__(256) kie_pf_attention_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ kc,
+                                                               const uint8_t* __restrict__ vc, int layer, int H,
+                                                               int max_ctx, int pos0, int T, float scale,
+                                                               float* __restrict__ O) {
+    constexpr int LD = HD + 4, PLD = 68, ND = HD / 16;   // ND float4 groups of output dims per part
+    extern __shared__ __align__(16) float smf[];
+    float* Qs = smf;                 // [64][LD]
+    float* Ks = Qs + 64 * LD;        // [64][LD]
+    float* Vs = Ks + 64 * LD;        // [64][LD]
+    float* Ps = Vs + 64 * LD;        // [64][PLD]
+    const int h = blockIdx.y, q0 = blockIdx.x * 64, tid = threadIdx.x;
+    const int r = tid >> 2, c = tid & 3;
+    const int HDall = H * HD;
+    for (int i = tid; i < 64 * HD; i += 256) {
+        const int rr = i / HD, dd = i % HD;
+        Qs[rr * LD + dd] = (q0 + rr < T) ? Q[size_t(q0 + rr) * HDall + h * HD + dd] * scale : 0.f;
+    }
+    const int qpos = pos0 + q0 + r;                       // this thread's query position
+    const int last = pos0 + min(T, q0 + 64) - 1;          // the block's largest query position
+    float m = -INFINITY, l = 0.f;
+    float4 acc[ND];
+#pragma unroll
+    for (int j = 0; j < ND; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t head_base = (size_t(layer) * H + h) * max_ctx;
+    for (int k0 = 0; k0 <= last; k0 += 64) {
+        __syncthreads();   // the previous tile's K, V, P are no longer read
+        for (int i = tid; i < 64 * HD; i += 256) {
+            const int jr = i / HD, dd = i % HD, j = k0 + jr;
+            float kv = 0.f, vv = 0.f;
+            if (j <= last) {
+                const size_t at = (head_base + j) * HD + dd;
+                if (KVF == KV_F16) {
+                    kv = __half2float(reinterpret_cast<const __half*>(kc)[at]);
+                    vv = __half2float(reinterpret_cast<const __half*>(vc)[at]);
+                } else {   // E5M2: the byte is the top half of an fp16
+                    kv = __half2float(__ushort_as_half((unsigned short)(uint32_t(kc[at]) << 8)));
+                    vv = __half2float(__ushort_as_half((unsigned short)(uint32_t(vc[at]) << 8)));
+                }
+            }
+            Ks[jr * LD + dd] = kv;
+            Vs[jr * LD + dd] = vv;
+        }
+        __syncthreads();
+        float s[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[i] = 0.f;
+        for (int d4 = 0; d4 < HD; d4 += 4) {
+            const float4 qv = *reinterpret_cast<const float4*>(Qs + r * LD + d4);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 kv = *reinterpret_cast<const float4*>(Ks + (c + 4 * i) * LD + d4);
+                s[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, s[i]))));
+            }
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (k0 + c + 4 * i > qpos) s[i] = -INFINITY;
+            mt = fmaxf(mt, s[i]);
+        }
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        const float mn = fmaxf(m, mt);
+        const float cf = (m == -INFINITY) ? 0.f : expf(m - mn);
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float p = (s[i] == -INFINITY) ? 0.f : expf(s[i] - mn);
+            Ps[r * PLD + c + 4 * i] = p;
+            ps += p;
+        }
+        l = l * cf + ps;
+        m = mn;
+#pragma unroll
+        for (int j = 0; j < ND; ++j) { acc[j].x *= cf; acc[j].y *= cf; acc[j].z *= cf; acc[j].w *= cf; }
+        __syncthreads();
+        for (int jr = 0; jr < 64; jr += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(Ps + r * PLD + jr);
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                for (int j = 0; j < ND; ++j) {
+                    const float4 v = *reinterpret_cast<const float4*>(Vs + (jr + u) * LD + 16 * j + 4 * c);
+                    acc[j].x = fmaf(pp[u], v.x, acc[j].x);
+                    acc[j].y = fmaf(pp[u], v.y, acc[j].y);
+                    acc[j].z = fmaf(pp[u], v.z, acc[j].z);
+                    acc[j].w = fmaf(pp[u], v.w, acc[j].w);
+                }
+            }
+        }
+    }
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (q0 + r < T) {
+        float* orow = O + size_t(q0 + r) * HDall + h * HD;
+#pragma unroll
+        for (int j = 0; j < ND; ++j)
+            *reinterpret_cast<float4*>(orow + 16 * j + 4 * c) =
+                make_float4(acc[j].x / l, acc[j].y / l, acc[j].z / l, acc[j].w / l);
+    }
+}
+
+template <int HD, int KVF>
+cudaError_t launch_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H, int max_ctx,
+                             int pos0, int T, float scale, float* O, cudaStream_t st) {
+    const size_t smem = size_t(3 * 64 * (HD + 4) + 64 * 68) * 4;
+    cudaError_t r = cudaFuncSetAttribute(kie_pf_attention_kernel<HD, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (r != cudaSuccess) return r;
+    kie_pf_attention_kernel<HD, KVF><<<dim3((T + 63) / 64, H), 256, smem, st>>>(Q, kc, vc, layer, H, max_ctx, pos0,
+                                                                                  T, scale, O);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// ---- launch wrappers (host code in kie_api.cu) -----------------------------------------------
+extern "C" size_t kie_pf_tile_elems(int rows_pad, int K) { return size_t(rows_pad) * K; }
+
+extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const __half* W, float* C, int ldc,
+                                   int M_pad, int N_pad, int K, int m_valid, uint64_t timeout_ns, int* err,
+                                   cudaStream_t st) {
+    cudaError_t r = cudaFuncSetAttribute(kie_pf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(GEMM_SMEM));
+    if (r != cudaSuccess) return r;
+    kie_pf_gemm_kernel<<<dim3(N_pad / BN, M_pad / BM), 128, GEMM_SMEM, st>>>(Ahi, Alo, W, C, ldc, K / BK, m_valid,
+                                                                            timeout_ns, err);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_pack(const __half* src, int n, int K, int row0, __half* dst, cudaStream_t st) {
+    const size_t work = size_t(n) * (K / 8);
+    const int blocks = int(std::min<size_t>((work + 255) / 256, 65535));
+    kie_pf_pack_kernel<<<blocks, 256, 0, st>>>(src, n, K, row0, dst);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_embed(const int32_t* tokens, int T, const uint16_t* emb, int d, float* x,
+                                    cudaStream_t st) {
+    kie_pf_embed_kernel<<<T, 256, 0, st>>>(tokens, emb, d, x);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_norm_split(const float* x, int ld, const float* g, float eps, int T, int T_pad, int d,
+                                         __half* hi, __half* lo, cudaStream_t st) {
+    kie_pf_norm_split_kernel<<<T_pad, 256, 0, st>>>(x, ld, g, eps, T, d, hi, lo);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_split(const float* src, int ld, int T, int T_pad, int K, __half* hi, __half* lo,
+                                    cudaStream_t st) {
+    kie_pf_split_kernel<<<T_pad, 256, 0, st>>>(src, ld, T, K, hi, lo);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_swiglu_split(const float* C, int ldc, int T, int T_pad, int F, __half* hi, __half* lo,
+                                           cudaStream_t st) {
+    kie_pf_swiglu_split_kernel<<<T_pad, 256, 0, st>>>(C, ldc, T, F, hi, lo);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_residual(float* x, const float* C, int ldc, int T, int d, cudaStream_t st) {
+    kie_pf_residual_kernel<<<T, 256, 0, st>>>(x, C, ldc, d);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0, int H, int hd, const float* inv_freq,
+                                       int kvfmt, uint8_t* kc, uint8_t* vc, int layer, int max_ctx, float* Q,
+                                       cudaStream_t st) {
+    kie_pf_qkv_post_kernel<<<T, 256, 0, st>>>(C, ldc, pos0, H, hd, inv_freq, kvfmt, kc, vc, layer, max_ctx, Q);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H,
+                                        int hd, int kvfmt, int max_ctx, int pos0, int T, float scale, float* O,
+                                        cudaStream_t st) {
+    if (hd == 128) {
+        return kvfmt == KV_F16 ? launch_attention<128, KV_F16>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st)
+                               : launch_attention<128, KV_E5M2>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st);
+    }
+    return kvfmt == KV_F16 ? launch_attention<64, KV_F16>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st)
+                           : launch_attention<64, KV_E5M2>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st);
+}
