@@ -167,6 +167,24 @@ def test_int4_ffn_decode():
     teacher_forced(e, o, O.argmax_lowest(lo), w.decode_steps, tol_for(w))
 
 
+@pytest.mark.parametrize("w", [WIDE, MEDIUM.with_(kv_dtype="fp8_e5m2")], ids=lambda w: w.name + "/" + w.kv_dtype)
+def test_prefill_in_pieces(w):
+    """A prompt prefilled in three calls (the later pieces attend to the cache the
+    earlier ones wrote) gives the oracle's logits after each piece, and then
+    decodes like the oracle."""
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights)
+    o = O.OracleDecoder(w, weights, max_ctx=w.max_ctx)
+    prompt = S.gen_prompt(w)
+    tol = tol_for(w)
+    for a, b in ((0, 7), (7, 8), (8, w.prompt_len)):
+        lg = e.prefill(prompt[a:b])
+        lo = o.prefill(prompt[a:b])
+        assert np.abs(lg - lo).max() <= tol
+        assert e.pos == o.pos == b
+    teacher_forced(e, o, O.argmax_lowest(lo), 4, tol)
+
+
 def test_context_edges():
     """Decode from position 0 (C = 1: attention returns V), fill the cache to
     max_ctx exactly, and reject one more step without writing."""
