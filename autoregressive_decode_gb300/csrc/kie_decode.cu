@@ -58,6 +58,7 @@ struct Smem {
     int32_t* clist;   // attention: contributors (2*cta + segment) of the head being combined
     float* rope;      // [2][hd/2] cos, sin of the current step's position
     float* red;       // reduction scratch: NW*(KIE_MAX_HEAD_DIM+2) + 64 floats
+    float* xres;      // [KIE_XRES] old x of the rows the next residual epilogue updates
     float* part;      // GEMV partial sums
     float* act;       // activation (piece-split layout) / attention scores
     uint8_t* ring;
@@ -74,6 +75,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const KieParams& P) {
     s.clist = reinterpret_cast<int32_t*>(base + l.clist);
     s.rope = reinterpret_cast<float*>(base + l.rope);
     s.red = reinterpret_cast<float*>(base + l.red);
+    s.xres = reinterpret_cast<float*>(base + l.xres);
     s.part = reinterpret_cast<float*>(base + l.part);
     s.act = reinterpret_cast<float*>(base + l.act);
     s.ring = base + l.ring;
@@ -443,9 +445,12 @@ __device__ __forceinline__ float block_max(float v, float* red, int tid) {
 // block-wide reduction sits between the barrier and the first slot.
 // src = x (fp32, global) or an embedding row (fp16).
 constexpr int NORM_SLOT = NW * (KIE_MAX_HEAD_DIM + 2) + 8;
-// x is tagged with parity `par` (polled until every element carries it).
+// x is tagged with parity `par` (polled until every element carries it).  The
+// raw values of elements [cap0, cap0 + ncap) (the rows this CTA's next residual
+// epilogue updates) are also kept in S.xres.
 __device__ void act_scaled(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* x,
-                           const uint16_t* emb_row, const float* g, uint32_t par, int tid, int cta) {
+                           const uint16_t* emb_row, const float* g, uint32_t par, int tid, int cta, int cap0,
+                           int ncap) {
     const int d = P.d, half = P.act_floats / 2, ng = d >> 2;
     float ss = 0.f;
     for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
@@ -482,6 +487,13 @@ __device__ void act_scaled(const KieParams& P, const KieLaunch& Lc, const Smem& 
             const int q = q0 + u * NCT;
             if (q < ng) {
                 ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+                const int k4 = 4 * q - cap0;
+                if (k4 > -4 && k4 < ncap) {
+                    const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (k4 + e >= 0 && k4 + e < ncap) S.xres[k4 + e] = vv[e];
+                }
                 const float4 gg = *reinterpret_cast<const float4*>(g + 4 * q);
                 // 4 consecutive elements share one plane of one 8-element piece
                 *reinterpret_cast<float4*>(S.act + act_idx(4 * q, half)) =
@@ -705,14 +717,15 @@ __device__ __forceinline__ uint32_t kv_store(const KieParams& P, int layer, int 
 // q / current-position K, V (for this step's attention), write number n.
 __device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int layer, int pos, uint32_t n,
                         int tid) {
-    const int hh = P.hd / 2;
+    const int hh = P.hd / 2, lhh = P.hd == 128 ? 6 : 5;   // hd is 64 or 128
     const int per = P.H * hh;  // units per matrix
     const uint32_t par = tag_par(n), ep16 = tag_ep16(n);
-    const float r = norm_r(P, S);
+    const float rinv = 1.0f / norm_r(P, S);
     for (int u = tid; u < c.n_units; u += NCT) {
-        const float ya = row_sum(S, c, 2 * u) / r, yb = row_sum(S, c, 2 * u + 1) / r;
+        const float ya = row_sum(S, c, 2 * u) * rinv, yb = row_sum(S, c, 2 * u + 1) * rinv;
         const int U = c.unit0 + u;
-        const int which = U / per, rem = U % per, h = rem / hh, i = rem % hh;
+        const int which = (U >= per) + (U >= 2 * per), rem = U - which * per;
+        const int h = rem >> lhh, i = rem & (hh - 1);
         const int e0 = h * P.hd + i;
         if (which == 2) {
             const uint32_t b0 = kv_store(P, layer, 1, h, pos, i, ya), b1 = kv_store(P, layer, 1, h, pos, i + hh, yb);
@@ -731,25 +744,27 @@ __device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int 
             st_relaxed_u32(P.kcur + e0 + hh, (b1 << 16) | ep16);
         }
     }
-    // K/V written here are read in later steps by bulk copies (the async proxy).
-    fence_proxy_async_global();
 }
 
 // x[row] += y[row]; x is read with parity par_in (or, in the first layer's O
 // phase, is the embedding row erow) and written with parity par_out.
+// The old x[row] comes from S.xres when this launch ran the staging that kept
+// it (have_xres; at most KIE_XRES rows).
 __device__ void epi_residual(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c,
-                             const uint16_t* erow, uint32_t par_in, uint32_t par_out, int tid, int cta) {
+                             const uint16_t* erow, uint32_t par_in, uint32_t par_out, bool have_xres, int tid,
+                             int cta) {
     for (int r = tid; r < c.rows; r += NCT) {
         const int row = c.unit0 + r;
-        const float xo = erow ? __half2float(__ushort_as_half(erow[row])) : wait_f32(P, Lc, S, P.x + row, par_in, cta);
+        const float xo = (have_xres && c.rows <= KIE_XRES) ? S.xres[r]
+                         : erow ? __half2float(__ushort_as_half(erow[row])) : wait_f32(P, Lc, S, P.x + row, par_in, cta);
         st_relaxed_f32(P.x + row, tag_f32(xo + row_sum(S, c, r), par_out));
     }
 }
 
 __device__ void epi_swiglu(const KieParams& P, const Smem& S, const Cursor& c, uint32_t par, int tid) {
-    const float r = norm_r(P, S);
+    const float rinv = 1.0f / norm_r(P, S);
     for (int u = tid; u < c.n_units; u += NCT) {
-        const float gt = row_sum(S, c, 2 * u) / r, up = row_sum(S, c, 2 * u + 1) / r;
+        const float gt = row_sum(S, c, 2 * u) * rinv, up = row_sum(S, c, 2 * u + 1) * rinv;
         st_relaxed_f32(P.a + c.unit0 + u, tag_f32((gt / (1.f + expf(-gt))) * up, par));
     }
 }
@@ -1089,6 +1104,7 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
             qv[4 * i + 2] = v4[i].z * P.attn_scale; qv[4 * i + 3] = v4[i].w * P.attn_scale;
         }
     }
+    if (tid == 0) stamp(P, Lc, pos - (Lc.pos0 >= 0 ? Lc.pos0 : pos), 5 * layer + 1, 4, cta);
     // The current position is the last row of the head's last chunk; warp 0's
     // first row group fetches its tagged K and V together with q.  fp16 / E5M2
     // stream every other row through the ring; a uint8 cache reads the rest of
@@ -1204,6 +1220,7 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     }
     gc += nsl;
     if (!ok) S.flags[0] = 1;
+    if (lane == 0 && warp == 0) stamp(P, Lc, pos - (Lc.pos0 >= 0 ? Lc.pos0 : pos), 5 * layer + 1, 5, cta);
 
     // ---- direct rows [jt, j1)
     if (has_pos && warp == 0) {                         // uniform over warp 0
@@ -1391,6 +1408,10 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
             // the previous step's token and its K/V cache writes (read by this
             // step's bulk copies).  Inside a step the tags order everything.
             if (Lc.use_grid_barrier && !first_phase && layer == 0 && sub == 0) {
+                // the K/V this thread wrote into the cache during the step are read
+                // by the next steps' bulk copies (the async proxy): one proxy fence
+                // per step, before the barrier that publishes them
+                fence_proxy_async_global();
                 if (!grid_barrier(P, Lc, S, nbar, tid, cta)) return;
             }
             first_phase = false;
@@ -1432,8 +1453,16 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                     const float* g = type == PH_QKV ? gains : type == PH_GU ? gains + P.d
                                                                              : P.norms + size_t(P.L) * 2 * P.d;
                     if (type == PH_QKV) rope_table(P, S, pos, tid);
+                    // keep the raw x of the rows the next residual epilogue (O after
+                    // QKV, D after GU) updates
+                    int cap0 = 0, ncap = 0;
+                    if (type != PH_LM) {
+                        const int rt = type == PH_QKV ? PH_O : PH_D;
+                        cap0 = S.plan[rt * 4 + 0];
+                        ncap = S.plan[rt * 4 + 1] <= KIE_XRES ? S.plan[rt * 4 + 1] : 0;
+                    }
                     act_scaled(P, Lc, S, from_emb ? nullptr : P.x, from_emb ? erow : nullptr, g,
-                               type == PH_GU ? 1u : 0u, tid, cta);
+                               type == PH_GU ? 1u : 0u, tid, cta, cap0, ncap);
                 }
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
                 if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
@@ -1441,8 +1470,9 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 if (type == PH_QKV) epi_qkv(P, S, c, layer, pos, tn, tid);
                 else if (type == PH_GU) epi_swiglu(P, S, c, par, tid);
                 else if (type == PH_LM) epi_lm(P, Lc, S, c, cta, tid, t, pos);
-                else if (type == PH_O) epi_residual(P, Lc, S, c, layer == 0 ? erow : nullptr, 0u, 1u, tid, cta);
-                else epi_residual(P, Lc, S, c, nullptr, 1u, 0u, tid, cta);
+                else if (type == PH_O)
+                    epi_residual(P, Lc, S, c, layer == 0 ? erow : nullptr, 0u, 1u, phi - 2 >= Lc.phase_begin, tid, cta);
+                else epi_residual(P, Lc, S, c, nullptr, 1u, 0u, phi - 1 >= Lc.phase_begin, tid, cta);
             }
             if (tid == 0) stamp(P, Lc, t, phi, 3, cta);
         }

@@ -36,6 +36,7 @@
 #endif
 #define KIE_MAX_SLOTS 16
 #define KIE_SEG 128              // adaptive-range uint8 KV segment (tokens)
+#define KIE_XRES 64              // residual rows per CTA whose old x is kept in shared memory
 #define KIE_MAX_HEAD_DIM 128
 #define KIE_MAX_GRID 256         // CTAs of the persistent grid (one per SM)
 #define KIE_PROF_EVENTS 6        // trace stamps per (step, phase, CTA)
@@ -51,7 +52,7 @@
 // device (carving) both use this one function.  Offsets are relative to the
 // dynamic shared-memory base; the ring starts on a 128-byte boundary.
 struct KieSmemLayout {
-    uint32_t full, empty, cbase, flags, plan, clist, rope, red, part, act, ring, total;
+    uint32_t full, empty, cbase, flags, plan, clist, rope, red, xres, part, act, ring, total;
 };
 KIE_HD inline uint32_t kie_align(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot) {
@@ -65,6 +66,7 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
     l.clist = o; o += KIE_MAX_GRID * 4;
     l.rope = o;  o += KIE_MAX_HEAD_DIM * 4;     // cos/sin of the step's position, [2][hd/2]
     l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64) * 4;
+    l.xres = o;  o += KIE_XRES * 4;
     l.part = o;  o += uint32_t(part_floats) * 4;
     l.act = kie_align(o, 16); o = l.act + uint32_t(act_floats) * 4;
     l.ring = kie_align(o, 128);
@@ -166,8 +168,9 @@ struct KieLaunch {
     int32_t use_grid_barrier;    // 1 in the persistent (cooperative) launch
     // Optional trace: %globaltimer stamps [n_steps][5L+1][KIE_PROF_EVENTS][G]:
     // 0 phase start (after the grid barrier), 1 activation staged, 2 GEMV /
-    // attention done, 3 epilogue done, 4 producer issued the phase's first slot,
-    // 5 producer issued its last slot.  Null: no tracing.
+    // attention done, 3 epilogue done, 4 producer issued the phase's first slot
+    // (attention: q arrived), 5 producer issued its last slot (attention: warp 0
+    // done with its ring slots).  Null: no tracing.
     uint64_t* prof;
     // Optional ring trace of CTA 0: [KIE_PROF_SLOTS][4] stamps per slot index of
     // the launch: 0 copy issued, 1 data seen by the consumer warp, 2 released.
