@@ -18,6 +18,10 @@ Pages cited (titles as published):
             worked example min -1.2, max 2.8 -> scale ~0.0157, zero-point ~76).
   [Hunyuan] Hunyuan serving re-architecture — section 5.2 (INT4 dequant: keep the
             scale product in fp32, round once at the end).
+  [Kog] also, section "Memory bandwidth is the main bottleneck": an FP16 weight
+            is 2 bytes for one multiply-add (~1 FLOP/byte), FP8 ~2, FP4 ~4 —
+            the FP8 weight format below (E4M3, one fp32 scale per output row)
+            is this module's reading; the page names only the byte width.
 
 The decoder itself (RMSNorm, RoPE, SwiGLU, MHA, untied LM head) is fixed by the
 workload description, not by the pages; where the pages leave a step open this
@@ -114,6 +118,61 @@ def u8_quantize(x: np.ndarray):
 def u8_dequantize(codes: np.ndarray, scale, zp) -> np.ndarray:
     """x_hat = (code - zp) * scale in fp32 ([Grok3] 3.2)."""
     return (np.asarray(codes, dtype=np.int64) - int(zp)).astype(F32) * F32(scale)
+
+
+E4M3_MAX = 448.0  # largest finite FP8 E4M3 value (the variant without infinities)
+
+
+def _e4m3_table() -> np.ndarray:
+    """Values of the non-negative finite E4M3 codes 0x00..0x7E (float64, exact):
+    code = eeee.mmm, e = 0 subnormal m/8 * 2^-6, else (1 + m/8) * 2^(e-7)."""
+    c = np.arange(0x7F)
+    e, m = c >> 3, c & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+def e4m3_to_f32(b8: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 bytes -> fp32 (exact).  S.1111.111 is NaN; there is no infinity."""
+    b = np.asarray(b8, dtype=np.uint8).astype(np.int64)
+    mag = b & 0x7F
+    val = np.where(mag == 0x7F, np.nan, _e4m3_table()[np.minimum(mag, 0x7E)])
+    return np.where(b & 0x80, -val, val).astype(F32)
+
+
+def e4m3_from_f32(x: np.ndarray) -> np.ndarray:
+    """fp32 -> FP8 E4M3 bytes: the nearest representable value, ties to the even
+    code, magnitudes beyond 448 saturating to +-448, NaN -> sign | 0x7F."""
+    xf = np.asarray(x, dtype=F32).astype(np.float64)
+    t = _e4m3_table()
+    a = np.abs(xf)
+    hi = np.clip(np.searchsorted(t, a, side="left"), 0, len(t) - 1)   # first value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - t[lo], t[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= t[-1], 0x7E, code)            # saturate (satfinite)
+    code = np.where(np.isnan(xf), 0x7F, code)
+    sign = np.signbit(xf).astype(np.int64) << 7
+    return (code | sign).astype(np.uint8)
+
+
+def fp8_quantize_rows(w: np.ndarray):
+    """FP8 E4M3 weights with one scale per output row (this module's reading of
+    [Kog]'s "FP8 ~2 FLOP/byte"): s = absmax(row) / 448 in fp32, codes =
+    e4m3(w / s) with the division in fp32, rounding to nearest even and
+    saturation at +-448; an all-zero row gets s = 0 and codes 0.  Returns
+    (codes uint8 [rows, cols], scales fp32 [rows])."""
+    wf = np.asarray(w, dtype=np.float16).astype(F32)
+    absmax = np.abs(wf).max(axis=1)
+    s = (absmax / F32(E4M3_MAX)).astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s[:, None] > 0, wf / s[:, None], F32(0.0)).astype(F32)
+    return e4m3_from_f32(q), s
+
+
+def fp8_dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """w' = e4m3(code) * s in fp32."""
+    return (e4m3_to_f32(codes) * np.asarray(scales, dtype=F32)[:, None]).astype(F32)
 
 
 INT4_GROUP = 128  # [xAI] 3.3: int4, group_size 128, symmetric
@@ -298,14 +357,21 @@ class OracleDecoder:
         self.theta = cfg.rope_theta
         self.max_ctx = cfg.max_ctx if max_ctx is None else max_ctx
         f = lambda a: np.asarray(a, dtype=np.float16).astype(F32)  # noqa: E731
+        wd = getattr(cfg, "attn_wdtype", "fp16")
+        fp8 = lambda a: fp8_dequantize_rows(*fp8_quantize_rows(a))  # noqa: E731
+        attn_w = fp8 if wd == "fp8_e4m3" else f                     # q, k, v, o and the LM head
         self.tok_emb = f(weights["tok_emb"])
-        self.lm_head = f(weights["lm_head"])
+        self.lm_head = attn_w(weights["lm_head"])
         self.final_norm = f(weights["final_norm"])
         self.layers = []
         self.int4 = []
         for lw in weights["layers"]:
-            lay = {k: f(lw[k]) for k in ("attn_norm", "ffn_norm", "wq", "wk", "wv", "wo")}
-            if cfg.ffn_wdtype == "int4_g128":
+            lay = {k: f(lw[k]) for k in ("attn_norm", "ffn_norm")}
+            lay.update({k: attn_w(lw[k]) for k in ("wq", "wk", "wv", "wo")})
+            if cfg.ffn_wdtype == "fp8_e4m3":
+                for k in ("w_gate", "w_up", "w_down"):
+                    lay[k] = fp8(lw[k])
+            elif cfg.ffn_wdtype == "int4_g128":
                 q4 = {}
                 for k in ("w_gate", "w_up", "w_down"):
                     codes, s16 = int4_quantize_g128(lw[k])
@@ -430,13 +496,18 @@ def decode_bytes_per_token(cfg, ctx_len: int) -> dict:
     (C = positions attended, including the current one): every active weight
     once, plus the K and V of all C positions in every layer."""
     d, H, h, F, V, L = cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.ffn_dim, cfg.vocab, cfg.n_layers
-    attn_w = (3 * H * h * d + d * H * h) * 2
+    fp8_attn = getattr(cfg, "attn_wdtype", "fp16") == "fp8_e4m3"
+    # FP8 matrices: one byte per weight plus a 4-byte scale per row
+    attn_w = (3 * H * h * d + d * H * h) + (3 * H * h + d) * 4 if fp8_attn else (3 * H * h * d + d * H * h) * 2
     if cfg.ffn_wdtype == "int4_g128":
         ffn_w = 3 * F * d // 2 + 3 * F * d // INT4_GROUP * 2
+    elif cfg.ffn_wdtype == "fp8_e4m3":
+        ffn_w = 3 * F * d + (2 * F + d) * 4
     else:
         ffn_w = 3 * F * d * 2
+    lm_w = V * d + V * 4 if fp8_attn else V * d * 2
     norms = 2 * d * 2
-    weights = L * (attn_w + ffn_w + norms) + V * d * 2 + d * 2 + d * 2  # LM head, final norm, embedding row
+    weights = L * (attn_w + ffn_w + norms) + lm_w + d * 2 + d * 2  # LM head, final norm, embedding row
     if cfg.kv_dtype == "fp16":
         kv = L * 2 * C_bytes(ctx_len, H, h, 2)
     elif cfg.kv_dtype == "fp8_e5m2":

@@ -104,7 +104,8 @@ class Workload:
     rms_eps: float = 1e-5
     rope_theta: float = 10000.0
     kv_dtype: str = "fp16"          # "fp16" | "fp8_e5m2" | "u8"
-    ffn_wdtype: str = "fp16"        # "fp16" | "int4_g128"
+    ffn_wdtype: str = "fp16"        # "fp16" | "int4_g128" | "fp8_e4m3"
+    attn_wdtype: str = "fp16"       # q/k/v/o and LM head: "fp16" | "fp8_e4m3"
     prompt_len: int = 16            # prompt tokens (kv_source == "prefill")
     context_len: int = 0            # synthetic KV positions (kv_source == "synthetic")
     decode_steps: int = 32
@@ -143,6 +144,9 @@ WORKLOADS = {
                         kv_source="synthetic", prompt_len=0, context_len=8192, decode_steps=128),
     "7b_int4": Workload("7b_int4", 4, 32, 4096, 32, 128, 11008, 32000, ffn_wdtype="int4_g128",
                         prompt_len=4096, decode_steps=256),
+    # the 1.8B fp16 model (same seeds, index 1) with every GEMV matrix in FP8 E4M3
+    "1p8b_fp8": Workload("1p8b_fp8", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="fp8_e4m3",
+                         attn_wdtype="fp8_e4m3", prompt_len=2048, decode_steps=256),
 }
 
 # tensor ids for the generator: per layer base 64*(layer+1) + slot

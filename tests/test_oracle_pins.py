@@ -115,6 +115,69 @@ def test_e5m2_ties_to_even():
     np.testing.assert_array_equal(r, np.array([1.0, 1.5, -1.0, 1.0], np.float32))
 
 
+# ------------------------------------------------------------------ FP8 E4M3 weights (row F2)
+def test_e4m3_all_codes_vs_torch():
+    """Every one of the 256 E4M3 codes decodes to torch's float8_e4m3fn value
+    (NaN where torch has NaN: S.1111.111)."""
+    torch = pytest.importorskip("torch")
+    b = np.arange(256, dtype=np.uint8)
+    ours = O.e4m3_to_f32(b)
+    ref = torch.from_numpy(b.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    np.testing.assert_array_equal(ours[~np.isnan(ours)], ref[~np.isnan(ref)])
+    assert O.e4m3_to_f32(np.array([0x7E], np.uint8))[0] == O.E4M3_MAX == 448.0
+    assert O.e4m3_to_f32(np.array([0x01], np.uint8))[0] == 2.0 ** -9      # smallest subnormal
+
+
+def test_e4m3_encode_vs_torch_and_saturation():
+    """fp32 -> E4M3 equals torch's round-to-nearest-even cast inside +-448;
+    beyond it the encoder saturates (torch returns NaN there)."""
+    torch = pytest.importorskip("torch")
+    x = np.concatenate([S.normal_f32(21, 1, (200000,), std=60.0), S.normal_f32(21, 2, (100000,), std=0.01)])
+    x = x[np.abs(x) <= 448.0]
+    ref = torch.from_numpy(x.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(O.e4m3_from_f32(x), ref)
+    sat = O.e4m3_from_f32(np.array([449.0, 1e6, -3000.0, np.inf], np.float32))
+    np.testing.assert_array_equal(sat, np.array([0x7E, 0x7E, 0xFE, 0x7E], np.uint8))
+    assert O.e4m3_from_f32(np.array([np.nan], np.float32))[0] & 0x7F == 0x7F
+
+
+def test_e4m3_ties_to_even():
+    """1.0625 lies halfway between 1 (code 0x38) and 1.125 (0x39): even code, 1;
+    1.1875 between 1.125 and 1.25 (0x3A): even code, 1.25."""
+    r = O.e4m3_to_f32(O.e4m3_from_f32(np.array([1.0625, 1.1875, -1.0625], np.float32)))
+    np.testing.assert_array_equal(r, np.array([1.0, 1.25, -1.0], np.float32))
+
+
+def test_fp8_row_quantizer_bounds():
+    """Row absmax maps to +-448 exactly; every weight is within half an E4M3
+    step of its dequantised value (relative 2^-4 for normals, 2^-10 * s absolute
+    for subnormals, plus the fp32 scale product); an all-zero row has s = 0."""
+    w = S.normal_f32(22, 3, (64, 512), std=0.02).astype(np.float16)
+    w[5] = 0
+    codes, s = O.fp8_quantize_rows(w)
+    assert s[5] == 0 and not codes[5].any()
+    wf = w.astype(np.float32)
+    rows = np.arange(64) != 5
+    amax_idx = np.abs(wf).argmax(axis=1)
+    top = codes[np.arange(64), amax_idx][rows]
+    assert np.all((top & 0x7F) == 0x7E)
+    back = O.fp8_dequantize_rows(codes, s)
+    err = np.abs(back - wf)
+    bound = np.maximum(np.abs(wf) * 2.0 ** -4, s[:, None] * 2.0 ** -10) * (1 + 1e-6) + 1e-12
+    assert np.all(err <= bound)
+
+
+def test_fp8_byte_model():
+    """FP8 matrices cost one byte per weight plus a 4-byte scale per row."""
+    w = S.WORKLOADS["1p8b_fp8"]
+    b = O.decode_bytes_per_token(w, 1)["weights"]
+    d, H, h, F, V, L = w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, w.n_layers
+    per_layer = (4 * d * H * h + 3 * F * d) + (3 * H * h + d + 2 * F + d) * 4 + 2 * d * 2
+    assert b == L * per_layer + V * d + V * 4 + 2 * d * 2
+    assert abs(b / O.decode_bytes_per_token(S.WORKLOADS["1p8b"], 1)["weights"] - 0.5) < 0.01
+
+
 # ------------------------------------------------------------------ fp16 rounding
 def test_fp16_round_matches_torch_and_ties():
     torch = pytest.importorskip("torch")
