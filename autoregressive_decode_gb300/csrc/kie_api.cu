@@ -27,8 +27,11 @@ extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, co
                                             cudaStream_t st);
 // tensor-core prefill (kie_prefill.cu)
 extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const __half* W, float* C, int ldc,
-                                   int M_pad, int N_pad, int K, int m_valid, uint64_t timeout_ns, int* err,
-                                   cudaStream_t st);
+                                   int M_pad, int N_pad, int K, int m_valid, const float* col_scale,
+                                   uint64_t timeout_ns, int* err, cudaStream_t st);
+extern "C" cudaError_t kie_pf_pack_e4m3(const uint8_t* codes, int n, int K, int row0, __half* dst, cudaStream_t st);
+extern "C" cudaError_t kie_launch_quant_fp8(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales,
+                                            cudaStream_t st);
 extern "C" cudaError_t kie_pf_pack(const __half* src, int n, int K, int row0, __half* dst, cudaStream_t st);
 extern "C" cudaError_t kie_pf_embed(const int32_t* tokens, int T, const uint16_t* emb, int d, float* x,
                                     cudaStream_t st);
@@ -72,18 +75,20 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Plan of one GEMV phase type (host copy).
 struct HostPhase {
-    int K = 0, KC = 0, nK = 0, rpu = 1, wfmt = WF_F16, n_units = 0;
+    int K = 0, KC = 0, nK = 0, rpu = 1, wfmt = WF_F16, n_units = 0, R = KIE_R;
     std::vector<int32_t> unit_begin;   // G+1
     std::vector<uint32_t> bytes;       // G
     std::vector<uint32_t> nslots;      // G
     uint64_t unit_bytes() const {      // stream bytes of one unit (approximate, for balancing)
-        const uint64_t row = wfmt == WF_F16 ? uint64_t(K) * 2 : uint64_t(K) / 2 + uint64_t(K) / 64;
+        const uint64_t row = wfmt == WF_F16 ? uint64_t(K) * 2 : wfmt == WF_F8 ? uint64_t(K)
+                                                                            : uint64_t(K) / 2 + uint64_t(K) / 64;
         return row * rpu;
     }
 };
 
 uint32_t slot_bytes_host(int wfmt, int rows_g, int kc) {
     if (wfmt == WF_F16) return uint32_t(rows_g) * uint32_t(kc) * 2u;
+    if (wfmt == WF_F8) return (uint32_t(rows_g) * uint32_t(kc) + 15u) & ~15u;
     uint32_t b = uint32_t(rows_g) * uint32_t(kc / 2) + uint32_t(rows_g) * uint32_t(kc / 64);
     return (b + 15u) & ~15u;
 }
@@ -92,6 +97,8 @@ struct Layout {  // byte offsets into the workspace
     size_t wstream, wstream_bytes;
     size_t emb, norms, inv_freq;
     size_t kc, vc, kv_bytes, tail, seg_scale, seg_zp;
+    // FP8 row scales (floats): per layer [QKV | O | GU | D] in each phase's row order, then the LM head
+    size_t wsc, wsc_layer, wsc_off[PH_NTYPES];
     size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl;
     size_t plan_i32, plan_u32, cta_base, cta_layer;
     size_t out_tokens, out_logits, forced, step_token, step_logits;
@@ -100,6 +107,7 @@ struct Layout {  // byte offsets into the workspace
     int pf_tc = 0;                    // prompt rows per prefill chunk (a multiple of 128)
     size_t pf_w, pf_layer_elems, pf_qkv, pf_o, pf_gu, pf_d, pf_lm;   // element offsets within a layer / of Wlm
     size_t pf_x, pf_ahi, pf_alo, pf_c, pf_q, pf_att, pf_err;
+    size_t pf_sc, pf_sc_layer;        // FP8: output-column scales (floats) per layer [QKV | O | GU | D], then Wlm
     size_t total;
     int nseg;
 };
@@ -110,7 +118,7 @@ int pad256(int n) { return (n + 255) / 256 * 256; }
 // (the uint8 cache changes stored values when a segment completes, and INT4
 // weights have no fp16 copy); every GEMM K must be a multiple of 64.
 bool prefill_tc_ok(const kie_config& c) {
-    return c.ffn_wdtype == KIE_W_FP16 && c.kv_dtype != KIE_KV_U8_ADAPTIVE && c.d_model % 64 == 0 &&
+    return c.ffn_wdtype != KIE_W_INT4_G128 && c.kv_dtype != KIE_KV_U8_ADAPTIVE && c.d_model % 64 == 0 &&
            (c.n_heads * c.head_dim) % 64 == 0 && c.ffn_dim % 64 == 0;
 }
 
@@ -132,7 +140,8 @@ bool valid_cfg(const kie_config* c, std::string& why) {
     if (c->head_dim != 64 && c->head_dim != 128) { why = "head_dim must be 64 or 128"; return false; }
     if (c->d_model % 8 || c->ffn_dim % 8 || (c->n_heads * c->head_dim) % 8) { why = "dims must be multiples of 8"; return false; }
     if (c->kv_dtype < 0 || c->kv_dtype > 2) { why = "bad kv_dtype"; return false; }
-    if (c->ffn_wdtype < 0 || c->ffn_wdtype > 1) { why = "bad ffn_wdtype"; return false; }
+    if (c->ffn_wdtype < 0 || c->ffn_wdtype > 2) { why = "bad ffn_wdtype"; return false; }
+    if (c->attn_wdtype != KIE_W_FP16 && c->attn_wdtype != KIE_W_FP8_E4M3) { why = "bad attn_wdtype"; return false; }
     if (c->ffn_wdtype == KIE_W_INT4_G128 && (c->d_model % 128 || c->ffn_dim % 128)) {
         why = "INT4 FFN needs d_model and ffn_dim multiples of 128";
         return false;
@@ -146,18 +155,21 @@ bool valid_cfg(const kie_config* c, std::string& why) {
 void build_plan(const kie_config& c, int G, Plan& pl) {
     pl.G = G;
     const int d = c.d_model, H = c.n_heads, hd = c.head_dim, F = c.ffn_dim, V = c.vocab;
-    const bool i4 = c.ffn_wdtype == KIE_W_INT4_G128;
+    const int ffn_fmt = c.ffn_wdtype == KIE_W_INT4_G128 ? WF_I4 : c.ffn_wdtype == KIE_W_FP8_E4M3 ? WF_F8 : WF_F16;
+    const int attn_fmt = c.attn_wdtype == KIE_W_FP8_E4M3 ? WF_F8 : WF_F16;
     auto setp = [&](int t, int K, int rpu, int units, int wfmt) {
         HostPhase& p = pl.ph[t];
         p.K = K; p.rpu = rpu; p.n_units = units; p.wfmt = wfmt;
-        p.KC = std::min(K, wfmt == WF_F16 ? KIE_KC_F16 : KIE_KC_I4);
+        // a 16 KB slot: 4 rows x 2048 fp16, 8 rows x 2048 FP8, or 4 rows x 4096 INT4 (+ scales)
+        p.KC = std::min(K, wfmt == WF_I4 ? KIE_KC_I4 : KIE_KC_F16);
+        p.R = wfmt == WF_F8 ? KIE_R8 : KIE_R;
         p.nK = (K + p.KC - 1) / p.KC;
     };
-    setp(PH_QKV, d, 2, 3 * H * (hd / 2), WF_F16);
-    setp(PH_O, H * hd, 1, d, WF_F16);
-    setp(PH_GU, d, 2, F, i4 ? WF_I4 : WF_F16);
-    setp(PH_D, F, 1, d, i4 ? WF_I4 : WF_F16);
-    setp(PH_LM, d, 1, V, WF_F16);
+    setp(PH_QKV, d, 2, 3 * H * (hd / 2), attn_fmt);
+    setp(PH_O, H * hd, 1, d, attn_fmt);
+    setp(PH_GU, d, 2, F, ffn_fmt);
+    setp(PH_D, F, 1, d, ffn_fmt);
+    setp(PH_LM, d, 1, V, attn_fmt);
 
     std::vector<uint64_t> cum(G, 0);
     auto assign = [&](int t, std::vector<uint64_t>& acc, uint64_t weight) {
@@ -174,10 +186,10 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
         p.nslots.assign(G, 0);
         for (int i = 0; i < G; ++i) {
             const int rows = cnt[i] * p.rpu;
-            const int groups = (rows + KIE_R - 1) / KIE_R;
+            const int groups = (rows + p.R - 1) / p.R;
             uint64_t b = 0;
             for (int g = 0; g < groups; ++g) {
-                const int rg = std::min(KIE_R, rows - g * KIE_R);
+                const int rg = std::min(p.R, rows - g * p.R);
                 for (int ch = 0; ch < p.nK; ++ch) {
                     const int kc = std::min(p.KC, p.K - ch * p.KC);
                     b += slot_bytes_host(p.wfmt, rg, kc);
@@ -210,7 +222,7 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
         const HostPhase& p = pl.ph[t];
         for (int i = 0; i < G; ++i) {
             const int rows = (p.unit_begin[i + 1] - p.unit_begin[i]) * p.rpu;
-            part = std::max<int64_t>(part, ((rows + KIE_R - 1) / KIE_R) * KIE_R * p.nK);
+            part = std::max<int64_t>(part, int64_t((rows + p.R - 1) / p.R) * p.R * std::max(p.nK, 1));
         }
     }
     // attention: head h gets floor((h+1)G/H) - floor(hG/H) >= floor(G/H) CTAs; a
@@ -240,6 +252,15 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.norms = take((size_t(c.n_layers) * 2 + 1) * d * 4);
     L.inv_freq = take(size_t(hd / 2) * 4);
     const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
+    {
+        const size_t rows[PH_NTYPES] = {size_t(3) * H * hd, size_t(d), size_t(2) * F, size_t(d), size_t(V)};
+        const bool f8 = c.attn_wdtype == KIE_W_FP8_E4M3 || c.ffn_wdtype == KIE_W_FP8_E4M3;
+        size_t o8 = 0;
+        for (int t : {PH_QKV, PH_O, PH_GU, PH_D}) { L.wsc_off[t] = o8; o8 += rows[t]; }
+        L.wsc_layer = o8;
+        L.wsc_off[PH_LM] = o8 * c.n_layers;
+        L.wsc = take(f8 ? (L.wsc_off[PH_LM] + rows[PH_LM]) * 4 : 0);
+    }
     L.kv_bytes = size_t(c.n_layers) * H * c.max_ctx * hd * esz;
     L.kc = take(L.kv_bytes);
     L.vc = take(L.kv_bytes);
@@ -292,6 +313,9 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
         L.pf_q = take(size_t(L.pf_tc) * HD * 4);
         L.pf_att = take(size_t(L.pf_tc) * HD * 4);
         L.pf_err = take(16);
+        const bool f8 = c.attn_wdtype == KIE_W_FP8_E4M3 || c.ffn_wdtype == KIE_W_FP8_E4M3;
+        L.pf_sc_layer = size_t(3) * HD + d + 2 * size_t(F) + d;
+        L.pf_sc = take(f8 ? (L.pf_sc_layer * c.n_layers + size_t(V)) * 4 : 0);
     }
     L.total = align_up(o, 256);
 }
@@ -521,6 +545,10 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
     const float scale = 1.0f / std::sqrt(float(hd));
     const int nqkv = pad256(3 * HD), ngu = pad256(2 * F), nd = pad256(d), nv = pad256(V);
     const uint64_t to = e->timeout_ns;
+    // FP8 matrices: the GEMM output columns take their row scales
+    const float* pfsc = reinterpret_cast<const float*>(e->dev(L.pf_sc));
+    const bool a8 = c.attn_wdtype == KIE_W_FP8_E4M3, f8 = c.ffn_wdtype == KIE_W_FP8_E4M3;
+    auto colsc = [&](bool on, size_t off) -> const float* { return on ? pfsc + off : nullptr; };
     KIE_CUDA(e, cudaMemsetAsync(err, 0, 4, st));
     KIE_CUDA(e, cudaMemcpyAsync(d_tok, tokens, size_t(n) * 4, cudaMemcpyHostToDevice, st));
     const int pos_start = e->pos;
@@ -531,28 +559,32 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
         KIE_CUDA(e, kie_pf_embed(d_tok + c0, Tn, emb, d, x, st));
         for (int l = 0; l < c.n_layers; ++l) {
             const __half* W = pfw + L.pf_layer_elems * l;
+            const size_t sb = L.pf_sc_layer * l;
             const float* g1 = norms + size_t(2 * l) * d;
             const float* g2 = g1 + d;
             KIE_CUDA(e, kie_pf_norm_split(x, d, g1, c.rms_eps, Tn, Tp, d, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, colsc(a8, sb), to, err, st));
             KIE_CUDA(e, kie_pf_qkv_post(C, nqkv, Tn, pos, H, hd, inv_freq, kvf, e->dev(L.kc), e->dev(L.vc), l,
                                         c.max_ctx, Q, st));
             KIE_CUDA(e, kie_pf_attention(Q, e->dev(L.kc), e->dev(L.vc), l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O,
                                          st));
             KIE_CUDA(e, kie_pf_split(O, HD, Tn, Tp, HD, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, colsc(a8, sb + 3 * HD), to, err, st));
             KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));
             KIE_CUDA(e, kie_pf_norm_split(x, d, g2, c.rms_eps, Tn, Tp, d, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_gu, C, ngu, Tp, ngu, d, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_gu, C, ngu, Tp, ngu, d, Tn, colsc(f8, sb + 3 * HD + d), to, err,
+                                    st));
             KIE_CUDA(e, kie_pf_swiglu_split(C, ngu, Tn, Tp, F, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_d, C, nd, Tp, nd, F, Tn, to, err, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_d, C, nd, Tp, nd, F, Tn,
+                                    colsc(f8, sb + 3 * HD + d + 2 * size_t(F)), to, err, st));
             KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));
         }
     }
     // logits of the last prompt row
     KIE_CUDA(e, kie_pf_norm_split(x + size_t(Tn - 1) * d, d, norms + size_t(2 * c.n_layers) * d, c.rms_eps, 1, 128, d,
                                   ahi, alo, st));
-    KIE_CUDA(e, kie_pf_gemm(ahi, alo, pfw + L.pf_lm, C, nv, 128, nv, d, 1, to, err, st));
+    KIE_CUDA(e, kie_pf_gemm(ahi, alo, pfw + L.pf_lm, C, nv, 128, nv, d, 1, colsc(a8, L.pf_sc_layer * c.n_layers), to,
+                            err, st));
     int herr = 0;
     KIE_CUDA(e, cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
     KIE_CUDA(e, cudaStreamSynchronize(st));
@@ -665,6 +697,9 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
         KiePhasePlan& q = P.ph[t];
         const HostPhase& h = pl.ph[t];
         q.K = h.K; q.KC = h.KC; q.nK = h.nK; q.rows_per_unit = h.rpu; q.wfmt = h.wfmt; q.n_units = h.n_units;
+        q.R = h.R;
+        q.wscale = h.wfmt == WF_F8 ? reinterpret_cast<const float*>(e->dev(L.wsc)) + L.wsc_off[t] : nullptr;
+        q.wscale_layer = int64_t(L.wsc_layer);
         q.unit_begin = reinterpret_cast<const int32_t*>(e->dev(L.plan_i32)) + size_t(t) * (G + 1);
         q.bytes = reinterpret_cast<const uint32_t*>(e->dev(L.plan_u32)) + size_t(t) * 2 * G;
         q.nslots = q.bytes + G;
@@ -782,17 +817,20 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
             }
             const int u0 = p.unit_begin[i], nu = p.unit_begin[i + 1] - u0;
             const int rows = nu * p.rpu;
-            const int groups = (rows + KIE_R - 1) / KIE_R;
+            const int groups = (rows + p.R - 1) / p.R;
             for (int g = 0; g < groups; ++g) {
-                const int rg = std::min(KIE_R, rows - g * KIE_R);
+                const int rg = std::min(p.R, rows - g * p.R);
                 for (int ch = 0; ch < p.nK; ++ch) {
                     const int kc = std::min(p.KC, K - ch * p.KC);
                     for (int r = 0; r < rg; ++r) {
-                        const int lr = g * KIE_R + r;
+                        const int lr = g * p.R + r;
                         int m, srow;
                         row_of(u0 + lr / p.rpu, lr % p.rpu, m, srow);
                         if (m != mat) continue;
-                        if (!int4) {
+                        if (p.wfmt == WF_F8) {   // source: the matrix's E4M3 codes [rows][K]
+                            desc.push_back({off + uint64_t(r) * kc, uint64_t(srow) * K + uint64_t(ch) * p.KC,
+                                            uint32_t(kc), 0});
+                        } else if (!int4) {
                             desc.push_back({off + uint64_t(r) * kc * 2, uint64_t(srow) * K * 2 + uint64_t(ch) * p.KC * 2,
                                             uint32_t(kc * 2), 0});
                         } else {
@@ -826,31 +864,77 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     __half* pfw = reinterpret_cast<__half*>(e->dev(L.pf_w));
     if (L.pf && cudaMemsetAsync(pfw, 0, (L.pf_lm + size_t(pad256(V)) * d) * 2, st) != cudaSuccess)
         result = fail(e, KIE_ERR_CUDA, "prefill weight clear failed");
-    auto pf_pack = [&](const uint8_t* src, int n, int K, int row0, size_t off) -> bool {
-        return !L.pf || kie_pf_pack(reinterpret_cast<const __half*>(src), n, K, row0, pfw + off, st) == cudaSuccess;
-    };
     const int HDm = H * hd;
+    // FP8 staging: one matrix's codes and row scales; host copies of the scales
+    const bool any_f8 = c.attn_wdtype == KIE_W_FP8_E4M3 || c.ffn_wdtype == KIE_W_FP8_E4M3;
+    const size_t max_rows = std::max({size_t(HDm), size_t(F), size_t(d), size_t(V)});
+    uint8_t* f8codes = nullptr;
+    float* f8sc = nullptr;
+    if (any_f8 && (cudaMalloc(&f8codes, max_mat / 2 + 256) != cudaSuccess || cudaMalloc(&f8sc, max_rows * 4) != cudaSuccess)) {
+        if (f8codes) cudaFree(f8codes);
+        f8codes = nullptr;
+        result = fail(e, KIE_ERR_OOM, "FP8 staging cudaMalloc failed");
+    }
+    std::vector<float> sc_host(max_rows), wsc_phase, pfsc;
+    if (L.pf && any_f8) pfsc.assign(L.pf_sc_layer * c.n_layers + size_t(V), 0.f);
+    // One matrix of phase t (source fp16 `s`, n rows x K): into the decode stream
+    // (fp16 as given or FP8 codes) and, for the prefill, into its weight tiles
+    // at rows [pf_row0, pf_row0 + n) of the tile array at pf_off (with its
+    // column scales at pf_sc_off + pf_row0 for FP8).
+    auto put_matrix = [&](int t, int l, int m, auto row_of, const uint8_t* s, int n, int K, size_t pf_off, int pf_row0,
+                          size_t pf_sc_off) -> bool {
+        const HostPhase& p = pl.ph[t];
+        if (p.wfmt != WF_F8) {
+            if (L.pf && kie_pf_pack(reinterpret_cast<const __half*>(s), n, K, pf_row0, pfw + pf_off, st) != cudaSuccess)
+                return false;
+            emit(t, l, m, row_of, false, 0, 0);
+            return flush(s);
+        }
+        if (kie_launch_quant_fp8(reinterpret_cast<const uint16_t*>(s), n, K, f8codes, f8sc, st) != cudaSuccess) return false;
+        if (L.pf && kie_pf_pack_e4m3(f8codes, n, K, pf_row0, pfw + pf_off, st) != cudaSuccess) return false;
+        emit(t, l, m, row_of, false, 0, 0);
+        if (!flush(f8codes)) return false;
+        if (cudaMemcpy(sc_host.data(), f8sc, size_t(n) * 4, cudaMemcpyDeviceToHost) != cudaSuccess) return false;
+        // scales in the phase's row order (phase row = unit * rows_per_unit + half)
+        for (int U = 0; U < p.n_units; ++U)
+            for (int half = 0; half < p.rpu; ++half) {
+                int mm, srow;
+                row_of(U, half, mm, srow);
+                if (mm == m) wsc_phase[size_t(U) * p.rpu + half] = sc_host[srow];
+            }
+        if (L.pf) std::copy(sc_host.begin(), sc_host.begin() + n, pfsc.begin() + pf_sc_off + pf_row0);
+        return true;
+    };
+    auto put_scales = [&](int t, int l) -> bool {   // the phase's FP8 row scales, once all its matrices are in
+        const HostPhase& p = pl.ph[t];
+        if (p.wfmt != WF_F8) return true;
+        const size_t at = t == PH_LM ? L.wsc_off[PH_LM] : L.wsc_layer * l + L.wsc_off[t];
+        return cudaMemcpy(e->dev(L.wsc) + at * 4, wsc_phase.data(), size_t(p.n_units) * p.rpu * 4,
+                          cudaMemcpyHostToDevice) == cudaSuccess;
+    };
     for (int l = 0; l < c.n_layers && result == KIE_OK; ++l) {
         const kie_layer_weights& lw = w->layers[l];
         const uint16_t* qkv[3] = {lw.wq, lw.wk, lw.wv};
-        const size_t lb = L.pf_layer_elems * l;
+        const size_t lb = L.pf_layer_elems * l, sb = L.pf_sc_layer * l;
+        wsc_phase.assign(size_t(3) * HDm, 0.f);
         for (int m = 0; m < 3 && result == KIE_OK; ++m) {
             const uint8_t* s = src_of(qkv[m], size_t(H) * hd * d * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
-            if (!pf_pack(s, HDm, d, m * HDm, lb + L.pf_qkv)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
-            emit(PH_QKV, l, m, qkv_row, false, 0, 0);
-            if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            if (!put_matrix(PH_QKV, l, m, qkv_row, s, HDm, d, lb + L.pf_qkv, m * HDm, sb))
+                result = fail(e, KIE_ERR_CUDA, "repack failed");
         }
+        if (result == KIE_OK && !put_scales(PH_QKV, l)) result = fail(e, KIE_ERR_CUDA, "scale upload failed");
         if (result != KIE_OK) break;
         {
+            wsc_phase.assign(size_t(d), 0.f);
             const uint8_t* s = src_of(lw.wo, size_t(d) * H * hd * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
-            if (!pf_pack(s, d, HDm, 0, lb + L.pf_o)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
-            emit(PH_O, l, 0, plain_row, false, 0, 0);
-            if (!flush(s)) { result = fail(e, KIE_ERR_CUDA, "repack failed"); break; }
+            if (!put_matrix(PH_O, l, 0, plain_row, s, d, HDm, lb + L.pf_o, 0, sb + size_t(3) * HDm) ||
+                !put_scales(PH_O, l)) { result = fail(e, KIE_ERR_CUDA, "repack failed"); break; }
         }
         const bool q4 = c.ffn_wdtype == KIE_W_INT4_G128;
         const uint16_t* gu[2] = {lw.w_gate, lw.w_up};
+        wsc_phase.assign(size_t(2) * F, 0.f);
         for (int m = 0; m < 2 && result == KIE_OK; ++m) {
             const uint8_t* s = src_of(gu[m], size_t(F) * d * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
@@ -863,14 +947,14 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
                 }
                 emit(PH_GU, l, m, gu_row, true, 0, sc_off);
                 if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
-            } else {
-                if (!pf_pack(s, F, d, m * F, lb + L.pf_gu)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
-                emit(PH_GU, l, m, gu_row, false, 0, 0);
-                if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            } else if (!put_matrix(PH_GU, l, m, gu_row, s, F, d, lb + L.pf_gu, m * F, sb + size_t(3) * HDm + d)) {
+                result = fail(e, KIE_ERR_CUDA, "repack failed");
             }
         }
+        if (result == KIE_OK && !put_scales(PH_GU, l)) result = fail(e, KIE_ERR_CUDA, "scale upload failed");
         if (result != KIE_OK) break;
         {
+            wsc_phase.assign(size_t(d), 0.f);
             const uint8_t* s = src_of(lw.w_down, size_t(d) * F * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
             if (q4) {
@@ -882,22 +966,25 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
                 }
                 emit(PH_D, l, 0, plain_row, true, 0, sc_off);
                 if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
-            } else {
-                if (!pf_pack(s, d, F, 0, lb + L.pf_d)) { result = fail(e, KIE_ERR_CUDA, "prefill pack failed"); break; }
-                emit(PH_D, l, 0, plain_row, false, 0, 0);
-                if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
+            } else if (!put_matrix(PH_D, l, 0, plain_row, s, d, F, lb + L.pf_d, 0, sb + size_t(3) * HDm + d + 2 * size_t(F)) ||
+                       !put_scales(PH_D, l)) {
+                result = fail(e, KIE_ERR_CUDA, "repack failed");
             }
         }
     }
     if (result == KIE_OK) {
+        wsc_phase.assign(size_t(V), 0.f);
         const uint8_t* s = src_of(w->lm_head, size_t(V) * d * 2);
         if (!s) result = fail(e, KIE_ERR_CUDA, "weight upload failed");
-        else if (!pf_pack(s, V, d, 0, L.pf_lm)) result = fail(e, KIE_ERR_CUDA, "prefill pack failed");
-        else {
-            emit(PH_LM, 0, 0, plain_row, false, 0, 0);
-            if (!flush(s)) result = fail(e, KIE_ERR_CUDA, "repack failed");
-        }
+        else if (!put_matrix(PH_LM, 0, 0, plain_row, s, V, d, L.pf_lm, 0, L.pf_sc_layer * c.n_layers) ||
+                 !put_scales(PH_LM, 0))
+            result = fail(e, KIE_ERR_CUDA, "repack failed");
     }
+    if (result == KIE_OK && L.pf && any_f8 &&
+        cudaMemcpy(e->dev(L.pf_sc), pfsc.data(), pfsc.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+        result = fail(e, KIE_ERR_CUDA, "prefill scale upload failed");
+    if (f8codes) cudaFree(f8codes);
+    if (f8sc) cudaFree(f8sc);
     cudaStreamSynchronize(st);
     free_all();
     if (result != KIE_OK) return result;
@@ -1160,6 +1247,24 @@ kie_status kie_quantize_int4_g128(const uint16_t* w_fp16, int32_t rows, int32_t 
         cudaMemcpy(codes, buf + o_codes, n, cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemcpy(scale_fp16, buf + o_sc, n / 128 * 2, cudaMemcpyDeviceToHost) != cudaSuccess)
         st = fail(nullptr, KIE_ERR_CUDA, "INT4 quantisation failed: %s", cudaGetErrorString(cudaGetLastError()));
+    cudaFree(buf);
+    return st;
+}
+
+kie_status kie_quantize_fp8_rows(const uint16_t* w_fp16, int32_t rows, int32_t cols, uint8_t* codes, float* scales) {
+    if (!w_fp16 || !codes || !scales || rows <= 0 || cols <= 0 || cols % 2)
+        return fail(nullptr, KIE_ERR_INVALID_ARG, "bad arguments");
+    const size_t n = size_t(rows) * cols;
+    uint8_t* buf = nullptr;
+    const size_t o_codes = align_up(n * 2, 256), o_sc = o_codes + align_up(n, 256);
+    if (cudaMalloc(&buf, o_sc + size_t(rows) * 4) != cudaSuccess) return fail(nullptr, KIE_ERR_OOM, "cudaMalloc failed");
+    kie_status st = KIE_OK;
+    if (cudaMemcpy(buf, w_fp16, n * 2, cudaMemcpyHostToDevice) != cudaSuccess ||
+        kie_launch_quant_fp8(reinterpret_cast<uint16_t*>(buf), rows, cols, buf + o_codes,
+                             reinterpret_cast<float*>(buf + o_sc), nullptr) != cudaSuccess ||
+        cudaMemcpy(codes, buf + o_codes, n, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(scales, buf + o_sc, size_t(rows) * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(nullptr, KIE_ERR_CUDA, "FP8 quantisation failed: %s", cudaGetErrorString(cudaGetLastError()));
     cudaFree(buf);
     return st;
 }

@@ -59,6 +59,7 @@ struct Smem {
     float* rope;      // [2][hd/2] cos, sin of the current step's position
     float* red;       // reduction scratch: NW*(KIE_MAX_HEAD_DIM+2) + 64 floats
     float* xres;      // [KIE_XRES] old x of the rows the next residual epilogue updates
+    float* wsc;       // FP8 phases: the row scales of this CTA's rows
     float* part;      // GEMV partial sums
     float* act;       // activation (piece-split layout) / attention scores
     uint8_t* ring;
@@ -76,6 +77,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const KieParams& P) {
     s.rope = reinterpret_cast<float*>(base + l.rope);
     s.red = reinterpret_cast<float*>(base + l.red);
     s.xres = reinterpret_cast<float*>(base + l.xres);
+    s.wsc = reinterpret_cast<float*>(base + l.wsc);
     s.part = reinterpret_cast<float*>(base + l.part);
     s.act = reinterpret_cast<float*>(base + l.act);
     s.ring = base + l.ring;
@@ -96,7 +98,7 @@ __device__ __forceinline__ int act_idx(int k, int half) {
 }
 
 struct Cursor {  // geometry of one GEMV phase for this CTA
-    int K, KC, nK, rpu, wfmt;
+    int K, KC, nK, rpu, wfmt, R;
     int unit0, n_units, rows;
     uint32_t nslots;
 };
@@ -104,7 +106,7 @@ struct Cursor {  // geometry of one GEMV phase for this CTA
 __device__ __forceinline__ Cursor cursor(const KieParams& P, const Smem& S, int type) {
     const KiePhasePlan& pp = P.ph[type];
     Cursor c;
-    c.K = pp.K; c.KC = pp.KC; c.nK = pp.nK; c.rpu = pp.rows_per_unit; c.wfmt = pp.wfmt;
+    c.K = pp.K; c.KC = pp.KC; c.nK = pp.nK; c.rpu = pp.rows_per_unit; c.wfmt = pp.wfmt; c.R = pp.R;
     c.unit0 = S.plan[type * 4 + 0];
     c.n_units = S.plan[type * 4 + 1];
     c.rows = c.n_units * c.rpu;
@@ -114,6 +116,7 @@ __device__ __forceinline__ Cursor cursor(const KieParams& P, const Smem& S, int 
 
 __device__ __forceinline__ uint32_t slot_bytes(int wfmt, int rows_g, int kc) {
     if (wfmt == WF_F16) return uint32_t(rows_g) * uint32_t(kc) * 2u;
+    if (wfmt == WF_F8) return (uint32_t(rows_g) * uint32_t(kc) + 15u) & ~15u;
     uint32_t b = uint32_t(rows_g) * uint32_t(kc / 2) + uint32_t(rows_g) * uint32_t(kc / 64);
     return (b + 15u) & ~15u;
 }
@@ -121,7 +124,7 @@ __device__ __forceinline__ uint32_t slot_bytes(int wfmt, int rows_g, int kc) {
 __device__ __forceinline__ void slot_geom(const Cursor& c, uint32_t j, int& g, int& ch, int& rows_g, int& kc) {
     g = int(j / uint32_t(c.nK));
     ch = int(j % uint32_t(c.nK));
-    rows_g = min(KIE_R, c.rows - g * KIE_R);
+    rows_g = min(c.R, c.rows - g * c.R);
     kc = min(c.KC, c.K - ch * c.KC);
 }
 
@@ -609,6 +612,33 @@ __device__ __forceinline__ void slot_f16_full(const uint8_t* slot, int k0, const
     }
 }
 
+// FP8 E4M3 slot: codes [rows_g][kc], row-major, up to KIE_R8 rows; the rows'
+// scales are applied in row_sum.  Each lane takes 8-element pieces, as for fp16.
+__device__ __forceinline__ void slot_f8(const uint8_t* slot, int rows_g, int kc, int k0, const float* act,
+                                        int half, int lane, float* acc) {
+    const int npc = kc >> 3;
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+#pragma unroll 2
+    for (int p = lane; p < npc; p += 32) {
+        const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
+#pragma unroll
+        for (int r = 0; r < KIE_R8; ++r) {
+            if (r < rows_g) {
+                const uint2 w = *reinterpret_cast<const uint2*>(slot + size_t(r) * kc + size_t(p) * 8);
+                float f[8];
+                e4m3x4_to_f32(w.x, f);
+                e4m3x4_to_f32(w.y, f + 4);
+                float t = acc[r];
+                t = fmaf(f[0], xl.x, t); t = fmaf(f[1], xl.y, t); t = fmaf(f[2], xl.z, t); t = fmaf(f[3], xl.w, t);
+                t = fmaf(f[4], xh.x, t); t = fmaf(f[5], xh.y, t); t = fmaf(f[6], xh.z, t); t = fmaf(f[7], xh.w, t);
+                acc[r] = t;
+            }
+        }
+    }
+}
+
 // INT4 slot: codes [rows_g][kc/2] (element 2b in the low nibble of byte b, two's
 // complement), then fp16 scales [rows_g][kc/128].  Each lane takes 8-element
 // pieces; a piece lies inside one 128-column group.
@@ -662,17 +692,27 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
         if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
         int g, ch, rows_g, kc;
         slot_geom(c, j, g, ch, rows_g, kc);
-        float acc[KIE_R] = {0.f, 0.f, 0.f, 0.f};
         const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
-        if (c.wfmt == WF_F16) {
-            if (rows_g == KIE_R && kc == KIE_KC_F16) slot_f16_full(sl, ch * c.KC, S.act, half, lane, acc);
-            else slot_f16(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
-        }
-        else slot_i4(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+        if (c.wfmt == WF_F8) {
+            float acc[KIE_R8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            slot_f8(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
 #pragma unroll
-        for (int r = 0; r < KIE_R; ++r) acc[r] = warp_sum(acc[r]);
-        if (lane == 0) {
-            for (int r = 0; r < rows_g; ++r) S.part[(g * KIE_R + r) * c.nK + ch] = acc[r];
+            for (int r = 0; r < KIE_R8; ++r) acc[r] = warp_sum(acc[r]);
+            if (lane == 0) {
+                for (int r = 0; r < rows_g; ++r) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
+            }
+        } else {
+            float acc[KIE_R] = {0.f, 0.f, 0.f, 0.f};
+            if (c.wfmt == WF_F16) {
+                if (rows_g == KIE_R && kc == KIE_KC_F16) slot_f16_full(sl, ch * c.KC, S.act, half, lane, acc);
+                else slot_f16(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+            }
+            else slot_i4(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+#pragma unroll
+            for (int r = 0; r < KIE_R; ++r) acc[r] = warp_sum(acc[r]);
+            if (lane == 0) {
+                for (int r = 0; r < rows_g; ++r) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
+            }
         }
         __syncwarp();
         if (lane == 0) {
@@ -686,10 +726,11 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
     return ld_volatile_i32(&S.flags[0]) == 0;
 }
 
+// Row r's output: the sum of its chunks' partials (times its scale for FP8).
 __device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) {
     float y = 0.f;
     for (int ch = 0; ch < c.nK; ++ch) y += S.part[r * c.nK + ch];
-    return y;
+    return c.wfmt == WF_F8 ? y * S.wsc[r] : y;
 }
 
 // store one element of the new K (kv=0) or V (kv=1) at position pos; returns
@@ -1431,6 +1472,12 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 // keeps the per-layer instruction working set small.
                 const int type = sub == 0 ? PH_QKV : sub == 2 ? PH_O : sub == 3 ? PH_GU : sub == 4 ? PH_D : PH_LM;
                 const Cursor c = cursor(P, S, type);
+                if (c.wfmt == WF_F8) {   // this CTA's row scales, visible after the staging's barrier
+                    const KiePhasePlan& pp = P.ph[type];
+                    const float* ws = pp.wscale + (type == PH_LM ? 0 : int64_t(layer) * pp.wscale_layer) +
+                                      int64_t(c.unit0) * c.rpu;
+                    for (int r = tid; r < c.rows; r += NCT) S.wsc[r] = __ldg(ws + r);
+                }
                 // the step's input token: read by the first layer's QKV phase,
                 // and again by its O phase when that phase starts a launch
                 if (layer == 0 && (type == PH_QKV || (type == PH_O && phi == Lc.phase_begin))) {

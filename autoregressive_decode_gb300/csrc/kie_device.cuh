@@ -207,6 +207,18 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t w) {
     return r;
 }
 
+// Four FP8 E4M3 values (byte i of w is element i) -> fp32, exactly (E4M3 -> fp16
+// is exact, then fp16 -> fp32).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+    const float2 x = h2_to_f2(lo), y = h2_to_f2(hi);
+    f[0] = x.x; f[1] = x.y; f[2] = y.x; f[3] = y.y;
+}
+
 // fp16 -> FP8 E5M2 (round to nearest even, saturate to +-57344, NaN stays NaN):
 // the hardware conversion of two fp16 values; returns two bytes (lo = a, hi = b).
 __device__ __forceinline__ uint16_t f16x2_to_e5m2x2(__half a, __half b) {

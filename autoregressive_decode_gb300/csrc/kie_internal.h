@@ -52,7 +52,7 @@
 // device (carving) both use this one function.  Offsets are relative to the
 // dynamic shared-memory base; the ring starts on a 128-byte boundary.
 struct KieSmemLayout {
-    uint32_t full, empty, cbase, flags, plan, clist, rope, red, xres, part, act, ring, total;
+    uint32_t full, empty, cbase, flags, plan, clist, rope, red, xres, wsc, part, act, ring, total;
 };
 KIE_HD inline uint32_t kie_align(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot) {
@@ -67,6 +67,7 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
     l.rope = o;  o += KIE_MAX_HEAD_DIM * 4;     // cos/sin of the step's position, [2][hd/2]
     l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64) * 4;
     l.xres = o;  o += KIE_XRES * 4;
+    l.wsc = o;   o += uint32_t(part_floats) * 4;   // FP8 row scales of the phase (part_floats >= rows)
     l.part = o;  o += uint32_t(part_floats) * 4;
     l.act = kie_align(o, 16); o = l.act + uint32_t(act_floats) * 4;
     l.ring = kie_align(o, 128);
@@ -75,7 +76,8 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
 }
 
 enum KiePhaseType { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3, PH_LM = 4, PH_NTYPES = 5 };
-enum KieWFmt { WF_F16 = 0, WF_I4 = 1 };
+enum KieWFmt { WF_F16 = 0, WF_I4 = 1, WF_F8 = 2 };
+#define KIE_R8 8                 // rows per FP8 slot (8 rows x KIE_KC_F16 one-byte weights)
 enum KieKv { KV_F16 = 0, KV_E5M2 = 1, KV_U8 = 2 };
 
 enum KieErr {
@@ -96,7 +98,10 @@ struct KiePhasePlan {
     int32_t nK;              // chunks per row = ceil(K / KC)
     int32_t rows_per_unit;   // 1 or 2
     int32_t wfmt;            // KieWFmt
+    int32_t R;               // rows per slot: KIE_R, or KIE_R8 for FP8
     int32_t n_units;         // units over the grid
+    const float* wscale;     // FP8: fp32 row scales of layer 0 in the phase's row order (null otherwise)
+    int64_t wscale_layer;    // FP8: floats between consecutive layers' scales
     const int32_t* unit_begin;   // [G+1] device: CTA i owns units [unit_begin[i], unit_begin[i+1])
     const uint32_t* bytes;       // [G]   device: stream bytes of this phase for CTA i
     const uint32_t* nslots;      // [G]   device: slots of this phase for CTA i

@@ -16,7 +16,8 @@
 // lo = fp16(a - hi) and each K step issues two MMAs, A_hi W^T + A_lo W^T, into
 // the same fp32 accumulator: the product then carries a's full precision up to
 // 2^-22 relative, well inside the fp32 reference's tolerance.  Weights are fp16
-// as given.
+// as given; FP8 E4M3 weights enter the MMA as their exact fp16 values and
+// their per-row scale multiplies the output column in the epilogue.
 //
 // Tile layout.  Both operands are stored in global memory already in the
 // tensor cores' canonical no-swizzle K-major layout, tile by tile (tiles of
@@ -65,8 +66,9 @@ __device__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns
 __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __restrict__ Ahi,
                                                              const __half* __restrict__ Alo,
                                                              const __half* __restrict__ W, float* __restrict__ C,
-                                                             int ldc, int KB, int m_valid, uint64_t timeout_ns,
-                                                             int* err) {
+                                                             int ldc, int KB, int m_valid,
+                                                             const float* __restrict__ col_scale,
+                                                             uint64_t timeout_ns, int* err) {
     extern __shared__ __align__(1024) uint8_t sm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + STAGES * STAGE_BYTES);
     uint64_t* empty = full + STAGES;
@@ -126,11 +128,14 @@ __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __res
             uint32_t v[32];
             tmem_ld_32x32b_x32(tacc + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
             if (row < m_valid) {
+                const float* cs = col_scale ? col_scale + size_t(nb) * BN + c0 : nullptr;
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4*>(crow + c0 + i) =
-                        make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                    __uint_as_float(v[i + 3]));
+                for (int i = 0; i < 32; i += 4) {
+                    float4 o = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                           __uint_as_float(v[i + 3]));
+                    if (cs) { o.x *= cs[i]; o.y *= cs[i + 1]; o.z *= cs[i + 2]; o.w *= cs[i + 3]; }
+                    *reinterpret_cast<float4*>(crow + c0 + i) = o;
+                }
             }
         }
     }
@@ -147,6 +152,23 @@ __global__ void kie_pf_pack_kernel(const __half* __restrict__ src, int n, int K,
         const int r = int(i / g8), k = int(i % g8) * 8;
         *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) =
             *reinterpret_cast<const uint4*>(src + size_t(r) * K + k);
+    }
+}
+
+// The same for E4M3 codes [n x K] (one byte each), written as their exact fp16 values.
+__global__ void kie_pf_pack_e4m3_kernel(const uint8_t* __restrict__ src, int n, int K, int row0,
+                                        __half* __restrict__ dst) {
+    const int KB = K / 64, g8 = K / 8;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < size_t(n) * g8; i += size_t(gridDim.x) * blockDim.x) {
+        const int r = int(i / g8), k = int(i % g8) * 8;
+        const uint2 c = *reinterpret_cast<const uint2*>(src + size_t(r) * K + k);
+        float f[8];
+        e4m3x4_to_f32(c.x, f);
+        e4m3x4_to_f32(c.y, f + 4);
+        __align__(16) __half h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(f[j]);   // exact: E4M3 values are fp16 values
+        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) = *reinterpret_cast<const uint4*>(h);
     }
 }
 
@@ -382,12 +404,19 @@ cudaError_t launch_attention(const float* Q, const uint8_t* kc, const uint8_t* v
 extern "C" size_t kie_pf_tile_elems(int rows_pad, int K) { return size_t(rows_pad) * K; }
 
 extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const __half* W, float* C, int ldc,
-                                   int M_pad, int N_pad, int K, int m_valid, uint64_t timeout_ns, int* err,
-                                   cudaStream_t st) {
+                                   int M_pad, int N_pad, int K, int m_valid, const float* col_scale,
+                                   uint64_t timeout_ns, int* err, cudaStream_t st) {
     cudaError_t r = cudaFuncSetAttribute(kie_pf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(GEMM_SMEM));
     if (r != cudaSuccess) return r;
     kie_pf_gemm_kernel<<<dim3(N_pad / BN, M_pad / BM), 128, GEMM_SMEM, st>>>(Ahi, Alo, W, C, ldc, K / BK, m_valid,
-                                                                            timeout_ns, err);
+                                                                            col_scale, timeout_ns, err);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_pack_e4m3(const uint8_t* codes, int n, int K, int row0, __half* dst, cudaStream_t st) {
+    const size_t work = size_t(n) * (K / 8);
+    const int blocks = int(std::min<size_t>((work + 255) / 256, 65535));
+    kie_pf_pack_e4m3_kernel<<<blocks, 256, 0, st>>>(codes, n, K, row0, dst);
     return cudaGetLastError();
 }
 

@@ -74,6 +74,33 @@ __global__ void kie_quant_int4_kernel(const uint16_t* w, int rows, int cols, uin
     if (lane == 0) scales[size_t(r) * ngrp + g] = __half_as_ushort(s16);
 }
 
+// ---- FP8 E4M3 weights, one scale per output row ----------------------------------------------
+// One warp per row: s = absmax / 448 in fp32 (IEEE division); code = E4M3 of
+// w / s (IEEE division; cvt round to nearest even, satfinite); s == 0 -> 0.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));   // first source -> upper byte
+    return r;
+}
+__global__ void kie_quant_fp8_kernel(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const uint16_t* src = w + size_t(warp) * cols;
+    float am = 0.f;
+    for (int k = lane; k < cols; k += 32) am = fmaxf(am, fabsf(__half2float(__ushort_as_half(src[k]))));
+    am = warp_max(am);
+    const float s = am / 448.0f;
+    uint8_t* dst = codes + size_t(warp) * cols;
+    for (int k = 2 * lane; k < cols; k += 64) {   // cols is even
+        const float a = __half2float(__ushort_as_half(src[k])), b = __half2float(__ushort_as_half(src[k + 1]));
+        const uint32_t c = s > 0.f ? f32x2_to_e4m3x2(a / s, b / s) : 0u;
+        dst[k] = uint8_t(c & 0xFFu);
+        dst[k + 1] = uint8_t(c >> 8);
+    }
+    if (lane == 0) scales[warp] = s;
+}
+
 // ---- adaptive-range uint8 quantisation ------------------------------------------------------
 // One CTA per segment.  A segment is `rows` rows of `row_elems` fp16 values;
 // element (r, k) of segment s is at src[s*src_seg + r*src_row + k] and its code
@@ -175,6 +202,14 @@ extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int co
     const int threads = 256;
     const long blocks = (warps * 32 + threads - 1) / threads;
     kie_quant_int4_kernel<<<unsigned(blocks), threads, 0, st>>>(w, rows, cols, packed, codes_i8, scales);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_quant_fp8(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales,
+                                            cudaStream_t st) {
+    const int threads = 256;
+    const long blocks = (long(rows) * 32 + threads - 1) / threads;
+    kie_quant_fp8_kernel<<<unsigned(blocks), threads, 0, st>>>(w, rows, cols, codes, scales);
     return cudaGetLastError();
 }
 

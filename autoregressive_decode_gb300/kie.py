@@ -23,7 +23,7 @@ KIE_OK, KIE_ERR_INVALID_ARG, KIE_ERR_OOM, KIE_ERR_CUDA = 0, -1, -2, -3
 KIE_ERR_NOT_LOADED, KIE_ERR_CTX_OVERFLOW, KIE_ERR_DEVICE_TIMEOUT = -4, -5, -6
 KIE_ERR_LAUNCH, KIE_ERR_UNSUPPORTED = -7, -8
 KV_DTYPES = {"fp16": 0, "fp8_e5m2": 1, "u8": 2}
-W_DTYPES = {"fp16": 0, "int4_g128": 1}
+W_DTYPES = {"fp16": 0, "int4_g128": 1, "fp8_e4m3": 2}
 MODES = {"persistent": 0, "graph": 1}
 
 STATUS_NAMES = {0: "KIE_OK", -1: "KIE_ERR_INVALID_ARG", -2: "KIE_ERR_OOM", -3: "KIE_ERR_CUDA",
@@ -42,7 +42,7 @@ class kie_config(C.Structure):
                 ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
                 ("max_ctx", C.c_int32), ("rms_eps", C.c_float), ("rope_theta", C.c_float),
                 ("kv_dtype", C.c_int32), ("ffn_wdtype", C.c_int32), ("mode", C.c_int32),
-                ("device", C.c_int32)]
+                ("device", C.c_int32), ("attn_wdtype", C.c_int32)]
 
 
 class kie_layer_weights(C.Structure):
@@ -80,6 +80,7 @@ EXPORTS = {
                               C.c_void_p, C.c_void_p, C.c_void_p]),
     "kie_quantize_kv_u8": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "kie_quantize_int4_g128": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
+    "kie_quantize_fp8_rows": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_convert_fp8_e5m2": (C.c_int, [C.c_void_p, C.c_size_t, C.c_void_p]),
 }
 
@@ -124,9 +125,9 @@ def _check(st, eng=None):
 
 
 def make_config(n_layers, d_model, n_heads, head_dim, ffn_dim, vocab, max_ctx, rms_eps=1e-5, rope_theta=10000.0,
-                kv_dtype="fp16", ffn_wdtype="fp16", mode="persistent", device=0) -> kie_config:
+                kv_dtype="fp16", ffn_wdtype="fp16", mode="persistent", device=0, attn_wdtype="fp16") -> kie_config:
     return kie_config(n_layers, d_model, n_heads, head_dim, ffn_dim, vocab, max_ctx, rms_eps, rope_theta,
-                      KV_DTYPES[kv_dtype], W_DTYPES[ffn_wdtype], MODES[mode], device)
+                      KV_DTYPES[kv_dtype], W_DTYPES[ffn_wdtype], MODES[mode], device, W_DTYPES[attn_wdtype])
 
 
 class Engine:
@@ -276,6 +277,16 @@ def quantize_int4_g128(w16: np.ndarray):
     sc = np.empty((rows, cols // 128), np.uint16)
     _check(load().kie_quantize_int4_g128(_ptr(w), rows, cols, _ptr(codes), _ptr(sc)))
     return codes, sc.view(np.float16)
+
+
+def quantize_fp8_rows(w16: np.ndarray):
+    """kie_quantize_fp8_rows: (codes uint8 [rows, cols], scales fp32 [rows])."""
+    w = np.ascontiguousarray(w16, dtype=np.float16)
+    rows, cols = w.shape
+    codes = np.empty((rows, cols), np.uint8)
+    sc = np.empty(rows, np.float32)
+    _check(load().kie_quantize_fp8_rows(_ptr(w), rows, cols, _ptr(codes), _ptr(sc)))
+    return codes, sc
 
 
 def convert_fp8_e5m2(x16: np.ndarray) -> np.ndarray:

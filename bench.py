@@ -53,14 +53,19 @@ def parse():
     ap.add_argument("--decode-tokens", type=int, default=None,
                     help="decode tokens per step (default: the workload's decode steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling only: the workload with this many layers (a small case of the same "
+                         "kernels for multi-pass ncu captures); the line's config records the depth")
     return ap.parse_args()
 
 
 def workload_desc(w: S.Workload) -> str:
     ctx = (f"{w.prompt_len}-token prompt" if w.kv_source == "prefill" else f"{w.context_len} synthetic KV positions")
-    ffn = "INT4 g128 FFN" if w.ffn_wdtype == "int4_g128" else "fp16 FFN"
+    names = {"int4_g128": "INT4 g128", "fp8_e4m3": "FP8 E4M3 (row scales)", "fp16": "fp16"}
+    ffn = f"{names[w.ffn_wdtype]} FFN"
+    attn = "" if w.attn_wdtype == "fp16" else f", {names[w.attn_wdtype]} q/k/v/o and LM head"
     return (f"{w.name}: {w.n_layers} layers, d {w.d_model}, {w.n_heads}x{w.head_dim} heads, FFN {w.ffn_dim}, "
-            f"vocab {w.vocab}, {ctx}, {w.decode_steps} greedy decode steps, {w.kv_dtype} KV, {ffn}")
+            f"vocab {w.vocab}, {ctx}, {w.decode_steps} greedy decode steps, {w.kv_dtype} KV, {ffn}{attn}")
 
 
 def peaks():
@@ -205,6 +210,8 @@ def run_reference(args, w: S.Workload):
 def main():
     args = parse()
     w = S.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
     if args.impl == "reference":
         return run_reference(args, w)
     import torch
@@ -220,7 +227,8 @@ def main():
     p0 = w.start_pos
     weights = S.gen_weights(w)
     cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, p0 + n_dec,
-                          w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, args.mode, local)
+                          w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, args.mode, local,
+                          attn_wdtype=w.attn_wdtype)
     stream = torch.cuda.Stream(device=local)
     eng = kie.Engine(cfg, stream=stream)
     eng.load_weights(weights)
@@ -239,7 +247,8 @@ def main():
         pf_ms = (time.perf_counter() - t0) * 1e3
         assert int(np.argmax(lg2)) == first
         prefill_info = {"tokens": len(prompt), "ms": pf_ms, "tokens_per_s": len(prompt) / (pf_ms / 1e3),
-                        "path": "tcgen05 GEMM" if w.ffn_wdtype == "fp16" and w.kv_dtype != "u8" else "decode kernel"}
+                        "path": "tcgen05 GEMM" if w.ffn_wdtype != "int4_g128" and w.kv_dtype != "u8"
+                        else "decode kernel"}
     else:
         for layer in range(w.n_layers):
             k, v = S.gen_kv(w, layer)
@@ -311,7 +320,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "storage": "fp16 weights, fp16 KV" if w.kv_dtype == "fp16" else w.kv_dtype,
+        "vs_baseline": None, "dtype": "f32", "storage": f"weights attn {w.attn_wdtype} / FFN {w.ffn_wdtype}, KV {w.kv_dtype}",
         "data": "synthetic",
         "config": {"workload": workload_desc(w), "decode_tokens_per_step": n_dec,
                    "positions": f"{p0}..{p0 + n_dec - 1}", "mode": args.mode,

@@ -63,9 +63,16 @@ typedef enum {
 } kie_status;
 
 typedef enum { KIE_KV_FP16 = 0, KIE_KV_FP8_E5M2 = 1, KIE_KV_U8_ADAPTIVE = 2 } kie_kv_dtype;
-typedef enum { KIE_W_FP16 = 0, KIE_W_INT4_G128 = 1 } kie_w_dtype;   /* FFN weights only */
-/* PERSISTENT: one cooperative launch runs all requested tokens (grid-wide
- * barriers between phases).  GRAPH: the same phases as separate launches,
+/* Weight storage of the GEMV matrices.  FP16: as given.  INT4_G128 (FFN only):
+ * symmetric INT4, group 128 (xAI page sections 2.3, 3.3).  FP8_E4M3: one byte
+ * per weight with one fp32 scale per output row, s = absmax/448, codes = E4M3
+ * of w/s rounded to nearest even, saturating (the Kog page's "FP8 ~2 FLOP per
+ * byte", section "Memory bandwidth is the main bottleneck"; the format and the
+ * scale granularity are this engine's reading). */
+typedef enum { KIE_W_FP16 = 0, KIE_W_INT4_G128 = 1, KIE_W_FP8_E4M3 = 2 } kie_w_dtype;
+/* PERSISTENT: one cooperative launch runs all requested tokens (a grid-wide
+ * barrier between steps; the phases of a step are ordered by tagged
+ * activations).  GRAPH: the same phases as separate launches,
  * captured once into a CUDA graph per engine and replayed once per token.
  * Both give bit-identical tokens and logits (same partitioning and reduction
  * order). */
@@ -82,16 +89,18 @@ typedef struct {
     float rms_eps;
     float rope_theta;
     int32_t kv_dtype;     /* kie_kv_dtype                                           */
-    int32_t ffn_wdtype;   /* kie_w_dtype                                            */
+    int32_t ffn_wdtype;   /* kie_w_dtype of w_gate, w_up, w_down                     */
     int32_t mode;         /* kie_mode                                               */
     int32_t device;       /* CUDA device ordinal                                    */
+    int32_t attn_wdtype;  /* kie_w_dtype of wq, wk, wv, wo and the LM head: FP16 or FP8_E4M3 */
 } kie_config;
 
 /* Per-layer weights, fp16 bit patterns, PyTorch Linear layout [out][in], row major.
  *   attn_norm[d]  wq,wk,wv[H*h][d]  wo[d][H*h]  ffn_norm[d]
  *   w_gate,w_up[F][d]  w_down[d][F]
  * For ffn_wdtype == KIE_W_INT4_G128 the engine quantises w_gate/w_up/w_down
- * itself (kie_quantize_int4_g128 below). */
+ * itself (kie_quantize_int4_g128 below); for KIE_W_FP8_E4M3 (ffn_wdtype or
+ * attn_wdtype) it quantises the matrices concerned with kie_quantize_fp8_rows. */
 typedef struct {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
 } kie_layer_weights;
@@ -242,6 +251,13 @@ kie_status kie_quantize_kv_u8(const uint16_t* x_fp16, int32_t n_seg, int32_t seg
  * [rows][cols/128].  cols must be a multiple of 128. */
 kie_status kie_quantize_int4_g128(const uint16_t* w_fp16, int32_t rows, int32_t cols, int8_t* codes,
                                   uint16_t* scale_fp16);
+
+/* FP8 E4M3 weight quantisation with one fp32 scale per output row (see
+ * kie_w_dtype): s = absmax(row)/448 in fp32; codes = E4M3(w/s), the division in
+ * fp32, round to nearest even, saturating at +-448; an all-zero row gets s = 0
+ * and codes 0.  Host pointers: w_fp16 [rows][cols] in, codes [rows][cols] and
+ * scales [rows] out.  Runs on the current CUDA device and synchronises it. */
+kie_status kie_quantize_fp8_rows(const uint16_t* w_fp16, int32_t rows, int32_t cols, uint8_t* codes, float* scales);
 
 /* fp16 -> FP8 E5M2, round to nearest even, saturating to +-57344 (the cache's
  * conversion; xAI page sections 2.3 and 4.3).  NaN stays NaN. */

@@ -17,12 +17,13 @@ MARGIN = 0.1
 
 
 def tol_for(w: S.Workload) -> float:
-    return TOL_FP16 if (w.kv_dtype == "fp16" and w.ffn_wdtype == "fp16") else TOL_QUANT
+    return TOL_FP16 if (w.kv_dtype == "fp16" and w.ffn_wdtype == "fp16" and w.attn_wdtype == "fp16") else TOL_QUANT
 
 
 def engine_for(w: S.Workload, weights: dict, mode: str = "persistent", max_ctx: int | None = None) -> kie.Engine:
     cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab,
-                          max_ctx or w.max_ctx, w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, mode)
+                          max_ctx or w.max_ctx, w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, mode,
+                          attn_wdtype=w.attn_wdtype)
     e = kie.Engine(cfg)
     e.load_weights(weights)
     return e

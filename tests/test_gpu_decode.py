@@ -112,6 +112,41 @@ def test_step_by_step_equals_generate(w):
         np.testing.assert_array_equal(lg, logs[i])
 
 
+@pytest.mark.parametrize("w", [TINY, MEDIUM, WIDE], ids=lambda w: w.name)
+def test_fp8_weights_prefill_and_decode(w):
+    """Every GEMV matrix in FP8 E4M3 with row scales (decode: 8-row slots, the
+    scale applied to the row sum; prefill: the codes' fp16 values in the MMA,
+    the scale on the output column): logits match the oracle's model with the
+    same quantised weights."""
+    w = w.with_(ffn_wdtype="fp8_e4m3", attn_wdtype="fp8_e4m3")
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    tol = tol_for(w)
+    assert np.abs(lg - lo).max() <= tol
+    teacher_forced(e, o, O.argmax_lowest(lo), 8, tol)
+
+
+def test_fp8_weights_graph_equals_persistent_and_u8_cache():
+    """FP8 weights in both launch modes (bit-identical), and with the uint8
+    cache (prefill through the decode kernel)."""
+    w = WIDE.with_(ffn_wdtype="fp8_e4m3", attn_wdtype="fp8_e4m3")
+    weights = S.gen_weights(w)
+    prompt = S.gen_prompt(w)
+    res = {}
+    for mode in ("persistent", "graph"):
+        e = engine_for(w, weights, mode)
+        lg = e.prefill(prompt)
+        toks, logs = e.generate_greedy(int(np.argmax(lg)), 6, want_logits=True)
+        res[mode] = (lg, toks, logs)
+        e.close()
+    for a, b in zip(res["persistent"], res["graph"]):
+        np.testing.assert_array_equal(a, b)
+    wu = w.with_(kv_dtype="u8")
+    e, o, lg, lo = _prefill_both(wu, weights)
+    assert np.abs(lg - lo).max() <= tol_for(wu)
+    teacher_forced(e, o, O.argmax_lowest(lo), 4, tol_for(wu))
+
+
 @pytest.mark.parametrize("kv", ["fp16", "fp8_e5m2"])
 def test_long_chunks_synthetic_context(kv):
     """2,300 context positions over 9-10 CTAs per head: chunks of ~240 rows need

@@ -89,3 +89,17 @@ def test_7b_int4_decode():
     o = O.OracleDecoder(w, weights, max_ctx=w.context_len + STEPS)
     _synthetic_context(w, e, o)
     teacher_forced(e, o, S.gen_first_token(w), STEPS, tol_for(w))
+
+
+def test_1p8b_fp8_weights_prefill_and_decode():
+    """The 1.8B model with every GEMV matrix in FP8 E4M3 (the bench's 1p8b_fp8):
+    2,048-token tensor-core prefill, then teacher-forced decode steps."""
+    w = S.WORKLOADS["1p8b_fp8"]
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights, max_ctx=w.prompt_len + STEPS)
+    o = O.OracleDecoder(w, weights, max_ctx=w.prompt_len + STEPS)
+    prompt = S.gen_prompt(w)
+    lg = e.prefill(prompt)
+    lo = o.prefill(prompt, q_block=512)
+    assert np.abs(lg - lo).max() <= tol_for(w)
+    teacher_forced(e, o, O.argmax_lowest(lo), STEPS, tol_for(w))

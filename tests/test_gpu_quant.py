@@ -49,3 +49,16 @@ def test_int4_bit_exact(shape):
     rc, rs = O.int4_quantize_g128(w)
     np.testing.assert_array_equal(sc.view(np.uint16), rs.view(np.uint16))
     np.testing.assert_array_equal(codes, rc)
+
+
+@pytest.mark.parametrize("shape", [(64, 2048), (37, 8192), (9, 250)])
+def test_fp8_rows_bit_exact(shape):
+    """FP8 E4M3 weight codes and fp32 row scales equal the oracle's, including
+    an all-zero row and a row with one large outlier."""
+    w = S.normal_f16(300 + shape[0], 9, shape)
+    w[0] = 0
+    w[1, 3] = np.float16(40.0)
+    codes, sc = kie.quantize_fp8_rows(w)
+    rc, rs = O.fp8_quantize_rows(w)
+    np.testing.assert_array_equal(sc.view(np.uint32), rs.view(np.uint32))
+    np.testing.assert_array_equal(codes, rc)
