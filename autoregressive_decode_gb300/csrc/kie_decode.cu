@@ -639,6 +639,31 @@ __device__ __forceinline__ void slot_f8(const uint8_t* slot, int rows_g, int kc,
     }
 }
 
+// The common full FP8 slot (KIE_R8 rows x KIE_KC_F16 columns) with compile-time
+// bounds, so that the loads of consecutive pieces can be in flight together.
+__device__ __forceinline__ void slot_f8_full(const uint8_t* slot, int k0, const float* act, int half, int lane,
+                                             float* acc) {
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+#pragma unroll 2
+    for (int it = 0; it < KIE_KC_F16 / 256; ++it) {
+        const int p = lane + it * 32;
+        const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
+#pragma unroll
+        for (int r = 0; r < KIE_R8; ++r) {
+            const uint2 w = *reinterpret_cast<const uint2*>(slot + size_t(r) * KIE_KC_F16 + size_t(p) * 8);
+            float f[8];
+            e4m3x4_to_f32(w.x, f);
+            e4m3x4_to_f32(w.y, f + 4);
+            float t = acc[r];
+            t = fmaf(f[0], xl.x, t); t = fmaf(f[1], xl.y, t); t = fmaf(f[2], xl.z, t); t = fmaf(f[3], xl.w, t);
+            t = fmaf(f[4], xh.x, t); t = fmaf(f[5], xh.y, t); t = fmaf(f[6], xh.z, t); t = fmaf(f[7], xh.w, t);
+            acc[r] = t;
+        }
+    }
+}
+
 // INT4 slot: codes [rows_g][kc/2] (element 2b in the low nibble of byte b, two's
 // complement), then fp16 scales [rows_g][kc/128].  Each lane takes 8-element
 // pieces; a piece lies inside one 128-column group.
@@ -695,11 +720,14 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
         const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
         if (c.wfmt == WF_F8) {
             float acc[KIE_R8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            slot_f8(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+            if (rows_g == KIE_R8 && kc == KIE_KC_F16) slot_f8_full(sl, ch * c.KC, S.act, half, lane, acc);
+            else slot_f8(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
 #pragma unroll
             for (int r = 0; r < KIE_R8; ++r) acc[r] = warp_sum(acc[r]);
             if (lane == 0) {
-                for (int r = 0; r < rows_g; ++r) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
+#pragma unroll
+                for (int r = 0; r < KIE_R8; ++r)   // constant indices: acc stays in registers
+                    if (r < rows_g) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
             }
         } else {
             float acc[KIE_R] = {0.f, 0.f, 0.f, 0.f};
@@ -711,7 +739,9 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
 #pragma unroll
             for (int r = 0; r < KIE_R; ++r) acc[r] = warp_sum(acc[r]);
             if (lane == 0) {
-                for (int r = 0; r < rows_g; ++r) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
+#pragma unroll
+                for (int r = 0; r < KIE_R; ++r)
+                    if (r < rows_g) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
             }
         }
         __syncwarp();
