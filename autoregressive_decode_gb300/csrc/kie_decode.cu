@@ -60,6 +60,7 @@ struct Smem {
     float* red;       // reduction scratch: NW*(KIE_MAX_HEAD_DIM+2) + 64 floats
     float* xres;      // [KIE_XRES] old x of the rows the next residual epilogue updates
     float* wsc;       // FP8 phases: the row scales of this CTA's rows
+    int32_t* cnt;     // GEMV phases with several column chunks: chunks done per row group
     float* part;      // GEMV partial sums
     float* act;       // activation (piece-split layout) / attention scores
     uint8_t* ring;
@@ -78,6 +79,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const KieParams& P) {
     s.red = reinterpret_cast<float*>(base + l.red);
     s.xres = reinterpret_cast<float*>(base + l.xres);
     s.wsc = reinterpret_cast<float*>(base + l.wsc);
+    s.cnt = reinterpret_cast<int32_t*>(base + l.cnt);
     s.part = reinterpret_cast<float*>(base + l.part);
     s.act = reinterpret_cast<float*>(base + l.act);
     s.ring = base + l.ring;
@@ -702,10 +704,112 @@ __device__ __forceinline__ void slot_i4(const uint8_t* slot, int rows_g, int kc,
     }
 }
 
-// Consume this phase's slots (those with global index == warp mod NW) and leave
-// per-(row, chunk) partial sums in S.part.  Returns false on abort.
+// Row r's output: the sum of its chunks' partials (times its scale for FP8).
+__device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) {
+    float y = 0.f;
+    for (int ch = 0; ch < c.nK; ++ch) y += S.part[r * c.nK + ch];
+    return c.wfmt == WF_F8 ? y * S.wsc[r] : y;
+}
+
+// store one element of the new K (kv=0) or V (kv=1) at position pos; returns
+// the stored bits (fp16, or the E5M2 byte)
+__device__ __forceinline__ uint32_t kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v) {
+    const __half hv = __float2half_rn(v);
+    if (P.kv == KV_F16) {
+        uint8_t* base = kv ? P.vc : P.kc;
+        reinterpret_cast<__half*>(base)[kv_elem_index(P, layer, h, pos) + dim] = hv;
+    } else if (P.kv == KV_E5M2) {
+        uint8_t* base = kv ? P.vc : P.kc;
+        const uint32_t b = f16x2_to_e5m2x2(hv, hv) & 0xFFu;
+        base[kv_elem_index(P, layer, h, pos) + dim] = uint8_t(b);
+        return b;
+    } else {
+        reinterpret_cast<__half*>(P.tail)[tail_index(P, layer, kv, h, pos % KIE_SEG) + dim] = hv;
+    }
+    return __half_as_ushort(hv);
+}
+
+// ---------------------------------------------------------------------------------------------
+// phase epilogues
+// ---------------------------------------------------------------------------------------------
+// The epilogues of the QKV, O, GU and D phases run per row group, by the warp
+// that completes the group's last column chunk, as soon as it is complete:
+// the phase's outputs leave the CTA while its other warps are still in the
+// GEMV, and the last one right after the CTA's last slot.
+struct EpiArgs {
+    int type;              // PH_QKV, PH_O, PH_GU, PH_D; PH_LM: no group epilogue
+    int layer, pos;
+    uint32_t n;            // write number of the layer (tags of q, K, V, a)
+    float rinv;            // QKV, GU: 1 / sqrt(mean(x^2) + eps) of the staged x
+    const uint16_t* erow;  // first layer's O: the embedding row is the old x
+    uint32_t par_in, par_out;   // O, D: parity of the old and the new x
+    bool have_xres;        // O, D: the old x of this CTA's rows is in S.xres
+};
+
+// Unit u (local) of the QKV phase: the RoPE pair (i, i + hd/2) of q or K of
+// head h, or the same pair of V.  Writes the cache (for later steps) and the
+// tagged q / current-position K, V (for this step's attention).
+__device__ __forceinline__ void qkv_unit(const KieParams& P, const Smem& S, const Cursor& c, const EpiArgs& e,
+                                         int u, float ya, float yb) {
+    const int hh = P.hd / 2, lhh = P.hd == 128 ? 6 : 5;   // hd is 64 or 128
+    const int per = P.H * hh;  // units per matrix
+    const uint32_t par = tag_par(e.n), ep16 = tag_ep16(e.n);
+    const int U = c.unit0 + u;
+    const int which = (U >= per) + (U >= 2 * per), rem = U - which * per;
+    const int h = rem >> lhh, i = rem & (hh - 1);
+    const int e0 = h * P.hd + i;
+    if (which == 2) {
+        const uint32_t b0 = kv_store(P, e.layer, 1, h, e.pos, i, ya), b1 = kv_store(P, e.layer, 1, h, e.pos, i + hh, yb);
+        st_relaxed_u32(P.vcur + e0, (b0 << 16) | ep16);
+        st_relaxed_u32(P.vcur + e0 + hh, (b1 << 16) | ep16);
+        return;
+    }
+    const float cs = S.rope[i], sn = S.rope[hh + i];
+    const float ra = ya * cs - yb * sn, rb = yb * cs + ya * sn;
+    if (which == 0) {
+        st_relaxed_f32(P.q + e0, tag_f32(ra, par));
+        st_relaxed_f32(P.q + e0 + hh, tag_f32(rb, par));
+    } else {
+        const uint32_t b0 = kv_store(P, e.layer, 0, h, e.pos, i, ra), b1 = kv_store(P, e.layer, 0, h, e.pos, i + hh, rb);
+        st_relaxed_u32(P.kcur + e0, (b0 << 16) | ep16);
+        st_relaxed_u32(P.kcur + e0 + hh, (b1 << 16) | ep16);
+    }
+}
+
+// Row r (local) of the O or D phase: x[row] += y.  The old x[row] comes from
+// S.xres when this launch ran the staging that kept it (at most KIE_XRES
+// rows), is the embedding row in the first layer's O phase, and is otherwise
+// polled with parity par_in; the new x carries par_out.
+__device__ __forceinline__ void residual_row(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                             const Cursor& c, const EpiArgs& e, int r, float y, int cta) {
+    const int row = c.unit0 + r;
+    const float xo = (e.have_xres && c.rows <= KIE_XRES) ? S.xres[r]
+                     : e.erow ? __half2float(__ushort_as_half(e.erow[row]))
+                              : wait_f32(P, Lc, S, P.x + row, e.par_in, cta);
+    st_relaxed_f32(P.x + row, tag_f32(xo + y, e.par_out));
+}
+
+// The epilogue of row group g (rows_g rows from row g * R), one unit or row a lane.
+__device__ __forceinline__ void epi_group(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c,
+                                          const EpiArgs& e, int g, int rows_g, int lane, int cta) {
+    const int r0 = g * c.R;
+    if (e.type == PH_QKV || e.type == PH_GU) {   // units are row pairs
+        if (2 * lane < rows_g) {
+            const int u = (r0 >> 1) + lane;
+            const float ya = row_sum(S, c, 2 * u) * e.rinv, yb = row_sum(S, c, 2 * u + 1) * e.rinv;
+            if (e.type == PH_QKV) qkv_unit(P, S, c, e, u, ya, yb);
+            else st_relaxed_f32(P.a + c.unit0 + u, tag_f32((ya / (1.f + expf(-ya))) * yb, tag_par(e.n)));
+        }
+    } else if (lane < rows_g) {
+        residual_row(P, Lc, S, c, e, r0 + lane, row_sum(S, c, r0 + lane), cta);
+    }
+}
+
+// Consume this phase's slots (those with global index == warp mod NW), leave
+// per-(row, chunk) partial sums in S.part, and run the epilogue of every row
+// group this warp completes.  Returns false on abort.
 __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c, uint32_t& gc,
-                         int warp, int lane, int cta) {
+                         const EpiArgs& e, int warp, int lane, int cta) {
     const uint32_t nslot = uint32_t(P.nslot);
     const int half = P.act_floats / 2;
     bool ok = true;
@@ -749,95 +853,25 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
             slot_stamp(Lc, cta, gidx, 2);
             mbar_arrive_cnt(&S.empty[slot], NW);
         }
+        if (e.type != PH_LM) {
+            // the group is complete when its last chunk is in (one chunk: now)
+            int done = 1;
+            if (c.nK > 1) {
+                if (lane == 0) {
+                    __threadfence_block();
+                    done = atomicAdd(&S.cnt[g], 1) == c.nK - 1;
+                    __threadfence_block();
+                }
+                __syncwarp();
+                done = __shfl_sync(0xffffffffu, done, 0);
+            }
+            if (done) epi_group(P, Lc, S, c, e, g, rows_g, lane, cta);
+        }
     }
     gc += c.nslots;
     if (!ok) S.flags[0] = 1;
     consumer_sync(NCT);
     return ld_volatile_i32(&S.flags[0]) == 0;
-}
-
-// Row r's output: the sum of its chunks' partials (times its scale for FP8).
-__device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) {
-    float y = 0.f;
-    for (int ch = 0; ch < c.nK; ++ch) y += S.part[r * c.nK + ch];
-    return c.wfmt == WF_F8 ? y * S.wsc[r] : y;
-}
-
-// store one element of the new K (kv=0) or V (kv=1) at position pos; returns
-// the stored bits (fp16, or the E5M2 byte)
-__device__ __forceinline__ uint32_t kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v) {
-    const __half hv = __float2half_rn(v);
-    if (P.kv == KV_F16) {
-        uint8_t* base = kv ? P.vc : P.kc;
-        reinterpret_cast<__half*>(base)[kv_elem_index(P, layer, h, pos) + dim] = hv;
-    } else if (P.kv == KV_E5M2) {
-        uint8_t* base = kv ? P.vc : P.kc;
-        const uint32_t b = f16x2_to_e5m2x2(hv, hv) & 0xFFu;
-        base[kv_elem_index(P, layer, h, pos) + dim] = uint8_t(b);
-        return b;
-    } else {
-        reinterpret_cast<__half*>(P.tail)[tail_index(P, layer, kv, h, pos % KIE_SEG) + dim] = hv;
-    }
-    return __half_as_ushort(hv);
-}
-
-// ---------------------------------------------------------------------------------------------
-// phase epilogues
-// ---------------------------------------------------------------------------------------------
-// q, K and V of this CTA's rows: the cache (for later steps) and the tagged
-// q / current-position K, V (for this step's attention), write number n.
-__device__ void epi_qkv(const KieParams& P, const Smem& S, const Cursor& c, int layer, int pos, uint32_t n,
-                        int tid) {
-    const int hh = P.hd / 2, lhh = P.hd == 128 ? 6 : 5;   // hd is 64 or 128
-    const int per = P.H * hh;  // units per matrix
-    const uint32_t par = tag_par(n), ep16 = tag_ep16(n);
-    const float rinv = 1.0f / norm_r(P, S);
-    for (int u = tid; u < c.n_units; u += NCT) {
-        const float ya = row_sum(S, c, 2 * u) * rinv, yb = row_sum(S, c, 2 * u + 1) * rinv;
-        const int U = c.unit0 + u;
-        const int which = (U >= per) + (U >= 2 * per), rem = U - which * per;
-        const int h = rem >> lhh, i = rem & (hh - 1);
-        const int e0 = h * P.hd + i;
-        if (which == 2) {
-            const uint32_t b0 = kv_store(P, layer, 1, h, pos, i, ya), b1 = kv_store(P, layer, 1, h, pos, i + hh, yb);
-            st_relaxed_u32(P.vcur + e0, (b0 << 16) | ep16);
-            st_relaxed_u32(P.vcur + e0 + hh, (b1 << 16) | ep16);
-            continue;
-        }
-        const float cs = S.rope[i], sn = S.rope[hh + i];
-        const float ra = ya * cs - yb * sn, rb = yb * cs + ya * sn;
-        if (which == 0) {
-            st_relaxed_f32(P.q + e0, tag_f32(ra, par));
-            st_relaxed_f32(P.q + e0 + hh, tag_f32(rb, par));
-        } else {
-            const uint32_t b0 = kv_store(P, layer, 0, h, pos, i, ra), b1 = kv_store(P, layer, 0, h, pos, i + hh, rb);
-            st_relaxed_u32(P.kcur + e0, (b0 << 16) | ep16);
-            st_relaxed_u32(P.kcur + e0 + hh, (b1 << 16) | ep16);
-        }
-    }
-}
-
-// x[row] += y[row]; x is read with parity par_in (or, in the first layer's O
-// phase, is the embedding row erow) and written with parity par_out.
-// The old x[row] comes from S.xres when this launch ran the staging that kept
-// it (have_xres; at most KIE_XRES rows).
-__device__ void epi_residual(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c,
-                             const uint16_t* erow, uint32_t par_in, uint32_t par_out, bool have_xres, int tid,
-                             int cta) {
-    for (int r = tid; r < c.rows; r += NCT) {
-        const int row = c.unit0 + r;
-        const float xo = (have_xres && c.rows <= KIE_XRES) ? S.xres[r]
-                         : erow ? __half2float(__ushort_as_half(erow[row])) : wait_f32(P, Lc, S, P.x + row, par_in, cta);
-        st_relaxed_f32(P.x + row, tag_f32(xo + row_sum(S, c, r), par_out));
-    }
-}
-
-__device__ void epi_swiglu(const KieParams& P, const Smem& S, const Cursor& c, uint32_t par, int tid) {
-    const float rinv = 1.0f / norm_r(P, S);
-    for (int u = tid; u < c.n_units; u += NCT) {
-        const float gt = row_sum(S, c, 2 * u) * rinv, up = row_sum(S, c, 2 * u + 1) * rinv;
-        st_relaxed_f32(P.a + c.unit0 + u, tag_f32((gt / (1.f + expf(-gt))) * up, par));
-    }
 }
 
 // LM head: logits, per-CTA argmax (lowest index on ties), last CTA reduces.
@@ -1508,6 +1542,9 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                                       int64_t(c.unit0) * c.rpu;
                     for (int r = tid; r < c.rows; r += NCT) S.wsc[r] = __ldg(ws + r);
                 }
+                if (c.nK > 1) {   // chunk counters of the row groups, zero after the staging's barrier
+                    for (int i = tid; i * c.R < c.rows; i += NCT) S.cnt[i] = 0;
+                }
                 // the step's input token: read by the first layer's QKV phase,
                 // and again by its O phase when that phase starts a launch
                 if (layer == 0 && (type == PH_QKV || (type == PH_O && phi == Lc.phase_begin))) {
@@ -1542,14 +1579,20 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                                type == PH_GU ? 1u : 0u, tid, cta, cap0, ncap);
                 }
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);
-                if (!run_gemv(P, Lc, S, c, gc, warp, lane, cta)) return;
+                EpiArgs ea;
+                ea.type = type;
+                ea.layer = layer;
+                ea.pos = pos;
+                ea.n = tn;
+                ea.rinv = (type == PH_QKV || type == PH_GU) ? 1.0f / norm_r(P, S) : 1.f;
+                ea.erow = (type == PH_O && layer == 0) ? erow : nullptr;
+                ea.par_in = type == PH_O ? 0u : 1u;    // x: 0 after a D epilogue, 1 after an O epilogue
+                ea.par_out = type == PH_O ? 1u : 0u;
+                // the staging that kept the old x (QKV for O, GU for D) ran in this launch
+                ea.have_xres = type == PH_O ? phi - 2 >= Lc.phase_begin : phi - 1 >= Lc.phase_begin;
+                if (!run_gemv(P, Lc, S, c, gc, ea, warp, lane, cta)) return;
                 if (tid == 0) stamp(P, Lc, t, phi, 2, cta);
-                if (type == PH_QKV) epi_qkv(P, S, c, layer, pos, tn, tid);
-                else if (type == PH_GU) epi_swiglu(P, S, c, par, tid);
-                else if (type == PH_LM) epi_lm(P, Lc, S, c, cta, tid, t, pos);
-                else if (type == PH_O)
-                    epi_residual(P, Lc, S, c, layer == 0 ? erow : nullptr, 0u, 1u, phi - 2 >= Lc.phase_begin, tid, cta);
-                else epi_residual(P, Lc, S, c, nullptr, 1u, 0u, phi - 1 >= Lc.phase_begin, tid, cta);
+                if (type == PH_LM) epi_lm(P, Lc, S, c, cta, tid, t, pos);
             }
             if (tid == 0) stamp(P, Lc, t, phi, 3, cta);
         }

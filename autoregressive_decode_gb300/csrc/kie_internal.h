@@ -52,7 +52,7 @@
 // device (carving) both use this one function.  Offsets are relative to the
 // dynamic shared-memory base; the ring starts on a 128-byte boundary.
 struct KieSmemLayout {
-    uint32_t full, empty, cbase, flags, plan, clist, rope, red, xres, wsc, part, act, ring, total;
+    uint32_t full, empty, cbase, flags, plan, clist, rope, red, xres, wsc, cnt, part, act, ring, total;
 };
 KIE_HD inline uint32_t kie_align(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
 KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot) {
@@ -68,6 +68,7 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
     l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64) * 4;
     l.xres = o;  o += KIE_XRES * 4;
     l.wsc = o;   o += uint32_t(part_floats) * 4;   // FP8 row scales of the phase (part_floats >= rows)
+    l.cnt = o;   o += (uint32_t(part_floats) / KIE_R + 4) * 4;   // per row group: chunks done (>= groups)
     l.part = o;  o += uint32_t(part_floats) * 4;
     l.act = kie_align(o, 16); o = l.act + uint32_t(act_floats) * 4;
     l.ring = kie_align(o, 128);
