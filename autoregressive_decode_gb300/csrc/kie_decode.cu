@@ -293,12 +293,11 @@ __device__ __forceinline__ uint32_t att_nslots(const KieParams& P, const AttChun
     return uint32_t((a.jt - a.j0 + rps - 1) / rps);
 }
 
-// Producer: wait until global slot g's ring slot was released by its previous user.
-__device__ __forceinline__ bool producer_wait_empty(const KieParams& P, const KieLaunch& Lc, const Smem& S,
-                                                    uint32_t g, int cta) {
-    const uint32_t nslot = uint32_t(P.nslot);
-    if (g < nslot) return true;
-    const uint32_t slot = g % nslot, par = ((g / nslot) - 1u) & 1u;
+// Producer: wait until ring slot `slot` was released by its previous user
+// (the phase of parity `par` of its "empty" barrier).
+__device__ __forceinline__ bool producer_wait_slot(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                                   uint32_t slot, uint32_t par, int cta) {
+    if (mbar_test_wait(&S.empty[slot], par)) return true;
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&S.empty[slot], par)) {
         if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
@@ -339,7 +338,7 @@ __device__ __forceinline__ bool warp_wait_full(const KieParams& P, const KieLaun
 __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
     const uint64_t pol = policy_evict_first();
     const uint32_t nslot = uint32_t(P.nslot);
-    uint32_t g = 0;
+    uint32_t g = 0, rs = 0, rq = 0;   // global slot index, its ring slot and generation
     bool abort = false;
     const uint64_t pol_kv = policy_evict_first();
     const int pos0 = Lc.pos0 >= 0 ? Lc.pos0 : ld_volatile_i32(&P.ctl->pos);
@@ -372,18 +371,19 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 const uint32_t nsl = att_nslots(P, a);
                 const int rps = att_rows_per_slot(P, a), rb = att_row_bytes(P);
                 for (uint32_t j = 0; j < nsl && !abort; ++j, ++g) {
-                    const uint32_t slot = g % nslot;
-                    if (!producer_wait_empty(P, Lc, S, g, cta)) { abort = true; break; }
+                    const uint32_t slot = rs;
+                    if (g >= nslot && !producer_wait_slot(P, Lc, S, rs, (rq - 1u) & 1u, cta)) { abort = true; break; }
                     const int r0 = int(j) * rps;
                     const int rows = min(rps, a.jt - a.j0 - r0);
                     const size_t off = kv_elem_index(P, layer, a.h, a.j0 + r0) * size_t(rb / P.hd);
                     const uint32_t bytes = uint32_t(rows * rb);
-                    uint64_t* fb = &S.full[2 * slot + ((g / nslot) & 1u)];
+                    uint64_t* fb = &S.full[2 * slot + (rq & 1u)];
                     uint8_t* dst = S.ring + size_t(slot) * KIE_SLOT_BYTES;
                     mbar_arrive_expect_tx(fb, 2u * bytes);
                     bulk_g2s(dst, P.kc + off, bytes, fb, pol_kv);
                     bulk_g2s(dst + size_t(rps) * rb, P.vc + off, bytes, fb, pol_kv);
                     slot_stamp(Lc, cta, g, 0);
+                    if (++rs == nslot) { rs = 0; ++rq; }
                 }
                 continue;
             }
@@ -391,19 +391,26 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
             if (type == PH_LM && t < Lc.lm_from_step) continue;
             const Cursor c = cursor(P, S, type);
             const uint8_t* src = P.wstream + stream_offset(P, S, layer, type);
-            for (uint32_t j = 0; j < c.nslots; ++j, ++g) {
-                const uint32_t slot = g % nslot;
-                if (!producer_wait_empty(P, Lc, S, g, cta)) { abort = true; break; }
-                int gg, ch, rows_g, kc;
-                slot_geom(c, j, gg, ch, rows_g, kc);
-                const uint32_t bytes = slot_bytes(c.wfmt, rows_g, kc);
-                uint64_t* fb = &S.full[2 * slot + ((g / nslot) & 1u)];
-                mbar_arrive_expect_tx(fb, bytes);
-                bulk_g2s(S.ring + size_t(slot) * KIE_SLOT_BYTES, src, bytes, fb, pol);
-                slot_stamp(Lc, cta, g, 0);
-                src += bytes;
-                if (j == 0) stamp(P, Lc, t, phi, 4, cta);
-                if (j + 1 == c.nslots) stamp(P, Lc, t, phi, 5, cta);
+            // slots j = group * nK + chunk, walked without divisions; the ring
+            // position (rs, rq) = (g % nslot, g / nslot) is kept incrementally
+            const uint32_t j_end = c.nslots;
+            uint32_t j = 0;
+            for (int gg = 0; j < j_end && !abort; ++gg) {
+                const int rows_g = min(c.R, c.rows - gg * c.R);
+                for (int ch = 0; ch < c.nK; ++ch, ++j) {
+                    if (g >= nslot && !producer_wait_slot(P, Lc, S, rs, (rq - 1u) & 1u, cta)) { abort = true; break; }
+                    const int kc = min(c.KC, c.K - ch * c.KC);
+                    const uint32_t bytes = slot_bytes(c.wfmt, rows_g, kc);
+                    uint64_t* fb = &S.full[2 * rs + (rq & 1u)];
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(S.ring + size_t(rs) * KIE_SLOT_BYTES, src, bytes, fb, pol);
+                    slot_stamp(Lc, cta, g, 0);
+                    src += bytes;
+                    if (j == 0) stamp(P, Lc, t, phi, 4, cta);
+                    if (j + 1 == j_end) stamp(P, Lc, t, phi, 5, cta);
+                    ++g;
+                    if (++rs == nslot) { rs = 0; ++rq; }
+                }
             }
         }
     }
