@@ -38,6 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synthetic as S  # noqa: E402
+from autoregressive_decode_gb300 import traffic  # noqa: E402
 
 METRIC = "batch-1 decode tokens/s per request; achieved HBM GB/s (MBU) vs GB300 peak"
 
@@ -100,8 +101,7 @@ def measured_traffic(w: S.Workload, bpl: float):
 
 
 def bytes_per_launch(w: S.Workload, p0: int, n: int) -> float:
-    import oracle as O  # the byte model lives with the bound it restates
-    return float(sum(O.decode_bytes_per_token(w, p + 1)["total"] for p in range(p0, p0 + n)))
+    return float(traffic.launch_bytes(w, p0, n))
 
 
 class Clocks:
