@@ -812,6 +812,50 @@ __device__ __forceinline__ void epi_group(const KieParams& P, const KieLaunch& L
     }
 }
 
+// The common full INT4 slot (KIE_R rows x KIE_KC_I4 columns) with compile-time
+// bounds: each iteration loads the codes of all rows, their group scales and
+// the piece's activations first, so several iterations' loads are in flight.
+// Same arithmetic and order as slot_i4.
+__device__ __forceinline__ void slot_i4_full(const uint8_t* slot, int k0, const float* act, int half, int lane,
+                                             float* acc) {
+    constexpr int KC = KIE_KC_I4, NPC = KC / 8;
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + size_t(KIE_R) * (KC / 2));
+    const __half2 bias = __floats2half2_rn(1032.f, 1032.f);
+#pragma unroll 4
+    for (int it = 0; it < NPC / 32; ++it) {
+        const int p = lane + it * 32;
+        const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
+        const float xlo[4] = {xl.x, xl.y, xl.z, xl.w};
+        const float xhi[4] = {xh.x, xh.y, xh.z, xh.w};
+        const int grp = p >> 4;
+        uint32_t w[KIE_R];
+        float scale[KIE_R];
+#pragma unroll
+        for (int r = 0; r < KIE_R; ++r) {
+            w[r] = *reinterpret_cast<const uint32_t*>(slot + size_t(r) * (KC / 2) + size_t(p) * 4);
+            scale[r] = __half2float(__ushort_as_half(sc[r * (KC >> 7) + grp]));
+        }
+#pragma unroll
+        for (int r = 0; r < KIE_R; ++r) {
+            const uint32_t u = w[r] ^ 0x88888888u;  // nibble q -> q + 8 in [0, 15]
+            float t = 0.f;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                // (1024 + n) as fp16 for nibbles s4 and s4+4, minus 1032 -> exact q
+                uint32_t hbits = ((u >> (4 * s4)) & 0x000F000Fu) | 0x64006400u;
+                const __half2 q2 = __hsub2(*reinterpret_cast<__half2*>(&hbits), bias);
+                const float2 f = __half22float2(q2);
+                t = fmaf(f.x, xlo[s4], t);
+                t = fmaf(f.y, xhi[s4], t);
+            }
+            acc[r] = fmaf(scale[r], t, acc[r]);
+        }
+    }
+}
+
 // Consume this phase's slots (those with global index == warp mod NW), leave
 // per-(row, chunk) partial sums in S.part, and run the epilogue of every row
 // group this warp completes.  Returns false on abort.
@@ -846,6 +890,7 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 if (rows_g == KIE_R && kc == KIE_KC_F16) slot_f16_full(sl, ch * c.KC, S.act, half, lane, acc);
                 else slot_f16(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
             }
+            else if (rows_g == KIE_R && kc == KIE_KC_I4) slot_i4_full(sl, ch * c.KC, S.act, half, lane, acc);
             else slot_i4(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
 #pragma unroll
             for (int r = 0; r < KIE_R; ++r) acc[r] = warp_sum(acc[r]);
@@ -1131,6 +1176,19 @@ __device__ __forceinline__ void smem_row16(const uint8_t* row, int dim0, float s
     }
 }
 
+// The 16 uint8 codes [dim0, dim0 + 16) of a ring row as exact floats: each
+// byte goes into the low mantissa of 2^23 (one byte permute) and 2^23 is
+// subtracted, two instructions a code.  The segment's zero point and scale are
+// applied outside, once per row: q.k = sc (sum q_i c_i - zp sum q_i), and
+// sum_j p_j v_j = sum_j (p_j sc_j) c_j - sum_j (p_j sc_j) zp_j.
+__device__ __forceinline__ void u8_codes16(const uint8_t* row, int dim0, float* c) {
+    const uint4 a = *reinterpret_cast<const uint4*>(row + dim0);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        c[i] = __uint_as_float(__byte_perm(w[i >> 2], 0x4B000000u, 0x7650u + (i & 3))) - 8388608.f;
+}
+
 // Online-softmax state of one lane: running max m, sum l and weighted V sum of
 // its 16 dims over the rows its row group has seen.
 struct SoftState {
@@ -1239,6 +1297,12 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     st.l = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) st.acc[i] = 0.f;
+    // uint8 ring rows: sum of this lane's q dims, and the weighted V zero points
+    float qsum = 0.f, vcorr = 0.f;
+    if (KVF == KV_U8) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qsum += qv[i];
+    }
 
     // ---- ring slots: slot j holds rows [j*rps, j*rps + rs) of the chunk, K
     // then V.  The first nrr (whole rounds) go to warp j % NW, whose row groups
@@ -1267,18 +1331,25 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
             for (int u = 0; u < RU; ++u) {
                 const int rl = rbase + rw + (k0 + u) * rstr;
                 float kf[16];
-                float scl = 0.f;
-                int zp = 0;
-                if (KVF == KV_U8 && rl < rs) {
-                    const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
-                    scl = segm[2 * sg];
-                    zp = __float_as_int(segm[2 * sg + 1]);
-                }
-                smem_row16<KVF>(ks + size_t(min(rl, rs - 1)) * RB, dim0, scl, zp, kf);
-                float d0 = 0.f, d1 = 0.f;
+                if (KVF == KV_U8) {
+                    float scl = 0.f, zpf = 0.f;
+                    if (rl < rs) {
+                        const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
+                        scl = segm[2 * sg];
+                        zpf = float(__float_as_int(segm[2 * sg + 1]));
+                    }
+                    u8_codes16(ks + size_t(min(rl, rs - 1)) * RB, dim0, kf);
+                    float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) { d0 = fmaf(qv[i], kf[i], d0); d1 = fmaf(qv[i + 1], kf[i + 1], d1); }
-                dsum[u] = d0 + d1;
+                    for (int i = 0; i < 16; i += 2) { d0 = fmaf(qv[i], kf[i], d0); d1 = fmaf(qv[i + 1], kf[i + 1], d1); }
+                    dsum[u] = scl * fmaf(-zpf, qsum, d0 + d1);
+                } else {
+                    smem_row16<KVF>(ks + size_t(min(rl, rs - 1)) * RB, dim0, 0.f, 0, kf);
+                    float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) { d0 = fmaf(qv[i], kf[i], d0); d1 = fmaf(qv[i + 1], kf[i + 1], d1); }
+                    dsum[u] = d0 + d1;
+                }
             }
 #pragma unroll
             for (int o = 1; o < LPR; o <<= 1) {
@@ -1297,6 +1368,7 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
         if (mn > -INFINITY) {
             const float cf = expf(st.m - mn);
             st.l *= cf;
+            if (KVF == KV_U8) vcorr *= cf;
 #pragma unroll
             for (int i = 0; i < 16; ++i) st.acc[i] *= cf;
 #pragma unroll
@@ -1307,18 +1379,20 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
                     const int rl = rbase + rw + (k0 + u) * rstr;
                     if (rl < rs) {
                         float vf[16];
-                        float scl = 0.f;
-                        int zp = 0;
-                        if (KVF == KV_U8) {
-                            const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
-                            scl = segm[2 * (nsegc + sg)];
-                            zp = __float_as_int(segm[2 * (nsegc + sg) + 1]);
-                        }
-                        smem_row16<KVF>(vs + size_t(rl) * RB, dim0, scl, zp, vf);
                         const float p = expf(sc[k0 + u] - mn);
                         st.l += p;
+                        if (KVF == KV_U8) {
+                            const int sg = (j0 + r0 + rl) / KIE_SEG - seg0;
+                            const float wv = p * segm[2 * (nsegc + sg)];
+                            vcorr = fmaf(wv, float(__float_as_int(segm[2 * (nsegc + sg) + 1])), vcorr);
+                            u8_codes16(vs + size_t(rl) * RB, dim0, vf);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(p, vf[i], st.acc[i]);
+                            for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(wv, vf[i], st.acc[i]);
+                        } else {
+                            smem_row16<KVF>(vs + size_t(rl) * RB, dim0, 0.f, 0, vf);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(p, vf[i], st.acc[i]);
+                        }
                     }
                 }
             }
@@ -1331,6 +1405,10 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
         }
     }
     gc += nsl;
+    if (KVF == KV_U8) {   // the zero points of the uint8 V rows folded in above
+#pragma unroll
+        for (int i = 0; i < 16; ++i) st.acc[i] -= vcorr;
+    }
     if (!ok) S.flags[0] = 1;
     if (lane == 0 && warp == 0) stamp(P, Lc, pos - (Lc.pos0 >= 0 ? Lc.pos0 : pos), 5 * layer + 1, 5, cta);
 
