@@ -654,7 +654,8 @@ __device__ __forceinline__ void slot_f8_full(const uint8_t* slot, int k0, const 
                                              float* acc) {
     const float* alo = act + (k0 >> 3) * 4;
     const float* ahi = alo + half;
-#pragma unroll 2
+    constexpr int kUnroll = KIE_F8_UNROLL;
+#pragma unroll kUnroll
     for (int it = 0; it < KIE_KC_F16 / 256; ++it) {
         const int p = lane + it * 32;
         const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
@@ -823,7 +824,8 @@ __device__ __forceinline__ void slot_i4_full(const uint8_t* slot, int k0, const 
     const float* ahi = alo + half;
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + size_t(KIE_R) * (KC / 2));
     const __half2 bias = __floats2half2_rn(1032.f, 1032.f);
-#pragma unroll 4
+    constexpr int kUnroll = KIE_I4_UNROLL;
+#pragma unroll kUnroll
     for (int it = 0; it < NPC / 32; ++it) {
         const int p = lane + it * 32;
         const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);

@@ -31,6 +31,12 @@
 #ifndef KIE_F16_UNROLL
 #define KIE_F16_UNROLL 8         // unroll of the full-slot fp16 GEMV loop (KIE_KC_F16 / 256 iterations)
 #endif
+#ifndef KIE_I4_UNROLL
+#define KIE_I4_UNROLL 2          // unroll of the full-slot INT4 GEMV loop (KIE_KC_I4 / 256 iterations); 4 and 8 measured slower
+#endif
+#ifndef KIE_F8_UNROLL
+#define KIE_F8_UNROLL 1          // unroll of the full-slot FP8 GEMV loop (KIE_KC_F16 / 256 iterations); 2 and 4 measured slower
+#endif
 #ifndef KIE_SLOT_BYTES
 #define KIE_SLOT_BYTES 16384     // slot capacity (KIE_R rows x KIE_KC_F16 fp16); 8 KB slots measured slower
 #endif
