@@ -1,4 +1,4 @@
-// Prompt prefill on the tensor cores (SURVEY row a0): the whole prompt goes
+// Prompt prefill on the tensor cores: the whole prompt goes
 // through each layer as [T x K] GEMMs instead of T single-token decode steps.
 //
 //   per layer:  u = RMSNorm(x) g1             kie_pf_norm_split   (fp32 -> fp16 hi + lo tiles)
