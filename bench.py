@@ -179,6 +179,24 @@ def cpu_baseline(w: S.Workload, weights: dict, p0: int, n_steps: int = 6):
                       f"of {w.name} over a synthetic {p0}-position KV context; numpy fp32 with OpenBLAS"}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (timing: the slowest replica sets
+    the whole job's time); x itself when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world_size: int, tokens_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput of world_size independent replicas (weak scaling:
+    every replica decodes tokens_per_step per step) timed by the slowest one."""
+    return world_size * tokens_per_step / (ms_per_step / 1e3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -283,9 +301,7 @@ def main():
     total_ms = ev0.elapsed_time(ev1)
     launch_ms = [a.elapsed_time(b) for a, b in per]
     if ws > 1:
-        t = torch.tensor([total_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, f"cuda:{local}")
         dist.barrier()
     tokens_gpu = list(d_tok.cpu().numpy())
 
@@ -301,9 +317,7 @@ def main():
             e2e_ms.append(dt)
     assert list(toks) == tokens_gpu, "host-API tokens differ from the device-timed run"
     if ws > 1:
-        t = torch.tensor([max(e2e_ms)], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_max = float(t.item())
+        e2e_max = max_over_ranks(max(e2e_ms), f"cuda:{local}")
     else:
         e2e_max = statistics.median(e2e_ms)
 
@@ -312,7 +326,7 @@ def main():
             dist.destroy_process_group()
         return
     ms_per_step = total_ms / args.steps
-    value = ws * n_dec / (ms_per_step / 1e3)
+    value = job_tokens_per_s(ws, n_dec, ms_per_step)
     peak, peak_kind = peaks()
     bpl = bytes_per_launch(w, p0, n_dec)
     launch_avg = statistics.mean(launch_ms)
@@ -332,7 +346,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": measured_traffic(w, bpl), "peak_source": peak_kind, "kernel": "kie_decode_kernel",
                      "algorithmic_bytes_per_launch": bpl, "launch_ms": launch_avg},
-        "e2e": {"value": ws * n_dec / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+        "e2e": {"value": job_tokens_per_s(ws, n_dec, e2e_max), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 4 * n_dec},
         "clocks": clk.summary(),
     }
