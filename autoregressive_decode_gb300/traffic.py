@@ -11,6 +11,8 @@ Storage formats counted:
   * FP8 E4M3 matrices: 1 byte per weight plus one fp32 scale per output row;
   * INT4 g128 FFN matrices: half a byte per weight plus one fp16 scale per
     128-column group of a row;
+  * NVFP4 matrices: half a byte per weight, one E4M3 scale byte per 16-column
+    block of a row and one fp32 scale per row;
   * KV cache: fp16 (2 bytes), FP8 E5M2 (1 byte), or uint8 codes for completed
     128-token segments (1 byte, plus an fp32 scale and an int32 zero point per
     segment, layer, K/V and head) with the open segment's tail in fp16;
@@ -21,6 +23,7 @@ from __future__ import annotations
 
 SEGMENT = 128     # uint8 KV segment (tokens)
 INT4_GROUP = 128  # INT4 scale group (columns)
+FP4_BLOCK = 16    # NVFP4 scale block (columns)
 
 
 def _matrix(rows: int, cols: int, fmt: str) -> int:
@@ -30,6 +33,8 @@ def _matrix(rows: int, cols: int, fmt: str) -> int:
         return rows * cols + rows * 4
     if fmt == "int4_g128":
         return rows * cols // 2 + rows * (cols // INT4_GROUP) * 2
+    if fmt == "nvfp4":
+        return rows * cols // 2 + rows * (cols // FP4_BLOCK) + rows * 4
     raise ValueError(f"unknown weight format {fmt}")
 
 

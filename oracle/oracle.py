@@ -21,7 +21,9 @@ Pages cited (titles as published):
   [Kog] also, section "Memory bandwidth is the main bottleneck": an FP16 weight
             is 2 bytes for one multiply-add (~1 FLOP/byte), FP8 ~2, FP4 ~4 —
             the FP8 weight format below (E4M3, one fp32 scale per output row)
-            is this module's reading; the page names only the byte width.
+            and the NVFP4 format (E2M1, E4M3 scale per 16 columns, fp32 scale
+            per row) are this module's readings; the page names only the byte
+            width.
 
 The decoder itself (RMSNorm, RoPE, SwiGLU, MHA, untied LM head) is fixed by the
 workload description, not by the pages; where the pages leave a step open this
@@ -173,6 +175,81 @@ def fp8_quantize_rows(w: np.ndarray):
 def fp8_dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """w' = e4m3(code) * s in fp32."""
     return (e4m3_to_f32(codes) * np.asarray(scales, dtype=F32)[:, None]).astype(F32)
+
+
+# NVFP4 weights (this module's reading of [Kog]'s "FP4 ~4 FLOP/byte" for a
+# Blackwell GPU, whose native 4-bit format is E2M1 with one FP8 E4M3 scale per
+# block of 16 values): E2M1 codes, an E4M3 scale per 16 consecutive input
+# columns of a row, and one fp32 scale per output row chosen so that the row's
+# largest block scale is 448 (the largest E4M3 value).
+E2M1_MAX = 6.0    # largest E2M1 magnitude
+FP4_BLOCK = 16    # input columns sharing one E4M3 block scale
+
+
+def _e2m1_table() -> np.ndarray:
+    """Magnitudes of the E2M1 codes 0..7 (float64, exact): code = ee.m,
+    e = 0 subnormal m/2, else (1 + m/2) * 2^(e-1): 0, 0.5, 1, 1.5, 2, 3, 4, 6."""
+    c = np.arange(8)
+    e, m = c >> 1, c & 1
+    return np.where(e == 0, m / 2.0, (1.0 + m / 2.0) * 2.0 ** (e - 1.0))
+
+
+def e2m1_to_f32(n4: np.ndarray) -> np.ndarray:
+    """E2M1 codes (low 4 bits: sign, 2 exponent bits, 1 mantissa bit) -> fp32
+    (exact; code 8 is -0)."""
+    n = np.asarray(n4, dtype=np.uint8).astype(np.int64) & 0xF
+    val = _e2m1_table()[n & 7]
+    return np.where(n & 8, -val, val).astype(F32)
+
+
+def e2m1_from_f32(x: np.ndarray) -> np.ndarray:
+    """fp32 -> E2M1 codes: the nearest value, ties to the even code, magnitudes
+    beyond 6 saturating to +-6; the sign bit follows the input's sign (also
+    for zero).  E2M1 has no NaN; the input must be finite."""
+    xf = np.asarray(x, dtype=F32).astype(np.float64)
+    assert np.all(np.isfinite(xf)), "E2M1 has no NaN or infinity"
+    t = _e2m1_table()
+    a = np.abs(xf)
+    hi = np.clip(np.searchsorted(t, a, side="left"), 0, len(t) - 1)   # first value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - t[lo], t[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= t[-1], 7, code)               # saturate
+    sign = np.signbit(xf).astype(np.int64) << 3
+    return (code | sign).astype(np.uint8)
+
+
+def fp4_quantize_rows(w: np.ndarray):
+    """NVFP4 weights of a [rows, cols] matrix (cols a multiple of 16), in fp32:
+      rs   = absmax(row) / (6 * 448)                      one per row
+      bs_b = e4m3(absmax(block b) / (6 * rs))             one per 16 columns
+      code = e2m1(w / (bs_b * rs))                        ties to even, +-6 saturation
+    An all-zero row gets rs = 0, and a block whose scale rounds to 0 gets
+    codes 0.  Returns (codes uint8 [rows, cols] in 0..15, block scale codes
+    uint8 [rows, cols/16], row scales fp32 [rows])."""
+    wf = np.asarray(w, dtype=np.float16).astype(F32)
+    rows, cols = wf.shape
+    assert cols % FP4_BLOCK == 0
+    rs = (np.abs(wf).max(axis=1) / F32(E2M1_MAX * E4M3_MAX)).astype(F32)
+    wb = wf.reshape(rows, cols // FP4_BLOCK, FP4_BLOCK)
+    amax_b = np.abs(wb).max(axis=2)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        bs_real = np.where(rs[:, None] > 0, amax_b / (F32(E2M1_MAX) * rs[:, None]), F32(0.0)).astype(F32)
+        bs_codes = e4m3_from_f32(bs_real)
+        denom = (e4m3_to_f32(bs_codes) * rs[:, None]).astype(F32)
+        q = np.where(denom[:, :, None] > 0, wb / denom[:, :, None], F32(0.0)).astype(F32)
+    codes = e2m1_from_f32(q).reshape(rows, cols)
+    return codes, bs_codes, rs
+
+
+def fp4_dequantize_rows(codes: np.ndarray, bs_codes: np.ndarray, rs: np.ndarray) -> np.ndarray:
+    """w' = (e2m1(code) * e4m3(block scale)) * row scale in fp32 (the first
+    product is exact: 2 and 4 significant bits)."""
+    rows, cols = codes.shape
+    v = e2m1_to_f32(codes).reshape(rows, cols // FP4_BLOCK, FP4_BLOCK)
+    b = e4m3_to_f32(bs_codes)[:, :, None]
+    return ((v * b).astype(F32) * np.asarray(rs, dtype=F32)[:, None, None]).astype(F32).reshape(rows, cols)
 
 
 INT4_GROUP = 128  # [xAI] 3.3: int4, group_size 128, symmetric
@@ -359,7 +436,8 @@ class OracleDecoder:
         f = lambda a: np.asarray(a, dtype=np.float16).astype(F32)  # noqa: E731
         wd = getattr(cfg, "attn_wdtype", "fp16")
         fp8 = lambda a: fp8_dequantize_rows(*fp8_quantize_rows(a))  # noqa: E731
-        attn_w = fp8 if wd == "fp8_e4m3" else f                     # q, k, v, o and the LM head
+        fp4 = lambda a: fp4_dequantize_rows(*fp4_quantize_rows(a))  # noqa: E731
+        attn_w = {"fp8_e4m3": fp8, "nvfp4": fp4}.get(wd, f)          # q, k, v, o and the LM head
         self.tok_emb = f(weights["tok_emb"])
         self.lm_head = attn_w(weights["lm_head"])
         self.final_norm = f(weights["final_norm"])
@@ -368,9 +446,9 @@ class OracleDecoder:
         for lw in weights["layers"]:
             lay = {k: f(lw[k]) for k in ("attn_norm", "ffn_norm")}
             lay.update({k: attn_w(lw[k]) for k in ("wq", "wk", "wv", "wo")})
-            if cfg.ffn_wdtype == "fp8_e4m3":
+            if cfg.ffn_wdtype in ("fp8_e4m3", "nvfp4"):
                 for k in ("w_gate", "w_up", "w_down"):
-                    lay[k] = fp8(lw[k])
+                    lay[k] = (fp8 if cfg.ffn_wdtype == "fp8_e4m3" else fp4)(lw[k])
             elif cfg.ffn_wdtype == "int4_g128":
                 q4 = {}
                 for k in ("w_gate", "w_up", "w_down"):
@@ -496,16 +574,31 @@ def decode_bytes_per_token(cfg, ctx_len: int) -> dict:
     (C = positions attended, including the current one): every active weight
     once, plus the K and V of all C positions in every layer."""
     d, H, h, F, V, L = cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.ffn_dim, cfg.vocab, cfg.n_layers
-    fp8_attn = getattr(cfg, "attn_wdtype", "fp16") == "fp8_e4m3"
-    # FP8 matrices: one byte per weight plus a 4-byte scale per row
-    attn_w = (3 * H * h * d + d * H * h) + (3 * H * h + d) * 4 if fp8_attn else (3 * H * h * d + d * H * h) * 2
+    wd = getattr(cfg, "attn_wdtype", "fp16")
+    fp8_attn, fp4_attn = wd == "fp8_e4m3", wd == "nvfp4"
+    # FP8 matrices: one byte per weight plus a 4-byte scale per row; NVFP4: half
+    # a byte per weight, one byte per 16 weights and a 4-byte scale per row
+    n_attn, rows_attn = 3 * H * h * d + d * H * h, 3 * H * h + d
+    if fp8_attn:
+        attn_w = n_attn + rows_attn * 4
+    elif fp4_attn:
+        attn_w = n_attn // 2 + n_attn // FP4_BLOCK + rows_attn * 4
+    else:
+        attn_w = n_attn * 2
     if cfg.ffn_wdtype == "int4_g128":
         ffn_w = 3 * F * d // 2 + 3 * F * d // INT4_GROUP * 2
     elif cfg.ffn_wdtype == "fp8_e4m3":
         ffn_w = 3 * F * d + (2 * F + d) * 4
+    elif cfg.ffn_wdtype == "nvfp4":
+        ffn_w = 3 * F * d // 2 + 3 * F * d // FP4_BLOCK + (2 * F + d) * 4
     else:
         ffn_w = 3 * F * d * 2
-    lm_w = V * d + V * 4 if fp8_attn else V * d * 2
+    if fp8_attn:
+        lm_w = V * d + V * 4
+    elif fp4_attn:
+        lm_w = V * d // 2 + V * d // FP4_BLOCK + V * 4
+    else:
+        lm_w = V * d * 2
     norms = 2 * d * 2
     weights = L * (attn_w + ffn_w + norms) + lm_w + d * 2 + d * 2  # LM head, final norm, embedding row
     if cfg.kv_dtype == "fp16":

@@ -178,6 +178,82 @@ def test_fp8_byte_model():
     assert abs(b / O.decode_bytes_per_token(S.WORKLOADS["1p8b"], 1)["weights"] - 0.5) < 0.01
 
 
+# ------------------------------------------------------------------ NVFP4 (E2M1 + E4M3 block scales)
+# The E2M1 element of the OCP microscaling formats: sign, 2 exponent bits (bias
+# 1), 1 mantissa bit; its eight magnitudes as the format publishes them.
+E2M1_PUBLISHED = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_all_codes():
+    """All 16 codes decode to the published magnitudes, the sign in bit 3."""
+    vals = O.e2m1_to_f32(np.arange(16, dtype=np.uint8))
+    np.testing.assert_array_equal(vals[:8], np.array(E2M1_PUBLISHED, np.float32))
+    np.testing.assert_array_equal(vals[8:], -np.array(E2M1_PUBLISHED, np.float32))
+    assert np.signbit(vals[8])
+
+
+def test_e2m1_encode_brute_force():
+    """Encoding equals an exhaustive nearest-value search (ties to the even
+    code, beyond 6 saturating) on a grid holding every midpoint."""
+    x = np.concatenate([np.arange(-7.0, 7.0001, 0.03125), [-100.0, 100.0, 6.5, -6.5]]).astype(np.float32)
+    mags = np.array(E2M1_PUBLISHED)
+    got = O.e2m1_from_f32(x)
+    for xi, ci in zip(x.astype(np.float64), got):
+        a = min(abs(xi), 6.0)
+        dist = np.abs(mags - a)
+        best = np.flatnonzero(dist == dist.min())
+        code = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert (ci & 7) == code, (xi, ci)
+        assert ((ci >> 3) & 1) == int(np.signbit(xi)), (xi, ci)
+
+
+def test_e2m1_ties():
+    """Midpoints go to the even code: 0.25 -> 0, 0.75 -> 1, 1.25 -> 1,
+    1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4; 7 saturates to 6."""
+    x = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, -5.0], np.float32)
+    r = O.e2m1_to_f32(O.e2m1_from_f32(x))
+    np.testing.assert_array_equal(r, np.array([0, 1, 1, 2, 2, 4, 4, 6, -4], np.float32))
+
+
+def test_fp4_row_quantizer_bounds():
+    """The block holding a row's absmax gets the largest E4M3 scale (448); every
+    weight is within half the local E2M1 spacing of its dequantised value, in
+    units of its block's scale times the row scale (saturation after the E4M3
+    rounding of a block scale stays inside that bound); zero rows and zero
+    blocks quantise to zero."""
+    w = S.normal_f32(23, 4, (32, 256), std=0.02).astype(np.float16)
+    w[3] = 0
+    w[7, 16:32] = 0
+    codes, bsc, rs = O.fp4_quantize_rows(w)
+    assert rs[3] == 0 and not (codes[3] & 7).any()
+    assert not (codes[7, 16:32] & 7).any()
+    wf = w.astype(np.float32)
+    rows = np.arange(32) != 3
+    amax_block = np.abs(wf).argmax(axis=1) // 16
+    assert np.all(O.e4m3_to_f32(bsc[np.arange(32), amax_block])[rows] == 448.0)
+    back = O.fp4_dequantize_rows(codes, bsc, rs)
+    unit = np.repeat(O.e4m3_to_f32(bsc) * rs[:, None], 16, axis=1)
+    mags = np.array(E2M1_PUBLISHED)
+    spacing = np.diff(mags)                                 # 0.5 0.5 0.5 0.5 1 1 2
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(unit > 0, np.abs(wf) / unit, 0.0)
+    seg = np.clip(np.searchsorted(mags, q, side="right") - 1, 0, len(spacing) - 1)
+    bound = 0.5 * spacing[seg] * unit * (1 + 1e-6) + 1e-12
+    assert np.all(np.abs(back - wf) <= bound)
+
+
+def test_fp4_byte_model():
+    """NVFP4 matrices cost half a byte per weight, one scale byte per 16 weights
+    and a 4-byte scale per row: 983,585,792 bytes for the 1.8B model."""
+    w = S.WORKLOADS["1p8b"].with_(attn_wdtype="nvfp4", ffn_wdtype="nvfp4")
+    n_weights = 25 * (4 * 2048 * 2048 + 3 * 2048 * 8192) + 32000 * 2048      # 1,743,257,600
+    n_rows = 25 * (3 * 2048 + 2048 + 2 * 8192 + 2048) + 32000                 # 697,600
+    gains_and_emb = 25 * 2 * 2048 * 2 + 2048 * 2 + 2048 * 2
+    expect = n_weights // 2 + n_weights // 16 + n_rows * 4 + gains_and_emb
+    assert expect == 983_585_792
+    assert O.decode_bytes_per_token(w, 1)["weights"] == expect
+
+
 # ------------------------------------------------------------------ fp16 rounding
 def test_fp16_round_matches_torch_and_ties():
     torch = pytest.importorskip("torch")

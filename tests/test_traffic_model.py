@@ -16,6 +16,13 @@ def test_step_bytes_match_oracle(name):
         assert traffic.step_bytes(w, ctx) == O.decode_bytes_per_token(w, ctx)
 
 
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
+def test_step_bytes_match_oracle_weight_formats(fmt):
+    w = S.WORKLOADS["1p8b"].with_(attn_wdtype=fmt, ffn_wdtype=fmt)
+    for ctx in (1, 2049):
+        assert traffic.step_bytes(w, ctx) == O.decode_bytes_per_token(w, ctx)
+
+
 def test_launch_bytes_sum_of_steps():
     w = S.WORKLOADS["1p8b"]
     total = traffic.launch_bytes(w, 2048, 4)
