@@ -25,6 +25,27 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+@pytest.mark.parametrize("lang,std,cc", [("c", "c11", "gcc"), ("c++", "c++17", "g++")])
+def test_header_compiles_standalone(lang, std, cc, tmp_path):
+    """include/kie.h is a self-contained C header (plain pointers and sizes, no
+    torch or CUDA types): a translation unit that includes only it compiles as
+    C11 and C++17 with warnings as errors, and the struct layout the Python
+    binding mirrors has the size the binding expects."""
+    import shutil
+    import subprocess
+    if shutil.which(cc) is None:
+        pytest.skip(f"{cc} not available")
+    ext = "c" if lang == "c" else "cpp"
+    src = tmp_path / f"t.{ext}"
+    src.write_text('#include "kie.h"\n#include <stdio.h>\n'
+                   'int main(void) { printf("%zu\\n", sizeof(kie_config)); return 0; }\n')
+    exe = tmp_path / "t"
+    subprocess.check_call([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)]).decode().strip()
+    assert int(out) == C.sizeof(kie.kie_config)
+
+
 def test_library_exports_every_declared_symbol():
     lib = kie.load()
     for name in declared_entry_points():
