@@ -41,6 +41,7 @@ import synthetic as S  # noqa: E402
 from autoregressive_decode_gb300 import traffic  # noqa: E402
 
 METRIC = "batch-1 decode tokens/s per request; achieved HBM GB/s (MBU) vs GB300 peak"
+REF_TOKENS = 8       # oracle decode steps per reference-arm bench step
 
 
 def parse():
@@ -157,25 +158,39 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def cpu_baseline(w: S.Workload, weights: dict, p0: int, n_steps: int = 6):
-    """Time the oracle's decode on this host: a synthetic fp16 context of p0
-    positions (prefill cost excluded, as for the GPU metric), then n_steps
-    decode steps."""
-    import oracle as O
+class OracleSample:
+    """The oracle decoding the workload on this host: a synthetic fp16 context
+    of p0 positions (prefill cost excluded, as for the GPU metric), then timed
+    samples of n decode steps from position p0."""
+
+    def __init__(self, w: S.Workload, weights: dict, p0: int, n_steps: int):
+        import oracle as O
+        self.O = O
+        self.p0, self.n = p0, n_steps
+        self.dec = O.OracleDecoder(w, weights, max_ctx=p0 + n_steps + 1)
+        for layer in range(w.n_layers):
+            k, v = S.gen_kv(w.with_(context_len=p0), layer)
+            self.dec.set_kv(layer, k, v)
+        self.first = S.gen_first_token(w)
+        self.dec.pos = p0
+        self.dec.decode(self.first)          # warm-up step (page-in, BLAS threads)
+
+    def time(self) -> float:
+        """Seconds for n greedy decode steps at positions p0 .. p0 + n - 1."""
+        self.dec.pos = self.p0
+        tok = self.first
+        t0 = time.perf_counter()
+        for _ in range(self.n):
+            tok = self.O.argmax_lowest(self.dec.decode(tok))
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(w: S.Workload, weights: dict, p0: int, n_steps: int = 8):
+    """Time the oracle's decode on this host over n_steps decode steps."""
     threads = len(os.sched_getaffinity(0))
-    dec = O.OracleDecoder(w, weights, max_ctx=p0 + n_steps)
-    for layer in range(w.n_layers):
-        k, v = S.gen_kv(w.with_(context_len=p0), layer)
-        dec.set_kv(layer, k, v)
-    dec.pos = p0
-    tok = S.gen_first_token(w)
-    dec.decode(tok)                      # warm-up step (page-in, BLAS threads)
-    t0 = time.perf_counter()
-    for _ in range(n_steps - 1):
-        tok = O.argmax_lowest(dec.decode(tok))
-    dt = time.perf_counter() - t0
-    return {"value": (n_steps - 1) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n_steps - 1} timed decode steps (after 1 warm-up) at positions {p0 + 1}..{p0 + n_steps - 1} "
+    dt = OracleSample(w, weights, p0, n_steps).time()
+    return {"value": n_steps / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_steps} timed decode steps (after 1 warm-up) at positions {p0}..{p0 + n_steps - 1} "
                       f"of {w.name} over a synthetic {p0}-position KV context; numpy fp32 with OpenBLAS"}
 
 
@@ -204,23 +219,42 @@ def dist_env():
     return ws, rank, local
 
 
+def gpu_config(w: S.Workload, n_dec: int, mode: str, replicas: int) -> dict:
+    p0 = w.start_pos
+    return {"workload": workload_desc(w), "decode_tokens_per_step": n_dec,
+            "positions": f"{p0}..{p0 + n_dec - 1}", "mode": mode,
+            "l2": "inputs larger than L2 (all weights streamed from HBM every token)",
+            "replicas": replicas}
+
+
 def run_reference(args, w: S.Workload):
+    """The reference arm: the CPU oracle as it stands, on this host's cores.
+    One bench step = one timed sample of REF_TOKENS greedy decode steps of the
+    same workload (its full 256-token chain would take minutes per step on the
+    CPU); ms_per_step is that sample's measured time."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    n_dec = args.decode_tokens or w.decode_steps
+    n_ref = REF_TOKENS
     weights = S.gen_weights(w)
-    steps = []
+    sample = OracleSample(w, weights, w.start_pos, n_ref)
+    times = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, weights, w.start_pos, n_steps=3)
+        dt = sample.time()
         if i >= args.warmup:
-            steps.append(cb)
-    val = statistics.median(s["value"] for s in steps)
+            times.append(dt)
+    sec = statistics.median(times)
+    val = n_ref / sec
+    cores = len(os.sched_getaffinity(0))
+    desc = (f"{n_ref} greedy decode steps per bench step at positions {w.start_pos}..{w.start_pos + n_ref - 1} of "
+            f"{w.name} over a synthetic {w.start_pos}-position KV context (prefill excluded); numpy fp32 with "
+            f"OpenBLAS; median of {args.steps} timed samples after {args.warmup} warm-up")
+    cfg = gpu_config(w, n_ref, "oracle (CPU)", 1)
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": n_dec / val * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": workload_desc(w), "decode_tokens_per_step": n_dec},
-            "cpu_baseline": {**steps[-1], "value": val},
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -336,10 +370,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "storage": f"weights attn {w.attn_wdtype} / FFN {w.ffn_wdtype}, KV {w.kv_dtype}",
         "data": "synthetic",
-        "config": {"workload": workload_desc(w), "decode_tokens_per_step": n_dec,
-                   "positions": f"{p0}..{p0 + n_dec - 1}", "mode": args.mode,
-                   "l2": "inputs larger than L2 (all weights streamed from HBM every token)",
-                   "replicas": ws},
+        "config": gpu_config(w, n_dec, args.mode, ws),
         # per step: the control-block kernel of set_pos, then one cooperative decode launch
         # (persistent) or a control kernel plus (5L+1) phase kernels per token (graph)
         "gpu_launches": args.steps * (2 if args.mode == "persistent" else 2 + (5 * w.n_layers + 1) * n_dec),
