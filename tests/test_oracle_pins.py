@@ -500,6 +500,56 @@ def test_int4_decoder_uses_dequantised_ffn():
     np.testing.assert_array_equal(a.decode(3), b.decode(3))
 
 
+def test_fp8_decoder_matches_torch_quantised_weights():
+    """With FP8 E4M3 weights the decoder equals an fp16-weight decoder whose
+    matrices (q, k, v, o, gate, up, down and the LM head) are replaced by
+    e4m3(w / s) * s, s = absmax(row) / 448 in fp32, with the E4M3 rounding done
+    by torch's float8_e4m3fn cast instead of the oracle's own encoder."""
+    torch = pytest.importorskip("torch")
+    cfg = S.Workload("micro8", 0, 1, 128, 2, 64, 256, 160, ffn_wdtype="fp8_e4m3", attn_wdtype="fp8_e4m3")
+    w = S.gen_weights(cfg, seed=83)
+    a = O.OracleDecoder(cfg, w, max_ctx=4)
+    b = O.OracleDecoder(cfg.with_(ffn_wdtype="fp16", attn_wdtype="fp16"), w, max_ctx=4)
+
+    def torch_fp8(m16):
+        wf = m16.astype(np.float32)
+        s = (np.abs(wf).max(axis=1) / np.float32(448.0)).astype(np.float32)
+        q = torch.from_numpy((wf / s[:, None]).astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float32)
+        return (q.numpy() * s[:, None]).astype(np.float32)
+
+    for k in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+        b.layers[0][k] = torch_fp8(w["layers"][0][k])
+    b.lm_head = torch_fp8(w["lm_head"])
+    for t in (3, 77, 5):
+        np.testing.assert_array_equal(a.decode(t), b.decode(t))
+
+
+def test_int4_byte_model_hand_count():
+    """The 7B INT4 model's bytes per decode token, counted by hand: per layer
+    4 x 4096^2 fp16 attention weights (134,217,728 B), 3 x 11008 x 4096 INT4
+    codes at half a byte (67,633,152 B) with one fp16 scale per 128 (2,113,536 B)
+    and two fp16 gain vectors (16,384 B); 32 layers; the 32000 x 4096 fp16 LM
+    head, the final gains and one embedding row; K and V of 32 heads x 128 fp16
+    per position and layer."""
+    w = S.WORKLOADS["7b_int4"]
+    b = O.decode_bytes_per_token(w, 4097)
+    assert b["weights"] == 32 * 203_980_800 + 262_144_000 + 8_192 + 8_192 == 6_789_545_984
+    assert b["kv"] == 524_288 * 4097
+
+
+def test_u8_byte_model_hand_count():
+    """The 1.8B uint8-cache model's KV bytes, counted by hand: at C = 8193 the
+    64 complete 128-token segments are one byte per value (8192 x 16 x 128 B per
+    layer, K and V), the open segment's one position stays fp16 (16 x 128 x 2 B)
+    and each complete segment carries a fp32 scale and an int32 zero point per
+    head (16 x 64 x 8 B); at C = 8320 segment 65 has just completed (65
+    segments, no fp16 position)."""
+    w = S.WORKLOADS["1p8b_u8"]
+    assert O.decode_bytes_per_token(w, 8193)["kv"] == 25 * 2 * (16_777_216 + 4_096 + 8_192) == 839_475_200
+    assert O.decode_bytes_per_token(w, 8320)["kv"] == 25 * 2 * (17_039_360 + 8_320) == 852_384_000
+    assert O.decode_bytes_per_token(w, 8193)["weights"] == O.decode_bytes_per_token(S.WORKLOADS["1p8b"], 1)["weights"]
+
+
 # ------------------------------------------------------------------ the bound (P-4) and shapes (P-12)
 def test_kog_bound_arithmetic():
     g = gold("kog_bound_arithmetic.json")
