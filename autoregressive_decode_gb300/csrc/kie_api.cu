@@ -9,9 +9,9 @@
 
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <numeric>
 #include <string>
@@ -48,6 +48,8 @@ extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0,
 extern "C" cudaError_t kie_pf_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H,
                                         int hd, int kvfmt, int max_ctx, int pos0, int T, float scale, float* O,
                                         cudaStream_t st);
+extern "C" cudaError_t kie_launch_quant_fp4(const uint16_t* w, int rows, int cols, uint8_t* packed, uint8_t* codes,
+                                            uint8_t* bscales, float* rscales, cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
                                              int8_t* codes_i8, uint16_t* scales, cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_u8(const uint16_t* src, int n_seg, int64_t src_seg, int64_t src_row,
@@ -79,11 +81,6 @@ struct HostPhase {
     std::vector<int32_t> unit_begin;   // G+1
     std::vector<uint32_t> bytes;       // G
     std::vector<uint32_t> nslots;      // G
-    uint64_t unit_bytes() const {      // stream bytes of one unit (approximate, for balancing)
-        const uint64_t row = wfmt == WF_F16 ? uint64_t(K) * 2 : wfmt == WF_F8 ? uint64_t(K)
-                                                                            : uint64_t(K) / 2 + uint64_t(K) / 64;
-        return row * rpu;
-    }
 };
 
 uint32_t slot_bytes_host(int wfmt, int rows_g, int kc) {
@@ -344,6 +341,8 @@ struct kie_engine {
     uint64_t timeout_ns = kDefaultTimeoutNs;
     cudaGraphExec_t graph[2] = {nullptr, nullptr};   // graph mode, by tag_fill of the step's position
     KieControl* h_ctl = nullptr;  // pinned staging
+    void* static_scratch = nullptr;   // device address of the library's static scratch array on this device
+    int skip_arrival_cta = -1;        // failure injection for the next persistent launch (tests)
     std::string err;
 
     uint8_t* dev(size_t off) const { return static_cast<uint8_t*>(ws) + off; }
@@ -412,6 +411,7 @@ KieLaunch base_launch(kie_engine* e) {
     l.out_logits = nullptr;
     l.timeout_ns = e->timeout_ns;
     l.use_grid_barrier = 1;
+    l.skip_arrival_cta = -1;
     return l;
 }
 
@@ -501,6 +501,10 @@ kie_status run_steps(kie_engine* e, int n, int first_tok, const int32_t* d_force
         l.lm_from_step = lm_from;
         l.out_tokens = d_tokens;
         l.out_logits = d_logits;
+        if (n > 1) {   // only a launch of several steps meets a grid barrier
+            l.skip_arrival_cta = e->skip_arrival_cta;
+            e->skip_arrival_cta = -1;
+        }
         if ((st = launch_persistent(e, l)) != KIE_OK) return st;
     } else {
         for (int f = 0; f < 2; ++f)
@@ -596,6 +600,64 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
 
 }  // namespace
 
+// ---- scratch in a static device array (for the allocation-free decode step) -------------------
+//
+// For callers that must not allocate device memory while decoding: code running
+// inside another framework's memory pool or an allocator-less plugin host, a
+// real-time service that forbids allocation after start-up, or a process whose
+// device memory is already fully committed.  Together with an engine created on
+// a caller-provided workspace, kie_decode_step_static_scratch performs no
+// cudaMalloc, cudaFree or other allocating call.  The decode kernel's scratch
+// (residual stream, q, attention output and partials, SwiGLU output, argmax
+// partials, control block) lives in the array below; weights and the KV cache
+// stay in the engine.
+
+#define KIE_STATIC_SCRATCH_BYTES (256u * 1024u)
+
+// The array belongs to this file's device module.  With CUDA's lazy module
+// loading the module (and so the array's device memory) is loaded the first
+// time its address is looked up; kie_create does that, with the engine's
+// device current, so the decode step itself never triggers the load.  Host
+// code must not use the array's name as an address.
+static __device__ __align__(256) uint8_t kie_static_scratch[KIE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+struct StaticScratchLayout {
+    size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl, total;
+};
+
+StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
+    StaticScratchLayout l;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
+    const size_t hq = size_t(c.n_heads) * c.head_dim * 4;
+    // tagged activations, reset per step as in the engine's workspace
+    l.x = take(size_t(c.d_model) * 4);
+    l.kcur = take(hq);
+    l.vcur = take(hq);
+    l.zero_bytes = l.vcur + hq - l.x;
+    l.q = take(hq);
+    l.a = take(size_t(c.ffn_dim) * 4);
+    l.o = take(hq);
+    l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
+    l.par_bytes = l.att_part + size_t(G) * (c.head_dim + 4) * 4 - l.q;
+    l.amax_val = take(size_t(G) * 4);
+    l.amax_idx = take(size_t(G) * 4);
+    l.ctl = take(sizeof(KieControl));
+    l.total = align_up(o, 256);
+    return l;
+}
+
+// Device address of kie_static_scratch on the current device (the caller has
+// made the engine's device current).  This loads the module that holds it.
+cudaError_t static_scratch_address(void** out) {
+    *out = nullptr;
+    return cudaGetSymbolAddress(out, kie_static_scratch);
+}
+
+}  // namespace
+
 // =============================================================================================
 // C ABI
 // =============================================================================================
@@ -659,6 +721,10 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     int per_sm = 0;
     r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, e->kernel, KIE_THREADS, e->plan.smem);
     if (r != cudaSuccess || per_sm < 1) { kie_destroy(e); return fail(nullptr, KIE_ERR_LAUNCH, "decode kernel does not fit on an SM"); }
+    // the static scratch array of the allocation-free decode step: looked up
+    // now, so that its module is loaded here and never by that step
+    r = static_scratch_address(&e->static_scratch);
+    if (r != cudaSuccess) { kie_destroy(e); return fail(nullptr, KIE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(r)); }
 
     // plan tables and parameters
     const Layout& L = e->lay;
@@ -723,6 +789,10 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     P.amax_idx = reinterpret_cast<int32_t*>(e->dev(L.amax_idx));
     P.ctl = reinterpret_cast<KieControl*>(e->dev(L.ctl));
     P.nslot = pl.nslot;
+    P.inflight = pl.nslot;
+    if (const char* v = std::getenv("KIE_INFLIGHT")) P.inflight = std::max(1, std::min(pl.nslot, std::atoi(v)));
+    P.poll_ns = 0;
+    if (const char* v = std::getenv("KIE_POLL_NS")) P.poll_ns = uint32_t(std::max(0, std::min(1000, std::atoi(v))));
     P.act_floats = pl.act_floats;
     P.part_floats = pl.part_floats;
     *out = e;
@@ -1114,6 +1184,13 @@ kie_status kie_set_timeout_ms(kie_engine* e, int32_t ms) {
     return KIE_OK;
 }
 
+kie_status kie_debug_skip_grid_arrival(kie_engine* e, int32_t cta) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    if (cta < -1 || cta >= e->G) return fail(e, KIE_ERR_INVALID_ARG, "cta %d outside [-1, %d)", cta, e->G);
+    e->skip_arrival_cta = cta;
+    return KIE_OK;
+}
+
 void* kie_get_stream(const kie_engine* e) { return e ? static_cast<void*>(e->stream) : nullptr; }
 int32_t kie_grid_size(const kie_engine* e) { return e ? e->G : 0; }
 
@@ -1198,8 +1275,11 @@ kie_status kie_read_kv(kie_engine* e, int32_t layer, int32_t which, int32_t p0, 
                 KIE_CUDA(e, cudaMemcpy(zp + size_t(h) * (s1 - s0), e->dev(L.seg_zp) + mi * 4, size_t(s1 - s0) * 4, cudaMemcpyDeviceToHost));
         }
         if (tail_fp16) {
-            // positions of [p0, p0+n) in the open segment (the one holding pos)
-            const int open0 = (e->pos / KIE_SEG) * KIE_SEG;
+            // positions of [p0, p0+n) in the open segment (the one holding
+            // pos); when pos sits on a segment boundary nothing of the new
+            // open segment is written yet and the tail still holds the fp16
+            // values of the segment that has just been quantised
+            const int open0 = (e->pos % KIE_SEG == 0 && e->pos > 0) ? e->pos - KIE_SEG : (e->pos / KIE_SEG) * KIE_SEG;
             std::vector<uint16_t> t(size_t(H) * KIE_SEG * hd);
             KIE_CUDA(e, cudaMemcpy(t.data(), e->dev(L.tail) + (size_t(layer) * 2 + which) * H * KIE_SEG * hd * 2, t.size() * 2, cudaMemcpyDeviceToHost));
             for (int h = 0; h < H; ++h)
@@ -1269,6 +1349,26 @@ kie_status kie_quantize_fp8_rows(const uint16_t* w_fp16, int32_t rows, int32_t c
     return st;
 }
 
+kie_status kie_quantize_nvfp4_rows(const uint16_t* w_fp16, int32_t rows, int32_t cols, uint8_t* codes,
+                                   uint8_t* block_scales, float* row_scales) {
+    if (!w_fp16 || !codes || !block_scales || !row_scales || rows <= 0 || cols <= 0 || cols % 16)
+        return fail(nullptr, KIE_ERR_INVALID_ARG, "bad arguments");
+    const size_t n = size_t(rows) * cols;
+    uint8_t* buf = nullptr;
+    const size_t o_codes = align_up(n * 2, 256), o_bs = o_codes + align_up(n, 256), o_rs = o_bs + align_up(n / 16, 256);
+    if (cudaMalloc(&buf, o_rs + size_t(rows) * 4) != cudaSuccess) return fail(nullptr, KIE_ERR_OOM, "cudaMalloc failed");
+    kie_status st = KIE_OK;
+    if (cudaMemcpy(buf, w_fp16, n * 2, cudaMemcpyHostToDevice) != cudaSuccess ||
+        kie_launch_quant_fp4(reinterpret_cast<uint16_t*>(buf), rows, cols, nullptr, buf + o_codes, buf + o_bs,
+                             reinterpret_cast<float*>(buf + o_rs), nullptr) != cudaSuccess ||
+        cudaMemcpy(codes, buf + o_codes, n, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(block_scales, buf + o_bs, n / 16, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(row_scales, buf + o_rs, size_t(rows) * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        st = fail(nullptr, KIE_ERR_CUDA, "NVFP4 quantisation failed: %s", cudaGetErrorString(cudaGetLastError()));
+    cudaFree(buf);
+    return st;
+}
+
 kie_status kie_convert_fp8_e5m2(const uint16_t* x_fp16, size_t n, uint8_t* out) {
     if (!x_fp16 || !out) return fail(nullptr, KIE_ERR_INVALID_ARG, "bad arguments");
     if (n == 0) return KIE_OK;
@@ -1284,77 +1384,6 @@ kie_status kie_convert_fp8_e5m2(const uint16_t* x_fp16, size_t n, uint8_t* out) 
     return st;
 }
 
-// ---- decode step with scratch in a static device array (no allocation) -------------------------
-//
-// For callers that must not allocate device memory while decoding: code running
-// inside another framework's memory pool or allocator-less plugin host, a real-
-// time service that forbids allocation after start-up, or a process whose device
-// memory is already fully committed.  Together with an engine created on a
-// caller-provided workspace, this step performs no cudaMalloc, cudaFree or other
-// allocating call.  The decode kernel's scratch (residual stream, q, attention
-// output and partials, SwiGLU output, argmax partials, head counters, control
-// block) lives in the array below; weights and the KV cache stay in the engine.
-
-#define KIE_STATIC_SCRATCH_BYTES (256u * 1024u)
-
-// Every GPU that loads libkie holds this array until the process exits.  Host
-// code must not use its name as an address: the address comes from
-// cudaGetSymbolAddress, once per device, in static_scratch_ptr below.
-static __device__ __align__(256) uint8_t kie_static_scratch[KIE_STATIC_SCRATCH_BYTES];
-
-namespace {
-
-struct StaticScratchLayout {
-    size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl, total;
-};
-
-StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
-    StaticScratchLayout l;
-    size_t o = 0;
-    auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
-    const size_t hq = size_t(c.n_heads) * c.head_dim * 4;
-    // tagged activations, reset per step as in the engine's workspace
-    l.x = take(size_t(c.d_model) * 4);
-    l.kcur = take(hq);
-    l.vcur = take(hq);
-    l.zero_bytes = l.vcur + hq - l.x;
-    l.q = take(hq);
-    l.a = take(size_t(c.ffn_dim) * 4);
-    l.o = take(hq);
-    l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
-    l.par_bytes = l.att_part + size_t(G) * (c.head_dim + 4) * 4 - l.q;
-    l.amax_val = take(size_t(G) * 4);
-    l.amax_idx = take(size_t(G) * 4);
-    l.ctl = take(sizeof(KieControl));
-    l.total = align_up(o, 256);
-    return l;
-}
-
-std::mutex g_static_scratch_mu;
-void* g_static_scratch_dev[64] = {};
-
-// Device address of kie_static_scratch on `device` (looked up once per device,
-// with that device current).
-cudaError_t static_scratch_ptr(int device, void** out) {
-    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-    if (!g_static_scratch_dev[device]) {
-        int prev = 0;
-        cudaError_t r = cudaGetDevice(&prev);
-        if (r != cudaSuccess) return r;
-        if (prev != device && (r = cudaSetDevice(device)) != cudaSuccess) return r;
-        void* ptr = nullptr;
-        r = cudaGetSymbolAddress(&ptr, kie_static_scratch);
-        if (prev != device) cudaSetDevice(prev);
-        if (r != cudaSuccess) return r;
-        g_static_scratch_dev[device] = ptr;
-    }
-    *out = g_static_scratch_dev[device];
-    return cudaSuccess;
-}
-
-}  // namespace
-
 extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t token, int32_t* d_next_token,
                                                      float* d_logits) {
     kie_status st = ready(e, 1);
@@ -1366,10 +1395,7 @@ extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t toke
     if (sl.total > KIE_STATIC_SCRATCH_BYTES)
         return fail(e, KIE_ERR_UNSUPPORTED, "scratch of %zu bytes exceeds the static maximum of %u bytes", sl.total,
                     KIE_STATIC_SCRATCH_BYTES);
-    void* base = nullptr;
-    cudaError_t r = static_scratch_ptr(e->cfg.device, &base);
-    if (r != cudaSuccess) return fail(e, KIE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(r));
-    uint8_t* b = static_cast<uint8_t*>(base);
+    uint8_t* b = static_cast<uint8_t*>(e->static_scratch);
     // the control block (barrier count, error word, argmax arrivals) starts at
     // zero and the activation tags are reset; everything else is written
     // before it is read
@@ -1393,7 +1419,7 @@ extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t toke
     l.out_tokens = d_next_token;
     l.out_logits = d_logits;
     void* args[] = {(void*)&P, (void*)&l};
-    r = cudaLaunchCooperativeKernel(e->kernel, dim3(e->G), dim3(KIE_THREADS), args, e->plan.smem, e->stream);
+    const cudaError_t r = cudaLaunchCooperativeKernel(e->kernel, dim3(e->G), dim3(KIE_THREADS), args, e->plan.smem, e->stream);
     if (r == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
         return fail(e, KIE_ERR_LAUNCH, "persistent grid of %d CTAs cannot be co-resident", e->G);

@@ -147,13 +147,13 @@ __device__ __forceinline__ uint64_t stream_offset(const KieParams& P, const Smem
 }
 
 __device__ __forceinline__ void slot_stamp(const KieLaunch& Lc, int cta, uint32_t g, int ev) {
-    if (Lc.prof_slots && cta == 0 && g < KIE_PROF_SLOTS) Lc.prof_slots[size_t(g) * 4 + ev] = globaltimer();
+    if (Lc.prof_slots && cta == 0 && g < KIE_PROF_SLOTS) Lc.prof_slots[size_t(g) * 4 + ev] = globaltimer_stamp();
 }
 
 __device__ __forceinline__ void stamp(const KieParams& P, const KieLaunch& Lc, int t, int phi, int ev, int cta) {
     if (Lc.prof) {
         const size_t nph = size_t(5 * P.L + 1);
-        Lc.prof[((size_t(t) * nph + phi) * KIE_PROF_EVENTS + ev) * P.G + cta] = globaltimer();
+        Lc.prof[((size_t(t) * nph + phi) * KIE_PROF_EVENTS + ev) * P.G + cta] = globaltimer_stamp();
     }
 }
 
@@ -205,6 +205,7 @@ struct TagWait {
     uint32_t spins;
     __device__ TagWait() : t0(globaltimer()), spins(0) {}
     __device__ __forceinline__ bool again(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
+        if (P.poll_ns) __nanosleep(P.poll_ns);
         if ((++spins & 15u) != 0u) return true;
         if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
         if (globaltimer() - t0 > Lc.timeout_ns) {
@@ -309,6 +310,28 @@ __device__ __forceinline__ bool producer_wait_slot(const KieParams& P, const Kie
     return true;
 }
 
+// Producer: wait until global slot g has landed (its copy completed), so that
+// at most P.inflight copies are outstanding.  Slot g's full barrier can be in
+// its phase for generation q (in flight) or the next (landed) only: generation
+// q + 2 is issued later than the slot being issued now.
+__device__ __forceinline__ bool producer_wait_landed(const KieParams& P, const KieLaunch& Lc, const Smem& S,
+                                                     uint32_t g, int cta) {
+    const uint32_t nslot = uint32_t(P.nslot);
+    const uint32_t slot = g % nslot, q = g / nslot;
+    uint64_t* fb = &S.full[2 * slot + (q & 1u)];
+    const uint32_t par = (q >> 1) & 1u;
+    if (mbar_test_wait(fb, par)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(fb, par)) {
+        if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
+        if (globaltimer() - t0 > Lc.timeout_ns) {
+            set_error(P, KERR_TIMEOUT_FULL, cta);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Consumer warp: wait until global slot gidx has landed.  Every lane probes the
 // barrier (each lane needs the acquire of the bulk-copy data) but the decision
 // to continue or abort is warp-uniform, so no lane can leave the slot loop while
@@ -338,6 +361,9 @@ __device__ __forceinline__ bool warp_wait_full(const KieParams& P, const KieLaun
 __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
     const uint64_t pol = policy_evict_first();
     const uint32_t nslot = uint32_t(P.nslot);
+    // copies outstanding at most (the rest of the ring holds landed slots that
+    // absorb the consumers' waits instead of more queued copies)
+    const uint32_t inflight = uint32_t(min(max(P.inflight, 1), P.nslot));
     uint32_t g = 0, rs = 0, rq = 0;   // global slot index, its ring slot and generation
     bool abort = false;
     const uint64_t pol_kv = policy_evict_first();
@@ -373,6 +399,7 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 for (uint32_t j = 0; j < nsl && !abort; ++j, ++g) {
                     const uint32_t slot = rs;
                     if (g >= nslot && !producer_wait_slot(P, Lc, S, rs, (rq - 1u) & 1u, cta)) { abort = true; break; }
+                    if (g >= inflight && !producer_wait_landed(P, Lc, S, g - inflight, cta)) { abort = true; break; }
                     const int r0 = int(j) * rps;
                     const int rows = min(rps, a.jt - a.j0 - r0);
                     const size_t off = kv_elem_index(P, layer, a.h, a.j0 + r0) * size_t(rb / P.hd);
@@ -399,6 +426,7 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 const int rows_g = min(c.R, c.rows - gg * c.R);
                 for (int ch = 0; ch < c.nK; ++ch, ++j) {
                     if (g >= nslot && !producer_wait_slot(P, Lc, S, rs, (rq - 1u) & 1u, cta)) { abort = true; break; }
+                    if (g >= inflight && !producer_wait_landed(P, Lc, S, g - inflight, cta)) { abort = true; break; }
                     const int kc = min(c.KC, c.K - ch * c.KC);
                     const uint32_t bytes = slot_bytes(c.wfmt, rows_g, kc);
                     uint64_t* fb = &S.full[2 * rs + (rq & 1u)];
@@ -573,12 +601,30 @@ __device__ void act_copy(const KieParams& P, const KieLaunch& Lc, const Smem& S,
     consumer_sync(NCT);
 }
 
+// The GEMV loops accumulate with the packed fp32 FMA (fma.rn.f32x2): each row
+// keeps two fp32 partial sums (even and odd elements of its 8-element pieces),
+// which halves the FMA instructions and doubles the independent chains; the
+// two are added once at the end of the slot.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// acc += w[0..7] * (xl, xh) for one 8-element piece; w as four fp16 pairs.
+__device__ __forceinline__ float2 piece_f16(const uint4& w, const float4& xl, const float4& xh, float2 s) {
+    s = ffma2(h2_to_f2(w.x), make_float2(xl.x, xl.y), s);
+    s = ffma2(h2_to_f2(w.y), make_float2(xl.z, xl.w), s);
+    s = ffma2(h2_to_f2(w.z), make_float2(xh.x, xh.y), s);
+    s = ffma2(h2_to_f2(w.w), make_float2(xh.z, xh.w), s);
+    return s;
+}
+
 // y-partials of one fp16 slot: rows_g rows x kc columns, row-major; columns start at k0.
 __device__ __forceinline__ void slot_f16(const uint8_t* slot, int rows_g, int kc, int k0, const float* act,
                                          int half, int lane, float* acc) {
     const int npc = kc >> 3;
     const float* alo = act + (k0 >> 3) * 4;
     const float* ahi = alo + half;
+    float2 a2[KIE_R];
+#pragma unroll
+    for (int r = 0; r < KIE_R; ++r) a2[r] = make_float2(0.f, 0.f);
     for (int p = lane; p < npc; p += 32) {
         const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
         const float4 xh = *reinterpret_cast<const float4*>(ahi + p * 4);
@@ -586,14 +632,12 @@ __device__ __forceinline__ void slot_f16(const uint8_t* slot, int rows_g, int kc
         for (int r = 0; r < KIE_R; ++r) {
             if (r < rows_g) {
                 const uint4 w = *reinterpret_cast<const uint4*>(slot + size_t(r) * kc * 2 + size_t(p) * 16);
-                const float2 a = h2_to_f2(w.x), b = h2_to_f2(w.y), c = h2_to_f2(w.z), e = h2_to_f2(w.w);
-                float s = acc[r];
-                s = fmaf(a.x, xl.x, s); s = fmaf(a.y, xl.y, s); s = fmaf(b.x, xl.z, s); s = fmaf(b.y, xl.w, s);
-                s = fmaf(c.x, xh.x, s); s = fmaf(c.y, xh.y, s); s = fmaf(e.x, xh.z, s); s = fmaf(e.y, xh.w, s);
-                acc[r] = s;
+                a2[r] = piece_f16(w, xl, xh, a2[r]);
             }
         }
     }
+#pragma unroll
+    for (int r = 0; r < KIE_R; ++r) acc[r] = a2[r].x + a2[r].y;
 }
 
 // The common full slot (KIE_R rows x KIE_KC_F16 columns) with compile-time
@@ -603,6 +647,9 @@ __device__ __forceinline__ void slot_f16_full(const uint8_t* slot, int k0, const
     constexpr int NPC = KIE_KC_F16 / 8;
     const float* alo = act + (k0 >> 3) * 4;
     const float* ahi = alo + half;
+    float2 a2[KIE_R];
+#pragma unroll
+    for (int r = 0; r < KIE_R; ++r) a2[r] = make_float2(0.f, 0.f);
     constexpr int kUnroll = KIE_F16_UNROLL;
 #pragma unroll kUnroll
     for (int it = 0; it < NPC / 32; ++it) {
@@ -612,13 +659,23 @@ __device__ __forceinline__ void slot_f16_full(const uint8_t* slot, int k0, const
 #pragma unroll
         for (int r = 0; r < KIE_R; ++r) {
             const uint4 w = *reinterpret_cast<const uint4*>(slot + size_t(r) * KIE_KC_F16 * 2 + size_t(p) * 16);
-            const float2 a = h2_to_f2(w.x), b = h2_to_f2(w.y), c = h2_to_f2(w.z), e = h2_to_f2(w.w);
-            float s = acc[r];
-            s = fmaf(a.x, xl.x, s); s = fmaf(a.y, xl.y, s); s = fmaf(b.x, xl.z, s); s = fmaf(b.y, xl.w, s);
-            s = fmaf(c.x, xh.x, s); s = fmaf(c.y, xh.y, s); s = fmaf(e.x, xh.z, s); s = fmaf(e.y, xh.w, s);
-            acc[r] = s;
+            a2[r] = piece_f16(w, xl, xh, a2[r]);
         }
     }
+#pragma unroll
+    for (int r = 0; r < KIE_R; ++r) acc[r] = a2[r].x + a2[r].y;
+}
+
+// acc += w[0..7] * (xl, xh) for one 8-element piece of FP8 E4M3 codes.
+__device__ __forceinline__ float2 piece_f8(const uint2& w, const float4& xl, const float4& xh, float2 s) {
+    float f[8];
+    e4m3x4_to_f32(w.x, f);
+    e4m3x4_to_f32(w.y, f + 4);
+    s = ffma2(make_float2(f[0], f[1]), make_float2(xl.x, xl.y), s);
+    s = ffma2(make_float2(f[2], f[3]), make_float2(xl.z, xl.w), s);
+    s = ffma2(make_float2(f[4], f[5]), make_float2(xh.x, xh.y), s);
+    s = ffma2(make_float2(f[6], f[7]), make_float2(xh.z, xh.w), s);
+    return s;
 }
 
 // FP8 E4M3 slot: codes [rows_g][kc], row-major, up to KIE_R8 rows; the rows'
@@ -628,6 +685,9 @@ __device__ __forceinline__ void slot_f8(const uint8_t* slot, int rows_g, int kc,
     const int npc = kc >> 3;
     const float* alo = act + (k0 >> 3) * 4;
     const float* ahi = alo + half;
+    float2 a2[KIE_R8];
+#pragma unroll
+    for (int r = 0; r < KIE_R8; ++r) a2[r] = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int p = lane; p < npc; p += 32) {
         const float4 xl = *reinterpret_cast<const float4*>(alo + p * 4);
@@ -636,16 +696,12 @@ __device__ __forceinline__ void slot_f8(const uint8_t* slot, int rows_g, int kc,
         for (int r = 0; r < KIE_R8; ++r) {
             if (r < rows_g) {
                 const uint2 w = *reinterpret_cast<const uint2*>(slot + size_t(r) * kc + size_t(p) * 8);
-                float f[8];
-                e4m3x4_to_f32(w.x, f);
-                e4m3x4_to_f32(w.y, f + 4);
-                float t = acc[r];
-                t = fmaf(f[0], xl.x, t); t = fmaf(f[1], xl.y, t); t = fmaf(f[2], xl.z, t); t = fmaf(f[3], xl.w, t);
-                t = fmaf(f[4], xh.x, t); t = fmaf(f[5], xh.y, t); t = fmaf(f[6], xh.z, t); t = fmaf(f[7], xh.w, t);
-                acc[r] = t;
+                a2[r] = piece_f8(w, xl, xh, a2[r]);
             }
         }
     }
+#pragma unroll
+    for (int r = 0; r < KIE_R8; ++r) acc[r] = a2[r].x + a2[r].y;
 }
 
 // The common full FP8 slot (KIE_R8 rows x KIE_KC_F16 columns) with compile-time
@@ -654,6 +710,9 @@ __device__ __forceinline__ void slot_f8_full(const uint8_t* slot, int k0, const 
                                              float* acc) {
     const float* alo = act + (k0 >> 3) * 4;
     const float* ahi = alo + half;
+    float2 a2[KIE_R8];
+#pragma unroll
+    for (int r = 0; r < KIE_R8; ++r) a2[r] = make_float2(0.f, 0.f);
     constexpr int kUnroll = KIE_F8_UNROLL;
 #pragma unroll kUnroll
     for (int it = 0; it < KIE_KC_F16 / 256; ++it) {
@@ -663,15 +722,11 @@ __device__ __forceinline__ void slot_f8_full(const uint8_t* slot, int k0, const 
 #pragma unroll
         for (int r = 0; r < KIE_R8; ++r) {
             const uint2 w = *reinterpret_cast<const uint2*>(slot + size_t(r) * KIE_KC_F16 + size_t(p) * 8);
-            float f[8];
-            e4m3x4_to_f32(w.x, f);
-            e4m3x4_to_f32(w.y, f + 4);
-            float t = acc[r];
-            t = fmaf(f[0], xl.x, t); t = fmaf(f[1], xl.y, t); t = fmaf(f[2], xl.z, t); t = fmaf(f[3], xl.w, t);
-            t = fmaf(f[4], xh.x, t); t = fmaf(f[5], xh.y, t); t = fmaf(f[6], xh.z, t); t = fmaf(f[7], xh.w, t);
-            acc[r] = t;
+            a2[r] = piece_f8(w, xl, xh, a2[r]);
         }
     }
+#pragma unroll
+    for (int r = 0; r < KIE_R8; ++r) acc[r] = a2[r].x + a2[r].y;
 }
 
 // INT4 slot: codes [rows_g][kc/2] (element 2b in the low nibble of byte b, two's
@@ -1563,7 +1618,9 @@ __device__ __forceinline__ bool grid_barrier(const KieParams& P, const KieLaunch
     if (tid == 0) {
         // red.release is cumulative: the block's writes ordered before it by the
         // consumer barrier above become visible to every acquirer of the count.
-        red_release_gpu_add(&P.ctl->bar, 1u);
+        // (A test can make one CTA skip its first arrival: the others' bounded
+        // waits then run out and report a timeout.)
+        if (!(nbar == 0u && cta == Lc.skip_arrival_cta)) red_release_gpu_add(&P.ctl->bar, 1u);
         const uint32_t target = (nbar + 1u) * uint32_t(P.G);
         const uint64_t t0 = globaltimer();
         int spins = 0;

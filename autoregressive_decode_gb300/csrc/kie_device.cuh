@@ -15,6 +15,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// The timer read as a trace stamp: ordered with this thread's memory accesses
+// (the compiler may not move loads or stores across it).
+__device__ __forceinline__ uint64_t globaltimer_stamp() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t) :: "memory");
+    return t;
+}
 
 // ---- mbarrier ------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

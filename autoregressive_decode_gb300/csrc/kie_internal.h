@@ -83,8 +83,9 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
 }
 
 enum KiePhaseType { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3, PH_LM = 4, PH_NTYPES = 5 };
-enum KieWFmt { WF_F16 = 0, WF_I4 = 1, WF_F8 = 2 };
+enum KieWFmt { WF_F16 = 0, WF_I4 = 1, WF_F8 = 2, WF_F4 = 3 };
 #define KIE_R8 8                 // rows per FP8 slot (8 rows x KIE_KC_F16 one-byte weights)
+#define KIE_R4 14                // rows per NVFP4 slot (14 rows x KIE_KC_F16 half-byte codes + block scales: 15.75 KB)
 enum KieKv { KV_F16 = 0, KV_E5M2 = 1, KV_U8 = 2 };
 
 enum KieErr {
@@ -105,10 +106,10 @@ struct KiePhasePlan {
     int32_t nK;              // chunks per row = ceil(K / KC)
     int32_t rows_per_unit;   // 1 or 2
     int32_t wfmt;            // KieWFmt
-    int32_t R;               // rows per slot: KIE_R, or KIE_R8 for FP8
+    int32_t R;               // rows per slot: KIE_R, KIE_R8 for FP8, KIE_R4 for NVFP4
     int32_t n_units;         // units over the grid
-    const float* wscale;     // FP8: fp32 row scales of layer 0 in the phase's row order (null otherwise)
-    int64_t wscale_layer;    // FP8: floats between consecutive layers' scales
+    const float* wscale;     // FP8 / NVFP4: fp32 row scales of layer 0 in the phase's row order (null otherwise)
+    int64_t wscale_layer;    // FP8 / NVFP4: floats between consecutive layers' scales
     const int32_t* unit_begin;   // [G+1] device: CTA i owns units [unit_begin[i], unit_begin[i+1])
     const uint32_t* bytes;       // [G]   device: stream bytes of this phase for CTA i
     const uint32_t* nslots;      // [G]   device: slots of this phase for CTA i
@@ -162,6 +163,8 @@ struct KieParams {
     KieControl* ctl;
     // shared-memory layout
     int32_t nslot;               // ring slots
+    int32_t inflight;            // bulk copies the producer keeps outstanding at most (<= nslot)
+    uint32_t poll_ns;            // pause between two polls of another CTA's tagged data (0: none)
     int32_t act_floats;          // activation buffer (floats)
     int32_t part_floats;         // GEMV partial buffer (floats)
 };
@@ -178,6 +181,7 @@ struct KieLaunch {
     float* out_logits;           // device [n_steps - lm_from_step][V] or null
     uint64_t timeout_ns;
     int32_t use_grid_barrier;    // 1 in the persistent (cooperative) launch
+    int32_t skip_arrival_cta;    // failure injection: this CTA skips its arrival at the first grid barrier (-1: none)
     // Optional trace: %globaltimer stamps [n_steps][5L+1][KIE_PROF_EVENTS][G]:
     // 0 phase start (after the grid barrier), 1 activation staged, 2 GEMV /
     // attention done, 3 epilogue done, 4 producer issued the phase's first slot

@@ -101,6 +101,69 @@ __global__ void kie_quant_fp8_kernel(const uint16_t* w, int rows, int cols, uint
     if (lane == 0) scales[warp] = s;
 }
 
+// ---- NVFP4 weights: E2M1 codes, an E4M3 scale per 16 columns, an fp32 scale per row --------
+// One warp per row, one lane per 16-column block at a time, every step in fp32
+// with IEEE division and products rounded once:
+//   rs = absmax(row) / 2688                       (2688 = 6 * 448)
+//   bs = e4m3(absmax(block) / (6 * rs))           (round to nearest even, saturating)
+//   code = e2m1(w / (float(bs) * rs))             (round to nearest even, saturating at +-6)
+// rs == 0 gives bs = 0 and codes 0; a block scale of 0 gives codes 0.
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(x));   // x -> the low byte
+    return r & 0xFFu;
+}
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {          // lo -> low nibble
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r & 0xFFu;
+}
+__device__ __forceinline__ float e4m3_to_f32_exact(uint32_t b) {
+    float f[4];
+    e4m3x4_to_f32(b & 0xFFu, f);
+    return f[0];
+}
+// packed: [rows][cols/2] (element 2j in the low nibble of byte j) or null;
+// codes: [rows][cols] one code (0..15) per byte, or null; bscales [rows][cols/16]; rscales [rows].
+__global__ void kie_quant_fp4_kernel(const uint16_t* w, int rows, int cols, uint8_t* packed, uint8_t* codes,
+                                     uint8_t* bscales, float* rscales) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const uint16_t* src = w + size_t(warp) * cols;
+    float am = 0.f;
+    for (int k = lane; k < cols; k += 32) am = fmaxf(am, fabsf(__half2float(__ushort_as_half(src[k]))));
+    am = warp_max(am);
+    const float rs = am / 2688.0f;
+    const float six_rs = 6.0f * rs;
+    const int nb = cols / 16;
+    for (int b = lane; b < nb; b += 32) {
+        float v[16];
+        float bm = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            v[j] = __half2float(__ushort_as_half(src[b * 16 + j]));
+            bm = fmaxf(bm, fabsf(v[j]));
+        }
+        const uint32_t bsc = rs > 0.f ? f32_to_e4m3(bm / six_rs) : 0u;
+        const float denom = e4m3_to_f32_exact(bsc) * rs;
+        uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            const uint32_t c2 = denom > 0.f ? f32x2_to_e2m1x2(v[j] / denom, v[j + 1] / denom) : 0u;
+            pk[j >> 3] |= c2 << (4 * (j & 7));
+            if (codes) {
+                codes[size_t(warp) * cols + b * 16 + j] = uint8_t(c2 & 0xFu);
+                codes[size_t(warp) * cols + b * 16 + j + 1] = uint8_t(c2 >> 4);
+            }
+        }
+        if (packed) *reinterpret_cast<uint2*>(packed + size_t(warp) * (cols / 2) + b * 8) = make_uint2(pk[0], pk[1]);
+        bscales[size_t(warp) * nb + b] = uint8_t(bsc);
+    }
+    if (lane == 0) rscales[warp] = rs;
+}
+
 // ---- adaptive-range uint8 quantisation ------------------------------------------------------
 // One CTA per segment.  A segment is `rows` rows of `row_elems` fp16 values;
 // element (r, k) of segment s is at src[s*src_seg + r*src_row + k] and its code
@@ -210,6 +273,14 @@ extern "C" cudaError_t kie_launch_quant_fp8(const uint16_t* w, int rows, int col
     const int threads = 256;
     const long blocks = (long(rows) * 32 + threads - 1) / threads;
     kie_quant_fp8_kernel<<<unsigned(blocks), threads, 0, st>>>(w, rows, cols, codes, scales);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_quant_fp4(const uint16_t* w, int rows, int cols, uint8_t* packed, uint8_t* codes,
+                                            uint8_t* bscales, float* rscales, cudaStream_t st) {
+    const int threads = 256;
+    const long blocks = (long(rows) * 32 + threads - 1) / threads;
+    kie_quant_fp4_kernel<<<unsigned(blocks), threads, 0, st>>>(w, rows, cols, packed, codes, bscales, rscales);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,7 @@ KIE_OK, KIE_ERR_INVALID_ARG, KIE_ERR_OOM, KIE_ERR_CUDA = 0, -1, -2, -3
 KIE_ERR_NOT_LOADED, KIE_ERR_CTX_OVERFLOW, KIE_ERR_DEVICE_TIMEOUT = -4, -5, -6
 KIE_ERR_LAUNCH, KIE_ERR_UNSUPPORTED = -7, -8
 KV_DTYPES = {"fp16": 0, "fp8_e5m2": 1, "u8": 2}
-W_DTYPES = {"fp16": 0, "int4_g128": 1, "fp8_e4m3": 2}
+W_DTYPES = {"fp16": 0, "int4_g128": 1, "fp8_e4m3": 2, "nvfp4": 3}
 MODES = {"persistent": 0, "graph": 1}
 
 STATUS_NAMES = {0: "KIE_OK", -1: "KIE_ERR_INVALID_ARG", -2: "KIE_ERR_OOM", -3: "KIE_ERR_CUDA",
@@ -71,6 +71,7 @@ EXPORTS = {
     "kie_get_pos": (C.c_int32, [C.c_void_p]),
     "kie_set_pos": (C.c_int, [C.c_void_p, C.c_int32]),
     "kie_set_timeout_ms": (C.c_int, [C.c_void_p, C.c_int32]),
+    "kie_debug_skip_grid_arrival": (C.c_int, [C.c_void_p, C.c_int32]),
     "kie_get_stream": (C.c_void_p, [C.c_void_p]),
     "kie_grid_size": (C.c_int32, [C.c_void_p]),
     "kie_last_error": (C.c_char_p, [C.c_void_p]),
@@ -81,6 +82,7 @@ EXPORTS = {
     "kie_quantize_kv_u8": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "kie_quantize_int4_g128": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_quantize_fp8_rows": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
+    "kie_quantize_nvfp4_rows": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "kie_convert_fp8_e5m2": (C.c_int, [C.c_void_p, C.c_size_t, C.c_void_p]),
 }
 
@@ -229,6 +231,11 @@ class Engine:
     def set_timeout_ms(self, ms: int):
         _check(load().kie_set_timeout_ms(self.h, int(ms)), self.h)
 
+    def debug_skip_grid_arrival(self, cta: int):
+        """Failure injection (tests): CTA `cta` skips its first grid-barrier
+        arrival in the next persistent launch of several steps."""
+        _check(load().kie_debug_skip_grid_arrival(self.h, int(cta)), self.h)
+
     @property
     def stream(self) -> int:
         return load().kie_get_stream(self.h) or 0
@@ -287,6 +294,18 @@ def quantize_fp8_rows(w16: np.ndarray):
     sc = np.empty(rows, np.float32)
     _check(load().kie_quantize_fp8_rows(_ptr(w), rows, cols, _ptr(codes), _ptr(sc)))
     return codes, sc
+
+
+def quantize_nvfp4_rows(w16: np.ndarray):
+    """kie_quantize_nvfp4_rows: (E2M1 codes uint8 [rows, cols] in 0..15,
+    E4M3 block-scale bytes uint8 [rows, cols/16], row scales fp32 [rows])."""
+    w = np.ascontiguousarray(w16, dtype=np.float16)
+    rows, cols = w.shape
+    codes = np.empty((rows, cols), np.uint8)
+    bs = np.empty((rows, cols // 16), np.uint8)
+    rs = np.empty(rows, np.float32)
+    _check(load().kie_quantize_nvfp4_rows(_ptr(w), rows, cols, _ptr(codes), _ptr(bs), _ptr(rs)))
+    return codes, bs, rs
 
 
 def convert_fp8_e5m2(x16: np.ndarray) -> np.ndarray:

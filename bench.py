@@ -19,6 +19,11 @@ cpu_baseline  the CPU oracle (numpy fp32) timed on this host's cores on a short
 Multi-GPU (torchrun): independent replicas, one engine per rank, no
 collective on the data path; value = tokens of all ranks / max rank time.
 
+workloads  (1 GPU, default run) a compact record for each of the other four
+        workloads -- 1.8B with FP8 E4M3 weights, 1.8B over a 32K FP8-E5M2 cache,
+        1.8B over an 8K adaptive uint8 cache, 7B with INT4 FFN -- with its
+        decode tokens/s, roofline fraction and a CPU-oracle figure.
+
 `--impl reference` times the CPU oracle as the reference arm.
 """
 from __future__ import annotations
@@ -55,6 +60,8 @@ def parse():
     ap.add_argument("--decode-tokens", type=int, default=None,
                     help="decode tokens per step (default: the workload's decode steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the compact records of the other four workloads (1 GPU runs only)")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: the workload with this many layers (a small case of the same "
                          "kernels for multi-pass ncu captures); the line's config records the depth")
@@ -259,6 +266,111 @@ def run_reference(args, w: S.Workload):
     print(json.dumps(line), flush=True)
 
 
+def cpu_baseline_by_depth(w: S.Workload, weights: dict, p0: int, n_steps: int = 3):
+    """The oracle on this host for a large workload, from a bounded sample: its
+    first one and first two layers (same weights, LM head and a synthetic
+    p0-position context) each decode n_steps tokens; the per-layer time (the
+    difference) extrapolates linearly to the workload's full depth."""
+    per = []
+    for depth in (1, 2):
+        wd = w.with_(n_layers=depth)
+        wt = dict(weights, layers=weights["layers"][:depth])
+        sample = OracleSample(wd, wt, p0, n_steps)
+        per.append(statistics.median(sample.time() / n_steps for _ in range(2)))
+        del sample
+    t_layer = max(per[1] - per[0], 0.0)
+    t_full = per[0] + (w.n_layers - 1) * t_layer
+    return {"value": 1.0 / t_full, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{n_steps} decode steps at positions {p0}..{p0 + n_steps - 1} of {w.name} at depth 1 "
+                      f"({per[0] * 1e3:.0f} ms/token) and depth 2 ({per[1] * 1e3:.0f} ms/token), extrapolated "
+                      f"linearly to {w.n_layers} layers; numpy fp32 with OpenBLAS"}
+
+
+def time_decode(eng, torch, stream, first: int, p0: int, n_dec: int, steps: int, warmup: int, device):
+    """Mean ms of `steps` device-timed generate launches of n_dec tokens from p0."""
+    d_tok = torch.empty(n_dec, dtype=torch.int32, device=device)
+    for _ in range(warmup):
+        eng.set_pos(p0)
+        eng.generate_greedy_device(first, n_dec, d_tok)
+    eng.sync()
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in per:
+        eng.set_pos(p0)
+        a.record(stream)
+        eng.generate_greedy_device(first, n_dec, d_tok)
+        b.record(stream)
+    eng.sync()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in per)
+
+
+# The other four workloads (a compact record each): their decode steps over the
+# context the workload names, prefilled on the GPU where the tensor-core path
+# covers it and otherwise (uint8 cache; the 7B model, whose decode bytes do not
+# depend on how its 4,096-position context was made) a synthetic one.
+EXTRA = ("1p8b_fp8", "1p8b_32k", "1p8b_u8", "7b_int4")
+
+
+def extra_workloads(args, local, kie, torch, weights_1p8b):
+    peak, peak_kind = peaks()
+    out = {}
+    w7 = None
+    for name in EXTRA:
+        w = S.WORKLOADS[name]
+        rec = {"workload": workload_desc(w)}
+        try:
+            if w.d_model == 2048:
+                weights = weights_1p8b
+                rec["weights"] = "the 1p8b workload's seeded weights (the 1.8B variants share one weight set here)"
+            else:
+                w7 = w7 or S.gen_weights(w)
+                weights = w7
+            synth = w.kv_source == "synthetic" or w.ffn_wdtype == "int4_g128"
+            if synth and w.kv_source == "prefill":
+                w = w.with_(kv_source="synthetic", context_len=w.prompt_len, prompt_len=0)
+            p0, n_dec = w.start_pos, w.decode_steps
+            cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, p0 + n_dec,
+                                  w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, "persistent", local,
+                                  attn_wdtype=w.attn_wdtype)
+            stream = torch.cuda.Stream(device=local)
+            eng = kie.Engine(cfg, stream=stream)
+            eng.load_weights(weights)
+            if synth:
+                for layer in range(w.n_layers):
+                    k, v = S.gen_kv(w, layer)
+                    eng.set_kv(layer, k, v)
+                eng.set_pos(p0)
+                first = S.gen_first_token(w)
+                rec["context"] = f"synthetic, {p0} positions"
+            else:
+                prompt = S.gen_prompt(w)
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                first = int(np.argmax(eng.prefill(prompt)))
+                pf_ms = (time.perf_counter() - t0) * 1e3
+                rec["context"] = f"GPU prefill of the {p0}-token prompt"
+                rec["prefill"] = {"tokens": p0, "ms": pf_ms, "tokens_per_s": p0 / (pf_ms / 1e3),
+                                  "path": "tcgen05 GEMM"}
+            ms = time_decode(eng, torch, stream, first, p0, n_dec, 3, 2, f"cuda:{local}")
+            eng.close()
+            bpl = bytes_per_launch(w, p0, n_dec)
+            achieved = bpl / (ms / 1e3) / 1e9
+            rec.update({"value": n_dec / (ms / 1e3), "unit": "tokens/s", "steps": 3, "warmup": 2,
+                        "ms_per_step": ms, "decode_tokens_per_step": n_dec,
+                        "positions": f"{p0}..{p0 + n_dec - 1}",
+                        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                     "frac": achieved / peak, "peak_source": peak_kind,
+                                     "kernel": "kie_decode_kernel", "algorithmic_bytes_per_launch": bpl,
+                                     "launch_ms": ms}})
+            if not args.no_cpu_baseline:
+                rec["cpu_baseline"] = cpu_baseline_by_depth(w, weights, p0)
+        except Exception as ex:  # report, never hide
+            rec["error"] = repr(ex)
+        out[name] = rec
+    return out
+
+
 def main():
     args = parse()
     w = S.WORKLOADS[args.workload]
@@ -388,8 +500,10 @@ def main():
             line["cpu_baseline"] = cpu_baseline(w, weights, p0)
         except Exception as ex:  # report, never hide
             line["cpu_baseline"] = {"error": repr(ex)}
-    print(json.dumps(line), flush=True)
     eng.close()
+    if ws == 1 and not args.no_workloads and not args.layers and args.workload == "1p8b" and args.mode == "persistent":
+        line["workloads"] = extra_workloads(args, local, kie, torch, weights)
+    print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 

@@ -68,8 +68,13 @@ typedef enum { KIE_KV_FP16 = 0, KIE_KV_FP8_E5M2 = 1, KIE_KV_U8_ADAPTIVE = 2 } ki
  * per weight with one fp32 scale per output row, s = absmax/448, codes = E4M3
  * of w/s rounded to nearest even, saturating (the Kog page's "FP8 ~2 FLOP per
  * byte", section "Memory bandwidth is the main bottleneck"; the format and the
- * scale granularity are this engine's reading). */
-typedef enum { KIE_W_FP16 = 0, KIE_W_INT4_G128 = 1, KIE_W_FP8_E4M3 = 2 } kie_w_dtype;
+ * scale granularity are this engine's reading).  NVFP4: E2M1 codes (half a
+ * byte per weight), an E4M3 scale per 16 consecutive input columns and an fp32
+ * scale per output row (the same page's "FP4 ~4 FLOP per byte"; the format is
+ * this engine's reading: Blackwell's native 4-bit layout), quantised as
+ * kie_quantize_nvfp4_rows describes; the matrices' input dimension must be a
+ * multiple of 16. */
+typedef enum { KIE_W_FP16 = 0, KIE_W_INT4_G128 = 1, KIE_W_FP8_E4M3 = 2, KIE_W_NVFP4 = 3 } kie_w_dtype;
 /* PERSISTENT: one cooperative launch runs all requested tokens (a grid-wide
  * barrier between steps; the phases of a step are ordered by tagged
  * activations).  GRAPH: the same phases as separate launches,
@@ -92,15 +97,16 @@ typedef struct {
     int32_t ffn_wdtype;   /* kie_w_dtype of w_gate, w_up, w_down                     */
     int32_t mode;         /* kie_mode                                               */
     int32_t device;       /* CUDA device ordinal                                    */
-    int32_t attn_wdtype;  /* kie_w_dtype of wq, wk, wv, wo and the LM head: FP16 or FP8_E4M3 */
+    int32_t attn_wdtype;  /* kie_w_dtype of wq, wk, wv, wo and the LM head: FP16, FP8_E4M3 or NVFP4 */
 } kie_config;
 
 /* Per-layer weights, fp16 bit patterns, PyTorch Linear layout [out][in], row major.
  *   attn_norm[d]  wq,wk,wv[H*h][d]  wo[d][H*h]  ffn_norm[d]
  *   w_gate,w_up[F][d]  w_down[d][F]
  * For ffn_wdtype == KIE_W_INT4_G128 the engine quantises w_gate/w_up/w_down
- * itself (kie_quantize_int4_g128 below); for KIE_W_FP8_E4M3 (ffn_wdtype or
- * attn_wdtype) it quantises the matrices concerned with kie_quantize_fp8_rows. */
+ * itself (kie_quantize_int4_g128 below); for KIE_W_FP8_E4M3 or KIE_W_NVFP4
+ * (ffn_wdtype or attn_wdtype) it quantises the matrices concerned as
+ * kie_quantize_fp8_rows or kie_quantize_nvfp4_rows do. */
 typedef struct {
     const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
 } kie_layer_weights;
@@ -124,6 +130,8 @@ size_t kie_workspace_bytes(const kie_config* cfg);
  * frees on destroy) or a device buffer of at least kie_workspace_bytes(cfg)
  * bytes, 256-byte aligned, owned by the caller and kept alive until
  * kie_destroy.  cuda_stream: a cudaStream_t (NULL = the legacy default stream).
+ * It also resolves the device address of the library's static scratch array
+ * (see kie_decode_step_static_scratch), which loads the device code holding it.
  * On failure *out is NULL and kie_last_error(NULL) has the reason. */
 kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, void* cuda_stream,
                       kie_engine** out);
@@ -166,6 +174,14 @@ int32_t kie_get_pos(const kie_engine* e);
 kie_status kie_set_pos(kie_engine* e, int32_t pos);
 /* Bound on every wait inside the GPU program (default 2000 ms). */
 kie_status kie_set_timeout_ms(kie_engine* e, int32_t ms);
+/* Failure injection for tests of the device-timeout path: the next
+ * persistent launch that reaches a grid barrier lets CTA `cta` (0 <= cta <
+ * kie_grid_size) skip its arrival at the first one, so every other CTA's
+ * bounded wait there runs out after the kie_set_timeout_ms limit; the launch
+ * then ends with KIE_ERR_DEVICE_TIMEOUT and the engine stays poisoned until
+ * kie_reset.  The injection applies to one launch only; cta = -1 cancels it.
+ * Nothing hangs: every wait in the GPU program is bounded. */
+kie_status kie_debug_skip_grid_arrival(kie_engine* e, int32_t cta);
 /* The engine's stream (cudaStream_t) and number of CTAs of the persistent grid. */
 void* kie_get_stream(const kie_engine* e);
 int32_t kie_grid_size(const kie_engine* e);
@@ -205,10 +221,13 @@ kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint6
  * NULL or DEVICE fp32[vocab].  The step's scratch (activations, attention and
  * argmax partials, control block) is a fixed 256 KiB array inside the library
  * that every GPU loading the library keeps until the process exits; configs
- * whose scratch would exceed it (roughly d_model + 2*n_heads*head_dim +
- * ffn_dim + grid*(head_dim+4) floats) return KIE_ERR_UNSUPPORTED.  The first
- * call on a device looks up the array's device address (once per device), so
- * make that first call before any stream capture.  All calls on a device share
+ * whose scratch would exceed it (roughly d_model + 4*n_heads*head_dim +
+ * ffn_dim + grid*(head_dim+6) floats) return KIE_ERR_UNSUPPORTED.  The array
+ * is part of the library's device code: kie_create looks up its device address
+ * with the engine's device current, which (under CUDA's lazy module loading)
+ * is when the array's device memory is committed, so this call itself commits
+ * nothing.  A device reset invalidates the engine and the address with it.
+ * All calls on a device share
  * the array and it keeps the last call's contents: calls that may overlap on
  * the GPU (several engines, several streams) race and must be serialised by
  * the caller.  A device error of the step is reported by the engine's next
@@ -229,7 +248,10 @@ kie_status kie_set_kv(kie_engine* e, int32_t layer, const uint16_t* k_fp16, cons
  * [p0, p0+n), as raw storage: fp16 bits (2 bytes/elem), E5M2 bytes or uint8
  * codes (1 byte/elem), layout [n_heads][n][head_dim].  For uint8 caches the
  * positions of the open segment are returned as their fp16 values in
- * `tail_fp16` ([n_heads][n][head_dim], NULL allowed) and scale/zp of the
+ * `tail_fp16` ([n_heads][n][head_dim], NULL allowed; other positions are left
+ * untouched) -- when pos is a positive multiple of 128 no position of the new
+ * open segment exists yet, and the fp16 values returned are those of the
+ * segment [pos-128, pos) that was quantised last -- and scale/zp of the
  * segments covering the range in scale[n_heads][nseg], zp[n_heads][nseg]
  * (nseg = segments overlapping [p0, p0+n); NULL allowed). */
 kie_status kie_read_kv(kie_engine* e, int32_t layer, int32_t which, int32_t p0, int32_t n, void* out,
@@ -258,6 +280,20 @@ kie_status kie_quantize_int4_g128(const uint16_t* w_fp16, int32_t rows, int32_t 
  * and codes 0.  Host pointers: w_fp16 [rows][cols] in, codes [rows][cols] and
  * scales [rows] out.  Runs on the current CUDA device and synchronises it. */
 kie_status kie_quantize_fp8_rows(const uint16_t* w_fp16, int32_t rows, int32_t cols, uint8_t* codes, float* scales);
+
+/* NVFP4 weight quantisation (see kie_w_dtype), every step in fp32 with IEEE
+ * division and each product rounded once:
+ *   rs = absmax(row) / 2688                  (2688 = 6 * 448)
+ *   bs = E4M3(absmax(block) / (6 * rs))      per 16 consecutive columns, nearest even, saturating
+ *   code = E2M1(w / (bs * rs))               nearest even, saturating at +-6; the sign
+ *                                            bit follows w's sign (also for a zero)
+ * An all-zero row gets rs = 0, block scales 0 and codes 0.  Host pointers:
+ * w_fp16 [rows][cols] in (cols a multiple of 16); codes [rows][cols] out, one
+ * E2M1 code (0..15: sign, two exponent bits, one mantissa bit) per byte;
+ * block_scales [rows][cols/16] E4M3 bytes; row_scales [rows] fp32.  Runs on
+ * the current CUDA device and synchronises it. */
+kie_status kie_quantize_nvfp4_rows(const uint16_t* w_fp16, int32_t rows, int32_t cols, uint8_t* codes,
+                                   uint8_t* block_scales, float* row_scales);
 
 /* fp16 -> FP8 E5M2, round to nearest even, saturating to +-57344 (the cache's
  * conversion; xAI page sections 2.3 and 4.3).  NaN stays NaN. */

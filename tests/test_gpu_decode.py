@@ -258,3 +258,32 @@ def test_host_errors_on_gpu():
     e.reset()
     t, lg = e.decode_step(1)
     assert 0 <= t < w.vocab and np.isfinite(lg).all()
+
+
+def test_device_timeout_then_reset():
+    """A bounded wait that runs out, made on purpose without any fault: one CTA
+    skips its arrival at the first grid barrier of a launch, so every other
+    CTA's wait there expires after the 50 ms limit.  The call returns
+    KIE_ERR_DEVICE_TIMEOUT, the engine refuses further decode calls until
+    kie_reset, and afterwards it matches the oracle again."""
+    from autoregressive_decode_gb300 import kie
+    w = TINY
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    first = O.argmax_lowest(lo)
+    e.set_timeout_ms(50)
+    e.debug_skip_grid_arrival(e.grid // 2)
+    with pytest.raises(kie.KieError) as ei:
+        e.generate_greedy(first, 4)
+    assert ei.value.status == kie.KIE_ERR_DEVICE_TIMEOUT
+    with pytest.raises(kie.KieError) as ei:
+        e.decode_step(first)
+    assert ei.value.status == kie.KIE_ERR_DEVICE_TIMEOUT
+    e.reset()
+    e.set_timeout_ms(2000)
+    assert e.pos == 0
+    lg2 = e.prefill(S.gen_prompt(w))
+    np.testing.assert_array_equal(lg2, lg)
+    # the injection was one-shot: a launch of several steps runs normally now
+    toks, logs = e.generate_greedy(first, 6, want_logits=True)
+    check_free_running(o, first, toks, logs, tol_for(w))

@@ -1,31 +1,39 @@
-"""Full-size parity: the four large workloads in the launch configuration the
-bench times (persistent kernel, one CTA per SM), against the CPU oracle.
+"""Full-size parity: the large workloads in the launch configuration the bench
+times (persistent kernel, one CTA per SM, one cooperative launch for the whole
+greedy chain), against the CPU oracle.
 
   1p8b      GPU prefill of the 2048-token prompt vs the oracle's prefill (last
-            logits), then teacher-forced decode steps.
+            logits), then the bench's own launch: 256 free-running greedy steps
+            at positions 2048..2303 in ONE generate launch, every step's logits
+            and token validated against the oracle fed the GPU's tokens.
+  1p8b_fp8  every GEMV matrix in FP8 E4M3, synthetic 2,048-position context, 32 steps.
   1p8b_32k  FP8-E5M2 cache over a 32,768-position synthetic context (decode-only
-            parity: the same fp16 K/V loaded into both sides).
+            parity: the same fp16 K/V loaded into both sides), 32 steps.
   1p8b_u8   adaptive-range uint8 cache over the 8,192-position synthetic context
-            (N(0,1) with 0.1% +-20 outliers); stored codes, scales and
-            zero-points bit-exact on sampled layers.
-  7b_int4   INT4 g128 FFN, fp16 cache over a 4,096-position synthetic context;
-            INT4 codes and scales bit-exact on a sampled matrix.
+            (N(0,1) with 0.1% +-20 outliers): all 128 bench steps, so the
+            segment of positions 8192..8319 completes at the last step; its
+            codes, scales and zero-points bit-exact (against the oracle's
+            quantiser of the GPU's own fp16 values) on sampled layers.
+  7b_int4   INT4 g128 FFN, fp16 cache over a 4,096-position synthetic context,
+            32 steps; INT4 codes and scales bit-exact on a sampled matrix.
+  7b_int4 prompt prefill at reduced depth (4 layers): the 4,096-token prompt
+            through the decode kernel's teacher-forced prefill (the path INT4
+            FFN weights take) against the oracle's prefill.
 
 Logits: max |delta| <= 5e-2 (fp16 paths) or 1.5e-1 (FP8 / uint8 / INT4), over
 all vocab entries of every compared step; argmax equal where the oracle's
-top-2 margin exceeds 0.1.
+top-2 margin exceeds 0.1 (elsewhere the GPU's token must be within 2 x tol of
+the oracle's maximum).
 """
 import numpy as np
 import pytest
 
 import oracle as O
 import synthetic as S
-from _common import engine_for, teacher_forced, tol_for
+from _common import check_free_running, engine_for, teacher_forced, tol_for
 from autoregressive_decode_gb300 import kie
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
-
-STEPS = 3
 
 
 def _synthetic_context(w, e, o):
@@ -37,69 +45,133 @@ def _synthetic_context(w, e, o):
     o.pos = w.context_len
 
 
-def test_1p8b_prefill_and_decode():
+def _generate_on_device(e, first, n):
+    """n greedy steps in one persistent launch (the bench's call), with the
+    logits of every step kept on the device; returns host copies."""
+    torch = pytest.importorskip("torch")
+    d_tok = torch.zeros(n, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros((n, e.vocab), dtype=torch.float32, device="cuda")
+    e.generate_greedy_device(first, n, d_tok, d_log)
+    e.sync()
+    return d_tok.cpu().numpy(), d_log.cpu().numpy()
+
+
+def test_1p8b_prefill_and_bench_chain():
     w = S.WORKLOADS["1p8b"]
     weights = S.gen_weights(w)
-    e = engine_for(w, weights, max_ctx=w.prompt_len + STEPS)
-    o = O.OracleDecoder(w, weights, max_ctx=w.prompt_len + STEPS)
+    e = engine_for(w, weights)
+    o = O.OracleDecoder(w, weights)
     prompt = S.gen_prompt(w)
     lg = e.prefill(prompt)
     lo = o.prefill(prompt, q_block=512)
     assert np.abs(lg - lo).max() <= tol_for(w)
-    teacher_forced(e, o, O.argmax_lowest(lo), STEPS, tol_for(w))
+    first = O.argmax_lowest(lo)
+    assert e.pos == w.start_pos == 2048
+    toks, logs = _generate_on_device(e, first, w.decode_steps)
+    clear = check_free_running(o, first, toks, logs, tol_for(w))
+    assert clear >= w.decode_steps // 2
+
+
+def test_1p8b_fp8_weights_decode():
+    """The 1.8B model with every GEMV matrix in FP8 E4M3 over a synthetic
+    2,048-position fp16 context: 32 free-running steps in one launch (its
+    tensor-core prefill is checked on the smaller models)."""
+    n = 32
+    w = S.WORKLOADS["1p8b_fp8"].with_(kv_source="synthetic", context_len=2048, prompt_len=0)
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights, max_ctx=w.context_len + n)
+    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + n)
+    _synthetic_context(w, e, o)
+    first = S.gen_first_token(w)
+    toks, logs = _generate_on_device(e, first, n)
+    check_free_running(o, first, toks, logs, tol_for(w))
 
 
 def test_1p8b_32k_fp8_decode():
+    n = 32
     w = S.WORKLOADS["1p8b_32k"].with_(kv_source="synthetic", context_len=32768, prompt_len=0)
     weights = S.gen_weights(w)
-    e = engine_for(w, weights, max_ctx=w.context_len + STEPS)
-    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + STEPS)
+    e = engine_for(w, weights, max_ctx=w.context_len + n)
+    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + n)
     _synthetic_context(w, e, o)
-    # stored E5M2 bytes equal the oracle's conversion (sampled layer, K, first heads)
+    # stored E5M2 bytes equal the oracle's conversion (sampled layer, K, first positions)
     data, _, _, _ = e.read_kv(7, 0, 0, 4096)
     k, _ = S.gen_kv(w, 7, n_pos=4096)
     ref = O.e5m2_from_f16_bits(k.view(np.uint16)).reshape(4096, w.n_heads, w.head_dim).transpose(1, 0, 2)
     np.testing.assert_array_equal(data, ref)
-    teacher_forced(e, o, S.gen_first_token(w), STEPS, tol_for(w))
+    first = S.gen_first_token(w)
+    toks, logs = _generate_on_device(e, first, n)
+    check_free_running(o, first, toks, logs, tol_for(w))
 
 
-def test_1p8b_u8_decode():
+def test_1p8b_u8_decode_full_chain():
     w = S.WORKLOADS["1p8b_u8"]
     weights = S.gen_weights(w)
-    e = engine_for(w, weights, max_ctx=w.context_len + STEPS)
-    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + STEPS)
+    e = engine_for(w, weights)
+    o = O.OracleDecoder(w, weights)
     _synthetic_context(w, e, o)
-    for layer in (0, 13, 24):
+    for layer in (0, 24):
         for which in (0, 1):
             data, _, sc, zp = e.read_kv(layer, which, 0, w.context_len)
             np.testing.assert_array_equal(data, o.cache.codes[layer][which][:, :w.context_len])
             np.testing.assert_array_equal(sc, o.cache.scale[layer][which][:, :w.context_len // 128])
             np.testing.assert_array_equal(zp, o.cache.zp[layer][which][:, :w.context_len // 128])
-    teacher_forced(e, o, S.gen_first_token(w), STEPS, tol_for(w))
+    first = S.gen_first_token(w)
+    toks, logs = _generate_on_device(e, first, w.decode_steps)
+    check_free_running(o, first, toks, logs, tol_for(w))
+    # positions 8192..8319 form the segment the last step completed, quantised
+    # once on the GPU during decoding.  Its inputs are K/V the GPU computed,
+    # which may differ from the oracle's by an fp16 rounding flip, so the codes,
+    # scale and zero point are checked bit-exactly against the oracle's
+    # quantiser applied to the GPU's own fp16 values (still held by the tail at
+    # this segment boundary), and those values against the oracle's K/V.
+    s0 = w.context_len
+    assert e.pos == o.pos == s0 + 128
+    for layer in (0, 13, 24):
+        for which in (0, 1):
+            data, tail, sc, zp = e.read_kv(layer, which, s0, 128)
+            x16 = tail.view(np.float16)
+            for hh in range(w.n_heads):
+                codes, scale, zpt = O.u8_quantize(x16[hh])
+                np.testing.assert_array_equal(data[hh], codes)
+                assert sc[hh, 0] == scale and zp[hh, 0] == zpt
+            # layer 0's K/V depend on the current token only (rare one-ulp flips
+            # from summation order); deeper layers inherit flips of earlier
+            # positions through attention and are held to a relative bound
+            ref = o.cache.raw16[layer][which][:, s0:s0 + 128].astype(np.float32)
+            got = x16.astype(np.float32)
+            if layer == 0:
+                assert np.mean(got != ref) < 0.01
+            assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
 
 
 def test_7b_int4_decode():
+    n = 32
     w = S.WORKLOADS["7b_int4"].with_(kv_source="synthetic", context_len=4096, prompt_len=0)
     weights = S.gen_weights(w)
     codes, sc = kie.quantize_int4_g128(weights["layers"][17]["w_down"])
     rc, rs = O.int4_quantize_g128(weights["layers"][17]["w_down"])
     np.testing.assert_array_equal(codes, rc)
     np.testing.assert_array_equal(sc.view(np.uint16), rs.view(np.uint16))
-    e = engine_for(w, weights, max_ctx=w.context_len + STEPS)
-    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + STEPS)
+    e = engine_for(w, weights, max_ctx=w.context_len + n)
+    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + n)
     _synthetic_context(w, e, o)
-    teacher_forced(e, o, S.gen_first_token(w), STEPS, tol_for(w))
+    first = S.gen_first_token(w)
+    toks, logs = _generate_on_device(e, first, n)
+    check_free_running(o, first, toks, logs, tol_for(w))
 
 
-def test_1p8b_fp8_weights_prefill_and_decode():
-    """The 1.8B model with every GEMV matrix in FP8 E4M3 (the bench's 1p8b_fp8):
-    2,048-token tensor-core prefill, then teacher-forced decode steps."""
-    w = S.WORKLOADS["1p8b_fp8"]
+def test_7b_int4_prompt_prefill_reduced_depth():
+    """The 7B INT4 model's own prompt path at 4 of its 32 layers: the 4,096-token
+    prompt is prefilled through the decode kernel (teacher-forced, LM head on the
+    last token only), then decoded."""
+    w = S.WORKLOADS["7b_int4"].with_(n_layers=4)
+    n = 4
     weights = S.gen_weights(w)
-    e = engine_for(w, weights, max_ctx=w.prompt_len + STEPS)
-    o = O.OracleDecoder(w, weights, max_ctx=w.prompt_len + STEPS)
+    e = engine_for(w, weights, max_ctx=w.prompt_len + n)
+    o = O.OracleDecoder(w, weights, max_ctx=w.prompt_len + n)
     prompt = S.gen_prompt(w)
     lg = e.prefill(prompt)
     lo = o.prefill(prompt, q_block=512)
     assert np.abs(lg - lo).max() <= tol_for(w)
-    teacher_forced(e, o, O.argmax_lowest(lo), STEPS, tol_for(w))
+    teacher_forced(e, o, O.argmax_lowest(lo), n, tol_for(w))

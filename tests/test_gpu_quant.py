@@ -62,3 +62,20 @@ def test_fp8_rows_bit_exact(shape):
     rc, rs = O.fp8_quantize_rows(w)
     np.testing.assert_array_equal(sc.view(np.uint32), rs.view(np.uint32))
     np.testing.assert_array_equal(codes, rc)
+
+
+@pytest.mark.parametrize("shape", [(64, 2048), (37, 4096 + 16)])
+def test_nvfp4_quantiser_bit_exact(shape):
+    """NVFP4 codes, E4M3 block scales and fp32 row scales from the GPU
+    quantiser equal the oracle's, bit for bit (including an all-zero row, a
+    row with negative zeros and a row of tiny values)."""
+    rows, cols = shape
+    w = S.normal_f16(77, 5, shape)
+    w[3] = 0
+    w[5, ::3] = np.float16(-0.0)
+    w[7] = (w[7].astype(np.float32) * 1e-3).astype(np.float16)
+    codes, bs, rs = kie.quantize_nvfp4_rows(w)
+    rc, rb, rr = O.fp4_quantize_rows(w)
+    np.testing.assert_array_equal(rs.view(np.uint32), rr.view(np.uint32))
+    np.testing.assert_array_equal(bs, rb)
+    np.testing.assert_array_equal(codes, rc)

@@ -4,8 +4,10 @@ Some callers may not allocate device memory while decoding: code hosted inside
 another framework's allocator, plugins without allocation rights, services that
 forbid allocation after start-up.  This entry point runs the decode step with
 its scratch in a fixed array inside the library.  Here it must give the same
-tokens and logits as the ordinary kie_decode_step on two calls in a row, and the
-second call must leave the device's free memory unchanged.
+tokens and logits as the ordinary kie_decode_step on two calls in a row, and
+neither call may change the device's free memory or torch's reserved memory
+(the array's device memory is committed when the engine is created, not by the
+step).  A config whose scratch does not fit the array is refused.
 
 Kept in a file that pytest collects last, so a failure here stops a run only
 after every other test has run.
@@ -15,13 +17,18 @@ import pytest
 
 import synthetic as S
 from _common import TOL_FP16, engine_for
+from autoregressive_decode_gb300 import kie
 
 pytestmark = pytest.mark.gpu
 
+# d_model 4096 with a 32 x 128 attention and FFN 11008 (the 7B shape) at one
+# layer: the step's scratch is about 206 KiB of the array's 256 KiB
+NEAR_BOUND = S.Workload("near_bound", 4, 1, 4096, 32, 128, 11008, 4096, prompt_len=12, decode_steps=4)
 
-def test_static_scratch_step_matches_decode_step():
+
+@pytest.mark.parametrize("w", [S.WORKLOADS["tiny"], NEAR_BOUND], ids=lambda w: w.name)
+def test_static_scratch_step_matches_decode_step(w):
     torch = pytest.importorskip("torch")
-    w = S.WORKLOADS["tiny"]
     weights = S.gen_weights(w)
     prompt = S.gen_prompt(w)
     ref = engine_for(w, weights)
@@ -34,13 +41,13 @@ def test_static_scratch_step_matches_decode_step():
     t_ref = t_new = first
     for call in range(2):
         nxt_ref, lg_ref = ref.decode_step(t_ref)
-        if call == 1:
-            torch.cuda.synchronize()
-            free_before = torch.cuda.mem_get_info()[0]
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
+        reserved_before = torch.cuda.memory_reserved()
         eng.decode_step_static_scratch(t_new, d_tok, d_log)
         eng.sync()
-        if call == 1:
-            assert torch.cuda.mem_get_info()[0] == free_before
+        assert torch.cuda.mem_get_info()[0] == free_before, f"call {call} changed the device's free memory"
+        assert torch.cuda.memory_reserved() == reserved_before
         nxt_new = int(d_tok.cpu().item())
         lg_new = d_log.cpu().numpy()
         assert np.abs(lg_new - lg_ref).max() <= TOL_FP16
@@ -51,3 +58,22 @@ def test_static_scratch_step_matches_decode_step():
     nxt_a, lg_a = ref.decode_step(t_ref)
     nxt_b, lg_b = eng.decode_step(t_new)
     assert nxt_a == nxt_b and np.abs(lg_a - lg_b).max() <= TOL_FP16
+
+
+def test_static_scratch_rejects_oversized_config():
+    """d_model 4096, 32 x 128 heads, FFN 24576: the step's scratch (262,400
+    bytes: residual, q, current K/V, attention output, SwiGLU output, 152
+    attention partials, argmax partials, control block) exceeds the 256 KiB
+    array, so the call is refused without launching."""
+    torch = pytest.importorskip("torch")
+    w = S.Workload("wide_ffn", 0, 1, 4096, 32, 128, 24576, 4096, prompt_len=4, decode_steps=2)
+    weights = S.gen_weights(w)
+    eng = engine_for(w, weights)
+    d_tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(kie.KieError) as ei:
+        eng.decode_step_static_scratch(1, d_tok)
+    assert ei.value.status == -8          # KIE_ERR_UNSUPPORTED
+    assert eng.pos == 0
+    # the engine is not poisoned: the ordinary step still runs
+    nxt, lg = eng.decode_step(1)
+    assert 0 <= nxt < w.vocab and np.isfinite(lg).all()
