@@ -11,7 +11,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <numeric>
 #include <string>
@@ -789,10 +788,6 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     P.amax_idx = reinterpret_cast<int32_t*>(e->dev(L.amax_idx));
     P.ctl = reinterpret_cast<KieControl*>(e->dev(L.ctl));
     P.nslot = pl.nslot;
-    P.inflight = pl.nslot;
-    if (const char* v = std::getenv("KIE_INFLIGHT")) P.inflight = std::max(1, std::min(pl.nslot, std::atoi(v)));
-    P.poll_ns = 0;
-    if (const char* v = std::getenv("KIE_POLL_NS")) P.poll_ns = uint32_t(std::max(0, std::min(1000, std::atoi(v))));
     P.act_floats = pl.act_floats;
     P.part_floats = pl.part_floats;
     *out = e;

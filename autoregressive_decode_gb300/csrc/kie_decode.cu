@@ -205,7 +205,6 @@ struct TagWait {
     uint32_t spins;
     __device__ TagWait() : t0(globaltimer()), spins(0) {}
     __device__ __forceinline__ bool again(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
-        if (P.poll_ns) __nanosleep(P.poll_ns);
         if ((++spins & 15u) != 0u) return true;
         if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
         if (globaltimer() - t0 > Lc.timeout_ns) {
@@ -310,28 +309,6 @@ __device__ __forceinline__ bool producer_wait_slot(const KieParams& P, const Kie
     return true;
 }
 
-// Producer: wait until global slot g has landed (its copy completed), so that
-// at most P.inflight copies are outstanding.  Slot g's full barrier can be in
-// its phase for generation q (in flight) or the next (landed) only: generation
-// q + 2 is issued later than the slot being issued now.
-__device__ __forceinline__ bool producer_wait_landed(const KieParams& P, const KieLaunch& Lc, const Smem& S,
-                                                     uint32_t g, int cta) {
-    const uint32_t nslot = uint32_t(P.nslot);
-    const uint32_t slot = g % nslot, q = g / nslot;
-    uint64_t* fb = &S.full[2 * slot + (q & 1u)];
-    const uint32_t par = (q >> 1) & 1u;
-    if (mbar_test_wait(fb, par)) return true;
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(fb, par)) {
-        if (ld_volatile_i32(&S.flags[0]) != 0 || ld_volatile_i32(&P.ctl->err) != 0) return false;
-        if (globaltimer() - t0 > Lc.timeout_ns) {
-            set_error(P, KERR_TIMEOUT_FULL, cta);
-            return false;
-        }
-    }
-    return true;
-}
-
 // Consumer warp: wait until global slot gidx has landed.  Every lane probes the
 // barrier (each lane needs the acquire of the bulk-copy data) but the decision
 // to continue or abort is warp-uniform, so no lane can leave the slot loop while
@@ -361,9 +338,6 @@ __device__ __forceinline__ bool warp_wait_full(const KieParams& P, const KieLaun
 __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S, int cta) {
     const uint64_t pol = policy_evict_first();
     const uint32_t nslot = uint32_t(P.nslot);
-    // copies outstanding at most (the rest of the ring holds landed slots that
-    // absorb the consumers' waits instead of more queued copies)
-    const uint32_t inflight = uint32_t(min(max(P.inflight, 1), P.nslot));
     uint32_t g = 0, rs = 0, rq = 0;   // global slot index, its ring slot and generation
     bool abort = false;
     const uint64_t pol_kv = policy_evict_first();
@@ -399,7 +373,6 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 for (uint32_t j = 0; j < nsl && !abort; ++j, ++g) {
                     const uint32_t slot = rs;
                     if (g >= nslot && !producer_wait_slot(P, Lc, S, rs, (rq - 1u) & 1u, cta)) { abort = true; break; }
-                    if (g >= inflight && !producer_wait_landed(P, Lc, S, g - inflight, cta)) { abort = true; break; }
                     const int r0 = int(j) * rps;
                     const int rows = min(rps, a.jt - a.j0 - r0);
                     const size_t off = kv_elem_index(P, layer, a.h, a.j0 + r0) * size_t(rb / P.hd);
@@ -426,7 +399,6 @@ __device__ void producer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 const int rows_g = min(c.R, c.rows - gg * c.R);
                 for (int ch = 0; ch < c.nK; ++ch, ++j) {
                     if (g >= nslot && !producer_wait_slot(P, Lc, S, rs, (rq - 1u) & 1u, cta)) { abort = true; break; }
-                    if (g >= inflight && !producer_wait_landed(P, Lc, S, g - inflight, cta)) { abort = true; break; }
                     const int kc = min(c.KC, c.K - ch * c.KC);
                     const uint32_t bytes = slot_bytes(c.wfmt, rows_g, kc);
                     uint64_t* fb = &S.full[2 * rs + (rq & 1u)];

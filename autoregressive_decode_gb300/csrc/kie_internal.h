@@ -163,8 +163,6 @@ struct KieParams {
     KieControl* ctl;
     // shared-memory layout
     int32_t nslot;               // ring slots
-    int32_t inflight;            // bulk copies the producer keeps outstanding at most (<= nslot)
-    uint32_t poll_ns;            // pause between two polls of another CTA's tagged data (0: none)
     int32_t act_floats;          // activation buffer (floats)
     int32_t part_floats;         // GEMV partial buffer (floats)
 };
