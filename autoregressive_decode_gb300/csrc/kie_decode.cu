@@ -466,8 +466,13 @@ __device__ void act_scaled(const KieParams& P, const KieLaunch& Lc, const Smem& 
     const int d = P.d, half = P.act_floats / 2, ng = d >> 2;
     float ss = 0.f;
     for (int q0 = tid; q0 < ng; q0 += 4 * NCT) {
-        float4 v[4];
+        float4 v[4], gg[4];
         uint32_t bad = 0;
+        // the gains first: their loads do not depend on x, so their latency
+        // passes while x is polled instead of after it has arrived
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (q0 + u * NCT < ng) gg[u] = __ldg(reinterpret_cast<const float4*>(g + 4 * (q0 + u * NCT)));
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int q = q0 + u * NCT;
@@ -506,10 +511,9 @@ __device__ void act_scaled(const KieParams& P, const KieLaunch& Lc, const Smem& 
                     for (int e = 0; e < 4; ++e)
                         if (k4 + e >= 0 && k4 + e < ncap) S.xres[k4 + e] = vv[e];
                 }
-                const float4 gg = *reinterpret_cast<const float4*>(g + 4 * q);
                 // 4 consecutive elements share one plane of one 8-element piece
                 *reinterpret_cast<float4*>(S.act + act_idx(4 * q, half)) =
-                    make_float4(v[u].x * gg.x, v[u].y * gg.y, v[u].z * gg.z, v[u].w * gg.w);
+                    make_float4(v[u].x * gg[u].x, v[u].y * gg[u].y, v[u].z * gg[u].z, v[u].w * gg[u].w);
             }
         }
     }
@@ -543,7 +547,7 @@ __device__ __forceinline__ void rope_table(const KieParams& P, const Smem& S, in
 __device__ void act_copy(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* src, int n,
                          uint32_t par, int tid, int cta) {
     const int half = P.act_floats / 2, ng = n >> 2;
-    constexpr int U = 9;    // loads in flight per thread (9 x 224 covers most of an 8192-float vector)
+    constexpr int U = 9;   // loads in flight per thread (9 x 224 covers most of an 8192-float vector)
     for (int q0 = tid; q0 < ng; q0 += U * NCT) {
         float4 v[U];
         uint32_t bad = 0;
@@ -1085,18 +1089,22 @@ __device__ __forceinline__ void convert_row(const RawRow& r, const float* fz, fl
 // The current position's 16 dims [dim0, dim0+16) of K (kv=0) or V, from the
 // tagged copy written in this step's QKV epilogue, as a RawRow of the stored
 // format (fp16 pairs; E5M2 bytes).  The uint8 cache keeps the open segment in
-// fp16, so its current row is fp16 too.
-template <int KVF>
-__device__ __forceinline__ void cur_row(const KieParams& P, const KieLaunch& Lc, const Smem& S, int kv, int h,
-                                        int dim0, uint32_t ep16, int cta, RawRow& r) {
+// fp16, so its current row is fp16 too.  cur_row_issue starts the loads (K's
+// and V's together), cur_row_finish polls whatever has not arrived yet and
+// packs the row.
+__device__ __forceinline__ void cur_row_issue(const KieParams& P, int kv, int h, int dim0, uint4* w) {
     const uint32_t* src = (kv ? P.vcur : P.kcur) + h * P.hd + dim0;
-    uint4 w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = ld_relaxed_u4(src + 4 * i);
+}
+template <int KVF>
+__device__ __forceinline__ void cur_row_finish(const KieParams& P, const KieLaunch& Lc, const Smem& S, int kv, int h,
+                                               int dim0, uint32_t ep16, int cta, uint4* w, RawRow& r) {
+    const uint32_t* src = (kv ? P.vcur : P.kcur) + h * P.hd + dim0;
     uint32_t bad = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        w[i] = ld_relaxed_u4(src + 4 * i);
+    for (int i = 0; i < 4; ++i)
         if (!has_ep4(w[i], ep16)) bad |= 1u << i;
-    }
     if (bad) {
         TagWait tw;
         do {
@@ -1275,6 +1283,8 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
         }
         consumer_sync(NCT);
     }
+    const bool has_pos = (j1 == pos + 1);
+    const bool own_pos = has_pos && warp == 0 && rw == 0;
     float qv[16];
     {
         const float* qp = P.q + h * HD + dim0;
@@ -1310,14 +1320,16 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     // its open segment directly (mode 1: fp16 tail; mode 2: the segment
     // completes in this step and is quantised with its fresh scale / zp).
     const int dmode = (KVF == KV_U8) ? (u8_fresh ? 2 : 1) : 0;
-    const bool has_pos = (j1 == pos + 1);
     const int ndir = has_pos ? n - 1 : n;        // direct rows other than pos: [nt, ndir)
     RawRow kpos, vpos;
     kpos.a = kpos.b = vpos.a = vpos.b = make_uint4(0, 0, 0, 0);
     kpos.sc = vpos.sc = 0.f; kpos.zp = vpos.zp = 0; kpos.mode = vpos.mode = dmode;
-    if (has_pos && warp == 0 && rw == 0) {
-        cur_row<KVF>(P, Lc, S, 0, h, dim0, ep16, cta, kpos);
-        cur_row<KVF>(P, Lc, S, 1, h, dim0, ep16, cta, vpos);
+    if (own_pos) {   // K and V loads travel together: one round trip
+        uint4 wk[4], wv[4];
+        cur_row_issue(P, 0, h, dim0, wk);
+        cur_row_issue(P, 1, h, dim0, wv);
+        cur_row_finish<KVF>(P, Lc, S, 0, h, dim0, ep16, cta, wk, kpos);
+        cur_row_finish<KVF>(P, Lc, S, 1, h, dim0, ep16, cta, wv, vpos);
         kpos.mode = vpos.mode = dmode;
     }
 
