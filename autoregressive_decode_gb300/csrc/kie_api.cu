@@ -267,13 +267,13 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.seg_zp = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
     // tagged activations, reset before each launch sequence (reset_tags):
     // x .. vcur to zero, q .. att_part to one parity
-    L.x = take(size_t(d) * 4);
+    L.x = take(size_t(KIE_REPL) * d * 4);
     L.kcur = take(size_t(H) * hd * 4);
     L.vcur = take(size_t(H) * hd * 4);
     L.zero_bytes = L.vcur + size_t(H) * hd * 4 - L.x;
     L.q = take(size_t(H) * hd * 4);
-    L.a = take(size_t(F) * 4);
-    L.o = take(size_t(H) * hd * 4);
+    L.a = take(size_t(KIE_REPL) * F * 4);
+    L.o = take(size_t(KIE_REPL) * H * hd * 4);
     L.att_part = take(size_t(G) * (hd + 4) * 4);
     L.par_bytes = L.att_part + size_t(G) * (hd + 4) * 4 - L.q;
     L.amax_val = take(size_t(G) * 4);
@@ -611,7 +611,7 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
 // partials, control block) lives in the array below; weights and the KV cache
 // stay in the engine.
 
-#define KIE_STATIC_SCRATCH_BYTES (256u * 1024u)
+#define KIE_STATIC_SCRATCH_BYTES (320u * 1024u)
 
 // The array belongs to this file's device module.  With CUDA's lazy module
 // loading the module (and so the array's device memory) is loaded the first
@@ -632,13 +632,13 @@ StaticScratchLayout static_scratch_layout(const kie_config& c, int G) {
     auto take = [&](size_t bytes) { size_t at = align_up(o, 256); o = at + bytes; return at; };
     const size_t hq = size_t(c.n_heads) * c.head_dim * 4;
     // tagged activations, reset per step as in the engine's workspace
-    l.x = take(size_t(c.d_model) * 4);
+    l.x = take(size_t(KIE_REPL) * c.d_model * 4);
     l.kcur = take(hq);
     l.vcur = take(hq);
     l.zero_bytes = l.vcur + hq - l.x;
     l.q = take(hq);
-    l.a = take(size_t(c.ffn_dim) * 4);
-    l.o = take(hq);
+    l.a = take(size_t(KIE_REPL) * c.ffn_dim * 4);
+    l.o = take(size_t(KIE_REPL) * hq);
     l.att_part = take(size_t(G) * (c.head_dim + 4) * 4);
     l.par_bytes = l.att_part + size_t(G) * (c.head_dim + 4) * 4 - l.q;
     l.amax_val = take(size_t(G) * 4);

@@ -547,7 +547,7 @@ __device__ __forceinline__ void rope_table(const KieParams& P, const Smem& S, in
 __device__ void act_copy(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* src, int n,
                          uint32_t par, int tid, int cta) {
     const int half = P.act_floats / 2, ng = n >> 2;
-    constexpr int U = 9;   // loads in flight per thread (9 x 224 covers most of an 8192-float vector)
+    constexpr int U = 10;   // loads in flight per thread: 10 x 224 float4 cover an 8192-float vector in one poll round
     for (int q0 = tid; q0 < ng; q0 += U * NCT) {
         float4 v[U];
         uint32_t bad = 0;
@@ -825,7 +825,9 @@ __device__ __forceinline__ void residual_row(const KieParams& P, const KieLaunch
     const float xo = (e.have_xres && c.rows <= KIE_XRES) ? S.xres[r]
                      : e.erow ? __half2float(__ushort_as_half(e.erow[row]))
                               : wait_f32(P, Lc, S, P.x + row, e.par_in, cta);
-    st_relaxed_f32(P.x + row, tag_f32(xo + y, e.par_out));
+    const float xn = tag_f32(xo + y, e.par_out);
+#pragma unroll
+    for (int k = 0; k < KIE_REPL; ++k) st_relaxed_f32(P.x + k * P.d + row, xn);
 }
 
 // The epilogue of row group g (rows_g rows from row g * R), one unit or row a lane.
@@ -837,7 +839,11 @@ __device__ __forceinline__ void epi_group(const KieParams& P, const KieLaunch& L
             const int u = (r0 >> 1) + lane;
             const float ya = row_sum(S, c, 2 * u) * e.rinv, yb = row_sum(S, c, 2 * u + 1) * e.rinv;
             if (e.type == PH_QKV) qkv_unit(P, S, c, e, u, ya, yb);
-            else st_relaxed_f32(P.a + c.unit0 + u, tag_f32((ya / (1.f + expf(-ya))) * yb, tag_par(e.n)));
+            else {
+                const float av = tag_f32((ya / (1.f + expf(-ya))) * yb, tag_par(e.n));
+#pragma unroll
+                for (int k = 0; k < KIE_REPL; ++k) st_relaxed_f32(P.a + k * P.F + c.unit0 + u, av);
+            }
         }
     } else if (lane < rows_g) {
         residual_row(P, Lc, S, c, e, r0 + lane, row_sum(S, c, r0 + lane), cta);
@@ -1251,7 +1257,10 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
     constexpr int UR = 4;              // direct rows in flight per lane group
     constexpr int RB = HD * (KVF == KV_F16 ? 2 : 1);
     constexpr int RMAX = KIE_SLOT_BYTES / (2 * RB * RPI);   // rows of one row group in a slot
-    constexpr int RU = 4;              // ring rows in flight per row group
+#ifndef KIE_ATT_RU
+#define KIE_ATT_RU 4
+#endif
+    constexpr int RU = KIE_ATT_RU;     // ring rows in flight per row group
     const AttChunk a = att_chunk(P, cta, pos);
     const int h = a.h, j0 = a.j0, j1 = a.j1, jt = a.jt;
     const int n = j1 - j0, nt = jt - j0;
@@ -1591,7 +1600,9 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
             }
             M = Mb;
         }
-        st_relaxed_f32(P.o + h * HD + tid, tag_f32(Os / Ls, par));
+        const float ov = tag_f32(Os / Ls, par);
+#pragma unroll
+        for (int k = 0; k < KIE_REPL; ++k) st_relaxed_f32(P.o + k * P.H * HD + h * HD + tid, ov);
     }
     return true;
 }
@@ -1688,7 +1699,11 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 const uint16_t* erow = P.emb + size_t(tok) * P.d;   // the residual stream before layer 0
                 if (type == PH_O || type == PH_D) {
                     // o and a carry this layer's parity
-                    act_copy(P, Lc, S, type == PH_O ? P.o : P.a, type == PH_O ? P.H * P.hd : P.F, par, tid, cta);
+                    // every reader polls the copy its CTA index selects (copies spread the
+                    // all-CTA polling of one vector over more L2 lines)
+                    const int rep = cta % KIE_REPL;
+                    act_copy(P, Lc, S, type == PH_O ? P.o + rep * P.H * P.hd : P.a + rep * P.F,
+                             type == PH_O ? P.H * P.hd : P.F, par, tid, cta);
                 } else {
                     // x: parity 0 after a D epilogue (QKV, LM), 1 after an O epilogue (GU)
                     const bool from_emb = type == PH_QKV && layer == 0;
@@ -1703,7 +1718,7 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                         cap0 = S.plan[rt * 4 + 0];
                         ncap = S.plan[rt * 4 + 1] <= KIE_XRES ? S.plan[rt * 4 + 1] : 0;
                     }
-                    act_scaled(P, Lc, S, from_emb ? nullptr : P.x, from_emb ? erow : nullptr, g,
+                    act_scaled(P, Lc, S, from_emb ? nullptr : P.x + (cta % KIE_REPL) * P.d, from_emb ? erow : nullptr, g,
                                type == PH_GU ? 1u : 0u, tid, cta, cap0, ncap);
                 }
                 if (tid == 0) stamp(P, Lc, t, phi, 1, cta);

@@ -41,6 +41,9 @@
 #define KIE_SLOT_BYTES 16384     // slot capacity (KIE_R rows x KIE_KC_F16 fp16); 8 KB slots measured slower
 #endif
 #define KIE_MAX_SLOTS 16
+#ifndef KIE_REPL
+#define KIE_REPL 2               // copies of the activations x, a, o that CTAs exchange (readers poll copy cta % KIE_REPL)
+#endif
 #define KIE_SEG 128              // adaptive-range uint8 KV segment (tokens)
 #define KIE_XRES 64              // residual rows per CTA whose old x is kept in shared memory
 #define KIE_MAX_HEAD_DIM 128
@@ -151,12 +154,12 @@ struct KieParams {
     // position's K and V hold (storage bits << 16 | 16-bit epoch).  The host
     // resets x, kcur, vcur (to zero) and q, a, o, att_part (to one parity)
     // before every launch sequence.
-    float* x;                    // [d] residual stream
+    float* x;                    // [KIE_REPL][d] residual stream
     uint32_t* kcur;              // [H*hd] K of the current position, as stored, tagged
     uint32_t* vcur;              // [H*hd] V of the current position, as stored, tagged
     float* q;                    // [H*hd] rotated query
-    float* a;                    // [F] SwiGLU output
-    float* o;                    // [H*hd] attention output
+    float* a;                    // [KIE_REPL][F] SwiGLU output
+    float* o;                    // [KIE_REPL][H*hd] attention output
     float* att_part;             // [G][hd+4] per-CTA attention partial: m, l, -, -, o[hd]
     float* amax_val;             // [G]
     int32_t* amax_idx;           // [G]

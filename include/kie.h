@@ -219,10 +219,10 @@ kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint6
  * K/V, pos += 1) in persistent mode, enqueued on the engine's stream without
  * synchronising.  d_next_token: DEVICE int32 receiving the argmax; d_logits:
  * NULL or DEVICE fp32[vocab].  The step's scratch (activations, attention and
- * argmax partials, control block) is a fixed 256 KiB array inside the library
+ * argmax partials, control block) is a fixed 320 KiB array inside the library
  * that every GPU loading the library keeps until the process exits; configs
- * whose scratch would exceed it (roughly d_model + 4*n_heads*head_dim +
- * ffn_dim + grid*(head_dim+6) floats) return KIE_ERR_UNSUPPORTED.  The array
+ * whose scratch would exceed it (roughly 2*d_model + 5*n_heads*head_dim +
+ * 2*ffn_dim + grid*(head_dim+6) floats) return KIE_ERR_UNSUPPORTED.  The array
  * is part of the library's device code: kie_create looks up its device address
  * with the engine's device current, which (under CUDA's lazy module loading)
  * is when the array's device memory is committed, so this call itself commits
