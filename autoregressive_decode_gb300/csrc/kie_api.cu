@@ -29,6 +29,8 @@ extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const _
                                    int M_pad, int N_pad, int K, int m_valid, const float* col_scale,
                                    uint64_t timeout_ns, int* err, cudaStream_t st);
 extern "C" cudaError_t kie_pf_pack_e4m3(const uint8_t* codes, int n, int K, int row0, __half* dst, cudaStream_t st);
+extern "C" cudaError_t kie_pf_pack_fp4(const uint8_t* codes, const uint8_t* bscales, int n, int K, int row0, __half* dst,
+                                       cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_fp8(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales,
                                             cudaStream_t st);
 extern "C" cudaError_t kie_pf_pack(const __half* src, int n, int K, int row0, __half* dst, cudaStream_t st);
@@ -85,6 +87,7 @@ struct HostPhase {
 uint32_t slot_bytes_host(int wfmt, int rows_g, int kc) {
     if (wfmt == WF_F16) return uint32_t(rows_g) * uint32_t(kc) * 2u;
     if (wfmt == WF_F8) return (uint32_t(rows_g) * uint32_t(kc) + 15u) & ~15u;
+    if (wfmt == WF_F4) return (uint32_t(rows_g) * uint32_t(kc / 2 + kc / 16) + 15u) & ~15u;
     uint32_t b = uint32_t(rows_g) * uint32_t(kc / 2) + uint32_t(rows_g) * uint32_t(kc / 64);
     return (b + 15u) & ~15u;
 }
@@ -109,6 +112,9 @@ struct Layout {  // byte offsets into the workspace
 };
 
 int pad256(int n) { return (n + 255) / 256 * 256; }
+
+// Weight formats stored with one fp32 scale per output row (FP8 E4M3, NVFP4).
+bool scaled_fmt(int32_t wdtype) { return wdtype == KIE_W_FP8_E4M3 || wdtype == KIE_W_NVFP4; }
 
 // The tensor-core prefill covers fp16 FFN weights with an fp16 or E5M2 cache
 // (the uint8 cache changes stored values when a segment completes, and INT4
@@ -136,8 +142,16 @@ bool valid_cfg(const kie_config* c, std::string& why) {
     if (c->head_dim != 64 && c->head_dim != 128) { why = "head_dim must be 64 or 128"; return false; }
     if (c->d_model % 8 || c->ffn_dim % 8 || (c->n_heads * c->head_dim) % 8) { why = "dims must be multiples of 8"; return false; }
     if (c->kv_dtype < 0 || c->kv_dtype > 2) { why = "bad kv_dtype"; return false; }
-    if (c->ffn_wdtype < 0 || c->ffn_wdtype > 2) { why = "bad ffn_wdtype"; return false; }
-    if (c->attn_wdtype != KIE_W_FP16 && c->attn_wdtype != KIE_W_FP8_E4M3) { why = "bad attn_wdtype"; return false; }
+    if (c->ffn_wdtype < 0 || c->ffn_wdtype > 3) { why = "bad ffn_wdtype"; return false; }
+    if (c->attn_wdtype != KIE_W_FP16 && c->attn_wdtype != KIE_W_FP8_E4M3 && c->attn_wdtype != KIE_W_NVFP4) {
+        why = "bad attn_wdtype";
+        return false;
+    }
+    if ((c->ffn_wdtype == KIE_W_NVFP4 || c->attn_wdtype == KIE_W_NVFP4) &&
+        (c->d_model % 16 || c->ffn_dim % 16 || (c->n_heads * c->head_dim) % 16)) {
+        why = "NVFP4 weights need d_model, ffn_dim and n_heads*head_dim multiples of 16";
+        return false;
+    }
     if (c->ffn_wdtype == KIE_W_INT4_G128 && (c->d_model % 128 || c->ffn_dim % 128)) {
         why = "INT4 FFN needs d_model and ffn_dim multiples of 128";
         return false;
@@ -151,14 +165,16 @@ bool valid_cfg(const kie_config* c, std::string& why) {
 void build_plan(const kie_config& c, int G, Plan& pl) {
     pl.G = G;
     const int d = c.d_model, H = c.n_heads, hd = c.head_dim, F = c.ffn_dim, V = c.vocab;
-    const int ffn_fmt = c.ffn_wdtype == KIE_W_INT4_G128 ? WF_I4 : c.ffn_wdtype == KIE_W_FP8_E4M3 ? WF_F8 : WF_F16;
-    const int attn_fmt = c.attn_wdtype == KIE_W_FP8_E4M3 ? WF_F8 : WF_F16;
+    const int ffn_fmt = c.ffn_wdtype == KIE_W_INT4_G128 ? WF_I4 : c.ffn_wdtype == KIE_W_FP8_E4M3 ? WF_F8
+                        : c.ffn_wdtype == KIE_W_NVFP4 ? WF_F4 : WF_F16;
+    const int attn_fmt = c.attn_wdtype == KIE_W_FP8_E4M3 ? WF_F8 : c.attn_wdtype == KIE_W_NVFP4 ? WF_F4 : WF_F16;
     auto setp = [&](int t, int K, int rpu, int units, int wfmt) {
         HostPhase& p = pl.ph[t];
         p.K = K; p.rpu = rpu; p.n_units = units; p.wfmt = wfmt;
-        // a 16 KB slot: 4 rows x 2048 fp16, 8 rows x 2048 FP8, or 4 rows x 4096 INT4 (+ scales)
+        // a slot: 4 rows x 2048 fp16, 8 rows x 2048 FP8, or 4 rows x 4096 INT4 (+ scales), 16 KB;
+        // KIE_R4 rows x 2048 NVFP4 (+ block scales)
         p.KC = std::min(K, wfmt == WF_I4 ? KIE_KC_I4 : KIE_KC_F16);
-        p.R = wfmt == WF_F8 ? KIE_R8 : KIE_R;
+        p.R = wfmt == WF_F8 ? KIE_R8 : wfmt == WF_F4 ? KIE_R4 : KIE_R;
         p.nK = (K + p.KC - 1) / p.KC;
     };
     setp(PH_QKV, d, 2, 3 * H * (hd / 2), attn_fmt);
@@ -250,7 +266,7 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
     {
         const size_t rows[PH_NTYPES] = {size_t(3) * H * hd, size_t(d), size_t(2) * F, size_t(d), size_t(V)};
-        const bool f8 = c.attn_wdtype == KIE_W_FP8_E4M3 || c.ffn_wdtype == KIE_W_FP8_E4M3;
+        const bool f8 = scaled_fmt(c.attn_wdtype) || scaled_fmt(c.ffn_wdtype);
         size_t o8 = 0;
         for (int t : {PH_QKV, PH_O, PH_GU, PH_D}) { L.wsc_off[t] = o8; o8 += rows[t]; }
         L.wsc_layer = o8;
@@ -309,7 +325,7 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
         L.pf_q = take(size_t(L.pf_tc) * HD * 4);
         L.pf_att = take(size_t(L.pf_tc) * HD * 4);
         L.pf_err = take(16);
-        const bool f8 = c.attn_wdtype == KIE_W_FP8_E4M3 || c.ffn_wdtype == KIE_W_FP8_E4M3;
+        const bool f8 = scaled_fmt(c.attn_wdtype) || scaled_fmt(c.ffn_wdtype);
         L.pf_sc_layer = size_t(3) * HD + d + 2 * size_t(F) + d;
         L.pf_sc = take(f8 ? (L.pf_sc_layer * c.n_layers + size_t(V)) * 4 : 0);
     }
@@ -550,7 +566,7 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
     const uint64_t to = e->timeout_ns;
     // FP8 matrices: the GEMM output columns take their row scales
     const float* pfsc = reinterpret_cast<const float*>(e->dev(L.pf_sc));
-    const bool a8 = c.attn_wdtype == KIE_W_FP8_E4M3, f8 = c.ffn_wdtype == KIE_W_FP8_E4M3;
+    const bool a8 = scaled_fmt(c.attn_wdtype), f8 = scaled_fmt(c.ffn_wdtype);
     auto colsc = [&](bool on, size_t off) -> const float* { return on ? pfsc + off : nullptr; };
     KIE_CUDA(e, cudaMemsetAsync(err, 0, 4, st));
     KIE_CUDA(e, cudaMemcpyAsync(d_tok, tokens, size_t(n) * 4, cudaMemcpyHostToDevice, st));
@@ -763,7 +779,8 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
         const HostPhase& h = pl.ph[t];
         q.K = h.K; q.KC = h.KC; q.nK = h.nK; q.rows_per_unit = h.rpu; q.wfmt = h.wfmt; q.n_units = h.n_units;
         q.R = h.R;
-        q.wscale = h.wfmt == WF_F8 ? reinterpret_cast<const float*>(e->dev(L.wsc)) + L.wsc_off[t] : nullptr;
+        q.wscale = (h.wfmt == WF_F8 || h.wfmt == WF_F4) ? reinterpret_cast<const float*>(e->dev(L.wsc)) + L.wsc_off[t]
+                                                         : nullptr;
         q.wscale_layer = int64_t(L.wsc_layer);
         q.unit_begin = reinterpret_cast<const int32_t*>(e->dev(L.plan_i32)) + size_t(t) * (G + 1);
         q.bytes = reinterpret_cast<const uint32_t*>(e->dev(L.plan_u32)) + size_t(t) * 2 * G;
@@ -895,6 +912,12 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
                         if (p.wfmt == WF_F8) {   // source: the matrix's E4M3 codes [rows][K]
                             desc.push_back({off + uint64_t(r) * kc, uint64_t(srow) * K + uint64_t(ch) * p.KC,
                                             uint32_t(kc), 0});
+                        } else if (p.wfmt == WF_F4) {   // source: packed E2M1 codes [rows][K/2], then block scales [rows][K/16]
+                            desc.push_back({off + uint64_t(r) * (kc / 2),
+                                            uint64_t(srow) * (K / 2) + uint64_t(ch) * (p.KC / 2), uint32_t(kc / 2), 0});
+                            desc.push_back({off + uint64_t(rg) * (kc / 2) + uint64_t(r) * (kc / 16),
+                                            scales_off + uint64_t(srow) * (K / 16) + uint64_t(ch) * (p.KC / 16),
+                                            uint32_t(kc / 16), 0});
                         } else if (!int4) {
                             desc.push_back({off + uint64_t(r) * kc * 2, uint64_t(srow) * K * 2 + uint64_t(ch) * p.KC * 2,
                                             uint32_t(kc * 2), 0});
@@ -931,7 +954,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
         result = fail(e, KIE_ERR_CUDA, "prefill weight clear failed");
     const int HDm = H * hd;
     // FP8 staging: one matrix's codes and row scales; host copies of the scales
-    const bool any_f8 = c.attn_wdtype == KIE_W_FP8_E4M3 || c.ffn_wdtype == KIE_W_FP8_E4M3;
+    const bool any_f8 = scaled_fmt(c.attn_wdtype) || scaled_fmt(c.ffn_wdtype);
     const size_t max_rows = std::max({size_t(HDm), size_t(F), size_t(d), size_t(V)});
     uint8_t* f8codes = nullptr;
     float* f8sc = nullptr;
@@ -949,15 +972,25 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     auto put_matrix = [&](int t, int l, int m, auto row_of, const uint8_t* s, int n, int K, size_t pf_off, int pf_row0,
                           size_t pf_sc_off) -> bool {
         const HostPhase& p = pl.ph[t];
-        if (p.wfmt != WF_F8) {
+        if (p.wfmt != WF_F8 && p.wfmt != WF_F4) {
             if (L.pf && kie_pf_pack(reinterpret_cast<const __half*>(s), n, K, pf_row0, pfw + pf_off, st) != cudaSuccess)
                 return false;
             emit(t, l, m, row_of, false, 0, 0);
             return flush(s);
         }
-        if (kie_launch_quant_fp8(reinterpret_cast<const uint16_t*>(s), n, K, f8codes, f8sc, st) != cudaSuccess) return false;
-        if (L.pf && kie_pf_pack_e4m3(f8codes, n, K, pf_row0, pfw + pf_off, st) != cudaSuccess) return false;
-        emit(t, l, m, row_of, false, 0, 0);
+        if (p.wfmt == WF_F8) {
+            if (kie_launch_quant_fp8(reinterpret_cast<const uint16_t*>(s), n, K, f8codes, f8sc, st) != cudaSuccess) return false;
+            if (L.pf && kie_pf_pack_e4m3(f8codes, n, K, pf_row0, pfw + pf_off, st) != cudaSuccess) return false;
+            emit(t, l, m, row_of, false, 0, 0);
+        } else {   // NVFP4: packed codes [n][K/2], then block scales [n][K/16] at bs_off
+            const uint64_t bs_off = align_up(size_t(n) * K / 2, 256);
+            if (kie_launch_quant_fp4(reinterpret_cast<const uint16_t*>(s), n, K, f8codes, nullptr, f8codes + bs_off, f8sc,
+                                     st) != cudaSuccess)
+                return false;
+            if (L.pf && kie_pf_pack_fp4(f8codes, f8codes + bs_off, n, K, pf_row0, pfw + pf_off, st) != cudaSuccess)
+                return false;
+            emit(t, l, m, row_of, false, 0, bs_off);
+        }
         if (!flush(f8codes)) return false;
         if (cudaMemcpy(sc_host.data(), f8sc, size_t(n) * 4, cudaMemcpyDeviceToHost) != cudaSuccess) return false;
         // scales in the phase's row order (phase row = unit * rows_per_unit + half)
@@ -972,7 +1005,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     };
     auto put_scales = [&](int t, int l) -> bool {   // the phase's FP8 row scales, once all its matrices are in
         const HostPhase& p = pl.ph[t];
-        if (p.wfmt != WF_F8) return true;
+        if (p.wfmt != WF_F8 && p.wfmt != WF_F4) return true;
         const size_t at = t == PH_LM ? L.wsc_off[PH_LM] : L.wsc_layer * l + L.wsc_off[t];
         return cudaMemcpy(e->dev(L.wsc) + at * 4, wsc_phase.data(), size_t(p.n_units) * p.rpu * 4,
                           cudaMemcpyHostToDevice) == cudaSuccess;

@@ -119,6 +119,7 @@ __device__ __forceinline__ Cursor cursor(const KieParams& P, const Smem& S, int 
 __device__ __forceinline__ uint32_t slot_bytes(int wfmt, int rows_g, int kc) {
     if (wfmt == WF_F16) return uint32_t(rows_g) * uint32_t(kc) * 2u;
     if (wfmt == WF_F8) return (uint32_t(rows_g) * uint32_t(kc) + 15u) & ~15u;
+    if (wfmt == WF_F4) return (uint32_t(rows_g) * uint32_t(kc / 2 + kc / 16) + 15u) & ~15u;
     uint32_t b = uint32_t(rows_g) * uint32_t(kc / 2) + uint32_t(rows_g) * uint32_t(kc / 64);
     return (b + 15u) & ~15u;
 }
@@ -723,6 +724,48 @@ __device__ __forceinline__ void slot_f8_full(const uint8_t* slot, int k0, const 
     for (int r = 0; r < KIE_R8; ++r) acc[r] = a2[r].x + a2[r].y;
 }
 
+// NVFP4 slot: E2M1 codes [rows_g][kc/2] (element 2b in the low nibble of byte
+// b), then the E4M3 block scales [rows_g][kc/16]; the rows' fp32 scales are
+// applied in row_sum.  Each lane takes one 16-column block (two 8-element
+// pieces of the activation) per iteration: the block's 16 codes become exact
+// fp16 pairs, are multiplied by the activation in fp32 and summed, and the
+// sum is scaled by the block's E4M3 scale (exact in fp32).
+__device__ __forceinline__ void slot_f4(const uint8_t* slot, int rows_g, int kc, int k0, const float* act, int half,
+                                        int lane, float* acc) {
+    const int nb = kc >> 4;
+    const uint8_t* bsc = slot + size_t(rows_g) * (kc / 2);
+    const float* alo = act + (k0 >> 3) * 4;
+    const float* ahi = alo + half;
+#pragma unroll
+    for (int r = 0; r < KIE_R4; ++r) acc[r] = 0.f;
+    for (int b = lane; b < nb; b += 32) {
+        const int p = 2 * b;   // first of the block's two pieces
+        const float4 xl0 = *reinterpret_cast<const float4*>(alo + p * 4);
+        const float4 xh0 = *reinterpret_cast<const float4*>(ahi + p * 4);
+        const float4 xl1 = *reinterpret_cast<const float4*>(alo + p * 4 + 4);
+        const float4 xh1 = *reinterpret_cast<const float4*>(ahi + p * 4 + 4);
+#pragma unroll
+        for (int r = 0; r < KIE_R4; ++r) {
+            if (r < rows_g) {
+                const uint2 w = *reinterpret_cast<const uint2*>(slot + size_t(r) * (kc / 2) + size_t(b) * 8);
+                float f[4];
+                e4m3x4_to_f32(uint32_t(bsc[r * (kc >> 4) + b]), f);
+                // piece p: codes 0..7 = bytes 0..3 of w.x; piece p+1: bytes 0..3 of w.y
+                float2 s = make_float2(0.f, 0.f);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2(w.x & 0xFFu)), make_float2(xl0.x, xl0.y), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2((w.x >> 8) & 0xFFu)), make_float2(xl0.z, xl0.w), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2((w.x >> 16) & 0xFFu)), make_float2(xh0.x, xh0.y), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2(w.x >> 24)), make_float2(xh0.z, xh0.w), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2(w.y & 0xFFu)), make_float2(xl1.x, xl1.y), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2((w.y >> 8) & 0xFFu)), make_float2(xl1.z, xl1.w), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2((w.y >> 16) & 0xFFu)), make_float2(xh1.x, xh1.y), s);
+                s = ffma2(h2_to_f2(e2m1x2_to_h2(w.y >> 24)), make_float2(xh1.z, xh1.w), s);
+                acc[r] = fmaf(f[0], s.x + s.y, acc[r]);
+            }
+        }
+    }
+}
+
 // INT4 slot: codes [rows_g][kc/2] (element 2b in the low nibble of byte b, two's
 // complement), then fp16 scales [rows_g][kc/128].  Each lane takes 8-element
 // pieces; a piece lies inside one 128-column group.
@@ -765,7 +808,7 @@ __device__ __forceinline__ void slot_i4(const uint8_t* slot, int rows_g, int kc,
 __device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) {
     float y = 0.f;
     for (int ch = 0; ch < c.nK; ++ch) y += S.part[r * c.nK + ch];
-    return c.wfmt == WF_F8 ? y * S.wsc[r] : y;
+    return (c.wfmt == WF_F8 || c.wfmt == WF_F4) ? y * S.wsc[r] : y;
 }
 
 // store one element of the new K (kv=0) or V (kv=1) at position pos; returns
@@ -930,7 +973,17 @@ __device__ bool run_gemv(const KieParams& P, const KieLaunch& Lc, const Smem& S,
         int g, ch, rows_g, kc;
         slot_geom(c, j, g, ch, rows_g, kc);
         const uint8_t* sl = S.ring + size_t(slot) * KIE_SLOT_BYTES;
-        if (c.wfmt == WF_F8) {
+        if (c.wfmt == WF_F4) {
+            float acc[KIE_R4];
+            slot_f4(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
+#pragma unroll
+            for (int r = 0; r < KIE_R4; ++r) acc[r] = warp_sum(acc[r]);
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < KIE_R4; ++r)   // constant indices: acc stays in registers
+                    if (r < rows_g) S.part[(g * c.R + r) * c.nK + ch] = acc[r];
+            }
+        } else if (c.wfmt == WF_F8) {
             float acc[KIE_R8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (rows_g == KIE_R8 && kc == KIE_KC_F16) slot_f8_full(sl, ch * c.KC, S.act, half, lane, acc);
             else slot_f8(sl, rows_g, kc, ch * c.KC, S.act, half, lane, acc);
@@ -1693,7 +1746,7 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                 // keeps the per-layer instruction working set small.
                 const int type = sub == 0 ? PH_QKV : sub == 2 ? PH_O : sub == 3 ? PH_GU : sub == 4 ? PH_D : PH_LM;
                 const Cursor c = cursor(P, S, type);
-                if (c.wfmt == WF_F8) {   // this CTA's row scales, visible after the staging's barrier
+                if (c.wfmt == WF_F8 || c.wfmt == WF_F4) {   // this CTA's row scales, visible after the staging's barrier
                     const KiePhasePlan& pp = P.ph[type];
                     const float* ws = pp.wscale + (type == PH_LM ? 0 : int64_t(layer) * pp.wscale_layer) +
                                       int64_t(c.unit0) * c.rpu;

@@ -238,6 +238,14 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
     f[0] = x.x; f[1] = x.y; f[2] = y.x; f[3] = y.y;
 }
 
+// Two E2M1 codes (one byte: element 2k in the low nibble) -> their exact fp16
+// values as an fp16 pair (low half = the low nibble's value).
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
+    return r;
+}
+
 // fp16 -> FP8 E5M2 (round to nearest even, saturate to +-57344, NaN stays NaN):
 // the hardware conversion of two fp16 values; returns two bytes (lo = a, hi = b).
 __device__ __forceinline__ uint16_t f16x2_to_e5m2x2(__half a, __half b) {

@@ -172,6 +172,29 @@ __global__ void kie_pf_pack_e4m3_kernel(const uint8_t* __restrict__ src, int n, 
     }
 }
 
+// The same for NVFP4: packed E2M1 codes [n x K/2] (element 2j in the low
+// nibble of byte j) and E4M3 block scales [n x K/16], written as the exact
+// fp16 values code * block scale (at most 6 significant bits, magnitude in
+// [2^-10, 2688]); the fp32 row scale is applied to the GEMM's output column.
+__global__ void kie_pf_pack_fp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ bscales, int n,
+                                       int K, int row0, __half* __restrict__ dst) {
+    const int KB = K / 64, g8 = K / 8;
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < size_t(n) * g8; i += size_t(gridDim.x) * blockDim.x) {
+        const int r = int(i / g8), k = int(i % g8) * 8;
+        const uint32_t c = *reinterpret_cast<const uint32_t*>(codes + size_t(r) * (K / 2) + k / 2);
+        float bs[4];
+        e4m3x4_to_f32(uint32_t(bscales[size_t(r) * (K / 16) + k / 16]), bs);
+        __align__(16) __half h[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 v = h2_to_f2(e2m1x2_to_h2((c >> (8 * j)) & 0xFFu));
+            h[2 * j] = __float2half_rn(v.x * bs[0]);       // exact (see above)
+            h[2 * j + 1] = __float2half_rn(v.y * bs[0]);
+        }
+        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) = *reinterpret_cast<const uint4*>(h);
+    }
+}
+
 __device__ __forceinline__ void put_split(__half* hi, __half* lo, size_t idx, float v) {
     const __half h = __float2half_rn(v);
     hi[idx] = h;
@@ -410,6 +433,14 @@ extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const _
     if (r != cudaSuccess) return r;
     kie_pf_gemm_kernel<<<dim3(N_pad / BN, M_pad / BM), 128, GEMM_SMEM, st>>>(Ahi, Alo, W, C, ldc, K / BK, m_valid,
                                                                             col_scale, timeout_ns, err);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_pf_pack_fp4(const uint8_t* codes, const uint8_t* bscales, int n, int K, int row0, __half* dst,
+                                       cudaStream_t st) {
+    const size_t work = size_t(n) * (K / 8);
+    const unsigned blocks = unsigned(std::min<size_t>((work + 255) / 256, 65535));
+    kie_pf_pack_fp4_kernel<<<blocks, 256, 0, st>>>(codes, bscales, n, K, row0, dst);
     return cudaGetLastError();
 }
 

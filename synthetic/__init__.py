@@ -147,6 +147,9 @@ WORKLOADS = {
     # the 1.8B fp16 model (same seeds, index 1) with every GEMV matrix in FP8 E4M3
     "1p8b_fp8": Workload("1p8b_fp8", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="fp8_e4m3",
                          attn_wdtype="fp8_e4m3", prompt_len=2048, decode_steps=256),
+    # ... and in NVFP4 (E2M1 codes, E4M3 scale per 16 columns, fp32 scale per row)
+    "1p8b_nvfp4": Workload("1p8b_nvfp4", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="nvfp4",
+                           attn_wdtype="nvfp4", prompt_len=2048, decode_steps=256),
 }
 
 # tensor ids for the generator: per layer base 64*(layer+1) + slot

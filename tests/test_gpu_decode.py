@@ -126,6 +126,41 @@ def test_fp8_weights_prefill_and_decode(w):
     teacher_forced(e, o, O.argmax_lowest(lo), 8, tol)
 
 
+@pytest.mark.parametrize("w", [TINY, MEDIUM, WIDE], ids=lambda w: w.name)
+def test_nvfp4_weights_prefill_and_decode(w):
+    """Every GEMV matrix in NVFP4 (E2M1 codes, an E4M3 scale per 16 columns, an
+    fp32 scale per row): decode with 14-row slots and the block scale applied
+    per 16-column block, prefill with the exact fp16 values code * block scale
+    in the MMA and the row scale on the output column; logits match the
+    oracle's model with the same quantised weights."""
+    w = w.with_(ffn_wdtype="nvfp4", attn_wdtype="nvfp4")
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    tol = tol_for(w)
+    assert np.abs(lg - lo).max() <= tol
+    teacher_forced(e, o, O.argmax_lowest(lo), 8, tol)
+
+
+def test_nvfp4_ffn_graph_equals_persistent_and_u8_cache():
+    """NVFP4 FFN weights with fp16 attention weights, in both launch modes
+    (bit-identical), with the uint8 cache (prefill through the decode kernel)."""
+    w = WIDE.with_(ffn_wdtype="nvfp4", kv_dtype="u8")
+    weights = S.gen_weights(w)
+    prompt = S.gen_prompt(w)
+    res = {}
+    for mode in ("persistent", "graph"):
+        e = engine_for(w, weights, mode)
+        lg = e.prefill(prompt)
+        toks, logs = e.generate_greedy(int(np.argmax(lg)), 6, want_logits=True)
+        res[mode] = (lg, toks, logs)
+    for a, b in zip(res["persistent"], res["graph"]):
+        np.testing.assert_array_equal(a, b)
+    o = O.OracleDecoder(w, weights)
+    lo = o.prefill(prompt)
+    assert np.abs(res["persistent"][0] - lo).max() <= tol_for(w)
+    check_free_running(o, int(np.argmax(res["persistent"][0])), res["persistent"][1], res["persistent"][2], tol_for(w))
+
+
 def test_fp8_weights_graph_equals_persistent_and_u8_cache():
     """FP8 weights in both launch modes (bit-identical), and with the uint8
     cache (prefill through the decode kernel)."""
