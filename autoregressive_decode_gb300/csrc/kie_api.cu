@@ -116,11 +116,12 @@ int pad256(int n) { return (n + 255) / 256 * 256; }
 // Weight formats stored with one fp32 scale per output row (FP8 E4M3, NVFP4).
 bool scaled_fmt(int32_t wdtype) { return wdtype == KIE_W_FP8_E4M3 || wdtype == KIE_W_NVFP4; }
 
-// The tensor-core prefill covers fp16 FFN weights with an fp16 or E5M2 cache
+// The tensor-core prefill covers non-INT4 weights with an fp16 or E5M2 cache
 // (the uint8 cache changes stored values when a segment completes, and INT4
 // weights have no fp16 copy); every GEMM K must be a multiple of 64.
 bool prefill_tc_ok(const kie_config& c) {
-    return c.ffn_wdtype != KIE_W_INT4_G128 && c.kv_dtype != KIE_KV_U8_ADAPTIVE && c.d_model % 64 == 0 &&
+    return c.ffn_wdtype != KIE_W_INT4_G128 && c.attn_wdtype != KIE_W_INT4_G128 && c.kv_dtype != KIE_KV_U8_ADAPTIVE &&
+           c.d_model % 64 == 0 &&
            (c.n_heads * c.head_dim) % 64 == 0 && c.ffn_dim % 64 == 0;
 }
 
@@ -143,8 +144,9 @@ bool valid_cfg(const kie_config* c, std::string& why) {
     if (c->d_model % 8 || c->ffn_dim % 8 || (c->n_heads * c->head_dim) % 8) { why = "dims must be multiples of 8"; return false; }
     if (c->kv_dtype < 0 || c->kv_dtype > 2) { why = "bad kv_dtype"; return false; }
     if (c->ffn_wdtype < 0 || c->ffn_wdtype > 3) { why = "bad ffn_wdtype"; return false; }
-    if (c->attn_wdtype != KIE_W_FP16 && c->attn_wdtype != KIE_W_FP8_E4M3 && c->attn_wdtype != KIE_W_NVFP4) {
-        why = "bad attn_wdtype";
+    if (c->attn_wdtype < 0 || c->attn_wdtype > 3) { why = "bad attn_wdtype"; return false; }
+    if (c->attn_wdtype == KIE_W_INT4_G128 && c->d_model % 128) {
+        why = "INT4 q/k/v weights need d_model a multiple of 128";
         return false;
     }
     if ((c->ffn_wdtype == KIE_W_NVFP4 || c->attn_wdtype == KIE_W_NVFP4) &&
@@ -168,6 +170,7 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
     const int ffn_fmt = c.ffn_wdtype == KIE_W_INT4_G128 ? WF_I4 : c.ffn_wdtype == KIE_W_FP8_E4M3 ? WF_F8
                         : c.ffn_wdtype == KIE_W_NVFP4 ? WF_F4 : WF_F16;
     const int attn_fmt = c.attn_wdtype == KIE_W_FP8_E4M3 ? WF_F8 : c.attn_wdtype == KIE_W_NVFP4 ? WF_F4 : WF_F16;
+    const int qkv_fmt = c.attn_wdtype == KIE_W_INT4_G128 ? WF_I4 : attn_fmt;   // INT4 reaches q, k, v only
     auto setp = [&](int t, int K, int rpu, int units, int wfmt) {
         HostPhase& p = pl.ph[t];
         p.K = K; p.rpu = rpu; p.n_units = units; p.wfmt = wfmt;
@@ -177,7 +180,7 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
         p.R = wfmt == WF_F8 ? KIE_R8 : wfmt == WF_F4 ? KIE_R4 : KIE_R;
         p.nK = (K + p.KC - 1) / p.KC;
     };
-    setp(PH_QKV, d, 2, 3 * H * (hd / 2), attn_fmt);
+    setp(PH_QKV, d, 2, 3 * H * (hd / 2), qkv_fmt);
     setp(PH_O, H * hd, 1, d, attn_fmt);
     setp(PH_GU, d, 2, F, ffn_fmt);
     setp(PH_D, F, 1, d, ffn_fmt);
@@ -857,7 +860,10 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
 
     // staging buffer on the device for one source matrix (plus INT4 codes/scales)
     const size_t max_mat = std::max({size_t(H) * hd * d, size_t(F) * d, size_t(V) * d}) * 2;
-    size_t i4_bytes = c.ffn_wdtype == KIE_W_INT4_G128 ? size_t(F) * d / 2 + size_t(F) * d / 128 * 2 + 256 : 0;
+    size_t i4_elems = 0;   // the largest INT4 matrix: F x d (FFN) or H*h x d (q, k, v)
+    if (c.ffn_wdtype == KIE_W_INT4_G128) i4_elems = size_t(F) * d;
+    if (c.attn_wdtype == KIE_W_INT4_G128) i4_elems = std::max(i4_elems, size_t(H) * hd * d);
+    const size_t i4_bytes = i4_elems ? i4_elems / 2 + i4_elems / 128 * 2 + 256 : 0;
     uint8_t* stage = nullptr;
     uint8_t* i4 = nullptr;
     CopyDesc* ddesc = nullptr;
@@ -972,6 +978,14 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     auto put_matrix = [&](int t, int l, int m, auto row_of, const uint8_t* s, int n, int K, size_t pf_off, int pf_row0,
                           size_t pf_sc_off) -> bool {
         const HostPhase& p = pl.ph[t];
+        if (p.wfmt == WF_I4) {   // INT4 g128: codes [n][K/2], then fp16 group scales [n][K/128] at sc_off
+            const uint64_t sc_off = align_up(size_t(n) * K / 2, 256);
+            if (kie_launch_quant_int4(reinterpret_cast<const uint16_t*>(s), n, K, i4, nullptr,
+                                      reinterpret_cast<uint16_t*>(i4 + sc_off), st) != cudaSuccess)
+                return false;
+            emit(t, l, m, row_of, true, 0, sc_off);
+            return flush(i4);
+        }
         if (p.wfmt != WF_F8 && p.wfmt != WF_F4) {
             if (L.pf && kie_pf_pack(reinterpret_cast<const __half*>(s), n, K, pf_row0, pfw + pf_off, st) != cudaSuccess)
                 return false;
@@ -1030,24 +1044,13 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
             if (!put_matrix(PH_O, l, 0, plain_row, s, d, HDm, lb + L.pf_o, 0, sb + size_t(3) * HDm) ||
                 !put_scales(PH_O, l)) { result = fail(e, KIE_ERR_CUDA, "repack failed"); break; }
         }
-        const bool q4 = c.ffn_wdtype == KIE_W_INT4_G128;
         const uint16_t* gu[2] = {lw.w_gate, lw.w_up};
         wsc_phase.assign(size_t(2) * F, 0.f);
         for (int m = 0; m < 2 && result == KIE_OK; ++m) {
             const uint8_t* s = src_of(gu[m], size_t(F) * d * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
-            if (q4) {
-                const uint64_t sc_off = align_up(size_t(F) * d / 2, 256);
-                if (kie_launch_quant_int4(reinterpret_cast<const uint16_t*>(s), F, d, i4, nullptr,
-                                          reinterpret_cast<uint16_t*>(i4 + sc_off), st) != cudaSuccess) {
-                    result = fail(e, KIE_ERR_CUDA, "INT4 quantisation failed");
-                    break;
-                }
-                emit(PH_GU, l, m, gu_row, true, 0, sc_off);
-                if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
-            } else if (!put_matrix(PH_GU, l, m, gu_row, s, F, d, lb + L.pf_gu, m * F, sb + size_t(3) * HDm + d)) {
+            if (!put_matrix(PH_GU, l, m, gu_row, s, F, d, lb + L.pf_gu, m * F, sb + size_t(3) * HDm + d))
                 result = fail(e, KIE_ERR_CUDA, "repack failed");
-            }
         }
         if (result == KIE_OK && !put_scales(PH_GU, l)) result = fail(e, KIE_ERR_CUDA, "scale upload failed");
         if (result != KIE_OK) break;
@@ -1055,17 +1058,8 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
             wsc_phase.assign(size_t(d), 0.f);
             const uint8_t* s = src_of(lw.w_down, size_t(d) * F * 2);
             if (!s) { result = fail(e, KIE_ERR_CUDA, "weight upload failed"); break; }
-            if (q4) {
-                const uint64_t sc_off = align_up(size_t(F) * d / 2, 256);
-                if (kie_launch_quant_int4(reinterpret_cast<const uint16_t*>(s), d, F, i4, nullptr,
-                                          reinterpret_cast<uint16_t*>(i4 + sc_off), st) != cudaSuccess) {
-                    result = fail(e, KIE_ERR_CUDA, "INT4 quantisation failed");
-                    break;
-                }
-                emit(PH_D, l, 0, plain_row, true, 0, sc_off);
-                if (!flush(i4)) result = fail(e, KIE_ERR_CUDA, "repack failed");
-            } else if (!put_matrix(PH_D, l, 0, plain_row, s, d, F, lb + L.pf_d, 0, sb + size_t(3) * HDm + d + 2 * size_t(F)) ||
-                       !put_scales(PH_D, l)) {
+            if (!put_matrix(PH_D, l, 0, plain_row, s, d, F, lb + L.pf_d, 0, sb + size_t(3) * HDm + d + 2 * size_t(F)) ||
+                !put_scales(PH_D, l)) {
                 result = fail(e, KIE_ERR_CUDA, "repack failed");
             }
         }

@@ -44,6 +44,10 @@
 #ifndef KIE_REPL
 #define KIE_REPL 2               // copies of the activations x, a, o that CTAs exchange (readers poll copy cta % KIE_REPL)
 #endif
+#define KIE_MAX_BATCH 8          // requests of a batched engine (one tensor-core fragment holds 8 requests' hi and lo)
+#define KIE_RB 16                // batched kernel: rows per slot (two 8-row MMA column groups)
+#define KIE_KCB 512              // batched kernel: input columns per slot (16 rows x 512 fp16 = 16 KB)
+#define KIE_KBLK 2048            // batched kernel: input columns staged at once (4 slots of a row tile)
 #define KIE_SEG 128              // adaptive-range uint8 KV segment (tokens)
 #define KIE_XRES 64              // residual rows per CTA whose old x is kept in shared memory
 #define KIE_MAX_HEAD_DIM 128
@@ -64,18 +68,21 @@ struct KieSmemLayout {
     uint32_t full, empty, cbase, flags, plan, clist, rope, red, xres, wsc, cnt, part, act, ring, total;
 };
 KIE_HD inline uint32_t kie_align(uint32_t x, uint32_t a) { return (x + a - 1u) / a * a; }
-KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot) {
+// nb > 0 (the batched kernel): per-request cos/sin tables, norm partials,
+// argmax partials and kept x rows for nb requests.
+KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int nslot, int nb = 0) {
     KieSmemLayout l;
     uint32_t o = 0;
+    const uint32_t req = nb > 0 ? uint32_t(nb) : 1u;
     l.full = o;  o += KIE_MAX_SLOTS * 2 * 8;   // two per slot: even / odd generations
     l.empty = o; o += KIE_MAX_SLOTS * 8;
     l.cbase = o; o += 16;
     l.flags = o; o += 64;
     l.plan = o;  o += 5 * 4 * 4;
     l.clist = o; o += KIE_MAX_GRID * 4;
-    l.rope = o;  o += KIE_MAX_HEAD_DIM * 4;     // cos/sin of the step's position, [2][hd/2]
-    l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64) * 4;
-    l.xres = o;  o += KIE_XRES * 4;
+    l.rope = o;  o += req * KIE_MAX_HEAD_DIM * 4;     // cos/sin of the step's position, [req][2][hd/2]
+    l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64 + (nb > 0 ? 3 * KIE_MAX_BATCH * KIE_NW : 0)) * 4;
+    l.xres = o;  o += req * KIE_XRES * 4;
     l.wsc = o;   o += uint32_t(part_floats) * 4;   // FP8 row scales of the phase (part_floats >= rows)
     l.cnt = o;   o += (uint32_t(part_floats) / KIE_R + 4) * 4;   // per row group: chunks done (>= groups)
     l.part = o;  o += uint32_t(part_floats) * 4;
@@ -111,7 +118,8 @@ struct KiePhasePlan {
     int32_t nK;              // chunks per row = ceil(K / KC)
     int32_t rows_per_unit;   // 1 or 2
     int32_t wfmt;            // KieWFmt
-    int32_t R;               // rows per slot: KIE_R, KIE_R8 for FP8, KIE_R4 for NVFP4
+    int32_t R;               // rows per slot: KIE_R, KIE_R8 for FP8, KIE_R4 for NVFP4, KIE_RB batched
+    int32_t cpb;             // chunks per staging block (batched: KIE_KBLK / KIE_KCB; single: nK)
     int32_t n_units;         // units over the grid
     const float* wscale;     // FP8 / NVFP4: fp32 row scales of layer 0 in the phase's row order (null otherwise)
     int64_t wscale_layer;    // FP8 / NVFP4: floats between consecutive layers' scales
@@ -166,6 +174,15 @@ struct KieParams {
     float* amax_val;             // [G]
     int32_t* amax_idx;           // [G]
     KieControl* ctl;
+    // batched kernel (kie_decode_batch.cu); the single-request kernel has nb == 0.
+    // Activations gain a request index after their copy index: x [KIE_REPL][nb][d],
+    // kcur, vcur, q [nb][H*hd], a [KIE_REPL][nb][F], o [KIE_REPL][nb][H*hd],
+    // amax_val/idx [nb][G]; the KV cache of request b starts kv_req elements
+    // after request b-1's.
+    int32_t nb;
+    int64_t kv_req;
+    int32_t* req_tok;            // [nb] input token of each request's next step
+    int32_t* req_pos;            // [nb] its position
     // shared-memory layout
     int32_t nslot;               // ring slots
     int32_t act_floats;          // activation buffer (floats)
@@ -180,8 +197,8 @@ struct KieLaunch {
     int32_t pos0;                // >= 0: position of step 0; < 0: read ctl->pos
     const int32_t* forced;       // device [n_steps] input tokens (prefill), or null
     int32_t lm_from_step;        // LM head only for steps >= this
-    int32_t* out_tokens;         // device [n_steps] or null
-    float* out_logits;           // device [n_steps - lm_from_step][V] or null
+    int32_t* out_tokens;         // device [n_steps] (batched: [n_steps][nb]) or null
+    float* out_logits;           // device [n_steps - lm_from_step][V] (batched: [..][nb][V]) or null
     uint64_t timeout_ns;
     int32_t use_grid_barrier;    // 1 in the persistent (cooperative) launch
     int32_t skip_arrival_cta;    // failure injection: this CTA skips its arrival at the first grid barrier (-1: none)

@@ -9,8 +9,8 @@ model shape and storage formats, for the bench's GB/s and roofline fraction.
 Storage formats counted:
   * fp16 matrices: 2 bytes per weight;
   * FP8 E4M3 matrices: 1 byte per weight plus one fp32 scale per output row;
-  * INT4 g128 FFN matrices: half a byte per weight plus one fp16 scale per
-    128-column group of a row;
+  * INT4 g128 matrices (the FFN, or the q/k/v projections): half a byte per
+    weight plus one fp16 scale per 128-column group of a row;
   * NVFP4 matrices: half a byte per weight, one E4M3 scale byte per 16-column
     block of a row and one fp32 scale per row;
   * KV cache: fp16 (2 bytes), FP8 E5M2 (1 byte), or uint8 codes for completed
@@ -58,10 +58,12 @@ def step_bytes(w, ctx: int) -> dict:
     optionally attn_wdtype) attending `ctx` positions including its own."""
     d, qkv = w.d_model, w.n_heads * w.head_dim
     attn_fmt = getattr(w, "attn_wdtype", "fp16")
-    layer = (_matrix(3 * qkv, d, attn_fmt) + _matrix(d, qkv, attn_fmt)
+    # INT4 attention weights cover q, k and v; O and the LM head stay fp16
+    o_fmt = "fp16" if attn_fmt == "int4_g128" else attn_fmt
+    layer = (_matrix(3 * qkv, d, attn_fmt) + _matrix(d, qkv, o_fmt)
              + 2 * _matrix(w.ffn_dim, d, w.ffn_wdtype) + _matrix(d, w.ffn_dim, w.ffn_wdtype)
              + 2 * d * 2)
-    weights = w.n_layers * layer + _matrix(w.vocab, d, attn_fmt) + d * 2 + d * 2
+    weights = w.n_layers * layer + _matrix(w.vocab, d, o_fmt) + d * 2 + d * 2
     kv = w.n_layers * _kv_layer(ctx, w.n_heads, w.head_dim, w.kv_dtype)
     return {"weights": weights, "kv": kv, "total": weights + kv}
 

@@ -19,8 +19,9 @@ cpu_baseline  the CPU oracle (numpy fp32) timed on this host's cores on a short
 Multi-GPU (torchrun): independent replicas, one engine per rank, no
 collective on the data path; value = tokens of all ranks / max rank time.
 
-workloads  (1 GPU, default run) a compact record for each of the other four
-        workloads -- 1.8B with FP8 E4M3 weights, 1.8B with NVFP4 weights, 1.8B over a 32K FP8-E5M2 cache,
+workloads  (1 GPU, default run) a compact record for each of the other
+        workloads -- 1.8B with FP8 E4M3 weights, 1.8B with NVFP4 weights, 1.8B with
+        INT4 q/k/v and FFN weights over an E5M2 cache, 1.8B over a 32K FP8-E5M2 cache,
         1.8B over an 8K adaptive uint8 cache, 7B with INT4 FFN -- with its
         decode tokens/s, roofline fraction and a CPU-oracle figure.
 
@@ -61,7 +62,7 @@ def parse():
                     help="decode tokens per step (default: the workload's decode steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
-                    help="skip the compact records of the other four workloads (1 GPU runs only)")
+                    help="skip the compact records of the other workloads (1 GPU runs only)")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: the workload with this many layers (a small case of the same "
                          "kernels for multi-pass ncu captures); the line's config records the depth")
@@ -73,7 +74,8 @@ def workload_desc(w: S.Workload) -> str:
     names = {"int4_g128": "INT4 g128", "fp8_e4m3": "FP8 E4M3 (row scales)", "fp16": "fp16",
              "nvfp4": "NVFP4 (E2M1, E4M3 scale per 16 columns, fp32 row scales)"}
     ffn = f"{names[w.ffn_wdtype]} FFN"
-    attn = "" if w.attn_wdtype == "fp16" else f", {names[w.attn_wdtype]} q/k/v/o and LM head"
+    attn = ("" if w.attn_wdtype == "fp16" else ", INT4 g128 q/k/v (fp16 O and LM head)" if w.attn_wdtype == "int4_g128"
+            else f", {names[w.attn_wdtype]} q/k/v/o and LM head")
     return (f"{w.name}: {w.n_layers} layers, d {w.d_model}, {w.n_heads}x{w.head_dim} heads, FFN {w.ffn_dim}, "
             f"vocab {w.vocab}, {ctx}, {w.decode_steps} greedy decode steps, {w.kv_dtype} KV, {ffn}{attn}")
 
@@ -306,11 +308,11 @@ def time_decode(eng, torch, stream, first: int, p0: int, n_dec: int, steps: int,
     return statistics.mean(a.elapsed_time(b) for a, b in per)
 
 
-# The other four workloads (a compact record each): their decode steps over the
+# The other workloads (a compact record each): their decode steps over the
 # context the workload names, prefilled on the GPU where the tensor-core path
 # covers it and otherwise (uint8 cache; the 7B model, whose decode bytes do not
 # depend on how its 4,096-position context was made) a synthetic one.
-EXTRA = ("1p8b_fp8", "1p8b_nvfp4", "1p8b_32k", "1p8b_u8", "7b_int4")
+EXTRA = ("1p8b_fp8", "1p8b_nvfp4", "1p8b_hpi", "1p8b_32k", "1p8b_u8", "7b_int4")
 
 
 def extra_workloads(args, local, kie, torch, weights_1p8b):

@@ -63,8 +63,11 @@ typedef enum {
 } kie_status;
 
 typedef enum { KIE_KV_FP16 = 0, KIE_KV_FP8_E5M2 = 1, KIE_KV_U8_ADAPTIVE = 2 } kie_kv_dtype;
-/* Weight storage of the GEMV matrices.  FP16: as given.  INT4_G128 (FFN only):
- * symmetric INT4, group 128 (xAI page sections 2.3, 3.3).  FP8_E4M3: one byte
+/* Weight storage of the GEMV matrices.  FP16: as given.  INT4_G128: symmetric
+ * INT4, group 128 (xAI page sections 2.3, 3.3); as ffn_wdtype it covers the
+ * three FFN matrices, as attn_wdtype the q, k and v projections only (the same
+ * page's section 2.3 names the QKV projection), with wo and the LM head kept
+ * in fp16.  FP8_E4M3: one byte
  * per weight with one fp32 scale per output row, s = absmax/448, codes = E4M3
  * of w/s rounded to nearest even, saturating (the Kog page's "FP8 ~2 FLOP per
  * byte", section "Memory bandwidth is the main bottleneck"; the format and the
@@ -85,7 +88,7 @@ typedef enum { KIE_MODE_PERSISTENT = 0, KIE_MODE_GRAPH = 1 } kie_mode;
 
 typedef struct {
     int32_t n_layers;
-    int32_t d_model;      /* multiple of 8                                          */
+    int32_t d_model;      /* multiple of 8 (of 128 for INT4 attention weights)      */
     int32_t n_heads;      /* query heads == KV heads (multi-head attention)         */
     int32_t head_dim;     /* 64 or 128                                              */
     int32_t ffn_dim;      /* multiple of 8 (of 128 for INT4 FFN)                    */
@@ -97,14 +100,15 @@ typedef struct {
     int32_t ffn_wdtype;   /* kie_w_dtype of w_gate, w_up, w_down                     */
     int32_t mode;         /* kie_mode                                               */
     int32_t device;       /* CUDA device ordinal                                    */
-    int32_t attn_wdtype;  /* kie_w_dtype of wq, wk, wv, wo and the LM head: FP16, FP8_E4M3 or NVFP4 */
+    int32_t attn_wdtype;  /* kie_w_dtype of wq, wk, wv, wo and the LM head (INT4_G128: of wq, wk, wv) */
 } kie_config;
 
 /* Per-layer weights, fp16 bit patterns, PyTorch Linear layout [out][in], row major.
  *   attn_norm[d]  wq,wk,wv[H*h][d]  wo[d][H*h]  ffn_norm[d]
  *   w_gate,w_up[F][d]  w_down[d][F]
  * For ffn_wdtype == KIE_W_INT4_G128 the engine quantises w_gate/w_up/w_down
- * itself (kie_quantize_int4_g128 below); for KIE_W_FP8_E4M3 or KIE_W_NVFP4
+ * itself (kie_quantize_int4_g128 below), and wq/wk/wv for attn_wdtype ==
+ * KIE_W_INT4_G128; for KIE_W_FP8_E4M3 or KIE_W_NVFP4
  * (ffn_wdtype or attn_wdtype) it quantises the matrices concerned as
  * kie_quantize_fp8_rows or kie_quantize_nvfp4_rows do. */
 typedef struct {

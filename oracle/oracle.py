@@ -424,8 +424,12 @@ class OracleDecoder:
     weights: dict as produced by ``synthetic.gen_weights`` (fp16 [out, in]).
     For ffn_wdtype == "int4_g128" the FFN matrices are quantised here with
     ``int4_quantize_g128`` and used dequantised in fp32 ([xAI] 2.3/3.3,
-    [Hunyuan] 5.2).  fp16 -> fp32 widening is exact, so widening every matrix
-    once at construction equals widening it at each use."""
+    [Hunyuan] 5.2).  attn_wdtype == "int4_g128" does the same for the q, k and
+    v projections only ([xAI] 2.3: the attention's QKV projection weights in
+    INT4); the O projection and the LM head stay fp16 ([xAI] 3.3 keeps
+    lm_head in fp16 and lists no other attention matrix as INT4).  fp16 ->
+    fp32 widening is exact, so widening every matrix once at construction
+    equals widening it at each use."""
 
     def __init__(self, cfg, weights: dict, max_ctx: int | None = None):
         self.cfg = cfg
@@ -438,6 +442,8 @@ class OracleDecoder:
         fp8 = lambda a: fp8_dequantize_rows(*fp8_quantize_rows(a))  # noqa: E731
         fp4 = lambda a: fp4_dequantize_rows(*fp4_quantize_rows(a))  # noqa: E731
         attn_w = {"fp8_e4m3": fp8, "nvfp4": fp4}.get(wd, f)          # q, k, v, o and the LM head
+        i4 = lambda a: int4_dequantize(*int4_quantize_g128(a))  # noqa: E731
+        qkv_w = i4 if wd == "int4_g128" else attn_w                    # INT4 reaches q, k, v only
         self.tok_emb = f(weights["tok_emb"])
         self.lm_head = attn_w(weights["lm_head"])
         self.final_norm = f(weights["final_norm"])
@@ -445,7 +451,8 @@ class OracleDecoder:
         self.int4 = []
         for lw in weights["layers"]:
             lay = {k: f(lw[k]) for k in ("attn_norm", "ffn_norm")}
-            lay.update({k: attn_w(lw[k]) for k in ("wq", "wk", "wv", "wo")})
+            lay.update({k: qkv_w(lw[k]) for k in ("wq", "wk", "wv")})
+            lay["wo"] = attn_w(lw["wo"])
             if cfg.ffn_wdtype in ("fp8_e4m3", "nvfp4"):
                 for k in ("w_gate", "w_up", "w_down"):
                     lay[k] = (fp8 if cfg.ffn_wdtype == "fp8_e4m3" else fp4)(lw[k])
@@ -583,6 +590,8 @@ def decode_bytes_per_token(cfg, ctx_len: int) -> dict:
         attn_w = n_attn + rows_attn * 4
     elif fp4_attn:
         attn_w = n_attn // 2 + n_attn // FP4_BLOCK + rows_attn * 4
+    elif wd == "int4_g128":   # q, k, v as INT4 codes + one fp16 scale per 128 weights; O in fp16
+        attn_w = 3 * H * h * d // 2 + 3 * H * h * d // INT4_GROUP * 2 + d * H * h * 2
     else:
         attn_w = n_attn * 2
     if cfg.ffn_wdtype == "int4_g128":

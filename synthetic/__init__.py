@@ -150,6 +150,10 @@ WORKLOADS = {
     # ... and in NVFP4 (E2M1 codes, E4M3 scale per 16 columns, fp32 scale per row)
     "1p8b_nvfp4": Workload("1p8b_nvfp4", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="nvfp4",
                            attn_wdtype="nvfp4", prompt_len=2048, decode_steps=256),
+    # ... and in the xAI page's mixed precision: INT4 g128 q/k/v and FFN matrices,
+    # fp16 O projection and LM head, an FP8 E5M2 KV cache
+    "1p8b_hpi": Workload("1p8b_hpi", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="int4_g128",
+                         attn_wdtype="int4_g128", kv_dtype="fp8_e5m2", prompt_len=2048, decode_steps=256),
 }
 
 # tensor ids for the generator: per layer base 64*(layer+1) + slot

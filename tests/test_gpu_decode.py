@@ -129,7 +129,7 @@ def test_fp8_weights_prefill_and_decode(w):
 @pytest.mark.parametrize("w", [TINY, MEDIUM, WIDE], ids=lambda w: w.name)
 def test_nvfp4_weights_prefill_and_decode(w):
     """Every GEMV matrix in NVFP4 (E2M1 codes, an E4M3 scale per 16 columns, an
-    fp32 scale per row): decode with 14-row slots and the block scale applied
+    fp32 scale per row): decode with 8-row slots and the block scale applied
     per 16-column block, prefill with the exact fp16 values code * block scale
     in the MMA and the row scale on the output column; logits match the
     oracle's model with the same quantised weights."""
@@ -139,6 +139,38 @@ def test_nvfp4_weights_prefill_and_decode(w):
     tol = tol_for(w)
     assert np.abs(lg - lo).max() <= tol
     teacher_forced(e, o, O.argmax_lowest(lo), 8, tol)
+
+
+@pytest.mark.parametrize("w", [TINY, MEDIUM, WIDE], ids=lambda w: w.name)
+@pytest.mark.parametrize("ffn", ["fp16", "int4_g128"])
+def test_int4_qkv_weights_decode(w, ffn):
+    """q, k and v projections in INT4 g128 (O and the LM head fp16), with fp16
+    or INT4 FFN weights and an E5M2 cache (the xAI page's mixed precision):
+    the prompt goes through the decode kernel, teacher-forced, and the logits
+    match the oracle's model with the same quantised weights."""
+    w = w.with_(attn_wdtype="int4_g128", ffn_wdtype=ffn, kv_dtype="fp8_e5m2")
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights)
+    tol = tol_for(w)
+    assert np.abs(lg - lo).max() <= tol
+    teacher_forced(e, o, O.argmax_lowest(lo), 8, tol)
+
+
+def test_int4_qkv_graph_equals_persistent():
+    """INT4 q/k/v weights in both launch modes: bit-identical prompt logits,
+    greedy tokens and logits."""
+    w = MEDIUM.with_(attn_wdtype="int4_g128", ffn_wdtype="int4_g128")
+    weights = S.gen_weights(w)
+    prompt = S.gen_prompt(w)[:24]
+    res = {}
+    for mode in ("persistent", "graph"):
+        e = engine_for(w, weights, mode)
+        lg = e.prefill(prompt)
+        toks, logs = e.generate_greedy(int(np.argmax(lg)), 6, want_logits=True)
+        res[mode] = (lg, toks, logs)
+        e.close()
+    for a, b in zip(res["persistent"], res["graph"]):
+        np.testing.assert_array_equal(a, b)
 
 
 def test_nvfp4_ffn_graph_equals_persistent_and_u8_cache():

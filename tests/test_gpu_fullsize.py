@@ -8,6 +8,8 @@ greedy chain), against the CPU oracle.
             and token validated against the oracle fed the GPU's tokens.
   1p8b_fp8  every GEMV matrix in FP8 E4M3, synthetic 2,048-position context, 32 steps.
   1p8b_nvfp4  every GEMV matrix in NVFP4, the same context, 32 steps.
+  1p8b_hpi  INT4 q/k/v and FFN matrices with an E5M2 cache, the same context
+            length, 32 steps.
   1p8b_32k  FP8-E5M2 cache over a 32,768-position synthetic context (decode-only
             parity: the same fp16 K/V loaded into both sides), 32 steps.
   1p8b_u8   adaptive-range uint8 cache over the 8,192-position synthetic context
@@ -93,6 +95,21 @@ def test_1p8b_nvfp4_weights_decode():
     2,048-position fp16 context: 32 free-running steps in one launch."""
     n = 32
     w = S.WORKLOADS["1p8b_nvfp4"].with_(kv_source="synthetic", context_len=2048, prompt_len=0)
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights, max_ctx=w.context_len + n)
+    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + n)
+    _synthetic_context(w, e, o)
+    first = S.gen_first_token(w)
+    toks, logs = _generate_on_device(e, first, n)
+    check_free_running(o, first, toks, logs, tol_for(w))
+
+
+def test_1p8b_hpi_int4_qkv_decode():
+    """The 1.8B model with INT4 g128 q/k/v and FFN matrices (fp16 O and LM head)
+    and an E5M2 cache over a synthetic 2,048-position context: 32 free-running
+    steps in one launch."""
+    n = 32
+    w = S.WORKLOADS["1p8b_hpi"].with_(kv_source="synthetic", context_len=2048, prompt_len=0)
     weights = S.gen_weights(w)
     e = engine_for(w, weights, max_ctx=w.context_len + n)
     o = O.OracleDecoder(w, weights, max_ctx=w.context_len + n)

@@ -500,6 +500,40 @@ def test_int4_decoder_uses_dequantised_ffn():
     np.testing.assert_array_equal(a.decode(3), b.decode(3))
 
 
+def test_int4_qkv_decoder_uses_dequantised_qkv_only():
+    """With INT4 attention weights the decoder equals an fp16-weight decoder
+    whose q, k and v matrices (and nothing else) are replaced by q * fp32(s) in
+    fp32: the O projection and the LM head stay fp16 (xAI page, section 2.3:
+    INT4 for the QKV projection; section 3.3 keeps lm_head fp16).  A planted
+    INT4 O matrix must change the logits, so the check can tell the two apart."""
+    cfg = S.Workload("micro4q", 0, 1, 128, 2, 64, 256, 128, attn_wdtype="int4_g128")
+    w = S.gen_weights(cfg, seed=84)
+    a = O.OracleDecoder(cfg, w, max_ctx=4)
+    b = O.OracleDecoder(cfg.with_(attn_wdtype="fp16"), w, max_ctx=4)
+    c = O.OracleDecoder(cfg.with_(attn_wdtype="fp16"), w, max_ctx=4)
+    for k in ("wq", "wk", "wv"):
+        b.layers[0][k] = c.layers[0][k] = O.int4_dequantize(*O.int4_quantize_g128(w["layers"][0][k]))
+    c.layers[0]["wo"] = O.int4_dequantize(*O.int4_quantize_g128(w["layers"][0]["wo"]))
+    la, lb, lc = a.decode(3), b.decode(3), c.decode(3)
+    np.testing.assert_array_equal(la, lb)
+    assert np.any(la != lc)
+    np.testing.assert_array_equal(a.lm_head, w["lm_head"].astype(np.float32))
+
+
+def test_int4_qkv_byte_model_hand_count():
+    """The 1.8B model with INT4 q/k/v and FFN matrices and an E5M2 cache, per
+    decode token, counted by hand: per layer 3 x 2048^2 INT4 q/k/v codes at half
+    a byte (6,291,456 B) with one fp16 scale per 128 (196,608 B), the 2048^2 fp16
+    O matrix (8,388,608 B), 3 x 8192 x 2048 INT4 FFN codes (25,165,824 B) with
+    their scales (786,432 B) and two fp16 gain vectors (8,192 B); 25 layers; the
+    32000 x 2048 fp16 LM head, the final gains and one embedding row; K and V of
+    16 heads x 128 one-byte codes per position and layer."""
+    w = S.WORKLOADS["1p8b_hpi"]
+    b = O.decode_bytes_per_token(w, 2049)
+    assert b["weights"] == 25 * 40_837_120 + 131_072_000 + 4_096 + 4_096 == 1_152_008_192
+    assert b["kv"] == 25 * 4_096 * 2049
+
+
 def test_fp8_decoder_matches_torch_quantised_weights():
     """With FP8 E4M3 weights the decoder equals an fp16-weight decoder whose
     matrices (q, k, v, o, gate, up, down and the LM head) are replaced by
