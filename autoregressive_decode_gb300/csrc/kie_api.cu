@@ -20,6 +20,8 @@
 #include "kie_internal.h"
 
 extern "C" void* kie_decode_kernel_ptr(int hd, int kv);
+extern "C" void* kie_decode_batch_kernel_ptr(int hd, int kv);
+extern "C" cudaError_t kie_launch_slot_chunk_major(uint8_t* stream, const uint4* table, int nslots, cudaStream_t st);
 extern "C" cudaError_t kie_launch_ctl(KieControl* c, int tok, int pos, int clear, cudaStream_t st);
 extern "C" cudaError_t kie_launch_err_merge(const KieControl* src, KieControl* dst, cudaStream_t st);
 extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, const void* desc, int n,
@@ -78,7 +80,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Plan of one GEMV phase type (host copy).
 struct HostPhase {
-    int K = 0, KC = 0, nK = 0, rpu = 1, wfmt = WF_F16, n_units = 0, R = KIE_R;
+    int K = 0, KC = 0, nK = 0, rpu = 1, wfmt = WF_F16, n_units = 0, R = KIE_R, cpb = 0;
     std::vector<int32_t> unit_begin;   // G+1
     std::vector<uint32_t> bytes;       // G
     std::vector<uint32_t> nslots;      // G
@@ -99,6 +101,7 @@ struct Layout {  // byte offsets into the workspace
     // FP8 row scales (floats): per layer [QKV | O | GU | D] in each phase's row order, then the LM head
     size_t wsc, wsc_layer, wsc_off[PH_NTYPES];
     size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl;
+    size_t req;                       // batched: [2][KIE_MAX_BATCH] int32 request tokens, then positions
     size_t plan_i32, plan_u32, cta_base, cta_layer;
     size_t out_tokens, out_logits, forced, step_token, step_logits;
     // tensor-core prefill: weight tiles (per layer: Wqkv, Wo, Wgu, Wd; then Wlm) and scratch
@@ -127,6 +130,7 @@ bool prefill_tc_ok(const kie_config& c) {
 
 struct Plan {
     int G = 0;
+    int nb = 0;   // batched engine: requests (0: the single-request kernel)
     HostPhase ph[PH_NTYPES];
     std::vector<uint64_t> cta_base, cta_layer;
     uint64_t stream_bytes = 0;
@@ -159,6 +163,16 @@ bool valid_cfg(const kie_config* c, std::string& why) {
         return false;
     }
     if (c->mode < 0 || c->mode > 1) { why = "bad mode"; return false; }
+    if (c->batch < 0 || c->batch > KIE_MAX_BATCH) { why = "batch outside [0, 8]"; return false; }
+    if (c->batch > 1) {
+        if (c->mode != KIE_MODE_PERSISTENT) { why = "a batched engine needs the persistent mode"; return false; }
+        if (c->attn_wdtype != KIE_W_FP16 || c->ffn_wdtype != KIE_W_FP16) { why = "a batched engine needs fp16 weights"; return false; }
+        if (c->kv_dtype == KIE_KV_U8_ADAPTIVE) { why = "a batched engine needs an fp16 or E5M2 cache"; return false; }
+        if (c->d_model % 64 || c->ffn_dim % 64 || (c->n_heads * c->head_dim) % 64) {
+            why = "a batched engine needs d_model, ffn_dim and n_heads*head_dim multiples of 64";
+            return false;
+        }
+    }
     if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) { why = "bad rms_eps or rope_theta"; return false; }
     return true;
 }
@@ -166,6 +180,8 @@ bool valid_cfg(const kie_config* c, std::string& why) {
 // Partition every phase over G CTAs, balancing each CTA's cumulative stream bytes.
 void build_plan(const kie_config& c, int G, Plan& pl) {
     pl.G = G;
+    pl.nb = c.batch > 1 ? c.batch : 0;
+    const bool bat = pl.nb > 0;
     const int d = c.d_model, H = c.n_heads, hd = c.head_dim, F = c.ffn_dim, V = c.vocab;
     const int ffn_fmt = c.ffn_wdtype == KIE_W_INT4_G128 ? WF_I4 : c.ffn_wdtype == KIE_W_FP8_E4M3 ? WF_F8
                         : c.ffn_wdtype == KIE_W_NVFP4 ? WF_F4 : WF_F16;
@@ -178,7 +194,12 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
         // KIE_R4 rows x 2048 NVFP4 (+ block scales)
         p.KC = std::min(K, wfmt == WF_I4 ? KIE_KC_I4 : KIE_KC_F16);
         p.R = wfmt == WF_F8 ? KIE_R8 : wfmt == WF_F4 ? KIE_R4 : KIE_R;
+        if (bat) {   // batched kernel: 16-row x 512-column fp16 slots, staged 2048 columns at a time
+            p.KC = std::min(K, KIE_KCB);
+            p.R = KIE_RB;
+        }
         p.nK = (K + p.KC - 1) / p.KC;
+        p.cpb = bat ? KIE_KBLK / KIE_KCB : p.nK;
     };
     setp(PH_QKV, d, 2, 3 * H * (hd / 2), qkv_fmt);
     setp(PH_O, H * hd, 1, d, attn_fmt);
@@ -248,13 +269,27 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
     const int64_t max_seg = (int64_t(c.max_ctx) + min_heads_cta - 1) / min_heads_cta + 2;
     part = std::max<int64_t>(part, 4 * (max_seg / KIE_SEG + 2));
     part = std::max<int64_t>(part, G + H);   // O-phase combine: per-CTA weights and per-head 1/L
-    pl.part_floats = int(align_up(size_t(std::max<int64_t>(part, 4)), 4));
     int act = std::max({d, F, H * hd, int(std::min<int64_t>(max_seg, 1 << 30))});
+    if (bat) {
+        // batched: a phase staged in several blocks keeps each row tile's running
+        // sums in the part buffer (128 floats a tile); the activations are one
+        // block of MMA fragments (2048 columns x 8 requests x hi/lo fp16)
+        part = std::max<int64_t>(G + H, 4);
+        for (int t = 0; t < PH_NTYPES; ++t) {
+            const HostPhase& p = pl.ph[t];
+            for (int i = 0; i < G; ++i) {
+                const int rows = (p.unit_begin[i + 1] - p.unit_begin[i]) * p.rpu;
+                part = std::max<int64_t>(part, int64_t((rows + KIE_RB - 1) / KIE_RB) * 128);
+            }
+        }
+        act = (KIE_KBLK / 16) * 128;
+    }
+    pl.part_floats = int(align_up(size_t(std::max<int64_t>(part, 4)), 4));
     pl.act_floats = int(align_up(act, 8));
-    const KieSmemLayout l0 = kie_smem_layout(pl.part_floats, pl.act_floats, 0);
+    const KieSmemLayout l0 = kie_smem_layout(pl.part_floats, pl.act_floats, 0, pl.nb);
     const long avail = long(kSmemLimit) - long(l0.total);
     pl.nslot = int(std::max<long>(0, std::min<long>(KIE_MAX_SLOTS, avail / KIE_SLOT_BYTES)));
-    pl.smem = kie_smem_layout(pl.part_floats, pl.act_floats, pl.nslot).total;
+    pl.smem = kie_smem_layout(pl.part_floats, pl.act_floats, pl.nslot, pl.nb).total;
 }
 
 void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
@@ -276,9 +311,11 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
         L.wsc_off[PH_LM] = o8 * c.n_layers;
         L.wsc = take(f8 ? (L.wsc_off[PH_LM] + rows[PH_LM]) * 4 : 0);
     }
+    // one request's cache (a batched engine keeps pl.nb of them back to back)
+    const size_t nbq = pl.nb > 0 ? size_t(pl.nb) : 1;
     L.kv_bytes = size_t(c.n_layers) * H * c.max_ctx * hd * esz;
-    L.kc = take(L.kv_bytes);
-    L.vc = take(L.kv_bytes);
+    L.kc = take(nbq * L.kv_bytes);
+    L.vc = take(nbq * L.kv_bytes);
     L.nseg = (c.max_ctx + KIE_SEG - 1) / KIE_SEG;
     const bool u8 = c.kv_dtype == KIE_KV_U8_ADAPTIVE;
     L.tail = take(u8 ? size_t(c.n_layers) * 2 * H * KIE_SEG * hd * 2 : 0);
@@ -286,24 +323,25 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.seg_zp = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
     // tagged activations, reset before each launch sequence (reset_tags):
     // x .. vcur to zero, q .. att_part to one parity
-    L.x = take(size_t(KIE_REPL) * d * 4);
-    L.kcur = take(size_t(H) * hd * 4);
-    L.vcur = take(size_t(H) * hd * 4);
-    L.zero_bytes = L.vcur + size_t(H) * hd * 4 - L.x;
-    L.q = take(size_t(H) * hd * 4);
-    L.a = take(size_t(KIE_REPL) * F * 4);
-    L.o = take(size_t(KIE_REPL) * H * hd * 4);
+    L.x = take(size_t(KIE_REPL) * nbq * d * 4);
+    L.kcur = take(nbq * H * hd * 4);
+    L.vcur = take(nbq * H * hd * 4);
+    L.zero_bytes = L.vcur + nbq * H * hd * 4 - L.x;
+    L.q = take(nbq * H * hd * 4);
+    L.a = take(size_t(KIE_REPL) * nbq * F * 4);
+    L.o = take(size_t(KIE_REPL) * nbq * H * hd * 4);
     L.att_part = take(size_t(G) * (hd + 4) * 4);
     L.par_bytes = L.att_part + size_t(G) * (hd + 4) * 4 - L.q;
-    L.amax_val = take(size_t(G) * 4);
-    L.amax_idx = take(size_t(G) * 4);
+    L.amax_val = take(nbq * G * 4);
+    L.amax_idx = take(nbq * G * 4);
     L.ctl = take(sizeof(KieControl));
+    L.req = take(size_t(2) * KIE_MAX_BATCH * 4);
     L.plan_i32 = take(size_t(PH_NTYPES) * (G + 1) * 4);
     L.plan_u32 = take(size_t(PH_NTYPES) * 2 * G * 4);
     L.cta_base = take(size_t(G) * 8);
     L.cta_layer = take(size_t(G) * 8);
-    L.out_tokens = take(size_t(c.max_ctx) * 4);
-    L.out_logits = take(size_t(kLogitChunk) * V * 4);
+    L.out_tokens = take(size_t(c.max_ctx) * nbq * 4);
+    L.out_logits = take(size_t(kLogitChunk) * nbq * V * 4);
     L.forced = take(size_t(c.max_ctx) * 4);
     L.step_token = take(4);
     L.step_logits = take(size_t(V) * 4);
@@ -354,7 +392,9 @@ struct kie_engine {
     KieParams P{};
     void* kernel = nullptr;
     bool loaded = false;
-    int pos = 0;
+    int pos = 0;                      // position of the selected request
+    int cur = 0;                      // batched engine: the request kie_prefill, kie_set_kv, ... address
+    int rpos[KIE_MAX_BATCH] = {};     // batched engine: every request's position (rpos[cur] is stale; pos is current)
     int sticky = 0;
     uint64_t timeout_ns = kDefaultTimeoutNs;
     cudaGraphExec_t graph[2] = {nullptr, nullptr};   // graph mode, by tag_fill of the step's position
@@ -364,6 +404,9 @@ struct kie_engine {
     std::string err;
 
     uint8_t* dev(size_t off) const { return static_cast<uint8_t*>(ws) + off; }
+    // byte offset of the selected request's K (or V) cache inside the cache arrays
+    size_t kv_off() const { return size_t(cur) * lay.kv_bytes; }
+    bool batched() const { return plan.nb > 0; }
 };
 
 namespace {
@@ -563,6 +606,8 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
     const float* inv_freq = reinterpret_cast<const float*>(e->dev(L.inv_freq));
     const uint16_t* emb = reinterpret_cast<const uint16_t*>(e->dev(L.emb));
     int32_t* d_tok = reinterpret_cast<int32_t*>(e->dev(L.forced));
+    uint8_t* kc = e->dev(L.kc) + e->kv_off();   // the selected request's cache
+    uint8_t* vc = e->dev(L.vc) + e->kv_off();
     const int kvf = c.kv_dtype == KIE_KV_FP16 ? KV_F16 : KV_E5M2;
     const float scale = 1.0f / std::sqrt(float(hd));
     const int nqkv = pad256(3 * HD), ngu = pad256(2 * F), nd = pad256(d), nv = pad256(V);
@@ -586,9 +631,9 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
             const float* g2 = g1 + d;
             KIE_CUDA(e, kie_pf_norm_split(x, d, g1, c.rms_eps, Tn, Tp, d, ahi, alo, st));
             KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, colsc(a8, sb), to, err, st));
-            KIE_CUDA(e, kie_pf_qkv_post(C, nqkv, Tn, pos, H, hd, inv_freq, kvf, e->dev(L.kc), e->dev(L.vc), l,
+            KIE_CUDA(e, kie_pf_qkv_post(C, nqkv, Tn, pos, H, hd, inv_freq, kvf, kc, vc, l,
                                         c.max_ctx, Q, st));
-            KIE_CUDA(e, kie_pf_attention(Q, e->dev(L.kc), e->dev(L.vc), l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O,
+            KIE_CUDA(e, kie_pf_attention(Q, kc, vc, l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O,
                                          st));
             KIE_CUDA(e, kie_pf_split(O, HD, Tn, Tp, HD, ahi, alo, st));
             KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, colsc(a8, sb + 3 * HD), to, err, st));
@@ -733,7 +778,12 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
         kie_destroy(e);
         return fail(nullptr, KIE_ERR_OOM, "cudaMallocHost failed");
     }
-    e->kernel = kie_decode_kernel_ptr(cfg->head_dim, cfg->kv_dtype);
+    if (e->batched() && cfg->batch * cfg->n_heads > G) {
+        kie_destroy(e);
+        return fail(nullptr, KIE_ERR_UNSUPPORTED, "batch * n_heads = %d exceeds the %d SMs", cfg->batch * cfg->n_heads, G);
+    }
+    e->kernel = e->batched() ? kie_decode_batch_kernel_ptr(cfg->head_dim, cfg->kv_dtype)
+                             : kie_decode_kernel_ptr(cfg->head_dim, cfg->kv_dtype);
     cudaError_t r = cudaFuncSetAttribute(e->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(e->plan.smem));
     if (r != cudaSuccess) { kie_destroy(e); return fail(nullptr, KIE_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(r)); }
     int per_sm = 0;
@@ -782,6 +832,7 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
         const HostPhase& h = pl.ph[t];
         q.K = h.K; q.KC = h.KC; q.nK = h.nK; q.rows_per_unit = h.rpu; q.wfmt = h.wfmt; q.n_units = h.n_units;
         q.R = h.R;
+        q.cpb = h.cpb;
         q.wscale = (h.wfmt == WF_F8 || h.wfmt == WF_F4) ? reinterpret_cast<const float*>(e->dev(L.wsc)) + L.wsc_off[t]
                                                          : nullptr;
         q.wscale_layer = int64_t(L.wsc_layer);
@@ -807,6 +858,10 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     P.amax_val = reinterpret_cast<float*>(e->dev(L.amax_val));
     P.amax_idx = reinterpret_cast<int32_t*>(e->dev(L.amax_idx));
     P.ctl = reinterpret_cast<KieControl*>(e->dev(L.ctl));
+    P.nb = pl.nb;
+    P.kv_req = int64_t(L.kv_bytes / (cfg->kv_dtype == KIE_KV_FP16 ? 2 : 1));
+    P.req_tok = reinterpret_cast<int32_t*>(e->dev(L.req));
+    P.req_pos = P.req_tok + KIE_MAX_BATCH;
     P.nslot = pl.nslot;
     P.act_floats = pl.act_floats;
     P.part_floats = pl.part_floats;
@@ -906,9 +961,12 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
             const int u0 = p.unit_begin[i], nu = p.unit_begin[i + 1] - u0;
             const int rows = nu * p.rpu;
             const int groups = (rows + p.R - 1) / p.R;
+            // slots in the order (staging block, row group, chunk); a block is the whole row
+            // except in the batched kernel (KIE_KBLK columns)
+            for (int ch0 = 0; ch0 < p.nK; ch0 += p.cpb)
             for (int g = 0; g < groups; ++g) {
                 const int rg = std::min(p.R, rows - g * p.R);
-                for (int ch = 0; ch < p.nK; ++ch) {
+                for (int ch = ch0; ch < std::min(p.nK, ch0 + p.cpb); ++ch) {
                     const int kc = std::min(p.KC, K - ch * p.KC);
                     for (int r = 0; r < rg; ++r) {
                         const int lr = g * p.R + r;
@@ -1075,6 +1133,37 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     if (result == KIE_OK && L.pf && any_f8 &&
         cudaMemcpy(e->dev(L.pf_sc), pfsc.data(), pfsc.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
         result = fail(e, KIE_ERR_CUDA, "prefill scale upload failed");
+    if (result == KIE_OK && e->batched()) {
+        // the batched kernel reads its fp16 slots chunk-major: rewrite every slot in place
+        std::vector<uint4> tab;
+        for (int i = 0; i < G; ++i) {
+            uint64_t off = pl.cta_base[i];
+            for (int l = 0; l <= c.n_layers; ++l) {
+                for (int t : {PH_QKV, PH_O, PH_GU, PH_D, PH_LM}) {
+                    if ((l == c.n_layers) != (t == PH_LM)) continue;
+                    const HostPhase& p = pl.ph[t];
+                    const int rows = (p.unit_begin[i + 1] - p.unit_begin[i]) * p.rpu;
+                    const int groups = (rows + p.R - 1) / p.R;
+                    for (int ch0 = 0; ch0 < p.nK; ch0 += p.cpb)
+                        for (int g = 0; g < groups; ++g)
+                            for (int ch = ch0; ch < std::min(p.nK, ch0 + p.cpb); ++ch) {
+                                const int rg = std::min(p.R, rows - g * p.R), kc = std::min(p.KC, p.K - ch * p.KC);
+                                tab.push_back(make_uint4(uint32_t(off), uint32_t(off >> 32), uint32_t(rg), uint32_t(kc)));
+                                off += slot_bytes_host(p.wfmt, rg, kc);
+                            }
+                }
+            }
+        }
+        uint4* dtab = nullptr;
+        if (cudaMalloc(&dtab, tab.size() * sizeof(uint4)) != cudaSuccess) result = fail(e, KIE_ERR_OOM, "slot table cudaMalloc failed");
+        else {
+            if (cudaMemcpyAsync(dtab, tab.data(), tab.size() * sizeof(uint4), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+                kie_launch_slot_chunk_major(e->dev(L.wstream), dtab, int(tab.size()), st) != cudaSuccess ||
+                cudaStreamSynchronize(st) != cudaSuccess)
+                result = fail(e, KIE_ERR_CUDA, "slot layout pass failed");
+            cudaFree(dtab);
+        }
+    }
     if (f8codes) cudaFree(f8codes);
     if (f8sc) cudaFree(f8sc);
     cudaStreamSynchronize(st);
@@ -1082,6 +1171,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     if (result != KIE_OK) return result;
     e->loaded = true;
     e->pos = 0;
+    std::fill(std::begin(e->rpos), std::end(e->rpos), 0);
     e->sticky = 0;
     return set_ctl(e, 0, 0, true);
 }
@@ -1108,6 +1198,7 @@ kie_status kie_generate_greedy_device(kie_engine* e, int32_t first_token, int32_
                                       float* d_out_logits) {
     kie_status st = ready(e, n);
     if (st != KIE_OK) return st;
+    if (e->batched()) return fail(e, KIE_ERR_UNSUPPORTED, "a batched engine decodes with kie_generate_greedy_batch");
     if (n == 0) return KIE_OK;
     if (!d_out_tokens) return fail(e, KIE_ERR_INVALID_ARG, "d_out_tokens is NULL");
     if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
@@ -1117,6 +1208,7 @@ kie_status kie_generate_greedy_device(kie_engine* e, int32_t first_token, int32_
 kie_status kie_generate_greedy(kie_engine* e, int32_t first_token, int32_t n, int32_t* out_tokens, float* out_logits) {
     kie_status st = ready(e, n);
     if (st != KIE_OK) return st;
+    if (e->batched()) return fail(e, KIE_ERR_UNSUPPORTED, "a batched engine decodes with kie_generate_greedy_batch");
     if (n == 0) return KIE_OK;
     if (!out_tokens) return fail(e, KIE_ERR_INVALID_ARG, "out_tokens is NULL");
     if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
@@ -1145,9 +1237,114 @@ kie_status kie_decode_step(kie_engine* e, int32_t token, int32_t* next_token, fl
     return kie_generate_greedy(e, token, 1, next_token, logits);
 }
 
+kie_status kie_select_request(kie_engine* e, int32_t request) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    const int nbq = e->batched() ? e->plan.nb : 1;
+    if (request < 0 || request >= nbq) return fail(e, KIE_ERR_INVALID_ARG, "request %d outside [0, %d)", request, nbq);
+    e->rpos[e->cur] = e->pos;
+    e->cur = request;
+    e->pos = e->rpos[request];
+    return KIE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+kie_status ready_batch(kie_engine* e, int n) {
+    if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
+    if (!e->batched()) return fail(e, KIE_ERR_UNSUPPORTED, "not a batched engine (kie_config.batch < 2)");
+    if (!e->loaded) return fail(e, KIE_ERR_NOT_LOADED, "weights not loaded");
+    if (e->sticky) return fail(e, KIE_ERR_DEVICE_TIMEOUT, "engine poisoned by an earlier device error; call kie_reset");
+    if (n < 0) return fail(e, KIE_ERR_INVALID_ARG, "negative count");
+    e->rpos[e->cur] = e->pos;
+    for (int b = 0; b < e->plan.nb; ++b)
+        if (int64_t(e->rpos[b]) + n > e->cfg.max_ctx)
+            return fail(e, KIE_ERR_CTX_OVERFLOW, "request %d: pos %d + %d > max_ctx %d", b, e->rpos[b], n, e->cfg.max_ctx);
+    return KIE_OK;
+}
+
+// n steps of every request of a batched engine, one persistent launch.  first:
+// host tokens [nb], or null to continue from the tokens the device holds.
+kie_status run_batch(kie_engine* e, const int32_t* first, int n, int32_t* d_tokens, float* d_logits) {
+    if (n <= 0) return KIE_OK;
+    const int nb = e->plan.nb;
+    int32_t h[2 * KIE_MAX_BATCH] = {};
+    for (int b = 0; b < nb; ++b) {
+        h[b] = first ? first[b] : 0;
+        h[KIE_MAX_BATCH + b] = e->rpos[b];
+    }
+    int32_t* dreq = reinterpret_cast<int32_t*>(e->dev(e->lay.req));
+    if (first) KIE_CUDA(e, cudaMemcpyAsync(dreq, h, sizeof(h), cudaMemcpyHostToDevice, e->stream));
+    else KIE_CUDA(e, cudaMemcpyAsync(dreq + KIE_MAX_BATCH, h + KIE_MAX_BATCH, KIE_MAX_BATCH * 4, cudaMemcpyHostToDevice, e->stream));
+    KieLaunch l = base_launch(e);
+    l.n_steps = n;
+    l.pos0 = e->rpos[0];   // the tags number writes by request 0's position
+    l.out_tokens = d_tokens;
+    l.out_logits = d_logits;
+    kie_status st = launch_persistent(e, l);
+    if (st != KIE_OK) return st;
+    for (int b = 0; b < nb; ++b) e->rpos[b] += n;
+    e->pos = e->rpos[e->cur];
+    return KIE_OK;
+}
+
+kie_status check_batch_tokens(kie_engine* e, const int32_t* t) {
+    if (!t) return fail(e, KIE_ERR_INVALID_ARG, "token array is NULL");
+    return check_tokens(e, t, e->plan.nb);
+}
+
+}  // namespace
+
+extern "C" {
+
+kie_status kie_generate_greedy_batch_device(kie_engine* e, const int32_t* first_tokens, int32_t n,
+                                            int32_t* d_out_tokens, float* d_out_logits) {
+    kie_status st = ready_batch(e, n);
+    if (st != KIE_OK) return st;
+    if (n == 0) return KIE_OK;
+    if (!d_out_tokens) return fail(e, KIE_ERR_INVALID_ARG, "d_out_tokens is NULL");
+    if ((st = check_batch_tokens(e, first_tokens)) != KIE_OK) return st;
+    return run_batch(e, first_tokens, n, d_out_tokens, d_out_logits);
+}
+
+kie_status kie_generate_greedy_batch(kie_engine* e, const int32_t* first_tokens, int32_t n, int32_t* out_tokens,
+                                     float* out_logits) {
+    kie_status st = ready_batch(e, n);
+    if (st != KIE_OK) return st;
+    if (n == 0) return KIE_OK;
+    if (!out_tokens) return fail(e, KIE_ERR_INVALID_ARG, "out_tokens is NULL");
+    if ((st = check_batch_tokens(e, first_tokens)) != KIE_OK) return st;
+    const int nb = e->plan.nb;
+    const size_t V = size_t(e->cfg.vocab);
+    int32_t* d_tok = reinterpret_cast<int32_t*>(e->dev(e->lay.out_tokens));
+    float* d_log = reinterpret_cast<float*>(e->dev(e->lay.out_logits));
+    if (!out_logits) {
+        if ((st = run_batch(e, first_tokens, n, d_tok, nullptr)) != KIE_OK) return st;
+    } else {
+        for (int done = 0; done < n;) {
+            const int m = std::min(kLogitChunk, n - done);
+            if ((st = run_batch(e, done == 0 ? first_tokens : nullptr, m, d_tok + size_t(done) * nb, d_log)) != KIE_OK)
+                return st;
+            KIE_CUDA(e, cudaMemcpyAsync(out_logits + size_t(done) * nb * V, d_log, size_t(m) * nb * V * 4,
+                                        cudaMemcpyDeviceToHost, e->stream));
+            if ((st = check_device(e)) != KIE_OK) return st;
+            done += m;
+        }
+    }
+    KIE_CUDA(e, cudaMemcpyAsync(out_tokens, d_tok, size_t(n) * nb * 4, cudaMemcpyDeviceToHost, e->stream));
+    return check_device(e);
+}
+
+kie_status kie_decode_batch(kie_engine* e, const int32_t* tokens, int32_t* next_tokens, float* logits) {
+    if (!next_tokens) return fail(e, KIE_ERR_INVALID_ARG, "next_tokens is NULL");
+    return kie_generate_greedy_batch(e, tokens, 1, next_tokens, logits);
+}
+
 kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint64_t* stamps, size_t cap) {
     kie_status st = ready(e, n);
     if (st != KIE_OK) return st;
+    if (e->batched()) return fail(e, KIE_ERR_UNSUPPORTED, "tracing covers the single-request kernel");
     if (e->cfg.mode != KIE_MODE_PERSISTENT) return fail(e, KIE_ERR_UNSUPPORTED, "tracing needs the persistent mode");
     if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
     const size_t nphase = size_t(n) * (5 * e->cfg.n_layers + 1) * KIE_PROF_EVENTS * e->G;
@@ -1184,6 +1381,7 @@ kie_status kie_reset(kie_engine* e) {
     cudaStreamSynchronize(e->stream);
     e->sticky = 0;
     e->pos = 0;
+    std::fill(std::begin(e->rpos), std::end(e->rpos), 0);
     KIE_CUDA(e, reset_tags(e->cfg, e->dev(e->lay.x), e->lay.zero_bytes, e->dev(e->lay.q), e->lay.par_bytes, 0,
                            e->stream));
     return set_ctl(e, 0, 0, true);
@@ -1244,7 +1442,7 @@ kie_status kie_set_kv(kie_engine* e, int32_t layer, const uint16_t* k_fp16, cons
     const Layout& L = e->lay;
     for (int kv = 0; kv < 2 && result == KIE_OK; ++kv) {
         const uint16_t* src = kv ? v_fp16 : k_fp16;
-        uint8_t* base = e->dev(kv ? L.vc : L.kc);
+        uint8_t* base = e->dev(kv ? L.vc : L.kc) + e->kv_off();
         if (cudaMemcpyAsync(stage, src, elems * 2, cudaMemcpyHostToDevice, st) != cudaSuccess) { result = fail(e, KIE_ERR_CUDA, "upload failed"); break; }
         const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
         uint8_t* dst = base + size_t(layer) * H * c.max_ctx * hd * esz;
@@ -1283,7 +1481,7 @@ kie_status kie_read_kv(kie_engine* e, int32_t layer, int32_t which, int32_t p0, 
     const Layout& L = e->lay;
     const int H = c.n_heads, hd = c.head_dim;
     const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
-    const uint8_t* base = e->dev(which ? L.vc : L.kc) + size_t(layer) * H * c.max_ctx * hd * esz;
+    const uint8_t* base = e->dev(which ? L.vc : L.kc) + e->kv_off() + size_t(layer) * H * c.max_ctx * hd * esz;
     for (int h = 0; h < H; ++h)
         KIE_CUDA(e, cudaMemcpy(static_cast<uint8_t*>(out) + size_t(h) * n * hd * esz,
                                base + (size_t(h) * c.max_ctx + p0) * hd * esz, size_t(n) * hd * esz, cudaMemcpyDeviceToHost));
@@ -1410,6 +1608,7 @@ extern "C" kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t toke
                                                      float* d_logits) {
     kie_status st = ready(e, 1);
     if (st != KIE_OK) return st;
+    if (e->batched()) return fail(e, KIE_ERR_UNSUPPORTED, "a batched engine decodes with kie_decode_batch");
     if (!d_next_token) return fail(e, KIE_ERR_INVALID_ARG, "d_next_token is NULL");
     if ((st = check_tokens(e, &token, 1)) != KIE_OK) return st;
     if (e->cfg.mode != KIE_MODE_PERSISTENT) return fail(e, KIE_ERR_UNSUPPORTED, "static-scratch step needs the persistent mode");

@@ -325,9 +325,10 @@ __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem&
     for (int blk = 0; blk < nblk; ++blk) {
         const int k0 = blk * KIE_KBLK, kb = min(KIE_KBLK, c.K - k0);
         const int nch = (kb + c.KC - 1) / c.KC;
+        // Every warp runs every block's barriers, also after a failed wait (the
+        // waits then return at once), so the barrier counts always match.
         if (blk > 0) consumer_sync(NCT);   // every warp is done with the previous block's fragments
         stage_b(P, Lc, S, src, n, from_emb, g, scaled, par_src, k0, kb, blk == 0, cap0, ncap, tid, cta);
-        if (ld_volatile_i32(&S.flags[0]) != 0) { ok = false; break; }
         for (int tile = warp; tile < ntiles && ok; tile += NW) {
             const int rows_g = min(KIE_RB, c.rows - tile * KIE_RB);
             float acc[4][4];
@@ -339,6 +340,7 @@ __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem&
                 const uint32_t gidx = gc + jbase + uint32_t(tile * nch + ch);
                 if (!wait_issued(P, Lc, S, gidx, cta, lane) || !warp_wait_full(P, Lc, S, gidx, cta, lane)) {
                     ok = false;
+                    S.flags[0] = 1;
                     break;
                 }
                 const uint32_t slot = gidx % nslot;
@@ -400,7 +402,6 @@ __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem&
                 }
             }
         }
-        if (!ok) break;
         jbase += uint32_t(ntiles * nch);
     }
     gc += c.nslots;

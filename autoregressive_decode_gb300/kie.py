@@ -42,7 +42,7 @@ class kie_config(C.Structure):
                 ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
                 ("max_ctx", C.c_int32), ("rms_eps", C.c_float), ("rope_theta", C.c_float),
                 ("kv_dtype", C.c_int32), ("ffn_wdtype", C.c_int32), ("mode", C.c_int32),
-                ("device", C.c_int32), ("attn_wdtype", C.c_int32)]
+                ("device", C.c_int32), ("attn_wdtype", C.c_int32), ("batch", C.c_int32)]
 
 
 class kie_layer_weights(C.Structure):
@@ -67,6 +67,10 @@ EXPORTS = {
     "kie_sync": (C.c_int, [C.c_void_p]),
     "kie_decode_step_static_scratch": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_trace_decode": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t]),
+    "kie_select_request": (C.c_int, [C.c_void_p, C.c_int32]),
+    "kie_decode_batch": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "kie_generate_greedy_batch": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
+    "kie_generate_greedy_batch_device": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "kie_reset": (C.c_int, [C.c_void_p]),
     "kie_get_pos": (C.c_int32, [C.c_void_p]),
     "kie_set_pos": (C.c_int, [C.c_void_p, C.c_int32]),
@@ -127,9 +131,11 @@ def _check(st, eng=None):
 
 
 def make_config(n_layers, d_model, n_heads, head_dim, ffn_dim, vocab, max_ctx, rms_eps=1e-5, rope_theta=10000.0,
-                kv_dtype="fp16", ffn_wdtype="fp16", mode="persistent", device=0, attn_wdtype="fp16") -> kie_config:
+                kv_dtype="fp16", ffn_wdtype="fp16", mode="persistent", device=0, attn_wdtype="fp16",
+                batch=1) -> kie_config:
     return kie_config(n_layers, d_model, n_heads, head_dim, ffn_dim, vocab, max_ctx, rms_eps, rope_theta,
-                      KV_DTYPES[kv_dtype], W_DTYPES[ffn_wdtype], MODES[mode], device, W_DTYPES[attn_wdtype])
+                      KV_DTYPES[kv_dtype], W_DTYPES[ffn_wdtype], MODES[mode], device, W_DTYPES[attn_wdtype],
+                      int(batch))
 
 
 class Engine:
@@ -146,6 +152,7 @@ class Engine:
         _check(lib.kie_create(C.byref(cfg), ws_ptr, ws_bytes, st_ptr, C.byref(h)))
         self.h = h
         self.vocab = cfg.vocab
+        self.batch = max(1, cfg.batch)
 
     # -- lifetime -------------------------------------------------------------------------
     def close(self):
@@ -214,6 +221,32 @@ class Engine:
     def decode_step_static_scratch(self, token: int, d_next_token, d_logits=None):
         """kie_decode_step_static_scratch: device outputs, no allocation, no sync."""
         _check(load().kie_decode_step_static_scratch(self.h, int(token), _ptr(d_next_token), _ptr(d_logits)), self.h)
+
+    # -- batched engines --------------------------------------------------------------------
+    def select_request(self, b: int):
+        """Address request b with prefill / set_kv / read_kv / set_pos / pos."""
+        _check(load().kie_select_request(self.h, int(b)), self.h)
+
+    def decode_batch(self, tokens, want_logits: bool = True):
+        """One step of every request: (next tokens [batch], logits [batch, vocab] or None)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        nxt = np.empty(self.batch, np.int32)
+        out = np.empty((self.batch, self.vocab), np.float32) if want_logits else None
+        _check(load().kie_decode_batch(self.h, _ptr(t), _ptr(nxt), _ptr(out)), self.h)
+        return nxt, out
+
+    def generate_greedy_batch(self, first_tokens, n: int, want_logits: bool = False):
+        """n greedy steps of every request: (tokens [n, batch], logits [n, batch, vocab] or None)."""
+        f = np.ascontiguousarray(first_tokens, dtype=np.int32)
+        toks = np.empty((n, self.batch), np.int32)
+        logs = np.empty((n, self.batch, self.vocab), np.float32) if want_logits else None
+        _check(load().kie_generate_greedy_batch(self.h, _ptr(f), int(n), _ptr(toks), _ptr(logs)), self.h)
+        return toks, logs
+
+    def generate_greedy_batch_device(self, first_tokens, n: int, d_tokens, d_logits=None):
+        f = np.ascontiguousarray(first_tokens, dtype=np.int32)
+        _check(load().kie_generate_greedy_batch_device(self.h, _ptr(f), int(n), _ptr(d_tokens), _ptr(d_logits)),
+               self.h)
 
     def sync(self):
         _check(load().kie_sync(self.h), self.h)

@@ -101,7 +101,16 @@ typedef struct {
     int32_t mode;         /* kie_mode                                               */
     int32_t device;       /* CUDA device ordinal                                    */
     int32_t attn_wdtype;  /* kie_w_dtype of wq, wk, wv, wo and the LM head (INT4_G128: of wq, wk, wv) */
+    int32_t batch;        /* 0 or 1: one request.  2..KIE_MAX_BATCH_REQUESTS: a batched engine (see
+                           * kie_decode_batch): that many independent requests, each with its
+                           * own KV cache (max_ctx positions) and position, decoded together
+                           * so that every weight byte is read once per step for all of them.
+                           * Needs PERSISTENT mode, FP16 weights, an FP16 or FP8_E5M2 cache,
+                           * d_model, ffn_dim and n_heads*head_dim multiples of 64, and
+                           * batch * n_heads <= the GPU's SM count. */
 } kie_config;
+
+#define KIE_MAX_BATCH_REQUESTS 8
 
 /* Per-layer weights, fp16 bit patterns, PyTorch Linear layout [out][in], row major.
  *   attn_norm[d]  wq,wk,wv[H*h][d]  wo[d][H*h]  ffn_norm[d]
@@ -166,6 +175,39 @@ kie_status kie_generate_greedy(kie_engine* e, int32_t first_token, int32_t n, in
  * program are reported by the next synchronising call (or kie_sync). */
 kie_status kie_generate_greedy_device(kie_engine* e, int32_t first_token, int32_t n,
                                       int32_t* d_out_tokens, float* d_out_logits);
+
+/* ---- batched engines (kie_config.batch >= 2) ------------------------------------------------
+ * Low-batch decode (the Kog page's TL;DR: batch 1 for its preview, larger
+ * batches for production): the requests share one pass over the weights per
+ * step.  Each request is the single-request model on its own cache: the same
+ * tokens and logits as a one-request engine up to fp32 summation order (the
+ * batched GEMV runs on the tensor cores with the activations split into fp16
+ * hi + lo parts, about 2^-22 relative).
+ *
+ * kie_select_request chooses the request that kie_prefill, kie_set_kv,
+ * kie_read_kv, kie_set_pos and kie_get_pos address (default 0; on a
+ * one-request engine only 0 is valid).  kie_decode_step, kie_generate_greedy
+ * and their variants are refused on a batched engine (KIE_ERR_UNSUPPORTED):
+ * use the calls below, which advance every request by the same number of
+ * tokens from its own position. */
+kie_status kie_select_request(kie_engine* e, int32_t request);
+
+/* One step for every request: tokens[b] (host, [batch]) is consumed at
+ * request b's position; next_tokens[b] (host) receives its argmax (lowest id
+ * on ties); logits: NULL or host fp32[batch][vocab].  Every position += 1. */
+kie_status kie_decode_batch(kie_engine* e, const int32_t* tokens, int32_t* next_tokens, float* logits);
+
+/* n greedy steps for every request, equal to n chained kie_decode_batch
+ * calls: out_tokens (host, [n][batch]) and out_logits (NULL or host
+ * fp32[n][batch][vocab]).  first_tokens: host [batch]. */
+kie_status kie_generate_greedy_batch(kie_engine* e, const int32_t* first_tokens, int32_t n, int32_t* out_tokens,
+                                     float* out_logits);
+
+/* The same with DEVICE output buffers (d_out_logits may be NULL), enqueued on
+ * the engine's stream without synchronising (first_tokens stays a host array,
+ * read before the call returns). */
+kie_status kie_generate_greedy_batch_device(kie_engine* e, const int32_t* first_tokens, int32_t n,
+                                            int32_t* d_out_tokens, float* d_out_logits);
 
 /* Synchronise the engine's stream and report any error the GPU program set. */
 kie_status kie_sync(kie_engine* e);
