@@ -272,17 +272,21 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
     int act = std::max({d, F, H * hd, int(std::min<int64_t>(max_seg, 1 << 30))});
     if (bat) {
         // batched: a phase staged in several blocks keeps each row tile's running
-        // sums in the part buffer (128 floats a tile); the activations are one
-        // block of MMA fragments (2048 columns x 8 requests x hi/lo fp16)
+        // sums in the part buffer (128 floats a tile), and one with fewer row
+        // tiles than consumer warps each slot's sums of a block (128 floats a
+        // (tile, chunk)); the activations are one block of MMA fragments (2048
+        // columns x 8 requests x hi/lo fp16)
         part = std::max<int64_t>(G + H, 4);
         for (int t = 0; t < PH_NTYPES; ++t) {
             const HostPhase& p = pl.ph[t];
+            const int nblk = (p.K + KIE_KBLK - 1) / KIE_KBLK;
             for (int i = 0; i < G; ++i) {
-                const int rows = (p.unit_begin[i + 1] - p.unit_begin[i]) * p.rpu;
-                part = std::max<int64_t>(part, int64_t((rows + KIE_RB - 1) / KIE_RB) * 128);
+                const int64_t tiles = ((p.unit_begin[i + 1] - p.unit_begin[i]) * p.rpu + KIE_RB - 1) / KIE_RB;
+                const int64_t need = (nblk > 1 ? tiles * 128 : 0) + (tiles < KIE_NW ? tiles * p.cpb * 128 : 0);
+                part = std::max<int64_t>(part, need);
             }
         }
-        act = (KIE_KBLK / 16) * 128;
+        act = (KIE_KBLK / 16) * 132;   // k-steps of 128 fragment words, 4 words of padding each
     }
     pl.part_floats = int(align_up(size_t(std::max<int64_t>(part, 4)), 4));
     pl.act_floats = int(align_up(act, 8));
@@ -1344,7 +1348,6 @@ kie_status kie_decode_batch(kie_engine* e, const int32_t* tokens, int32_t* next_
 kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint64_t* stamps, size_t cap) {
     kie_status st = ready(e, n);
     if (st != KIE_OK) return st;
-    if (e->batched()) return fail(e, KIE_ERR_UNSUPPORTED, "tracing covers the single-request kernel");
     if (e->cfg.mode != KIE_MODE_PERSISTENT) return fail(e, KIE_ERR_UNSUPPORTED, "tracing needs the persistent mode");
     if ((st = check_tokens(e, &first_token, 1)) != KIE_OK) return st;
     const size_t nphase = size_t(n) * (5 * e->cfg.n_layers + 1) * KIE_PROF_EVENTS * e->G;
@@ -1356,13 +1359,30 @@ kie_status kie_trace_decode(kie_engine* e, int32_t first_token, int32_t n, uint6
     l.n_steps = n;
     l.first_tok = first_token;
     l.pos0 = e->pos;
+    if (e->batched()) {   // every request starts from first_token at its own position
+        e->rpos[e->cur] = e->pos;
+        int32_t h[2 * KIE_MAX_BATCH] = {};
+        for (int b = 0; b < e->plan.nb; ++b) {
+            if (int64_t(e->rpos[b]) + n > e->cfg.max_ctx) { cudaFree(d); return fail(e, KIE_ERR_CTX_OVERFLOW, "request %d overflows", b); }
+            h[b] = first_token;
+            h[KIE_MAX_BATCH + b] = e->rpos[b];
+        }
+        cudaMemcpyAsync(e->dev(e->lay.req), h, sizeof(h), cudaMemcpyHostToDevice, e->stream);
+        l.first_tok = -1;
+        l.pos0 = e->rpos[0];
+    }
     l.out_tokens = reinterpret_cast<int32_t*>(e->dev(e->lay.out_tokens));
     l.prof = d;
     l.prof_slots = d + nphase;
     cudaMemsetAsync(d, 0, need * 8, e->stream);
     st = launch_persistent(e, l);
     if (st == KIE_OK) {
-        e->pos += n;
+        if (e->batched()) {
+            for (int b = 0; b < e->plan.nb; ++b) e->rpos[b] += n;
+            e->pos = e->rpos[e->cur];
+        } else {
+            e->pos += n;
+        }
         st = check_device(e);
     }
     if (st == KIE_OK && cudaMemcpy(stamps, d, need * 8, cudaMemcpyDeviceToHost) != cudaSuccess)

@@ -46,10 +46,12 @@ namespace {
 constexpr int NB = KIE_MAX_BATCH;
 // S.red regions of the batched kernel (after attention's per-warp partials and
 // its 64 floats of scratch)
-constexpr int RED_NORM = NW * (KIE_MAX_HEAD_DIM + 2) + 64;   // [NB][NW] sum of squares of the staged x
+constexpr int RED_NORM = NW * (KIE_MAX_HEAD_DIM + 2) + 64;   // [NB][NW] sums of squares of the staged x
 constexpr int RED_AMV = RED_NORM + NB * NW;                  // [NW][NB] LM argmax values
 constexpr int RED_AMI = RED_AMV + NB * NW;                   // [NW][NB] LM argmax indices
+
 constexpr int KSTEP_WORDS = 128;                             // fragment words per 16 columns (32 lanes x 4)
+constexpr int KSTEP_STRIDE = KSTEP_WORDS + 4;                // their stride in S.act (the pad spreads a warp's stores over the banks)
 
 __device__ __forceinline__ void mma16816(float* d, const uint4& a, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -58,126 +60,123 @@ __device__ __forceinline__ void mma16816(float* d, const uint4& a, uint32_t b0, 
         : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
+// No memory clobber: the ring data it reads is ordered by the (volatile) full-barrier
+// wait before and the release after, and the loads of several k-steps may overlap.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
 }
 
-__device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
-    return uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+// The A-fragment layout of a staged block: per 16 columns (one MMA k-step) 32
+// lanes x 4 words (k-steps KSTEP_STRIDE words apart); lane 4b + t holds {hi, lo} of columns 2t, 2t+1 (words 0, 1)
+// and of columns 8 + 2t, 8 + 2t + 1 (words 2, 3) of request b.  Request b's hi
+// is MMA row b, its lo row 8 + b.  One staging item is one lane's four words:
+// the fp32 values (a0, a1) of columns 2t, 2t+1 and (c0, c1) of 8 + 2t, 8 + 2t + 1.
+__device__ __forceinline__ uint4 frag_quad(float2 a, float2 c) {
+    // packed conversions (two values an instruction); the same roundings as one at a time
+    const __half2 ha = __float22half2_rn(a), hc = __float22half2_rn(c);
+    const float2 fa = __half22float2(ha), fc = __half22float2(hc);
+    const __half2 la = __float22half2_rn(make_float2(a.x - fa.x, a.y - fa.y));
+    const __half2 lc = __float22half2_rn(make_float2(c.x - fc.x, c.y - fc.y));
+    return make_uint4(*reinterpret_cast<const uint32_t*>(&ha), *reinterpret_cast<const uint32_t*>(&la),
+                      *reinterpret_cast<const uint32_t*>(&hc), *reinterpret_cast<const uint32_t*>(&lc));
 }
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ float2 ld_relaxed_f2(const float* p) {
     float2 v;
-    asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
     return v;
 }
 __device__ __forceinline__ bool has_tag2(const float2& v, uint32_t par) {
     return (((__float_as_uint(v.x) ^ par) | (__float_as_uint(v.y) ^ par)) & 1u) == 0u;
 }
 
-// The A-fragment layout of a staged block: per 16 columns (one MMA k-step) 32
-// lanes x 4 words; lane 4b + t holds {hi, lo} of columns 2t, 2t+1 (words 0, 1)
-// and of columns 8 + 2t, 8 + 2t + 1 (words 2, 3) of request b.  Request b's hi
-// is MMA row b, its lo row 8 + b.  One staging item is one lane's four words:
-// the fp32 values (a0, a1) of columns 2t, 2t+1 and (c0, c1) of 8 + 2t, 8 + 2t + 1.
-__device__ __forceinline__ uint4 frag_quad(float2 a, float2 c) {
-    const __half h0 = __float2half_rn(a.x), h1 = __float2half_rn(a.y);
-    const __half h2 = __float2half_rn(c.x), h3 = __float2half_rn(c.y);
-    const __half l0 = __float2half_rn(a.x - __half2float(h0)), l1 = __float2half_rn(a.y - __half2float(h1));
-    const __half l2 = __float2half_rn(c.x - __half2float(h2)), l3 = __float2half_rn(c.y - __half2float(h3));
-    return make_uint4(pack_h2(h0, h1), pack_h2(l0, l1), pack_h2(h2, h3), pack_h2(l2, l3));
-}
-
 // Stage columns [k0, k0 + kb) of every request's input vector into S.act as
-// MMA fragments (kb a multiple of 16).  scaled: x (tagged with parity par, the
+// MMA fragments (kb a multiple of 64).  scaled: x (tagged with parity par, the
 // copy at src, request stride n) or, for the first layer's QKV, the requests'
 // embedding rows, times the RMSNorm gains g; the sums of squares go to
-// S.red[RED_NORM] (set by the first block, added by later ones) and the raw x
-// of rows [cap0, cap0 + ncap) to S.xres (per request).  Otherwise: src (o or a,
-// tagged with parity par) as is.  Items run (k-step, request, lane quarter)
-// with the lane quarter fastest, so a warp's fragment stores are contiguous.
+// S.red[RED_NORM] (per request and warp: set by the first block, added by
+// later ones) and the raw x of rows [cap0, cap0 + ncap) to S.xres (per
+// request).  Otherwise: src (o or a, tagged with parity par) as is.
+// Every CTA reads every request's vector, so the time goes into round trips
+// to L2 under the weight stream's load: all of a block lands with one round of
+// asynchronous 16-byte copies (global -> shared, L2 only, no registers held)
+// into the fragment area itself, k-step by k-step (request b's 16 columns of
+// k-step s in words b*16 .. b*16+15 of its slot).  Then each warp turns its
+// k-steps into fragments in place: lane 4b + t reads columns 2t, 2t+1, 8+2t,
+// 9+2t of request b (re-polling with relaxed loads if a tag is not there
+// yet), and after a warp barrier writes its {hi, lo} words over the slot.
 // Ends with a consumer barrier.
 __device__ void stage_b(const KieParams& P, const KieLaunch& Lc, const Smem& S, const float* src, int n,
                         bool from_emb, const float* g, bool scaled, uint32_t par, int k0, int kb, bool first_blk,
                         int cap0, int ncap, int tid, int cta) {
-    const int nb = P.nb, items = (kb >> 4) * nb * 4;
-    const int warp = tid >> 5, lane = tid & 31;
-    uint4* act = reinterpret_cast<uint4*>(S.act);
-    float ss[NB];
-#pragma unroll
-    for (int b = 0; b < NB; ++b) ss[b] = 0.f;
-    constexpr int U = 8;
-    for (int i0 = tid; i0 < items; i0 += U * NCT) {
-        float2 va[U], vc[U];
-        uint32_t bad = 0;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * NCT;
-            if (i < items) {
-                const int q = i >> 2, b = q % nb, k = k0 + 16 * (q / nb) + 2 * (i & 3);
-                if (from_emb) {
-                    const uint16_t* er = P.emb + size_t(S.clist[b]) * P.d + k;
-                    va[u] = h2_to_f2(*reinterpret_cast<const uint32_t*>(er));
-                    vc[u] = h2_to_f2(*reinterpret_cast<const uint32_t*>(er + 8));
-                } else {
-                    va[u] = ld_relaxed_f2(src + size_t(b) * n + k);
-                    vc[u] = ld_relaxed_f2(src + size_t(b) * n + k + 8);
-                    if (!has_tag2(va[u], par) || !has_tag2(vc[u], par)) bad |= 1u << u;
-                }
-            }
+    const int warp = tid >> 5, lane = tid & 31, nb = P.nb, nks = kb >> 4;
+    uint32_t* act = reinterpret_cast<uint32_t*>(S.act);
+    if (!from_emb) {
+        const int q4 = kb >> 2, nq = nb * q4;   // 16-byte pieces: (request, 4 columns)
+        for (int i = tid; i < nq; i += NCT) {
+            const int b = i / q4, c4 = i - b * q4;
+            cp_async16(act + (c4 >> 2) * KSTEP_STRIDE + b * 16 + (c4 & 3) * 4, src + size_t(b) * n + k0 + 4 * c4);
         }
-        if (bad) {
-            TagWait w;
-            do {
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if ((bad >> u) & 1u) {
-                        const int i = i0 + u * NCT, q = i >> 2, b = q % nb, k = k0 + 16 * (q / nb) + 2 * (i & 3);
-                        va[u] = ld_relaxed_f2(src + size_t(b) * n + k);
-                        vc[u] = ld_relaxed_f2(src + size_t(b) * n + k + 8);
-                        if (has_tag2(va[u], par) && has_tag2(vc[u], par)) bad &= ~(1u << u);
-                    }
-                }
-            } while (bad && w.again(P, Lc, S, cta));
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * NCT;
-            if (i < items) {
-                const int q = i >> 2, b = q % nb, s = q / nb, k = k0 + 16 * s + 2 * (i & 3);
-                float2 a = va[u], c = vc[u];
-                if (scaled) {
-                    const float s2 = (a.x * a.x + a.y * a.y) + (c.x * c.x + c.y * c.y);
-#pragma unroll
-                    for (int bb = 0; bb < NB; ++bb)
-                        if (bb == b) ss[bb] += s2;
-                    if (ncap > 0) {
-                        const float xv[4] = {a.x, a.y, c.x, c.y};
-                        const int kk[4] = {k, k + 1, k + 8, k + 9};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (kk[e] >= cap0 && kk[e] < cap0 + ncap) S.xres[b * KIE_XRES + kk[e] - cap0] = xv[e];
-                    }
-                    const float2 ga = __ldg(reinterpret_cast<const float2*>(g + k));
-                    const float2 gc = __ldg(reinterpret_cast<const float2*>(g + k + 8));
-                    a = make_float2(a.x * ga.x, a.y * ga.y);
-                    c = make_float2(c.x * gc.x, c.y * gc.y);
-                }
-                act[s * (KSTEP_WORDS / 4) + b * 4 + (i & 3)] = frag_quad(a, c);
-            }
-        }
+        cp_async_wait_all();
+        consumer_sync(NCT);
     }
-    if (scaled) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const float t = warp_sum(ss[b]);
-            if (lane == 0 && b < nb) {
-                float* r = S.red + RED_NORM + b * NW + warp;
-                *r = first_blk ? t : *r + t;
+    const int b = lane >> 2, t2 = 2 * (lane & 3);
+    const bool live = b < nb;
+    float ss = 0.f;
+    for (int s = warp; s < nks; s += NW) {
+        const int k = k0 + 16 * s + t2;          // this lane's columns: k, k+1, k+8, k+9
+        uint32_t* blk = act + s * KSTEP_STRIDE;
+        float2 a = make_float2(0.f, 0.f), c = a;
+        if (live) {
+            if (from_emb) {
+                const uint16_t* er = P.emb + size_t(S.clist[b]) * P.d + k;
+                a = h2_to_f2(*reinterpret_cast<const uint32_t*>(er));
+                c = h2_to_f2(*reinterpret_cast<const uint32_t*>(er + 8));
+            } else {
+                a = *reinterpret_cast<const float2*>(blk + b * 16 + t2);
+                c = *reinterpret_cast<const float2*>(blk + b * 16 + 8 + t2);
+                if (!has_tag2(a, par) || !has_tag2(c, par)) {   // not written yet when the copy read it
+                    const float* gp = src + size_t(b) * n + k;
+                    TagWait w;
+                    do {
+                        a = ld_relaxed_f2(gp);
+                        c = ld_relaxed_f2(gp + 8);
+                    } while (!(has_tag2(a, par) && has_tag2(c, par)) && w.again(P, Lc, S, cta));
+                }
             }
+            if (scaled) {
+                ss += (a.x * a.x + a.y * a.y) + (c.x * c.x + c.y * c.y);
+                if (ncap > 0) {
+                    const float xv[4] = {a.x, a.y, c.x, c.y};
+                    const int kk[4] = {k, k + 1, k + 8, k + 9};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (kk[e] >= cap0 && kk[e] < cap0 + ncap) S.xres[b * KIE_XRES + kk[e] - cap0] = xv[e];
+                }
+                const float2 ga = __ldg(reinterpret_cast<const float2*>(g + k));
+                const float2 gc = __ldg(reinterpret_cast<const float2*>(g + k + 8));
+                a = make_float2(a.x * ga.x, a.y * ga.y);
+                c = make_float2(c.x * gc.x, c.y * gc.y);
+            }
+        }
+        const uint4 fq = frag_quad(a, c);
+        __syncwarp();   // every lane has read the slot's fp32 values
+        *reinterpret_cast<uint4*>(blk + lane * 4) = fq;
+    }
+    if (scaled) {   // lanes 4b .. 4b+3 hold request b
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if ((lane & 3) == 0 && live) {
+            float* r = S.red + RED_NORM + b * NW + warp;
+            *r = first_blk ? ss : *r + ss;
         }
     }
     consumer_sync(NCT);
@@ -231,14 +230,14 @@ __device__ __forceinline__ void slot_mma(const uint8_t* slot, int rows_g, int kc
     int s = 0;
 #pragma unroll 4
     for (; s + 1 < nks; s += 2) {
-        kstep(base + uint32_t(s) * kstr, af + s * (KSTEP_WORDS / 4), acc, 0);
-        kstep(base + uint32_t(s + 1) * kstr, af + (s + 1) * (KSTEP_WORDS / 4), acc, 1);
+        kstep(base + uint32_t(s) * kstr, af + s * (KSTEP_STRIDE / 4), acc, 0);
+        kstep(base + uint32_t(s + 1) * kstr, af + (s + 1) * (KSTEP_STRIDE / 4), acc, 1);
     }
-    if (s < nks) kstep(base + uint32_t(s) * kstr, af + s * (KSTEP_WORDS / 4), acc, 0);
+    if (s < nks) kstep(base + uint32_t(s) * kstr, af + s * (KSTEP_STRIDE / 4), acc, 0);
 }
 
 struct EpiB {
-    int type, layer, t;
+    int type, layer, t, phi;
     uint32_t n;                 // write number of the layer (tags)
     uint32_t par_in, par_out;   // O, D: parity of the old and the new x
 };
@@ -309,34 +308,97 @@ __device__ __forceinline__ void lm_row_b(const KieParams& P, const KieLaunch& Lc
     if (y > bv || (y == bv && row < bi)) { bv = y; bi = row; }
 }
 
-// One GEMV phase of the batched kernel: staging block by block, the warp's row
-// tiles on the tensor cores, the epilogue in the lanes holding the results.
-// Returns false on abort.
+// The epilogue of one lane's results for row tile `tile`: request gq's outputs
+// y of rows 2tq, 2tq+1, 8+2tq, 8+2tq+1 of the tile.
+__device__ __forceinline__ void epi_lane_b(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c,
+                                           const EpiB& e, int tile, int lane, const float* y, float& bv, int& bi,
+                                           int cta) {
+    const int gq = lane >> 2, tq = lane & 3;
+    if (gq >= P.nb) return;
+    const int rA = tile * KIE_RB + 2 * tq, rB = rA + 8;   // first rows of this lane's two pairs
+    if (e.type == PH_QKV || e.type == PH_GU) {
+        const float ri = rinv_b(P, S, gq);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int r = p ? rB : rA;
+            if (r < c.rows) {
+                const float ya = y[2 * p] * ri, yb = y[2 * p + 1] * ri;
+                if (e.type == PH_QKV) qkv_unit_b(P, S, c, e, gq, r >> 1, ya, yb);
+                else {
+                    const float av = tag_f32((ya / (1.f + expf(-ya))) * yb, tag_par(e.n));
+#pragma unroll
+                    for (int k = 0; k < KIE_REPL; ++k)
+                        st_relaxed_f32(P.a + (size_t(k) * P.nb + gq) * P.F + c.unit0 + (r >> 1), av);
+                }
+            }
+        }
+    } else if (e.type == PH_LM) {
+        const float ri = rinv_b(P, S, gq);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = (i < 2 ? rA : rB) + (i & 1);
+            if (r < c.rows) lm_row_b(P, Lc, c, gq, r, y[i] * ri, e.t, bv, bi);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = (i < 2 ? rA : rB) + (i & 1);
+            if (r < c.rows) residual_b(P, Lc, S, c, e, gq, r, y[i], cta);
+        }
+    }
+}
+
+// request lane/4's sums of rows 2(lane%4), +1 (group 0) and 8+2(lane%4), +1
+// (group 1) of a tile: hi + lo of the even and odd k-step accumulators
+__device__ __forceinline__ void tile_sums(const float (*acc)[4], float* y) {
+    y[0] = (acc[0][0] + acc[1][0]) + (acc[0][2] + acc[1][2]);
+    y[1] = (acc[0][1] + acc[1][1]) + (acc[0][3] + acc[1][3]);
+    y[2] = (acc[2][0] + acc[3][0]) + (acc[2][2] + acc[3][2]);
+    y[3] = (acc[2][1] + acc[3][1]) + (acc[2][3] + acc[3][3]);
+}
+
+// One GEMV phase of the batched kernel: staging block by block, the row tiles
+// on the tensor cores, the epilogue in the lanes holding the results.
+// A phase with at least NW row tiles gives each warp whole tiles (all chunks
+// of a tile accumulate in its registers).  One with fewer (the QKV, O and
+// down projections' 1-3 tiles a CTA) spreads its (tile, chunk) slots over the
+// warps in slot order; each slot's sums go to S.part and the tile's warp adds
+// them up in chunk order after the block.  Running sums of a phase staged in
+// several blocks stay in S.part as well.  Returns false on abort.
 __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem& S, const Cursor& c, uint32_t& gc,
                             const EpiB& e, const float* src, int n, bool from_emb, const float* g, bool scaled,
                             uint32_t par_src, int cap0, int ncap, int warp, int lane, int tid, int cta) {
-    const int nb = P.nb, nblk = (c.K + KIE_KBLK - 1) / KIE_KBLK, ntiles = (c.rows + KIE_RB - 1) / KIE_RB;
+    const int nblk = (c.K + KIE_KBLK - 1) / KIE_KBLK, ntiles = (c.rows + KIE_RB - 1) / KIE_RB;
+    const int cpb = KIE_KBLK / KIE_KCB;
+    const bool split = ntiles < NW;
     const uint32_t nslot = uint32_t(P.nslot);
-    const int gq = lane >> 2, tq = lane & 3;
-    float bv = -INFINITY;   // LM: this lane's argmax for request gq
+    const int tq = lane & 3;
+    float* run = S.part;                             // [ntiles][128] running sums over blocks
+    float* sp = S.part + (nblk > 1 ? ntiles : 0) * 128;   // split: [ntiles][cpb][128] per-slot sums
+    float bv = -INFINITY;   // LM: this lane's argmax for request lane / 4
     int bi = 0x7fffffff;
     bool ok = true;
     uint32_t jbase = 0;
+    (void)tq;
     for (int blk = 0; blk < nblk; ++blk) {
         const int k0 = blk * KIE_KBLK, kb = min(KIE_KBLK, c.K - k0);
         const int nch = (kb + c.KC - 1) / c.KC;
+        const bool last = blk == nblk - 1;
         // Every warp runs every block's barriers, also after a failed wait (the
         // waits then return at once), so the barrier counts always match.
         if (blk > 0) consumer_sync(NCT);   // every warp is done with the previous block's fragments
         stage_b(P, Lc, S, src, n, from_emb, g, scaled, par_src, k0, kb, blk == 0, cap0, ncap, tid, cta);
-        for (int tile = warp; tile < ntiles && ok; tile += NW) {
+        if (tid == 0 && blk == 0) stamp(P, Lc, e.t, e.phi, 1, cta);
+        const int nsl = ntiles * nch;
+        for (int j = split ? warp : warp * nch; ok && j < nsl; j += split ? NW : NW * nch) {
+            const int tile = j / nch;
             const int rows_g = min(KIE_RB, c.rows - tile * KIE_RB);
             float acc[4][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int a = 0; a < 4; ++a)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-            for (int ch = 0; ch < nch; ++ch) {
+                for (int q = 0; q < 4; ++q) acc[a][q] = 0.f;
+            for (int ch = j % nch; ch < (split ? j % nch + 1 : nch); ++ch) {
                 const uint32_t gidx = gc + jbase + uint32_t(tile * nch + ch);
                 if (!wait_issued(P, Lc, S, gidx, cta, lane) || !warp_wait_full(P, Lc, S, gidx, cta, lane)) {
                     ok = false;
@@ -346,7 +408,7 @@ __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem&
                 const uint32_t slot = gidx % nslot;
                 if (lane == 0) slot_stamp(Lc, cta, gidx, 1);
                 const int kc = min(c.KC, kb - ch * c.KC);
-                const uint4* af = reinterpret_cast<const uint4*>(S.act) + (ch * (c.KC >> 4)) * (KSTEP_WORDS / 4) + lane;
+                const uint4* af = reinterpret_cast<const uint4*>(S.act) + (ch * (c.KC >> 4)) * (KSTEP_STRIDE / 4) + lane;
                 slot_mma(S.ring + size_t(slot) * KIE_SLOT_BYTES, rows_g, kc, af, lane, acc);
                 __syncwarp();
                 if (lane == 0) {
@@ -355,54 +417,45 @@ __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem&
                 }
             }
             if (!ok) break;
-            // request gq's sums of rows 2tq, 2tq+1 (group 0) and 8+2tq, 8+2tq+1 (group 1): hi + lo
             float y[4];
-            y[0] = (acc[0][0] + acc[1][0]) + (acc[0][2] + acc[1][2]);
-            y[1] = (acc[0][1] + acc[1][1]) + (acc[0][3] + acc[1][3]);
-            y[2] = (acc[2][0] + acc[3][0]) + (acc[2][2] + acc[3][2]);
-            y[3] = (acc[2][1] + acc[3][1]) + (acc[2][3] + acc[3][3]);
-            if (nblk > 1) {   // blocks add up in this lane's own part words
-                float* pw = S.part + tile * 128 + lane * 4;
+            tile_sums(acc, y);
+            if (split) {   // this slot's sums; the tile's warp adds the block up below
+                float* pw = sp + ((tile * cpb) + j % nch) * 128 + lane * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pw[i] = y[i];
+                continue;
+            }
+            if (nblk > 1) {   // blocks add up in this lane's own words
+                float* pw = run + tile * 128 + lane * 4;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     y[i] = blk == 0 ? y[i] : pw[i] + y[i];
                     pw[i] = y[i];
                 }
             }
-            if (blk != nblk - 1 || gq >= nb) continue;
-            const int rA = tile * KIE_RB + 2 * tq, rB = rA + 8;   // first rows of this lane's two pairs
-            if (e.type == PH_QKV || e.type == PH_GU) {
-                const float ri = rinv_b(P, S, gq);
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int r = p ? rB : rA;
-                    if (r < c.rows) {
-                        const float ya = y[2 * p] * ri, yb = y[2 * p + 1] * ri;
-                        if (e.type == PH_QKV) qkv_unit_b(P, S, c, e, gq, r >> 1, ya, yb);
-                        else {
-                            const float av = tag_f32((ya / (1.f + expf(-ya))) * yb, tag_par(e.n));
-#pragma unroll
-                            for (int k = 0; k < KIE_REPL; ++k)
-                                st_relaxed_f32(P.a + (size_t(k) * nb + gq) * P.F + c.unit0 + (r >> 1), av);
-                        }
-                    }
-                }
-            } else if (e.type == PH_LM) {
-                const float ri = rinv_b(P, S, gq);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = (i < 2 ? rA : rB) + (i & 1);
-                    if (r < c.rows) lm_row_b(P, Lc, c, gq, r, y[i] * ri, e.t, bv, bi);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = (i < 2 ? rA : rB) + (i & 1);
-                    if (r < c.rows) residual_b(P, Lc, S, c, e, gq, r, y[i], cta);
-                }
-            }
+            if (last) epi_lane_b(P, Lc, S, c, e, tile, lane, y, bv, bi, cta);
         }
         jbase += uint32_t(ntiles * nch);
+        if (split) {
+            consumer_sync(NCT);   // every slot's sums are in
+            for (int tile = warp; tile < ntiles; tile += NW) {
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int ch = 0; ch < nch; ++ch) {
+                    const float* pw = sp + ((tile * cpb) + ch) * 128 + lane * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) y[i] += pw[i];
+                }
+                if (nblk > 1) {
+                    float* pw = run + tile * 128 + lane * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        y[i] = blk == 0 ? y[i] : pw[i] + y[i];
+                        pw[i] = y[i];
+                    }
+                }
+                if (last && ld_volatile_i32(&S.flags[0]) == 0) epi_lane_b(P, Lc, S, c, e, tile, lane, y, bv, bi, cta);
+            }
+        }
     }
     gc += c.nslots;
     if (!ok) S.flags[0] = 1;
@@ -413,9 +466,9 @@ __device__ bool run_phase_b(const KieParams& P, const KieLaunch& Lc, const Smem&
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
             if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
         }
-        if (tq == 0) {
-            S.red[RED_AMV + warp * NB + gq] = bv;
-            reinterpret_cast<int*>(S.red)[RED_AMI + warp * NB + gq] = bi;
+        if ((lane & 3) == 0) {
+            S.red[RED_AMV + warp * NB + (lane >> 2)] = bv;
+            reinterpret_cast<int*>(S.red)[RED_AMI + warp * NB + (lane >> 2)] = bi;
         }
     }
     consumer_sync(NCT);
@@ -529,6 +582,7 @@ __device__ void consumer_b(const KieParams& P, const KieLaunch& Lc, const Smem& 
             e.type = type;
             e.layer = layer;
             e.t = t;
+            e.phi = phi;
             e.n = tn;
             e.par_in = type == PH_O ? 0u : 1u;
             e.par_out = type == PH_O ? 1u : 0u;
@@ -568,7 +622,7 @@ __global__ void __launch_bounds__(KIE_THREADS, 1) kie_decode_batch_kernel(const 
     const int cta = blockIdx.x;
     if (kie_smem_layout(P.part_floats, P.act_floats, P.nslot, P.nb).total > dynamic_smem_size() ||
         P.nslot < NW || P.nslot > KIE_MAX_SLOTS || P.G > KIE_MAX_GRID || P.nb < 1 || P.nb > KIE_MAX_BATCH ||
-        P.nb * P.H > P.G || P.act_floats < (KIE_KBLK / 16) * KSTEP_WORDS) {
+        P.nb * P.H > P.G || P.act_floats < (KIE_KBLK / 16) * KSTEP_STRIDE) {
         if (threadIdx.x == 0) set_error(P, KERR_SMEM, cta);
         return;
     }

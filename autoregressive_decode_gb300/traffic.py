@@ -72,3 +72,13 @@ def launch_bytes(w, first_pos: int, n_steps: int) -> int:
     """Bytes of n_steps consecutive decode steps, the first at position
     first_pos (so it attends first_pos + 1 positions)."""
     return sum(step_bytes(w, p + 1)["total"] for p in range(first_pos, first_pos + n_steps))
+
+
+def batch_launch_bytes(w, first_pos, n_steps: int) -> int:
+    """Bytes of n_steps steps of a batched engine: every weight once per step
+    and each request's own K and V; first_pos: each request's first position."""
+    total = 0
+    for t in range(n_steps):
+        total += step_bytes(w, first_pos[0] + t + 1)["weights"]
+        total += sum(step_bytes(w, p + t + 1)["kv"] for p in first_pos)
+    return total

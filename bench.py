@@ -20,7 +20,7 @@ Multi-GPU (torchrun): independent replicas, one engine per rank, no
 collective on the data path; value = tokens of all ranks / max rank time.
 
 workloads  (1 GPU, default run) a compact record for each of the other
-        workloads -- 1.8B with FP8 E4M3 weights, 1.8B with NVFP4 weights, 1.8B with
+        workloads -- 1.8B decoding 8 requests at once (low-batch decode), 1.8B with FP8 E4M3 weights, 1.8B with NVFP4 weights, 1.8B with
         INT4 q/k/v and FFN weights over an E5M2 cache, 1.8B over a 32K FP8-E5M2 cache,
         1.8B over an 8K adaptive uint8 cache, 7B with INT4 FFN -- with its
         decode tokens/s, roofline fraction and a CPU-oracle figure.
@@ -76,8 +76,9 @@ def workload_desc(w: S.Workload) -> str:
     ffn = f"{names[w.ffn_wdtype]} FFN"
     attn = ("" if w.attn_wdtype == "fp16" else ", INT4 g128 q/k/v (fp16 O and LM head)" if w.attn_wdtype == "int4_g128"
             else f", {names[w.attn_wdtype]} q/k/v/o and LM head")
+    req = f", {w.batch} requests decoded together (each its own context)" if w.batch > 1 else ""
     return (f"{w.name}: {w.n_layers} layers, d {w.d_model}, {w.n_heads}x{w.head_dim} heads, FFN {w.ffn_dim}, "
-            f"vocab {w.vocab}, {ctx}, {w.decode_steps} greedy decode steps, {w.kv_dtype} KV, {ffn}{attn}")
+            f"vocab {w.vocab}, {ctx}, {w.decode_steps} greedy decode steps, {w.kv_dtype} KV, {ffn}{attn}{req}")
 
 
 def peaks():
@@ -308,11 +309,75 @@ def time_decode(eng, torch, stream, first: int, p0: int, n_dec: int, steps: int,
     return statistics.mean(a.elapsed_time(b) for a, b in per)
 
 
+def time_decode_batch(eng, torch, stream, firsts, p0: int, n_dec: int, steps: int, warmup: int, device):
+    """Mean ms of `steps` device-timed batched launches of n_dec tokens per
+    request, every request restarting from position p0."""
+    B = len(firsts)
+    d_tok = torch.empty((n_dec, B), dtype=torch.int32, device=device)
+
+    def restart():
+        for b in range(B):
+            eng.select_request(b)
+            eng.set_pos(p0)
+
+    for _ in range(warmup):
+        restart()
+        eng.generate_greedy_batch_device(firsts, n_dec, d_tok)
+    eng.sync()
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in per:
+        restart()
+        a.record(stream)
+        eng.generate_greedy_batch_device(firsts, n_dec, d_tok)
+        b.record(stream)
+    eng.sync()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in per)
+
+
+def batched_record(args, local, kie, torch, w, weights, peak, peak_kind):
+    """Low-batch decode: w.batch requests, each over its own synthetic context
+    (request b's KV and first token from its own seeds), decoded together."""
+    B, p0, n_dec = w.batch, w.context_len, w.decode_steps
+    cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, p0 + n_dec,
+                          w.rms_eps, w.rope_theta, w.kv_dtype, w.ffn_wdtype, "persistent", local,
+                          attn_wdtype=w.attn_wdtype, batch=B)
+    stream = torch.cuda.Stream(device=local)
+    eng = kie.Engine(cfg, stream=stream)
+    eng.load_weights(weights)
+    for b in range(B):
+        eng.select_request(b)
+        for layer in range(w.n_layers):
+            k, v = S.gen_kv(w, layer, seed=w.request_seed(w.kv_seed, b))
+            eng.set_kv(layer, k, v)
+        eng.set_pos(p0)
+    firsts = [S.gen_first_token(w, seed=w.request_seed(w.prompt_seed, b)) for b in range(B)]
+    ms = time_decode_batch(eng, torch, stream, firsts, p0, n_dec, 3, 2, f"cuda:{local}")
+    eng.close()
+    bpl = float(traffic.batch_launch_bytes(w, [p0] * B, n_dec))
+    achieved = bpl / (ms / 1e3) / 1e9
+    rec = {"context": f"synthetic, {p0} positions per request (own seeds)", "requests": B,
+           "value": B * n_dec / (ms / 1e3), "unit": "tokens/s (all requests)",
+           "per_request_tokens_per_s": n_dec / (ms / 1e3), "steps": 3, "warmup": 2, "ms_per_step": ms,
+           "decode_tokens_per_step": B * n_dec, "positions": f"{p0}..{p0 + n_dec - 1} in every request",
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "peak_source": peak_kind, "kernel": "kie_decode_batch_kernel",
+                        "algorithmic_bytes_per_launch": bpl, "launch_ms": ms,
+                        "bytes": "every weight once per step plus each request's own K and V"}}
+    if not args.no_cpu_baseline:
+        cb = cpu_baseline_by_depth(w.with_(batch=1), weights, p0)
+        cb["sample"] += "; per request: the oracle decodes the requests one after another, so its rate over " \
+                        "all requests is the same"
+        rec["cpu_baseline"] = cb
+    return rec
+
+
 # The other workloads (a compact record each): their decode steps over the
 # context the workload names, prefilled on the GPU where the tensor-core path
 # covers it and otherwise (uint8 cache; the 7B model, whose decode bytes do not
 # depend on how its 4,096-position context was made) a synthetic one.
-EXTRA = ("1p8b_fp8", "1p8b_nvfp4", "1p8b_hpi", "1p8b_32k", "1p8b_u8", "7b_int4")
+EXTRA = ("1p8b_b8", "1p8b_fp8", "1p8b_nvfp4", "1p8b_hpi", "1p8b_32k", "1p8b_u8", "7b_int4")
 
 
 def extra_workloads(args, local, kie, torch, weights_1p8b):
@@ -329,6 +394,10 @@ def extra_workloads(args, local, kie, torch, weights_1p8b):
             else:
                 w7 = w7 or S.gen_weights(w)
                 weights = w7
+            if w.batch > 1:
+                rec.update(batched_record(args, local, kie, torch, w, weights, peak, peak_kind))
+                out[name] = rec
+                continue
             synth = w.kv_source == "synthetic" or w.ffn_wdtype == "int4_g128"
             if synth and w.kv_source == "prefill":
                 w = w.with_(kv_source="synthetic", context_len=w.prompt_len, prompt_len=0)
@@ -379,6 +448,18 @@ def main():
     w = S.WORKLOADS[args.workload]
     if args.layers:
         w = w.with_(n_layers=args.layers)
+    if w.batch > 1 and args.impl != "reference":
+        # the batched workload is reported as a record of the default run
+        if not args.no_workloads:
+            raise SystemExit(f"{w.name}: run the default workload; its record is under 'workloads'")
+        import torch
+
+        from autoregressive_decode_gb300 import kie
+        torch.cuda.set_device(0)
+        peak, kind = peaks()
+        rec = batched_record(args, 0, kie, torch, w, S.gen_weights(w), peak, kind)
+        print(json.dumps({"workload": workload_desc(w), **rec}))
+        return
     if args.impl == "reference":
         return run_reference(args, w)
     import torch

@@ -110,6 +110,7 @@ class Workload:
     context_len: int = 0            # synthetic KV positions (kv_source == "synthetic")
     decode_steps: int = 32
     kv_source: str = "prefill"      # "prefill" | "synthetic"
+    batch: int = 1                  # requests decoded together (batched engine); each has its own seeds
 
     @property
     def start_pos(self) -> int:
@@ -134,6 +135,11 @@ class Workload:
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
 
+    def request_seed(self, base: int, b: int) -> int:
+        """Seed of request b's prompt / first token (base = prompt_seed) or
+        synthetic KV (base = kv_seed); request 0 keeps the workload's own."""
+        return base + 7919 * b
+
 
 WORKLOADS = {
     "tiny": Workload("tiny", 0, 2, 256, 4, 64, 1024, 4096, prompt_len=16, decode_steps=32),
@@ -154,6 +160,10 @@ WORKLOADS = {
     # fp16 O projection and LM head, an FP8 E5M2 KV cache
     "1p8b_hpi": Workload("1p8b_hpi", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="int4_g128",
                          attn_wdtype="int4_g128", kv_dtype="fp8_e5m2", prompt_len=2048, decode_steps=256),
+    # the 1.8B fp16 model decoding 8 requests at once (low-batch decode), each over
+    # its own synthetic 2048-position context, 256 steps
+    "1p8b_b8": Workload("1p8b_b8", 1, 25, 2048, 16, 128, 8192, 32000, kv_source="synthetic", prompt_len=0,
+                        context_len=2048, decode_steps=256, batch=8),
 }
 
 # tensor ids for the generator: per layer base 64*(layer+1) + slot

@@ -10,6 +10,9 @@ greedy chain), against the CPU oracle.
   1p8b_nvfp4  every GEMV matrix in NVFP4, the same context, 32 steps.
   1p8b_hpi  INT4 q/k/v and FFN matrices with an E5M2 cache, the same context
             length, 32 steps.
+  1p8b_b8   8 requests decoded together (batched engine), each over its own
+            synthetic 2,048-position context, 16 free-running steps in one
+            launch, every request against its own oracle.
   1p8b_32k  FP8-E5M2 cache over a 32,768-position synthetic context (decode-only
             parity: the same fp16 K/V loaded into both sides), 32 steps.
   1p8b_u8   adaptive-range uint8 cache over the 8,192-position synthetic context
@@ -117,6 +120,39 @@ def test_1p8b_hpi_int4_qkv_decode():
     first = S.gen_first_token(w)
     toks, logs = _generate_on_device(e, first, n)
     check_free_running(o, first, toks, logs, tol_for(w))
+
+
+def test_1p8b_batched_decode():
+    """The bench's batched launch at full size: 8 requests, each over its own
+    synthetic 2,048-position context, 16 greedy steps in one launch."""
+    torch = pytest.importorskip("torch")
+    n = 16
+    w = S.WORKLOADS["1p8b_b8"]
+    B, p0 = w.batch, w.context_len
+    weights = S.gen_weights(w)
+    cfg = kie.make_config(w.n_layers, w.d_model, w.n_heads, w.head_dim, w.ffn_dim, w.vocab, p0 + n, w.rms_eps,
+                          w.rope_theta, w.kv_dtype, w.ffn_wdtype, "persistent", batch=B)
+    e = kie.Engine(cfg)
+    e.load_weights(weights)
+    oracles = []
+    for b in range(B):
+        o = O.OracleDecoder(w, weights, max_ctx=p0 + n)
+        e.select_request(b)
+        for layer in range(w.n_layers):
+            k, v = S.gen_kv(w, layer, seed=w.request_seed(w.kv_seed, b))
+            e.set_kv(layer, k, v)
+            o.set_kv(layer, k, v)
+        e.set_pos(p0)
+        o.pos = p0
+        oracles.append(o)
+    firsts = [S.gen_first_token(w, seed=w.request_seed(w.prompt_seed, b)) for b in range(B)]
+    d_tok = torch.zeros((n, B), dtype=torch.int32, device="cuda")
+    d_log = torch.zeros((n, B, w.vocab), dtype=torch.float32, device="cuda")
+    e.generate_greedy_batch_device(firsts, n, d_tok, d_log)
+    e.sync()
+    toks, logs = d_tok.cpu().numpy(), d_log.cpu().numpy()
+    for b in range(B):
+        check_free_running(oracles[b], firsts[b], toks[:, b], logs[:, b], tol_for(w))
 
 
 def test_1p8b_32k_fp8_decode():

@@ -34,3 +34,14 @@ def test_1p8b_weight_bytes():
     # table (one row), i.e. 3,486,728,192 bytes of fp16 weights and gains
     w = S.WORKLOADS["1p8b"]
     assert traffic.step_bytes(w, 1)["weights"] == 3_486_728_192
+
+
+def test_batch_launch_bytes():
+    """A batched step reads the weights once and every request's own cache."""
+    w = S.WORKLOADS["1p8b_b8"]
+    pos = [2048, 100, 700]
+    total = traffic.batch_launch_bytes(w, pos, 3)
+    ref = sum(O.decode_bytes_per_token(w, pos[0] + t + 1)["weights"]
+              + sum(O.decode_bytes_per_token(w, p + t + 1)["kv"] for p in pos) for t in range(3))
+    assert total == ref
+    assert traffic.batch_launch_bytes(w, [2048], 4) == traffic.launch_bytes(w, 2048, 4)
