@@ -101,9 +101,9 @@ __device__ __forceinline__ bool has_tag2(const float2& v, uint32_t par) {
 // Stage columns [k0, k0 + kb) of every request's input vector into S.act as
 // MMA fragments (kb a multiple of 64).  scaled: x (tagged with parity par, the
 // copy at src, request stride n) or, for the first layer's QKV, the requests'
-// embedding rows, times the RMSNorm gains g; the sums of squares go to
-// S.red[RED_NORM] (per request and warp: set by the first block, added by
-// later ones) and the raw x of rows [cap0, cap0 + ncap) to S.xres (per
+// embedding rows, times the RMSNorm gains g (staged in S.wsc); the sums of
+// squares go to S.red[RED_NORM] (per request and warp: set by the first
+// block, added by later ones) and the raw x of rows [cap0, cap0 + ncap) to S.xres (per
 // request).  Otherwise: src (o or a, tagged with parity par) as is.
 // Every CTA reads every request's vector, so the time goes into round trips
 // to L2 under the weight stream's load: all of a block lands with one round of
@@ -119,12 +119,14 @@ __device__ void stage_b(const KieParams& P, const KieLaunch& Lc, const Smem& S, 
                         int cap0, int ncap, int tid, int cta) {
     const int warp = tid >> 5, lane = tid & 31, nb = P.nb, nks = kb >> 4;
     uint32_t* act = reinterpret_cast<uint32_t*>(S.act);
-    if (!from_emb) {
-        const int q4 = kb >> 2, nq = nb * q4;   // 16-byte pieces: (request, 4 columns)
+    {
+        const int q4 = kb >> 2, nq = from_emb ? 0 : nb * q4;   // 16-byte pieces: (request, 4 columns)
         for (int i = tid; i < nq; i += NCT) {
             const int b = i / q4, c4 = i - b * q4;
             cp_async16(act + (c4 >> 2) * KSTEP_STRIDE + b * 16 + (c4 & 3) * 4, src + size_t(b) * n + k0 + 4 * c4);
         }
+        if (scaled)   // the block's gains travel in the same round, into S.wsc
+            for (int i = tid; i < q4; i += NCT) cp_async16(S.wsc + 4 * i, g + k0 + 4 * i);
         cp_async_wait_all();
         consumer_sync(NCT);
     }
@@ -161,8 +163,8 @@ __device__ void stage_b(const KieParams& P, const KieLaunch& Lc, const Smem& S, 
                     for (int e = 0; e < 4; ++e)
                         if (kk[e] >= cap0 && kk[e] < cap0 + ncap) S.xres[b * KIE_XRES + kk[e] - cap0] = xv[e];
                 }
-                const float2 ga = __ldg(reinterpret_cast<const float2*>(g + k));
-                const float2 gc = __ldg(reinterpret_cast<const float2*>(g + k + 8));
+                const float2 ga = *reinterpret_cast<const float2*>(S.wsc + (k - k0));
+                const float2 gc = *reinterpret_cast<const float2*>(S.wsc + (k - k0) + 8);
                 a = make_float2(a.x * ga.x, a.y * ga.y);
                 c = make_float2(c.x * gc.x, c.y * gc.y);
             }

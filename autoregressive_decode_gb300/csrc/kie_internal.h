@@ -83,7 +83,9 @@ KIE_HD inline KieSmemLayout kie_smem_layout(int part_floats, int act_floats, int
     l.rope = o;  o += req * KIE_MAX_HEAD_DIM * 4;     // cos/sin of the step's position, [req][2][hd/2]
     l.red = o;   o += (KIE_NW * (KIE_MAX_HEAD_DIM + 2) + 64 + (nb > 0 ? 3 * KIE_MAX_BATCH * KIE_NW : 0)) * 4;
     l.xres = o;  o += req * KIE_XRES * 4;
-    l.wsc = o;   o += nb > 0 ? 0u : uint32_t(part_floats) * 4;   // FP8 row scales of the phase (part_floats >= rows)
+    // FP8 row scales of the phase (part_floats >= rows); batched: the staged block's RMSNorm gains
+    l.wsc = nb > 0 ? kie_align(o, 16) : o;
+    o = l.wsc + (nb > 0 ? uint32_t(KIE_KBLK) * 4 : uint32_t(part_floats) * 4);
     l.cnt = o;   o += nb > 0 ? 0u : (uint32_t(part_floats) / KIE_R + 4) * 4;   // per row group: chunks done (>= groups)
     l.part = o;  o += uint32_t(part_floats) * 4;
     l.act = kie_align(o, 16); o = l.act + uint32_t(act_floats) * 4;
