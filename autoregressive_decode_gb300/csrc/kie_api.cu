@@ -60,6 +60,10 @@ extern "C" cudaError_t kie_launch_quant_u8(const uint16_t* src, int n_seg, int64
                                            int64_t dst_row, float* scale, int32_t* zp, int64_t meta_stride,
                                            cudaStream_t st);
 extern "C" cudaError_t kie_launch_e5m2(const uint16_t* x, size_t n, uint8_t* out, cudaStream_t st);
+extern "C" cudaError_t kie_launch_kv_slice(const uint16_t* src, int p0, int p1, int H, int hd, int max_ctx, float* sc,
+                                           uint32_t* mx, int j, uint8_t* dst, cudaStream_t st);
+extern "C" cudaError_t kie_launch_kv_rescan(const uint8_t* kc, const uint8_t* vc, uint32_t* mx, int L, int H, int hd,
+                                            int max_ctx, int nslice, int pos, cudaStream_t st);
 extern "C" cudaError_t kie_launch_set_kv(const uint16_t* src, int n, int H, int hd, int max_ctx, int fmt,
                                          uint8_t* dst, uint16_t* tail, int first_tail, cudaStream_t st);
 
@@ -98,6 +102,8 @@ struct Layout {  // byte offsets into the workspace
     size_t wstream, wstream_bytes;
     size_t emb, norms, inv_freq;
     size_t kc, vc, kv_bytes, tail, seg_scale, seg_zp;
+    size_t kv_sc, kv_mx;              // scaled E5M2: [L][2][nslice] slice scales and running maxima
+    int nslice;
     // FP8 row scales (floats): per layer [QKV | O | GU | D] in each phase's row order, then the LM head
     size_t wsc, wsc_layer, wsc_off[PH_NTYPES];
     size_t x, kcur, vcur, zero_bytes, q, a, o, att_part, par_bytes, amax_val, amax_idx, ctl;
@@ -120,10 +126,12 @@ int pad256(int n) { return (n + 255) / 256 * 256; }
 bool scaled_fmt(int32_t wdtype) { return wdtype == KIE_W_FP8_E4M3 || wdtype == KIE_W_NVFP4; }
 
 // The tensor-core prefill covers non-INT4 weights with an fp16 or E5M2 cache
-// (the uint8 cache changes stored values when a segment completes, and INT4
-// weights have no fp16 copy); every GEMM K must be a multiple of 64.
+// (the uint8 cache changes stored values when a segment completes, the scaled
+// E5M2 cache's slice scales follow each other, and INT4 weights have no fp16
+// copy); every GEMM K must be a multiple of 64.
 bool prefill_tc_ok(const kie_config& c) {
     return c.ffn_wdtype != KIE_W_INT4_G128 && c.attn_wdtype != KIE_W_INT4_G128 && c.kv_dtype != KIE_KV_U8_ADAPTIVE &&
+           c.kv_dtype != KIE_KV_FP8_E5M2_SCALED &&
            c.d_model % 64 == 0 &&
            (c.n_heads * c.head_dim) % 64 == 0 && c.ffn_dim % 64 == 0;
 }
@@ -146,7 +154,7 @@ bool valid_cfg(const kie_config* c, std::string& why) {
     }
     if (c->head_dim != 64 && c->head_dim != 128) { why = "head_dim must be 64 or 128"; return false; }
     if (c->d_model % 8 || c->ffn_dim % 8 || (c->n_heads * c->head_dim) % 8) { why = "dims must be multiples of 8"; return false; }
-    if (c->kv_dtype < 0 || c->kv_dtype > 2) { why = "bad kv_dtype"; return false; }
+    if (c->kv_dtype < 0 || c->kv_dtype > 3) { why = "bad kv_dtype"; return false; }
     if (c->ffn_wdtype < 0 || c->ffn_wdtype > 3) { why = "bad ffn_wdtype"; return false; }
     if (c->attn_wdtype < 0 || c->attn_wdtype > 3) { why = "bad attn_wdtype"; return false; }
     if (c->attn_wdtype == KIE_W_INT4_G128 && c->d_model % 128) {
@@ -167,7 +175,10 @@ bool valid_cfg(const kie_config* c, std::string& why) {
     if (c->batch > 1) {
         if (c->mode != KIE_MODE_PERSISTENT) { why = "a batched engine needs the persistent mode"; return false; }
         if (c->attn_wdtype != KIE_W_FP16 || c->ffn_wdtype != KIE_W_FP16) { why = "a batched engine needs fp16 weights"; return false; }
-        if (c->kv_dtype == KIE_KV_U8_ADAPTIVE) { why = "a batched engine needs an fp16 or E5M2 cache"; return false; }
+        if (c->kv_dtype == KIE_KV_U8_ADAPTIVE || c->kv_dtype == KIE_KV_FP8_E5M2_SCALED) {
+            why = "a batched engine needs an fp16 or E5M2 cache";
+            return false;
+        }
         if (c->d_model % 64 || c->ffn_dim % 64 || (c->n_heads * c->head_dim) % 64) {
             why = "a batched engine needs d_model, ffn_dim and n_heads*head_dim multiples of 64";
             return false;
@@ -268,6 +279,7 @@ void build_plan(const kie_config& c, int G, Plan& pl) {
     const int64_t min_heads_cta = std::max(1, G / H);
     const int64_t max_seg = (int64_t(c.max_ctx) + min_heads_cta - 1) / min_heads_cta + 2;
     part = std::max<int64_t>(part, 4 * (max_seg / KIE_SEG + 2));
+    part = std::max<int64_t>(part, 2 * (max_seg / KIE_KV_SLICE + 2));   // scaled E5M2: the chunk's slice scales
     part = std::max<int64_t>(part, G + H);   // O-phase combine: per-CTA weights and per-head 1/L
     int act = std::max({d, F, H * hd, int(std::min<int64_t>(max_seg, 1 << 30))});
     if (bat) {
@@ -325,6 +337,10 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
     L.tail = take(u8 ? size_t(c.n_layers) * 2 * H * KIE_SEG * hd * 2 : 0);
     L.seg_scale = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
     L.seg_zp = take(u8 ? size_t(c.n_layers) * 2 * H * L.nseg * 4 : 0);
+    const bool e5s = c.kv_dtype == KIE_KV_FP8_E5M2_SCALED;
+    L.nslice = (c.max_ctx + KIE_KV_SLICE - 1) / KIE_KV_SLICE;
+    L.kv_sc = take(e5s ? size_t(c.n_layers) * 2 * L.nslice * 4 : 0);
+    L.kv_mx = take(e5s ? size_t(c.n_layers) * 2 * L.nslice * 4 : 0);
     // tagged activations, reset before each launch sequence (reset_tags):
     // x .. vcur to zero, q .. att_part to one parity
     L.x = take(size_t(KIE_REPL) * nbq * d * 4);
@@ -455,6 +471,23 @@ kie_status check_device(kie_engine* e) {
         e->sticky = e->h_ctl->err;
         return fail(e, KIE_ERR_DEVICE_TIMEOUT, "device error %d (info %d)", e->h_ctl->err, e->h_ctl->err_info);
     }
+    return KIE_OK;
+}
+
+// Scaled E5M2 cache, emptied: every slice's maximum zero, slice 0 of every
+// (layer, K or V) at the configured initial scale (the xAI page's hpi_config
+// values 0.0039 for K and 0.0042 for V unless the config gives others).
+kie_status init_kv_scales(kie_engine* e) {
+    const kie_config& c = e->cfg;
+    if (c.kv_dtype != KIE_KV_FP8_E5M2_SCALED) return KIE_OK;
+    const Layout& L = e->lay;
+    const float s0[2] = {c.kv_scale_k > 0.f ? c.kv_scale_k : 0.0039f, c.kv_scale_v > 0.f ? c.kv_scale_v : 0.0042f};
+    std::vector<float> sc(size_t(c.n_layers) * 2 * L.nslice, 0.f);
+    for (int l = 0; l < c.n_layers; ++l)
+        for (int kv = 0; kv < 2; ++kv) sc[(size_t(l) * 2 + kv) * L.nslice] = s0[kv];
+    KIE_CUDA(e, cudaMemcpyAsync(e->dev(L.kv_sc), sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, e->stream));
+    KIE_CUDA(e, cudaMemsetAsync(e->dev(L.kv_mx), 0, sc.size() * 4, e->stream));
+    KIE_CUDA(e, cudaStreamSynchronize(e->stream));
     return KIE_OK;
 }
 
@@ -820,6 +853,7 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
               cudaMemsetAsync(e->dev(L.x), 0, L.plan_i32 - L.x, st) == cudaSuccess &&
               cudaStreamSynchronize(st) == cudaSuccess;
     if (!ok) { kie_destroy(e); return fail(nullptr, KIE_ERR_CUDA, "initialising device tables failed"); }
+    if (init_kv_scales(e) != KIE_OK) { kie_destroy(e); return fail(nullptr, KIE_ERR_CUDA, "initialising KV scales failed"); }
 
     KieParams& P = e->P;
     P.L = cfg->n_layers; P.d = cfg->d_model; P.H = cfg->n_heads; P.hd = cfg->head_dim; P.F = cfg->ffn_dim;
@@ -852,6 +886,9 @@ kie_status kie_create(const kie_config* cfg, void* workspace, size_t ws_bytes, v
     P.tail = reinterpret_cast<uint16_t*>(e->dev(L.tail));
     P.seg_scale = reinterpret_cast<float*>(e->dev(L.seg_scale));
     P.seg_zp = reinterpret_cast<int32_t*>(e->dev(L.seg_zp));
+    P.kv_sc = reinterpret_cast<float*>(e->dev(L.kv_sc));
+    P.kv_mx = reinterpret_cast<uint32_t*>(e->dev(L.kv_mx));
+    P.nslice = L.nslice;
     P.x = reinterpret_cast<float*>(e->dev(L.x));
     P.q = reinterpret_cast<float*>(e->dev(L.q));
     P.a = reinterpret_cast<float*>(e->dev(L.a));
@@ -1177,6 +1214,7 @@ kie_status kie_load_weights(kie_engine* e, const kie_weights* w) {
     e->pos = 0;
     std::fill(std::begin(e->rpos), std::end(e->rpos), 0);
     e->sticky = 0;
+    if ((result = init_kv_scales(e)) != KIE_OK) return result;
     return set_ctl(e, 0, 0, true);
 }
 
@@ -1402,6 +1440,8 @@ kie_status kie_reset(kie_engine* e) {
     e->sticky = 0;
     e->pos = 0;
     std::fill(std::begin(e->rpos), std::end(e->rpos), 0);
+    kie_status st0 = init_kv_scales(e);
+    if (st0 != KIE_OK) return st0;
     KIE_CUDA(e, reset_tags(e->cfg, e->dev(e->lay.x), e->lay.zero_bytes, e->dev(e->lay.q), e->lay.par_bytes, 0,
                            e->stream));
     return set_ctl(e, 0, 0, true);
@@ -1413,6 +1453,12 @@ kie_status kie_set_pos(kie_engine* e, int32_t pos) {
     if (!e) return fail(nullptr, KIE_ERR_INVALID_ARG, "engine is NULL");
     if (pos < 0 || pos > e->cfg.max_ctx) return fail(e, KIE_ERR_INVALID_ARG, "pos %d outside [0, %d]", pos, e->cfg.max_ctx);
     e->pos = pos;
+    if (e->cfg.kv_dtype == KIE_KV_FP8_E5M2_SCALED) {
+        // positions >= pos leave the cache: pos's slice keeps the maximum of what stays
+        const kie_config& c = e->cfg;
+        KIE_CUDA(e, kie_launch_kv_rescan(e->dev(e->lay.kc), e->dev(e->lay.vc), reinterpret_cast<uint32_t*>(e->dev(e->lay.kv_mx)),
+                                         c.n_layers, c.n_heads, c.head_dim, c.max_ctx, e->lay.nslice, pos, e->stream));
+    }
     return set_ctl(e, 0, pos, false);
 }
 
@@ -1466,8 +1512,16 @@ kie_status kie_set_kv(kie_engine* e, int32_t layer, const uint16_t* k_fp16, cons
         if (cudaMemcpyAsync(stage, src, elems * 2, cudaMemcpyHostToDevice, st) != cudaSuccess) { result = fail(e, KIE_ERR_CUDA, "upload failed"); break; }
         const size_t esz = c.kv_dtype == KIE_KV_FP16 ? 2 : 1;
         uint8_t* dst = base + size_t(layer) * H * c.max_ctx * hd * esz;
-        cudaError_t r;
-        if (c.kv_dtype != KIE_KV_U8_ADAPTIVE) {
+        cudaError_t r = cudaSuccess;
+        if (c.kv_dtype == KIE_KV_FP8_E5M2_SCALED) {
+            // slice by slice: each slice's scale comes from the slice before it
+            const size_t ent = (size_t(layer) * 2 + kv) * L.nslice;
+            float* sc = reinterpret_cast<float*>(e->dev(L.kv_sc)) + ent;
+            uint32_t* mx = reinterpret_cast<uint32_t*>(e->dev(L.kv_mx)) + ent;
+            for (int j = 0; j * KIE_KV_SLICE < n && r == cudaSuccess; ++j)
+                r = kie_launch_kv_slice(stage, j * KIE_KV_SLICE, std::min(n, (j + 1) * KIE_KV_SLICE), H, hd, c.max_ctx,
+                                        sc, mx, j, dst, st);
+        } else if (c.kv_dtype != KIE_KV_U8_ADAPTIVE) {
             r = kie_launch_set_kv(stage, n, H, hd, c.max_ctx, c.kv_dtype == KIE_KV_FP16 ? 0 : 1, dst, nullptr, 0, st);
         } else {
             const int full = n / KIE_SEG;
@@ -1505,6 +1559,12 @@ kie_status kie_read_kv(kie_engine* e, int32_t layer, int32_t which, int32_t p0, 
     for (int h = 0; h < H; ++h)
         KIE_CUDA(e, cudaMemcpy(static_cast<uint8_t*>(out) + size_t(h) * n * hd * esz,
                                base + (size_t(h) * c.max_ctx + p0) * hd * esz, size_t(n) * hd * esz, cudaMemcpyDeviceToHost));
+    if (c.kv_dtype == KIE_KV_FP8_E5M2_SCALED && scale) {   // the scales of the slices [p0, p0 + n) meets
+        const int s0 = p0 / KIE_KV_SLICE, s1 = (p0 + n + KIE_KV_SLICE - 1) / KIE_KV_SLICE;
+        if (s1 > s0)
+            KIE_CUDA(e, cudaMemcpy(scale, e->dev(L.kv_sc) + ((size_t(layer) * 2 + which) * L.nslice + s0) * 4,
+                                   size_t(s1 - s0) * 4, cudaMemcpyDeviceToHost));
+    }
     if (c.kv_dtype == KIE_KV_U8_ADAPTIVE) {
         const int s0 = p0 / KIE_SEG, s1 = (p0 + n + KIE_SEG - 1) / KIE_SEG;
         for (int h = 0; h < H; ++h) {

@@ -97,6 +97,9 @@ __device__ void consumer(const KieParams& P, const KieLaunch& Lc, const Smem& S,
                     const float* g = type == PH_QKV ? gains : type == PH_GU ? gains + P.d
                                                                              : P.norms + size_t(P.L) * 2 * P.d;
                     if (type == PH_QKV) rope_table(P, S, pos, tid);
+                    // scaled E5M2 cache: the K and V scales this position is stored with
+                    // (visible to the epilogues after the staging's barrier)
+                    if (P.kv == KV_E5M2S && type == PH_QKV && tid < 2) S.red[KVS_SLOT + tid] = slice_scale(P, layer, tid, pos);
                     // keep the raw x of the rows the next residual epilogue (O after
                     // QKV, D after GU) updates
                     int cap0 = 0, ncap = 0;
@@ -210,11 +213,13 @@ extern "C" void* kie_decode_kernel_ptr(int hd, int kv) {
     if (hd == 128) {
         if (kv == KV_F16) return (void*)&kie_decode_kernel<128, KV_F16>;
         if (kv == KV_E5M2) return (void*)&kie_decode_kernel<128, KV_E5M2>;
+        if (kv == KV_E5M2S) return (void*)&kie_decode_kernel<128, KV_E5M2S>;
         return (void*)&kie_decode_kernel<128, KV_U8>;
     }
     if (hd == 64) {
         if (kv == KV_F16) return (void*)&kie_decode_kernel<64, KV_F16>;
         if (kv == KV_E5M2) return (void*)&kie_decode_kernel<64, KV_E5M2>;
+        if (kv == KV_E5M2S) return (void*)&kie_decode_kernel<64, KV_E5M2S>;
         return (void*)&kie_decode_kernel<64, KV_U8>;
     }
     return nullptr;

@@ -504,6 +504,8 @@ __device__ __forceinline__ float block_max(float v, float* red, int tid) {
 // block-wide reduction sits between the barrier and the first slot.
 // src = x (fp32, global) or an embedding row (fp16).
 constexpr int NORM_SLOT = NW * (KIE_MAX_HEAD_DIM + 2) + 8;
+// scaled E5M2 cache: the current position's K and V slice scales, set while the QKV phase stages
+constexpr int KVS_SLOT = NW * (KIE_MAX_HEAD_DIM + 2) + 16;
 // x is tagged with parity `par` (polled until every element carries it).  The
 // raw values of elements [cap0, cap0 + ncap) (the rows this CTA's next residual
 // epilogue updates) are also kept in S.xres.
@@ -857,10 +859,37 @@ __device__ __forceinline__ float row_sum(const Smem& S, const Cursor& c, int r) 
     return (c.wfmt == WF_F8 || c.wfmt == WF_F4) ? y * S.wsc[r] : y;
 }
 
+// Scaled E5M2 cache: the scale of the slice holding position pos.  The first
+// position of slice j >= 1 derives it from slice j-1 (its scale and largest
+// stored magnitude, both final since the previous step); every other position
+// reads the value written when its slice began (slice 0: set by the host).
+__device__ __forceinline__ size_t slice_index(const KieParams& P, int layer, int kv, int j) {
+    return (size_t(layer) * 2 + kv) * P.nslice + j;
+}
+__device__ __forceinline__ float slice_scale(const KieParams& P, int layer, int kv, int pos) {
+    const int j = pos / KIE_KV_SLICE;
+    if (j == 0 || pos % KIE_KV_SLICE != 0) return __ldcg(P.kv_sc + slice_index(P, layer, kv, j));
+    const float sp = __ldcg(P.kv_sc + slice_index(P, layer, kv, j - 1));
+    const float amax = __uint_as_float(__ldcg(P.kv_mx + slice_index(P, layer, kv, j - 1))) * sp;
+    return (isfinite(amax) && amax > 0.f) ? amax / KIE_KV_SCALE_TARGET : sp;
+}
+// |value| of an E5M2 byte (NaN stays NaN: fmaxf then ignores it)
+__device__ __forceinline__ float e5m2_mag(uint32_t b) {
+    return fabsf(__half2float(__ushort_as_half((unsigned short)((b & 0xFFu) << 8))));
+}
+
 // store one element of the new K (kv=0) or V (kv=1) at position pos; returns
-// the stored bits (fp16, or the E5M2 byte)
-__device__ __forceinline__ uint32_t kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v) {
+// the stored bits (fp16, or the E5M2 byte).  s: the slice's scale (scaled E5M2 cache).
+__device__ __forceinline__ uint32_t kv_store(const KieParams& P, int layer, int kv, int h, int pos, int dim, float v,
+                                             float s) {
     const __half hv = __float2half_rn(v);
+    if (P.kv == KV_E5M2S) {   // E5M2 of fp16(v) / s
+        uint8_t* base = kv ? P.vc : P.kc;
+        const __half y = __float2half_rn(__half2float(hv) / s);
+        const uint32_t b = f16x2_to_e5m2x2(y, y) & 0xFFu;
+        base[kv_elem_index(P, layer, h, pos) + dim] = uint8_t(b);
+        return b;
+    }
     if (P.kv == KV_F16) {
         uint8_t* base = kv ? P.vc : P.kc;
         reinterpret_cast<__half*>(base)[kv_elem_index(P, layer, h, pos) + dim] = hv;
@@ -896,7 +925,7 @@ struct EpiArgs {
 // head h, or the same pair of V.  Writes the cache (for later steps) and the
 // tagged q / current-position K, V (for this step's attention).
 __device__ __forceinline__ void qkv_unit(const KieParams& P, const Smem& S, const Cursor& c, const EpiArgs& e,
-                                         int u, float ya, float yb) {
+                                         int u, float ya, float yb, float& mk, float& mv) {
     const int hh = P.hd / 2, lhh = P.hd == 128 ? 6 : 5;   // hd is 64 or 128
     const int per = P.H * hh;  // units per matrix
     const uint32_t par = tag_par(e.n), ep16 = tag_ep16(e.n);
@@ -905,9 +934,15 @@ __device__ __forceinline__ void qkv_unit(const KieParams& P, const Smem& S, cons
     const int h = rem >> lhh, i = rem & (hh - 1);
     const int e0 = h * P.hd + i;
     if (which == 2) {
-        const uint32_t b0 = kv_store(P, e.layer, 1, h, e.pos, i, ya), b1 = kv_store(P, e.layer, 1, h, e.pos, i + hh, yb);
+        const float sv = S.red[KVS_SLOT + 1];
+        const uint32_t b0 = kv_store(P, e.layer, 1, h, e.pos, i, ya, sv), b1 = kv_store(P, e.layer, 1, h, e.pos, i + hh, yb, sv);
         st_relaxed_u32(P.vcur + e0, (b0 << 16) | ep16);
         st_relaxed_u32(P.vcur + e0 + hh, (b1 << 16) | ep16);
+        if (P.kv == KV_E5M2S) {
+            mv = fmaxf(mv, fmaxf(e5m2_mag(b0), e5m2_mag(b1)));
+            if (h == 0 && i == 0 && e.pos % KIE_KV_SLICE == 0)   // the slice's first position: publish its scale
+                P.kv_sc[slice_index(P, e.layer, 1, e.pos / KIE_KV_SLICE)] = sv;
+        }
         return;
     }
     const float cs = S.rope[i], sn = S.rope[hh + i];
@@ -916,9 +951,15 @@ __device__ __forceinline__ void qkv_unit(const KieParams& P, const Smem& S, cons
         st_relaxed_f32(P.q + e0, tag_f32(ra, par));
         st_relaxed_f32(P.q + e0 + hh, tag_f32(rb, par));
     } else {
-        const uint32_t b0 = kv_store(P, e.layer, 0, h, e.pos, i, ra), b1 = kv_store(P, e.layer, 0, h, e.pos, i + hh, rb);
+        const float sk = S.red[KVS_SLOT];
+        const uint32_t b0 = kv_store(P, e.layer, 0, h, e.pos, i, ra, sk), b1 = kv_store(P, e.layer, 0, h, e.pos, i + hh, rb, sk);
         st_relaxed_u32(P.kcur + e0, (b0 << 16) | ep16);
         st_relaxed_u32(P.kcur + e0 + hh, (b1 << 16) | ep16);
+        if (P.kv == KV_E5M2S) {
+            mk = fmaxf(mk, fmaxf(e5m2_mag(b0), e5m2_mag(b1)));
+            if (h == 0 && i == 0 && e.pos % KIE_KV_SLICE == 0)
+                P.kv_sc[slice_index(P, e.layer, 0, e.pos / KIE_KV_SLICE)] = sk;
+        }
     }
 }
 
@@ -942,15 +983,23 @@ __device__ __forceinline__ void epi_group(const KieParams& P, const KieLaunch& L
                                           const EpiArgs& e, int g, int rows_g, int lane, int cta) {
     const int r0 = g * c.R;
     if (e.type == PH_QKV || e.type == PH_GU) {   // units are row pairs
+        float mk = 0.f, mv = 0.f;   // scaled E5M2 cache: largest stored K / V magnitudes of this lane
         if (2 * lane < rows_g) {
             const int u = (r0 >> 1) + lane;
             const float ya = row_sum(S, c, 2 * u) * e.rinv, yb = row_sum(S, c, 2 * u + 1) * e.rinv;
-            if (e.type == PH_QKV) qkv_unit(P, S, c, e, u, ya, yb);
+            if (e.type == PH_QKV) qkv_unit(P, S, c, e, u, ya, yb, mk, mv);
             else {
                 const float av = tag_f32((ya / (1.f + expf(-ya))) * yb, tag_par(e.n));
 #pragma unroll
                 for (int k = 0; k < KIE_REPL; ++k) st_relaxed_f32(P.a + k * P.F + c.unit0 + u, av);
             }
+        }
+        if (P.kv == KV_E5M2S && e.type == PH_QKV) {   // the slice's running maxima (fp32 bits order as uints)
+            mk = warp_max(mk);
+            mv = warp_max(mv);
+            const int j = e.pos / KIE_KV_SLICE;
+            if (lane == 0 && mk > 0.f) atomicMax(P.kv_mx + slice_index(P, e.layer, 0, j), __float_as_uint(mk));
+            if (lane == 0 && mv > 0.f) atomicMax(P.kv_mx + slice_index(P, e.layer, 1, j), __float_as_uint(mv));
         }
     } else if (lane < rows_g) {
         residual_row(P, Lc, S, c, e, r0 + lane, row_sum(S, c, r0 + lane), cta);
@@ -1200,7 +1249,7 @@ __device__ __forceinline__ void convert_row(const RawRow& r, const float* fz, fl
                 f[i] = float(qv - zp) * sc;
             }
         }
-    } else if (KVF == KV_E5M2) {
+    } else if (KVF == KV_E5M2 || KVF == KV_E5M2S) {
         e5m2x4_to_f32(r.a.x, f); e5m2x4_to_f32(r.a.y, f + 4); e5m2x4_to_f32(r.a.z, f + 8); e5m2x4_to_f32(r.a.w, f + 12);
     } else {
         const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
@@ -1242,7 +1291,7 @@ __device__ __forceinline__ void cur_row_finish(const KieParams& P, const KieLaun
     }
     r.sc = 0.f;
     r.zp = 0;
-    if (KVF == KV_E5M2) {
+    if (KVF == KV_E5M2 || KVF == KV_E5M2S) {
         uint32_t b[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -1325,7 +1374,7 @@ __device__ __forceinline__ void smem_row16(const uint8_t* row, int dim0, float s
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) { const float2 t = h2_to_f2(w[i]); f[2 * i] = t.x; f[2 * i + 1] = t.y; }
-    } else if (KVF == KV_E5M2) {
+    } else if (KVF == KV_E5M2 || KVF == KV_E5M2S) {
         const uint4 a = *reinterpret_cast<const uint4*>(row + dim0);
         e5m2x4_to_f32(a.x, f); e5m2x4_to_f32(a.y, f + 4); e5m2x4_to_f32(a.z, f + 8); e5m2x4_to_f32(a.w, f + 12);
     } else {
@@ -1411,6 +1460,13 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
                 fence_proxy_async_global();
             }
         }
+        consumer_sync(NCT);
+    }
+    // scaled E5M2 cache: the scales of the slices the chunk's ring rows lie in, [K | V][slice]
+    // (all final: ring rows precede pos, and a slice's scale is written at its first position)
+    const int sl0 = j0 / KIE_KV_SLICE, nslc = (KVF == KV_E5M2S && nt > 0) ? (jt - 1) / KIE_KV_SLICE - sl0 + 1 : 0;
+    if (KVF == KV_E5M2S) {
+        for (int i = tid; i < 2 * nslc; i += NCT) segm[i] = __ldcg(P.kv_sc + slice_index(P, layer, i / nslc, sl0 + i % nslc));
         consumer_sync(NCT);
     }
     const bool has_pos = (j1 == pos + 1);
@@ -1520,6 +1576,7 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) { d0 = fmaf(qv[i], kf[i], d0); d1 = fmaf(qv[i + 1], kf[i + 1], d1); }
                     dsum[u] = d0 + d1;
+                    if (KVF == KV_E5M2S) dsum[u] *= segm[(j0 + r0 + min(rl, rs - 1)) / KIE_KV_SLICE - sl0];
                 }
             }
 #pragma unroll
@@ -1561,8 +1618,9 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
                             for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(wv, vf[i], st.acc[i]);
                         } else {
                             smem_row16<KVF>(vs + size_t(rl) * RB, dim0, 0.f, 0, vf);
+                            const float pw = (KVF == KV_E5M2S) ? p * segm[nslc + (j0 + r0 + rl) / KIE_KV_SLICE - sl0] : p;
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(p, vf[i], st.acc[i]);
+                            for (int i = 0; i < 16; ++i) st.acc[i] = fmaf(pw, vf[i], st.acc[i]);
                         }
                     }
                 }
@@ -1592,9 +1650,15 @@ __device__ bool attention(const KieParams& P, const KieLaunch& Lc, const Smem& S
         for (int i = 0; i < 16; ++i) dsum = fmaf(qv[i], kf[i], dsum);
 #pragma unroll
         for (int o = 1; o < LPR; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+        if (KVF == KV_E5M2S) dsum *= slice_scale(P, layer, 0, pos);
         if (rw == 0) {
             float vf[16];
             convert_row<KVF>(vpos, fz + 2, vf);
+            if (KVF == KV_E5M2S) {
+                const float sv = slice_scale(P, layer, 1, pos);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) vf[i] *= sv;
+            }
             soft_row(st, dsum, vf);
         }
     }

@@ -100,7 +100,9 @@ enum KieWFmt { WF_F16 = 0, WF_I4 = 1, WF_F8 = 2, WF_F4 = 3 };
 #ifndef KIE_R4
 #define KIE_R4 8                 // rows per NVFP4 slot (8 rows x KIE_KC_F16 half-byte codes + block scales: 9 KB);
 #endif                           // measured 1.8B NVFP4: 4 rows 985, 8 rows 1022, 14 rows 915 tok/s
-enum KieKv { KV_F16 = 0, KV_E5M2 = 1, KV_U8 = 2 };
+enum KieKv { KV_F16 = 0, KV_E5M2 = 1, KV_U8 = 2, KV_E5M2S = 3 };
+#define KIE_KV_SLICE 256         // scaled E5M2 cache: positions sharing one scale (per layer, K or V)
+#define KIE_KV_SCALE_TARGET 127.0f   // a new slice's scale maps the previous slice's largest magnitude here
 
 enum KieErr {
     KERR_NONE = 0,
@@ -160,6 +162,9 @@ struct KieParams {
     uint16_t* tail;              // u8: [L][2][H][SEG][hd] fp16, the open segment
     float* seg_scale;            // u8: [L][2][H][nseg]
     int32_t* seg_zp;             // u8: [L][2][H][nseg]
+    float* kv_sc;                // scaled E5M2: [L][2][nslice] scale of each slice (slice 0 set by the host)
+    uint32_t* kv_mx;             // scaled E5M2: [L][2][nslice] largest stored magnitude (fp32 bits), by red.max
+    int32_t nslice;
     // Activations passed between CTAs inside a step carry their own validity
     // tag, so no grid barrier separates the phases of a layer: fp32 vectors
     // hold a parity bit in the least significant mantissa bit; the current

@@ -247,7 +247,86 @@ __global__ void kie_set_kv_kernel(const uint16_t* src, int n, int H, int hd, int
 }
 
 // ---- launch wrappers (host) --------------------------------------------------------------------
+// ---- scaled E5M2 cache (context loading and rewinds) ---------------------------------------------
+__device__ __forceinline__ float e5m2_mag_prep(uint32_t b) {
+    return fabsf(__half2float(__ushort_as_half((unsigned short)((b & 0xFFu) << 8))));
+}
+
+// Slice j of one (layer, K or V) begins: for j >= 1 its scale from slice j-1
+// (largest stored magnitude m, scale s: m * s / 127, or s when that is zero or
+// not finite); its running maximum starts at zero.  sc, mx: that entry's [nslice].
+__global__ void kie_kv_slice_start_kernel(float* sc, uint32_t* mx, int j) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    if (j > 0) {
+        const float sp = sc[j - 1];
+        const float amax = __uint_as_float(mx[j - 1]) * sp;
+        sc[j] = (isfinite(amax) && amax > 0.f) ? amax / KIE_KV_SCALE_TARGET : sp;
+    }
+    mx[j] = 0u;
+}
+
+// Positions [p0, p1) of one layer's K or V (fp16 source [n][H][hd]) as E5M2
+// codes of x / sc[0] into dst ([H][max_ctx][hd] of that layer), folding their
+// magnitudes into *mx by atomic max (fp32 bits of non-negative values order as
+// unsigned integers).
+__global__ void kie_kv_slice_quant_kernel(const uint16_t* src, int p0, int p1, int H, int hd, int max_ctx,
+                                          const float* sc, uint8_t* dst, uint32_t* mx) {
+    const int per = H * hd;
+    const int64_t n = int64_t(p1 - p0) * per;
+    const float s = *sc;
+    float m = 0.f;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const int p = p0 + int(i / per), r = int(i % per), h = r / hd, d = r - h * hd;
+        const __half x = __ushort_as_half(src[size_t(p) * per + r]);
+        const __half y = __float2half_rn(__half2float(x) / s);
+        const uint32_t b = f16x2_to_e5m2x2(y, y) & 0xFFu;
+        dst[(size_t(h) * max_ctx + p) * hd + d] = uint8_t(b);
+        m = fmaxf(m, e5m2_mag_prep(b));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(mx, __float_as_uint(m));
+}
+
+// After a move of the position to pos: the running maximum of pos's slice over
+// the positions [slice start, pos) still in the cache, and zero for every later
+// slice.  One block per (layer, K or V).
+__global__ void kie_kv_rescan_kernel(const uint8_t* kc, const uint8_t* vc, uint32_t* mx, int H, int hd, int max_ctx,
+                                     int nslice, int pos) {
+    __shared__ float red[32];
+    const int lk = blockIdx.x, layer = lk >> 1, kv = lk & 1;
+    const uint8_t* base = (kv ? vc : kc) + size_t(layer) * H * max_ctx * hd;
+    const int j = pos / KIE_KV_SLICE, q0 = j * KIE_KV_SLICE, per_h = (pos - q0) * hd;
+    float m = 0.f;
+    for (int h = 0; h < H; ++h)
+        for (int i = threadIdx.x; i < per_h; i += blockDim.x)
+            m = fmaxf(m, e5m2_mag_prep(base[(size_t(h) * max_ctx + q0) * hd + i]));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < int(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+        if (j < nslice) mx[size_t(lk) * nslice + j] = __float_as_uint(m);
+    }
+    for (int s = j + 1 + int(threadIdx.x); s < nslice; s += blockDim.x) mx[size_t(lk) * nslice + s] = 0u;
+}
+
 #include <cuda_runtime.h>
+
+extern "C" cudaError_t kie_launch_kv_slice(const uint16_t* src, int p0, int p1, int H, int hd, int max_ctx, float* sc,
+                                           uint32_t* mx, int j, uint8_t* dst, cudaStream_t st) {
+    kie_kv_slice_start_kernel<<<1, 32, 0, st>>>(sc, mx, j);
+    if (p1 <= p0) return cudaGetLastError();
+    size_t blocks = (size_t(p1 - p0) * H * hd + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    kie_kv_slice_quant_kernel<<<unsigned(blocks), 256, 0, st>>>(src, p0, p1, H, hd, max_ctx, sc + j, dst, mx + j);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t kie_launch_kv_rescan(const uint8_t* kc, const uint8_t* vc, uint32_t* mx, int L, int H, int hd,
+                                            int max_ctx, int nslice, int pos, cudaStream_t st) {
+    kie_kv_rescan_kernel<<<2 * L, 256, 0, st>>>(kc, vc, mx, H, hd, max_ctx, nslice, pos);
+    return cudaGetLastError();
+}
 
 extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, const void* desc, int n,
                                             cudaStream_t st) {

@@ -22,7 +22,7 @@ from . import _build
 KIE_OK, KIE_ERR_INVALID_ARG, KIE_ERR_OOM, KIE_ERR_CUDA = 0, -1, -2, -3
 KIE_ERR_NOT_LOADED, KIE_ERR_CTX_OVERFLOW, KIE_ERR_DEVICE_TIMEOUT = -4, -5, -6
 KIE_ERR_LAUNCH, KIE_ERR_UNSUPPORTED = -7, -8
-KV_DTYPES = {"fp16": 0, "fp8_e5m2": 1, "u8": 2}
+KV_DTYPES = {"fp16": 0, "fp8_e5m2": 1, "u8": 2, "fp8_e5m2_scaled": 3}
 W_DTYPES = {"fp16": 0, "int4_g128": 1, "fp8_e4m3": 2, "nvfp4": 3}
 MODES = {"persistent": 0, "graph": 1}
 
@@ -42,7 +42,8 @@ class kie_config(C.Structure):
                 ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
                 ("max_ctx", C.c_int32), ("rms_eps", C.c_float), ("rope_theta", C.c_float),
                 ("kv_dtype", C.c_int32), ("ffn_wdtype", C.c_int32), ("mode", C.c_int32),
-                ("device", C.c_int32), ("attn_wdtype", C.c_int32), ("batch", C.c_int32)]
+                ("device", C.c_int32), ("attn_wdtype", C.c_int32), ("batch", C.c_int32),
+                ("kv_scale_k", C.c_float), ("kv_scale_v", C.c_float)]
 
 
 class kie_layer_weights(C.Structure):
@@ -132,10 +133,10 @@ def _check(st, eng=None):
 
 def make_config(n_layers, d_model, n_heads, head_dim, ffn_dim, vocab, max_ctx, rms_eps=1e-5, rope_theta=10000.0,
                 kv_dtype="fp16", ffn_wdtype="fp16", mode="persistent", device=0, attn_wdtype="fp16",
-                batch=1) -> kie_config:
+                batch=1, kv_scale=(0.0, 0.0)) -> kie_config:
     return kie_config(n_layers, d_model, n_heads, head_dim, ffn_dim, vocab, max_ctx, rms_eps, rope_theta,
                       KV_DTYPES[kv_dtype], W_DTYPES[ffn_wdtype], MODES[mode], device, W_DTYPES[attn_wdtype],
-                      int(batch))
+                      int(batch), float(kv_scale[0]), float(kv_scale[1]))
 
 
 class Engine:
@@ -284,11 +285,13 @@ class Engine:
 
     def read_kv(self, layer: int, which: int, p0: int, n: int):
         """Raw storage of K (which=0) or V (1): (data [H, n, h], tail fp16 or None,
-        scale [H, nseg] or None, zp [H, nseg] or None)."""
+        scale [H, nseg] (uint8) / [nslices] (scaled E5M2) or None, zp [H, nseg] or None)."""
         H, h = self.cfg.n_heads, self.cfg.head_dim
         kv = self.cfg.kv_dtype
         data = np.empty((H, n, h), np.uint16 if kv == 0 else np.uint8)
         tail = sc = zp = None
+        if kv == 3:   # scaled E5M2: the scales of the slices the range meets
+            sc = np.zeros((p0 + n + 255) // 256 - p0 // 256, np.float32)
         if kv == 2:
             tail = np.zeros((H, n, h), np.uint16)
             nseg = (p0 + n + 127) // 128 - p0 // 128

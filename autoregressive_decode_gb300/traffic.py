@@ -13,7 +13,8 @@ Storage formats counted:
     weight plus one fp16 scale per 128-column group of a row;
   * NVFP4 matrices: half a byte per weight, one E4M3 scale byte per 16-column
     block of a row and one fp32 scale per row;
-  * KV cache: fp16 (2 bytes), FP8 E5M2 (1 byte), or uint8 codes for completed
+  * KV cache: fp16 (2 bytes), FP8 E5M2 (1 byte; the scaled variant adds one
+    fp32 scale per layer, K/V and 256-position slice), or uint8 codes for completed
     128-token segments (1 byte, plus an fp32 scale and an int32 zero point per
     segment, layer, K/V and head) with the open segment's tail in fp16;
   * RMSNorm gains (two per layer), the final gain and the embedding row read
@@ -22,6 +23,7 @@ Storage formats counted:
 from __future__ import annotations
 
 SEGMENT = 128     # uint8 KV segment (tokens)
+SLICE = 256       # scaled FP8 KV: positions sharing one scale
 INT4_GROUP = 128  # INT4 scale group (columns)
 FP4_BLOCK = 16    # NVFP4 scale block (columns)
 
@@ -45,6 +47,8 @@ def _kv_layer(ctx: int, heads: int, head_dim: int, kv_dtype: str) -> int:
         return 2 * ctx * per_pos * 2
     if kv_dtype == "fp8_e5m2":
         return 2 * ctx * per_pos
+    if kv_dtype == "fp8_e5m2_scaled":   # one byte per value, one fp32 scale per 256-position slice
+        return 2 * (ctx * per_pos + 4 * ((ctx + SLICE - 1) // SLICE))
     if kv_dtype == "u8":
         done = ctx - ctx % SEGMENT
         meta = heads * (done // SEGMENT) * 8

@@ -22,7 +22,8 @@ collective on the data path; value = tokens of all ranks / max rank time.
 workloads  (1 GPU, default run) a compact record for each of the other
         workloads -- 1.8B decoding 8 requests at once (low-batch decode), 1.8B with FP8 E4M3 weights, 1.8B with NVFP4 weights, 1.8B with
         INT4 q/k/v and FFN weights over an E5M2 cache, 1.8B over a 32K FP8-E5M2 cache,
-        1.8B over an 8K adaptive uint8 cache, 7B with INT4 FFN -- with its
+        1.8B over a 32K scaled FP8-E5M2 cache, 1.8B over an 8K adaptive uint8 cache,
+        7B with INT4 FFN -- with its
         decode tokens/s, roofline fraction and a CPU-oracle figure.
 
 `--impl reference` times the CPU oracle as the reference arm.
@@ -377,7 +378,7 @@ def batched_record(args, local, kie, torch, w, weights, peak, peak_kind):
 # context the workload names, prefilled on the GPU where the tensor-core path
 # covers it and otherwise (uint8 cache; the 7B model, whose decode bytes do not
 # depend on how its 4,096-position context was made) a synthetic one.
-EXTRA = ("1p8b_b8", "1p8b_fp8", "1p8b_nvfp4", "1p8b_hpi", "1p8b_32k", "1p8b_u8", "7b_int4")
+EXTRA = ("1p8b_b8", "1p8b_fp8", "1p8b_nvfp4", "1p8b_hpi", "1p8b_32k", "1p8b_32k_scaled", "1p8b_u8", "7b_int4")
 
 
 def extra_workloads(args, local, kie, torch, weights_1p8b):

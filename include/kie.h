@@ -62,7 +62,17 @@ typedef enum {
     KIE_ERR_UNSUPPORTED = -8    /* shape or option outside what this build implements      */
 } kie_status;
 
-typedef enum { KIE_KV_FP16 = 0, KIE_KV_FP8_E5M2 = 1, KIE_KV_U8_ADAPTIVE = 2 } kie_kv_dtype;
+/* KV cache storage.  FP16.  FP8_E5M2: E5M2 of the fp16 value, no scale (xAI
+ * page section 2.3).  U8_ADAPTIVE: uint8 codes with a scale and zero point per
+ * 128-token segment and head (Grok-3 hot-update page section 3.2).
+ * FP8_E5M2_SCALED: E5M2 codes of fp16(v) / s, read back as code * s, with one
+ * scale s per layer, K or V and 256-position slice (xAI page section 3.3's
+ * per-tensor k_cache / v_cache scales, recomputed every 256 tokens from the
+ * cache): slice 0 uses kv_scale_k / kv_scale_v; slice j >= 1 takes, when its
+ * first position is written, the largest magnitude m of slice j-1's stored
+ * codes and s_j = (m * s_{j-1}) / 127, or s_{j-1} when that is zero or not
+ * finite.  Prompts prefill through the decode kernel for this format. */
+typedef enum { KIE_KV_FP16 = 0, KIE_KV_FP8_E5M2 = 1, KIE_KV_U8_ADAPTIVE = 2, KIE_KV_FP8_E5M2_SCALED = 3 } kie_kv_dtype;
 /* Weight storage of the GEMV matrices.  FP16: as given.  INT4_G128: symmetric
  * INT4, group 128 (xAI page sections 2.3, 3.3); as ffn_wdtype it covers the
  * three FFN matrices, as attn_wdtype the q, k and v projections only (the same
@@ -108,6 +118,8 @@ typedef struct {
                            * Needs PERSISTENT mode, FP16 weights, an FP16 or FP8_E5M2 cache,
                            * d_model, ffn_dim and n_heads*head_dim multiples of 64, and
                            * batch * n_heads <= the GPU's SM count. */
+    float kv_scale_k;     /* FP8_E5M2_SCALED: slice 0's K and V scales (<= 0: the xAI page's   */
+    float kv_scale_v;     /* hpi_config values, 0.0039 and 0.0042)                              */
 } kie_config;
 
 #define KIE_MAX_BATCH_REQUESTS 8
@@ -213,7 +225,7 @@ kie_status kie_generate_greedy_batch_device(kie_engine* e, const int32_t* first_
 kie_status kie_sync(kie_engine* e);
 
 /* pos = 0 (the cache contents become unreachable) and clear a sticky device
- * error. */
+ * error (a scaled E5M2 cache restarts from its initial scales). */
 kie_status kie_reset(kie_engine* e);
 int32_t kie_get_pos(const kie_engine* e);
 /* Set pos (0 <= pos <= max_ctx), e.g. after loading a context with kie_set_kv. */
@@ -285,14 +297,17 @@ kie_status kie_decode_step_static_scratch(kie_engine* e, int32_t token, int32_t*
 /* Write post-RoPE K and V for positions 0 .. n-1 of one layer through the
  * cache's storage format (fp16 as given; E5M2 converted from it; uint8: every
  * complete 128-token segment quantised, the rest kept fp16 as the open
- * segment).  k_fp16, v_fp16: host fp16 [n][n_heads][head_dim].  pos is not
- * changed (see kie_set_pos). */
+ * segment; scaled E5M2: slice by slice, each slice's scale from the one
+ * before as in decoding).  k_fp16, v_fp16: host fp16 [n][n_heads][head_dim].
+ * pos is not changed (see kie_set_pos). */
 kie_status kie_set_kv(kie_engine* e, int32_t layer, const uint16_t* k_fp16, const uint16_t* v_fp16,
                       int32_t n);
 
 /* Read back the stored K (which=0) or V (which=1) of one layer, positions
  * [p0, p0+n), as raw storage: fp16 bits (2 bytes/elem), E5M2 bytes or uint8
- * codes (1 byte/elem), layout [n_heads][n][head_dim].  For uint8 caches the
+ * codes (1 byte/elem), layout [n_heads][n][head_dim].  For scaled E5M2 caches
+ * `scale` receives the scales of the 256-position slices the range meets
+ * ([nslices], NULL allowed).  For uint8 caches the
  * positions of the open segment are returned as their fp16 values in
  * `tail_fp16` ([n_heads][n][head_dim], NULL allowed; other positions are left
  * untouched) -- when pos is a positive multiple of 128 no position of the new

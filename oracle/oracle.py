@@ -93,6 +93,39 @@ def e5m2_round(x_f16: np.ndarray) -> np.ndarray:
 
 SEG = 128  # [Grok3] 3.2: "each 128-token segment", 128 found optimal
 
+# Scaled FP8 E5M2 cache ([xAI] 3.3): per-tensor scales in hpi_config (k_cache
+# 0.0039, v_cache 0.0042), recomputed every 256 tokens from the current cache
+# slice; the scale maps the slice's largest magnitude to 127 ([xAI] 4.3's
+# max|k| / 127).
+KV_SLICE = 256
+KV_SCALE0 = (0.0039, 0.0042)   # K, V: the scales slice 0 is stored with
+KV_SCALE_TARGET = 127.0
+
+
+def e5m2s_quantize(x16: np.ndarray, s) -> np.ndarray:
+    """Scaled E5M2 codes of fp16 values with scale s: the fp16 value divided by
+    s in fp32, rounded to fp16, then to E5M2 (round to nearest even,
+    saturating) - the unscaled cache's fp16 -> E5M2 step applied to x / s."""
+    y = (np.asarray(x16, dtype=np.float16).astype(F32) / F32(s)).astype(np.float16)
+    return e5m2_from_f16_bits(y.view(np.uint16))
+
+
+def e5m2s_dequantize(codes: np.ndarray, s) -> np.ndarray:
+    """The value a scaled E5M2 cache returns: E5M2 -> fp16 (exact) -> fp32, times s."""
+    return (e5m2_to_f16_bits(codes).view(np.float16).astype(F32) * F32(s)).astype(F32)
+
+
+def e5m2s_next_scale(max_code: float, s_prev) -> np.float32:
+    """Scale of slice j from slice j-1 (its scale s_prev and the largest
+    magnitude max_code among its stored E5M2 values): the slice's largest
+    dequantised magnitude max_code * s_prev, mapped to 127.  A slice with no
+    usable magnitude (all zero, or not finite) keeps the previous scale (the
+    page keeps recent scales as the fallback)."""
+    amax = F32(F32(max_code) * F32(s_prev))
+    if not np.isfinite(amax) or amax <= 0:
+        return F32(s_prev)
+    return F32(amax / F32(KV_SCALE_TARGET))
+
 
 def u8_quantize(x: np.ndarray):
     """Adaptive-range uint8 quantisation of one segment ([Grok3] 3.2).
@@ -350,10 +383,15 @@ def argmax_lowest(logits: np.ndarray) -> int:
 
 
 class KVCache:
-    """Per-layer K and V caches in one of three storage formats.
+    """Per-layer K and V caches in one of four storage formats.
 
     fp16:      stored value = fp16(k).
     fp8_e5m2:  stored value = E5M2(fp16(k)), read back as fp16 ([xAI] 2.3).
+    fp8_e5m2_scaled: positions in slices of 256; slice j of a layer's K (or V)
+               is stored as E5M2 codes of fp16(k) / s_j and read back as
+               code * s_j ([xAI] 3.3).  s_0 is KV_SCALE0; s_j (j >= 1) comes
+               from slice j-1's stored values (e5m2s_next_scale), fixed when
+               slice j's first position is written.
     u8:        positions of a complete 128-token segment are stored as uint8
                codes with one (scale, zp) per (layer, K or V, head, segment)
                ([Grok3] 3.2); positions of the current, incomplete segment stay
@@ -361,8 +399,8 @@ class KVCache:
                the whole segment once.
     ``k[l]``/``v[l]`` hold, as fp32 [H, max_ctx, h], the value a reader sees."""
 
-    def __init__(self, n_layers, n_heads, head_dim, max_ctx, kv_dtype):
-        if kv_dtype not in ("fp16", "fp8_e5m2", "u8"):
+    def __init__(self, n_layers, n_heads, head_dim, max_ctx, kv_dtype, kv_scale0=KV_SCALE0):
+        if kv_dtype not in ("fp16", "fp8_e5m2", "u8", "fp8_e5m2_scaled"):
             raise ValueError(kv_dtype)
         self.kv_dtype = kv_dtype
         self.H, self.h, self.max_ctx = n_heads, head_dim, max_ctx
@@ -377,6 +415,15 @@ class KVCache:
                           for _ in range(n_layers)]
             self.scale = [[np.zeros((n_heads, nseg), F32) for _ in range(2)] for _ in range(n_layers)]
             self.zp = [[np.zeros((n_heads, nseg), np.int32) for _ in range(2)] for _ in range(n_layers)]
+        if kv_dtype == "fp8_e5m2_scaled":
+            nsl = (max_ctx + KV_SLICE - 1) // KV_SLICE
+            self.codes = [[np.zeros((n_heads, max_ctx, head_dim), np.uint8) for _ in range(2)]
+                          for _ in range(n_layers)]
+            # per layer, K/V, slice: its scale and the largest stored E5M2 magnitude
+            self.sc = [[np.zeros(nsl, F32) for _ in range(2)] for _ in range(n_layers)]
+            self.mcode = [[np.zeros(nsl, F32) for _ in range(2)] for _ in range(n_layers)]
+            for lay in self.sc:
+                lay[0][0], lay[1][0] = F32(kv_scale0[0]), F32(kv_scale0[1])
 
     def write(self, layer: int, pos: int, k: np.ndarray, v: np.ndarray):
         """Write positions pos .. pos+n-1 (k, v: fp32 or fp16 [n, H, h])."""
@@ -390,6 +437,25 @@ class KVCache:
         elif self.kv_dtype == "fp8_e5m2":
             self.k[layer][:, sl] = e5m2_round(k16).transpose(1, 0, 2)
             self.v[layer][:, sl] = e5m2_round(v16).transpose(1, 0, 2)
+        elif self.kv_dtype == "fp8_e5m2_scaled":
+            # slice by slice: a slice's scale is fixed when its first position is written
+            p = pos
+            while p < pos + n:
+                j = p // KV_SLICE
+                q = min(pos + n, (j + 1) * KV_SLICE)
+                for which, x16 in ((0, k16), (1, v16)):
+                    if p == j * KV_SLICE and j > 0:
+                        self.sc[layer][which][j] = e5m2s_next_scale(self.mcode[layer][which][j - 1],
+                                                                    self.sc[layer][which][j - 1])
+                        self.mcode[layer][which][j] = F32(0)
+                    s_j = self.sc[layer][which][j]
+                    codes = e5m2s_quantize(x16[p - pos:q - pos], s_j).transpose(1, 0, 2)
+                    self.codes[layer][which][:, p:q] = codes
+                    mag = np.abs(e5m2_to_f16_bits(codes).view(np.float16).astype(F32))
+                    self.mcode[layer][which][j] = max(self.mcode[layer][which][j], F32(mag.max()))
+                    dst = self.k[layer] if which == 0 else self.v[layer]
+                    dst[:, p:q] = e5m2s_dequantize(codes, s_j)
+                p = q
         else:
             for which, x16 in ((0, k16), (1, v16)):
                 self.raw16[layer][which][:, sl] = x16.transpose(1, 0, 2)
@@ -467,7 +533,8 @@ class OracleDecoder:
                 for k in ("w_gate", "w_up", "w_down"):
                     lay[k] = f(lw[k])
             self.layers.append(lay)
-        self.cache = KVCache(self.L, self.H, self.h, self.max_ctx, cfg.kv_dtype)
+        self.cache = KVCache(self.L, self.H, self.h, self.max_ctx, cfg.kv_dtype,
+                             getattr(cfg, "kv_scale0", KV_SCALE0))
         self.pos = 0
         self.scale = F32(1.0 / np.sqrt(self.h))
 
@@ -614,6 +681,8 @@ def decode_bytes_per_token(cfg, ctx_len: int) -> dict:
         kv = L * 2 * C_bytes(ctx_len, H, h, 2)
     elif cfg.kv_dtype == "fp8_e5m2":
         kv = L * 2 * C_bytes(ctx_len, H, h, 1)
+    elif cfg.kv_dtype == "fp8_e5m2_scaled":   # codes, plus the fp32 scale of every attended slice
+        kv = L * 2 * (C_bytes(ctx_len, H, h, 1) + 4 * ((ctx_len + KV_SLICE - 1) // KV_SLICE))
     else:
         full = (ctx_len // SEG) * SEG
         tail = ctx_len - full

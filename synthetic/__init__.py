@@ -103,7 +103,7 @@ class Workload:
     vocab: int
     rms_eps: float = 1e-5
     rope_theta: float = 10000.0
-    kv_dtype: str = "fp16"          # "fp16" | "fp8_e5m2" | "u8"
+    kv_dtype: str = "fp16"          # "fp16" | "fp8_e5m2" | "u8" | "fp8_e5m2_scaled"
     ffn_wdtype: str = "fp16"        # "fp16" | "int4_g128" | "fp8_e4m3"
     attn_wdtype: str = "fp16"       # q/k/v/o and LM head: "fp16" | "fp8_e4m3"
     prompt_len: int = 16            # prompt tokens (kv_source == "prefill")
@@ -160,6 +160,11 @@ WORKLOADS = {
     # fp16 O projection and LM head, an FP8 E5M2 KV cache
     "1p8b_hpi": Workload("1p8b_hpi", 1, 25, 2048, 16, 128, 8192, 32000, ffn_wdtype="int4_g128",
                          attn_wdtype="int4_g128", kv_dtype="fp8_e5m2", prompt_len=2048, decode_steps=256),
+    # the 32K workload with the scaled FP8 E5M2 cache (a scale per layer, K/V and
+    # 256-position slice), over a synthetic 32,768-position context
+    "1p8b_32k_scaled": Workload("1p8b_32k_scaled", 2, 25, 2048, 16, 128, 8192, 32000,
+                                kv_dtype="fp8_e5m2_scaled", kv_source="synthetic", prompt_len=0,
+                                context_len=32768, decode_steps=128),
     # the 1.8B fp16 model decoding 8 requests at once (low-batch decode), each over
     # its own synthetic 2048-position context, 256 steps
     "1p8b_b8": Workload("1p8b_b8", 1, 25, 2048, 16, 128, 8192, 32000, kv_source="synthetic", prompt_len=0,

@@ -173,6 +173,78 @@ def test_int4_qkv_graph_equals_persistent():
         np.testing.assert_array_equal(a, b)
 
 
+def _scaled(w):
+    return w.with_(kv_dtype="fp8_e5m2_scaled")
+
+
+def test_scaled_e5m2_prompt_crossing_slices():
+    """Scaled E5M2 cache: a 300-token prompt through the decode kernel crosses
+    the 256-position slice boundary (slice 1's scale derived in the kernel from
+    slice 0's stored maximum), then 20 teacher-forced steps; slice 0's scales
+    are the initial ones, slice 1's within one E5M2 step of the oracle's (the
+    GEMV's summation order can move the slice maximum by a rounding step)."""
+    w = _scaled(TINY).with_(prompt_len=300, decode_steps=20)
+    weights = S.gen_weights(w)
+    e, o, lg, lo = _prefill_both(w, weights, max_ctx=340)
+    assert np.abs(lg - lo).max() <= tol_for(w)
+    for which in (0, 1):
+        _, _, sc, _ = e.read_kv(1, which, 0, 300)
+        ref = o.cache.sc[1][which][:2]
+        assert sc[0] == ref[0] == np.float32(0.0039 if which == 0 else 0.0042)
+        assert 0.79 <= sc[1] / ref[1] <= 1.26
+    teacher_forced(e, o, O.argmax_lowest(lo), w.decode_steps, tol_for(w))
+
+
+@pytest.mark.parametrize("w", [TINY, WIDE], ids=lambda w: w.name)
+def test_scaled_e5m2_synthetic_context(w):
+    """A 700-position synthetic context loaded slice by slice: codes and slice
+    scales bit-exact against the oracle; 70 decode steps cross position 768
+    (slice 3 begins in the kernel); a rewind to 700 and the same steps again
+    give identical logits (the slice maximum is rebuilt from what stays)."""
+    w = _scaled(w).with_(kv_source="synthetic", context_len=700, prompt_len=0, decode_steps=70)
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights, max_ctx=800)
+    o = O.OracleDecoder(w, weights, max_ctx=800)
+    for layer in range(w.n_layers):
+        k, v = S.gen_kv(w, layer)
+        e.set_kv(layer, k, v)
+        o.set_kv(layer, k, v)
+    e.set_pos(700)
+    o.pos = 700
+    for which in (0, 1):
+        data, _, sc, _ = e.read_kv(0, which, 0, 700)
+        np.testing.assert_array_equal(data, o.cache.codes[0][which][:, :700])
+        np.testing.assert_array_equal(sc, o.cache.sc[0][which][:3])
+    first = S.gen_first_token(w)
+    worst, toks = teacher_forced(e, o, first, w.decode_steps, tol_for(w))
+    e.set_pos(700)
+    t = first
+    e2 = []
+    for tk in [first] + toks[:-1]:
+        _, lg = e.decode_step(tk)
+        e2.append(lg)
+    e.set_pos(700)
+    for i, tk in enumerate([first] + toks[:-1]):
+        _, lg = e.decode_step(tk)
+        np.testing.assert_array_equal(lg, e2[i])
+
+
+def test_scaled_e5m2_graph_equals_persistent():
+    w = _scaled(MEDIUM).with_(kv_source="synthetic", context_len=500, prompt_len=0)
+    weights = S.gen_weights(w)
+    res = {}
+    for mode in ("persistent", "graph"):
+        e = engine_for(w, weights, mode, max_ctx=560)
+        for layer in range(w.n_layers):
+            k, v = S.gen_kv(w, layer)
+            e.set_kv(layer, k, v)
+        e.set_pos(500)
+        res[mode] = e.generate_greedy(S.gen_first_token(w), 20, want_logits=True)
+        e.close()
+    for a, b in zip(res["persistent"], res["graph"]):
+        np.testing.assert_array_equal(a, b)
+
+
 def test_nvfp4_ffn_graph_equals_persistent_and_u8_cache():
     """NVFP4 FFN weights with fp16 attention weights, in both launch modes
     (bit-identical), with the uint8 cache (prefill through the decode kernel)."""

@@ -13,6 +13,9 @@ greedy chain), against the CPU oracle.
   1p8b_b8   8 requests decoded together (batched engine), each over its own
             synthetic 2,048-position context, 16 free-running steps in one
             launch, every request against its own oracle.
+  1p8b_32k_scaled  the scaled FP8-E5M2 cache over a synthetic 32,768-position
+            context (128 slices loaded slice by slice), 32 steps; position
+            32768 begins slice 128 in the kernel.
   1p8b_32k  FP8-E5M2 cache over a 32,768-position synthetic context (decode-only
             parity: the same fp16 K/V loaded into both sides), 32 steps.
   1p8b_u8   adaptive-range uint8 cache over the 8,192-position synthetic context
@@ -153,6 +156,20 @@ def test_1p8b_batched_decode():
     toks, logs = d_tok.cpu().numpy(), d_log.cpu().numpy()
     for b in range(B):
         check_free_running(oracles[b], firsts[b], toks[:, b], logs[:, b], tol_for(w))
+
+
+def test_1p8b_32k_scaled_decode():
+    n = 32
+    w = S.WORKLOADS["1p8b_32k_scaled"]
+    weights = S.gen_weights(w)
+    e = engine_for(w, weights, max_ctx=w.context_len + n)
+    o = O.OracleDecoder(w, weights, max_ctx=w.context_len + n)
+    _synthetic_context(w, e, o)
+    _, _, sc, _ = e.read_kv(3, 1, 0, w.context_len)
+    np.testing.assert_array_equal(sc, o.cache.sc[3][1][:128])
+    first = S.gen_first_token(w)
+    toks, logs = _generate_on_device(e, first, n)
+    check_free_running(o, first, toks, logs, tol_for(w))
 
 
 def test_1p8b_32k_fp8_decode():

@@ -115,6 +115,73 @@ def test_e5m2_ties_to_even():
     np.testing.assert_array_equal(r, np.array([1.0, 1.5, -1.0, 1.0], np.float32))
 
 
+# ------------------------------------------------------------------ scaled FP8 E5M2 cache (row F3)
+def test_scaled_e5m2_first_slice_vs_torch():
+    """Slice 0 is stored with the page's initial scales (K 0.0039, V 0.0042):
+    each value reads back as e5m2(fp16(fp16(x) / s)) * s, with the fp16 and
+    E5M2 roundings done by torch's casts instead of the oracle's encoder."""
+    torch = pytest.importorskip("torch")
+    H, h, n = 2, 8, 256
+    k = S.normal_f16(41, 1, (n, H, h), 1.0)
+    v = S.normal_f16(41, 2, (n, H, h), 3.0)
+    c = O.KVCache(1, H, h, 512, "fp8_e5m2_scaled")
+    c.write(0, 0, k, v)
+    for which, x, s in ((0, k, 0.0039), (1, v, 0.0042)):
+        t = torch.from_numpy(x.astype(np.float32))
+        y = (t / torch.tensor(s, dtype=torch.float32)).to(torch.float16).to(torch.float8_e5m2)
+        ref = (y.to(torch.float32) * torch.tensor(s, dtype=torch.float32)).numpy().transpose(1, 0, 2)
+        got = (c.k if which == 0 else c.v)[0][:, :n]
+        np.testing.assert_array_equal(got, ref)
+    assert c.sc[0][0][0] == np.float32(0.0039) and c.sc[0][1][0] == np.float32(0.0042)
+
+
+def test_scaled_e5m2_recalibration_hand_example():
+    """Slice 0 holds a single nonzero K value 1.0: stored as e5m2(fp16(1 / 0.0039))
+    = e5m2(256.5) = 256 (ties to even between 256 and 320), so the scale of slice
+    1, fixed when position 256 is written, is 256 * 0.0039 / 127 in fp32; a
+    slice of zeros keeps the scale before it (slice 2)."""
+    H, h = 1, 4
+    c = O.KVCache(1, H, h, 1024, "fp8_e5m2_scaled")
+    k = np.zeros((256, H, h), np.float16)
+    k[17, 0, 2] = 1.0
+    c.write(0, 0, k, np.zeros_like(k))
+    assert c.mcode[0][0][0] == np.float32(256.0)
+    assert c.k[0][0, 17, 2] == np.float32(np.float32(256.0) * np.float32(0.0039))
+    c.write(0, 256, np.zeros((256, H, h), np.float16), np.zeros((256, H, h), np.float16))
+    s1 = np.float32(np.float32(np.float32(256.0) * np.float32(0.0039)) / np.float32(127.0))
+    assert c.sc[0][0][1] == s1
+    assert c.sc[0][1][1] == np.float32(0.0042)          # V slice 0 was all zero: the scale stays
+    c.write(0, 512, np.ones((1, H, h), np.float16), np.ones((1, H, h), np.float16))
+    assert c.sc[0][0][2] == s1                          # slice 1 was all zero: fallback
+    assert c.k[0][0, 512, 0] == np.float32(1.0) or abs(c.k[0][0, 512, 0] - 1.0) <= 0.125
+
+
+def test_scaled_e5m2_round_trip_and_headroom():
+    """Three slices whose magnitudes grow 4x per slice: every value reads back
+    within E5M2's half step (2^-3 relative) of its fp16 value, and no code
+    saturates (a scale maps the previous slice's largest value to 127, far
+    below E5M2's 57344)."""
+    H, h = 2, 16
+    c = O.KVCache(1, H, h, 768, "fp8_e5m2_scaled")
+    xs = [S.normal_f16(43, j, (256, H, h), 0.5 * 4.0 ** j) for j in range(3)]
+    for j, x in enumerate(xs):
+        c.write(0, 256 * j, x, x)
+    got = c.k[0].transpose(1, 0, 2)
+    ref = np.concatenate(xs).astype(np.float32)
+    err = np.abs(got - ref)
+    assert np.all(err <= 0.125 * np.abs(ref) + 1e-6)
+    assert np.all(np.abs(O.e5m2_to_f16_bits(c.codes[0][0]).view(np.float16).astype(np.float32)) < 57344.0)
+    assert c.sc[0][0][1] > 0 and c.sc[0][0][2] > c.sc[0][0][1]
+
+
+def test_scaled_e5m2_byte_model_hand_count():
+    """The 1.8B model over a 32,768-position scaled E5M2 cache at C = 32769: K and
+    V of 16 heads x 128 one-byte codes per position and layer, plus one fp32
+    scale per layer, K/V and attended 256-position slice (129 slices)."""
+    w = S.WORKLOADS["1p8b_32k"].with_(kv_dtype="fp8_e5m2_scaled")
+    assert O.decode_bytes_per_token(w, 32769)["kv"] == 25 * 2 * (32769 * 2048 + 4 * 129)
+
+
 # ------------------------------------------------------------------ FP8 E4M3 weights (row F2)
 def test_e4m3_all_codes_vs_torch():
     """Every one of the 256 E4M3 codes decodes to torch's float8_e4m3fn value
@@ -449,7 +516,7 @@ def test_decoder_vs_f64_brute_force():
 def test_prefill_equals_stepwise_decode():
     w = S.gen_weights(MICRO, seed=79)
     toks = S.gen_prompt(MICRO, n=11, seed=80)
-    for kv in ("fp16", "fp8_e5m2"):
+    for kv in ("fp16", "fp8_e5m2", "fp8_e5m2_scaled"):
         cfg = MICRO.with_(kv_dtype=kv)
         a = O.OracleDecoder(cfg, w, max_ctx=16)
         la = a.prefill(toks, q_block=4)
@@ -460,7 +527,7 @@ def test_prefill_equals_stepwise_decode():
         # matmul vs matvec summation order can move a value across a rounding
         # boundary of the storage format: allow one step of that format, rarely
         ka, kb = a.cache.k[1], b.cache.k[1]
-        step = 2.0 ** -10 if kv == "fp16" else 2.0 ** -2
+        step = 2.0 ** -10 if kv == "fp16" else 2.0 ** -2   # E5M2 (scaled or not): 2 mantissa bits
         diff = ka != kb
         assert diff.mean() < 0.01
         assert np.all(np.abs(ka - kb)[diff] <= step * np.abs(kb)[diff] + 1e-7)
