@@ -91,8 +91,8 @@ def peaks():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ["autoregressive_decode_gb300/csrc/kie_decode.cu", "autoregressive_decode_gb300/csrc/kie_device.cuh",
-                  "autoregressive_decode_gb300/csrc/kie_internal.h"]
+KERNEL_SOURCES = ["autoregressive_decode_gb300/csrc/kie_decode.cu", "autoregressive_decode_gb300/csrc/kie_decode_core.cuh",
+                  "autoregressive_decode_gb300/csrc/kie_device.cuh", "autoregressive_decode_gb300/csrc/kie_internal.h"]
 
 
 def measured_traffic(w: S.Workload, bpl: float):
