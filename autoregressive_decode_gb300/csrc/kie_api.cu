@@ -50,7 +50,7 @@ extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0,
                                        cudaStream_t st);
 extern "C" cudaError_t kie_pf_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H,
                                         int hd, int kvfmt, int max_ctx, int pos0, int T, float scale, float* O,
-                                        cudaStream_t st);
+                                        uint64_t timeout_ns, int* err, cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_fp4(const uint16_t* w, int rows, int cols, uint8_t* packed, uint8_t* codes,
                                             uint8_t* bscales, float* rscales, cudaStream_t st);
 extern "C" cudaError_t kie_launch_quant_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
@@ -670,8 +670,7 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
             KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, colsc(a8, sb), to, err, st));
             KIE_CUDA(e, kie_pf_qkv_post(C, nqkv, Tn, pos, H, hd, inv_freq, kvf, kc, vc, l,
                                         c.max_ctx, Q, st));
-            KIE_CUDA(e, kie_pf_attention(Q, kc, vc, l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O,
-                                         st));
+            KIE_CUDA(e, kie_pf_attention(Q, kc, vc, l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O, to, err, st));
             KIE_CUDA(e, kie_pf_split(O, HD, Tn, Tp, HD, ahi, alo, st));
             KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, colsc(a8, sb + 3 * HD), to, err, st));
             KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));

@@ -4,7 +4,7 @@
 //   per layer:  u = RMSNorm(x) g1             kie_pf_norm_split   (fp32 -> fp16 hi + lo tiles)
 //               [q k v] = u Wqkv^T            kie_pf_gemm         (tcgen05, fp32 accumulate in TMEM)
 //               RoPE q, k; store k, v         kie_pf_qkv_post     (cache in its storage format)
-//               o = causal softmax(q k^T) v   kie_pf_attention    (reads the stored K/V, as decode does)
+//               o = causal softmax(q k^T) v   kie_pf_attention    (tcgen05; reads the stored K/V, as decode does)
 //               x += o Wo^T                   kie_pf_split, kie_pf_gemm, kie_pf_residual
 //               u = RMSNorm(x) g2             kie_pf_norm_split
 //               [g u] = u Wgu^T               kie_pf_gemm
@@ -300,124 +300,266 @@ __global__ void kie_pf_qkv_post_kernel(const float* __restrict__ C, int ldc, int
     }
 }
 
-// Causal attention of T query rows (positions pos0 + t) of head blockIdx.y over
-// the stored cache positions 0 .. pos0 + t.  A block takes 64 query rows; its
-// 256 threads are (row r = tid / 4, part c = tid % 4): part c scores keys
-// c + 4i of each 64-key tile and accumulates the output dims 16j + 4c .. +3.
-// Online softmax per row; the 4 parts of a row share the running max.
-template <int HD, int KVF>
-__global__ void __launch_bounds__(256) kie_pf_attention_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ kc,
-                                                               const uint8_t* __restrict__ vc, int layer, int H,
-                                                               int max_ctx, int pos0, int T, float scale,
-                                                               float* __restrict__ O) {
-    constexpr int LD = HD + 4, PLD = 68, ND = HD / 16;   // ND float4 groups of output dims per part
-    extern __shared__ __align__(16) float smf[];
-    float* Qs = smf;                 // [64][LD]
-    float* Ks = Qs + 64 * LD;        // [64][LD]
-    float* Vs = Ks + 64 * LD;        // [64][LD]
-    float* Ps = Vs + 64 * LD;        // [64][PLD]
-    const int h = blockIdx.y, q0 = blockIdx.x * 64, tid = threadIdx.x;
-    const int r = tid >> 2, c = tid & 3;
-    const int HDall = H * HD;
-    for (int i = tid; i < 64 * HD; i += 256) {
-        const int rr = i / HD, dd = i % HD;
-        Qs[rr * LD + dd] = (q0 + rr < T) ? Q[size_t(q0 + rr) * HDall + h * HD + dd] * scale : 0.f;
-    }
-    const int qpos = pos0 + q0 + r;                       // this thread's query position
-    const int last = pos0 + min(T, q0 + 64) - 1;          // the block's largest query position
-    float m = -INFINITY, l = 0.f;
-    float4 acc[ND];
+// ---- causal attention on the tensor cores ---------------------------------------------------
+// One CTA of 128 threads takes 128 query rows of one head; thread t owns query
+// row t (TMEM lane t) and its online softmax.  Per 128-key tile of the stored
+// cache (the values decode reads; E5M2 bytes become exact fp16):
+//   S = Q K^T     tcgen05.mma kind::f16, M 128 x N 128 keys, K = head_dim, into
+//                 TMEM columns [0, 128); Q (scaled by 1/sqrt(hd)) enters as
+//                 fp16 hi + lo, as in the GEMMs;
+//   softmax       each thread reads its row of S, masks keys after its position,
+//                 updates its running max m and sum l, rescales its row of O by
+//                 exp(m_old - m_new) (TMEM load / store), and writes
+//                 P = exp(S - m) as fp16 hi + lo into shared memory;
+//   O += P V      tcgen05.mma, M 128 x N head_dim, K = 128 keys, into TMEM columns
+//                 [128, 128 + head_dim), B = V^T (K-major: for each dim, the 128
+//                 keys), transposed 8 x 8 at a time while the tile is staged.
+// All operand tiles use the canonical no-swizzle K-major layout: element
+// (row, k) at (row/8)*SBO + (k/8)*128 + (row%8)*16 + (k%8)*2.
+template <int HD>
+struct AttnTc {
+    static constexpr uint32_t SBO_D = (HD / 8) * 128;   // Q and K tiles: K = head_dim
+    static constexpr uint32_t SBO_K = (128 / 8) * 128;  // P and V^T tiles: K = 128 keys
+    static constexpr uint32_t Q_BYTES = 128 * HD * 2, K_BYTES = 128 * HD * 2, V_BYTES = HD * 128 * 2,
+                              P_BYTES = 128 * 128 * 2;
+    static constexpr uint32_t SMEM = 2 * Q_BYTES + K_BYTES + V_BYTES + 2 * P_BYTES + 64;
+};
+
+__device__ __forceinline__ uint32_t kmaj(int row, int k, uint32_t sbo) {
+    return uint32_t(row >> 3) * sbo + uint32_t(k >> 3) * 128u + uint32_t(row & 7) * 16u + uint32_t(k & 7) * 2u;
+}
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// 8 fp32 values as fp16 hi (into *hi) and lo = fp16(v - hi) (into *lo)
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int j = 0; j < ND; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 4; ++i) {
+        const __half2 hh = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        const float2 f = __half22float2(hh);
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[i] = pack_half2(v[2 * i] - f.x, v[2 * i + 1] - f.y);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// 8 stored K or V values (fp16, or E5M2 bytes) of one position as fp16
+template <int KVF>
+__device__ __forceinline__ uint4 load8_f16(const uint8_t* base, size_t elem) {
+    if (KVF == KV_F16) return __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(base) + elem));
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(base + elem));   // E5M2 byte = fp16 top byte
+    return make_uint4(__byte_perm(b.x, 0u, 0x1404), __byte_perm(b.x, 0u, 0x3424), __byte_perm(b.y, 0u, 0x1404),
+                      __byte_perm(b.y, 0u, 0x3424));
+}
+
+template <int HD, int KVF>
+__global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ kc,
+                                                                const uint8_t* __restrict__ vc, int layer, int H,
+                                                                int max_ctx, int pos0, int T, float scale,
+                                                                float* __restrict__ O, uint64_t timeout_ns, int* err) {
+    using C = AttnTc<HD>;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    uint8_t* Qh = sm;
+    uint8_t* Ql = Qh + C::Q_BYTES;
+    uint8_t* Ks = Ql + C::Q_BYTES;
+    uint8_t* Vt = Ks + C::K_BYTES;
+    uint8_t* Ph = Vt + C::V_BYTES;
+    uint8_t* Pl = Ph + C::P_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(Pl + C::P_BYTES);   // [0] S ready, [1] O += P V done
+    uint32_t* taddr = reinterpret_cast<uint32_t*>(bar + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y, q0 = blockIdx.x * 128;
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(taddr, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = *taddr, tO = *taddr + 128u;
+    const int HDall = H * HD;
+    // Q block, scaled, as fp16 hi + lo tiles
+    for (int i = tid; i < 128 * (HD / 8); i += 128) {
+        const int r = i / (HD / 8), c8 = (i % (HD / 8)) * 8;
+        float v[8];
+        if (q0 + r < T) {
+            const float* src = Q + size_t(q0 + r) * HDall + size_t(h) * HD + c8;
+            const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+            v[0] = a.x * scale; v[1] = a.y * scale; v[2] = a.z * scale; v[3] = a.w * scale;
+            v[4] = b.x * scale; v[5] = b.y * scale; v[6] = b.z * scale; v[7] = b.w * scale;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        }
+        uint4 hi, lo;
+        split8(v, hi, lo);
+        *reinterpret_cast<uint4*>(Qh + kmaj(r, c8, C::SBO_D)) = hi;
+        *reinterpret_cast<uint4*>(Ql + kmaj(r, c8, C::SBO_D)) = lo;
+    }
+    const int row = warp * 32 + lane;                      // query row and TMEM lane of this thread
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const int qpos = pos0 + q0 + row;
+    const int last = pos0 + min(T, q0 + 128) - 1;          // the block's largest query position
+    const int ntile = last / 128 + 1;
     const size_t head_base = (size_t(layer) * H + h) * max_ctx;
-    for (int k0 = 0; k0 <= last; k0 += 64) {
-        __syncthreads();   // the previous tile's K, V, P are no longer read
-        for (int i = tid; i < 64 * HD; i += 256) {
-            const int jr = i / HD, dd = i % HD, j = k0 + jr;
-            float kv = 0.f, vv = 0.f;
-            if (j <= last) {
-                const size_t at = (head_base + j) * HD + dd;
-                if (KVF == KV_F16) {
-                    kv = __half2float(reinterpret_cast<const __half*>(kc)[at]);
-                    vv = __half2float(reinterpret_cast<const __half*>(vc)[at]);
-                } else {   // E5M2: the byte is the top half of an fp16
-                    kv = __half2float(__ushort_as_half((unsigned short)(uint32_t(kc[at]) << 8)));
-                    vv = __half2float(__ushort_as_half((unsigned short)(uint32_t(vc[at]) << 8)));
+    const uint32_t idesc_s = (1u << 4) | (uint32_t(128 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    const uint32_t idesc_o = (1u << 4) | (uint32_t(HD >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    int committed = 0;                                     // O commits issued (bar[1] phases to retire)
+    for (int kt = 0; kt < ntile && ok; ++kt) {
+        const int k0 = kt * 128;
+        // the previous tile's O += P V has read Vt, Ph, Pl (every decision below is
+        // CTA-uniform: the TMEM loads and stores are warp-collective)
+        if (kt > 0 && !__syncthreads_and(wait_bounded(&bar[1], uint32_t(kt - 1) & 1u, timeout_ns, err))) {
+            ok = false;
+            break;
+        }
+        // K tile (rows = keys) and V^T tile (rows = dims): 8 keys x 8 dims an item, dims fastest
+        for (int i = tid; i < 16 * (HD / 8); i += 128) {
+            const int db = i % (HD / 8), kb = i / (HD / 8);
+            uint4 kr[8], vr[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = k0 + kb * 8 + u;
+                if (j <= last && j < max_ctx) {
+                    const size_t at = (head_base + j) * HD + db * 8;
+                    kr[u] = load8_f16<KVF>(kc, at);
+                    vr[u] = load8_f16<KVF>(vc, at);
+                } else {
+                    kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            Ks[jr * LD + dd] = kv;
-            Vs[jr * LD + dd] = vv;
-        }
-        __syncthreads();
-        float s[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = 0.f;
-        for (int d4 = 0; d4 < HD; d4 += 4) {
-            const float4 qv = *reinterpret_cast<const float4*>(Qs + r * LD + d4);
+            for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(Ks + kmaj(kb * 8 + u, db * 8, C::SBO_D)) = kr[u];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 kv = *reinterpret_cast<const float4*>(Ks + (c + 4 * i) * LD + d4);
-                s[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, s[i]))));
+            for (int e = 0; e < 8; ++e) {   // dim db*8 + e over the 8 keys
+                const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+                const int wi = e >> 1;
+                const uint32_t w0 = __byte_perm((&vr[0].x)[wi], (&vr[1].x)[wi], sel);
+                const uint32_t w1 = __byte_perm((&vr[2].x)[wi], (&vr[3].x)[wi], sel);
+                const uint32_t w2 = __byte_perm((&vr[4].x)[wi], (&vr[5].x)[wi], sel);
+                const uint32_t w3 = __byte_perm((&vr[6].x)[wi], (&vr[7].x)[wi], sel);
+                *reinterpret_cast<uint4*>(Vt + kmaj(db * 8 + e, kb * 8, C::SBO_K)) = make_uint4(w0, w1, w2, w3);
             }
         }
+        fence_proxy_async_shared();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint64_t bd = smem_desc_noswz(Ks + kk * 256, 128, C::SBO_D);
+                tc_mma_f16(tS, smem_desc_noswz(Qh + kk * 256, 128, C::SBO_D), bd, idesc_s, kk != 0 ? 1u : 0u);
+                tc_mma_f16(tS, smem_desc_noswz(Ql + kk * 256, 128, C::SBO_D), bd, idesc_s, 1u);
+            }
+            tc_commit(&bar[0]);
+        }
+        __syncwarp();
+        if (!__syncthreads_and(wait_bounded(&bar[0], uint32_t(kt) & 1u, timeout_ns, err))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // this row's scores: the tile's maximum, then P = exp(S - m) as fp16 hi + lo
         float mt = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (k0 + c + 4 * i > qpos) s[i] = -INFINITY;
-            mt = fmaxf(mt, s[i]);
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t sv[32];
+            tmem_ld_32x32b_x32(tS + lane_off + uint32_t(c0), sv);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (k0 + c0 + e <= qpos) mt = fmaxf(mt, __uint_as_float(sv[e]));
         }
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
         const float mn = fmaxf(m, mt);
         const float cf = (m == -INFINITY) ? 0.f : expf(m - mn);
         float ps = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float p = (s[i] == -INFINITY) ? 0.f : expf(s[i] - mn);
-            Ps[r * PLD + c + 4 * i] = p;
-            ps += p;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t sv[32];
+            tmem_ld_32x32b_x32(tS + lane_off + uint32_t(c0), sv);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = k0 + c0 + 8 * g + e;
+                    p[e] = (j <= qpos && mn > -INFINITY) ? expf(__uint_as_float(sv[8 * g + e]) - mn) : 0.f;
+                    ps += p[e];
+                }
+                uint4 hi, lo;
+                split8(p, hi, lo);
+                *reinterpret_cast<uint4*>(Ph + kmaj(row, c0 + 8 * g, C::SBO_K)) = hi;
+                *reinterpret_cast<uint4*>(Pl + kmaj(row, c0 + 8 * g, C::SBO_K)) = lo;
+            }
         }
         l = l * cf + ps;
         m = mn;
+        if (kt > 0) {   // O row *= exp(m_old - m_new) before this tile's P V is added
 #pragma unroll
-        for (int j = 0; j < ND; ++j) { acc[j].x *= cf; acc[j].y *= cf; acc[j].z *= cf; acc[j].w *= cf; }
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld_32x32b_x32(tO + lane_off + uint32_t(c0), ov);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * cf);
+                tmem_st_32x32b_x32(tO + lane_off + uint32_t(c0), ov);
+            }
+        }
+        tc_fence_before();
+        fence_proxy_async_shared();
         __syncthreads();
-        for (int jr = 0; jr < 64; jr += 4) {
-            const float4 p4 = *reinterpret_cast<const float4*>(Ps + r * PLD + jr);
-            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+        if (tid == 0) {
+            tc_fence_after();
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int kk = 0; kk < 128 / 16; ++kk) {
+                const uint64_t bd = smem_desc_noswz(Vt + kk * 256, 128, C::SBO_K);
+                tc_mma_f16(tO, smem_desc_noswz(Ph + kk * 256, 128, C::SBO_K), bd, idesc_o,
+                           (kt > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_f16(tO, smem_desc_noswz(Pl + kk * 256, 128, C::SBO_K), bd, idesc_o, 1u);
+            }
+            tc_commit(&bar[1]);
+        }
+        __syncwarp();
+        committed = kt + 1;
+    }
+    // every issued O update has landed (also on the error path, bounded), then O / l
+    const bool done = __syncthreads_and(committed > 0 &&
+                                        wait_bounded(&bar[1], uint32_t(committed - 1) & 1u, timeout_ns, err));
+    tc_fence_after();
+    if (ok && done) {   // CTA-uniform; rows past T load with their warp but store nothing
+        float* orow = O + size_t(q0 + row) * HDall + size_t(h) * HD;
+        const float il = 1.f / l;
 #pragma unroll
-                for (int j = 0; j < ND; ++j) {
-                    const float4 v = *reinterpret_cast<const float4*>(Vs + (jr + u) * LD + 16 * j + 4 * c);
-                    acc[j].x = fmaf(pp[u], v.x, acc[j].x);
-                    acc[j].y = fmaf(pp[u], v.y, acc[j].y);
-                    acc[j].z = fmaf(pp[u], v.z, acc[j].z);
-                    acc[j].w = fmaf(pp[u], v.w, acc[j].w);
-                }
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tO + lane_off + uint32_t(c0), ov);
+            if (q0 + row < T) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(orow + c0 + e) =
+                        make_float4(__uint_as_float(ov[e]) * il, __uint_as_float(ov[e + 1]) * il,
+                                    __uint_as_float(ov[e + 2]) * il, __uint_as_float(ov[e + 3]) * il);
             }
         }
     }
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (q0 + r < T) {
-        float* orow = O + size_t(q0 + r) * HDall + h * HD;
-#pragma unroll
-        for (int j = 0; j < ND; ++j)
-            *reinterpret_cast<float4*>(orow + 16 * j + 4 * c) =
-                make_float4(acc[j].x / l, acc[j].y / l, acc[j].z / l, acc[j].w / l);
-    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(*taddr, 256);
 }
 
 template <int HD, int KVF>
 cudaError_t launch_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H, int max_ctx,
-                             int pos0, int T, float scale, float* O, cudaStream_t st) {
-    const size_t smem = size_t(3 * 64 * (HD + 4) + 64 * 68) * 4;
-    cudaError_t r = cudaFuncSetAttribute(kie_pf_attention_kernel<HD, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int pos0, int T, float scale, float* O, uint64_t timeout_ns, int* err, cudaStream_t st) {
+    const size_t smem = AttnTc<HD>::SMEM;
+    cudaError_t r = cudaFuncSetAttribute(kie_pf_attn_tc_kernel<HD, KVF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (r != cudaSuccess) return r;
-    kie_pf_attention_kernel<HD, KVF><<<dim3((T + 63) / 64, H), 256, smem, st>>>(Q, kc, vc, layer, H, max_ctx, pos0,
-                                                                                  T, scale, O);
+    kie_pf_attn_tc_kernel<HD, KVF><<<dim3((T + 127) / 128, H), 128, smem, st>>>(Q, kc, vc, layer, H, max_ctx, pos0,
+                                                                                  T, scale, O, timeout_ns, err);
     return cudaGetLastError();
 }
 
@@ -496,11 +638,13 @@ extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0,
 
 extern "C" cudaError_t kie_pf_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H,
                                         int hd, int kvfmt, int max_ctx, int pos0, int T, float scale, float* O,
-                                        cudaStream_t st) {
+                                        uint64_t timeout_ns, int* err, cudaStream_t st) {
     if (hd == 128) {
-        return kvfmt == KV_F16 ? launch_attention<128, KV_F16>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st)
-                               : launch_attention<128, KV_E5M2>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st);
+        return kvfmt == KV_F16
+                   ? launch_attention<128, KV_F16>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, timeout_ns, err, st)
+                   : launch_attention<128, KV_E5M2>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, timeout_ns, err, st);
     }
-    return kvfmt == KV_F16 ? launch_attention<64, KV_F16>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st)
-                           : launch_attention<64, KV_E5M2>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, st);
+    return kvfmt == KV_F16
+               ? launch_attention<64, KV_F16>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, timeout_ns, err, st)
+               : launch_attention<64, KV_E5M2>(Q, kc, vc, layer, H, max_ctx, pos0, T, scale, O, timeout_ns, err, st);
 }
