@@ -28,8 +28,8 @@ extern "C" cudaError_t kie_launch_copy_desc(uint8_t* dst, const uint8_t* src, co
                                             cudaStream_t st);
 // tensor-core prefill (kie_prefill.cu)
 extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const __half* W, float* C, int ldc,
-                                   int M_pad, int N_pad, int K, int m_valid, const float* col_scale,
-                                   uint64_t timeout_ns, int* err, cudaStream_t st);
+                                   int M_pad, int N_pad, int K, int m_valid, const float* col_scale, int ksplit,
+                                   size_t c_stride, uint64_t timeout_ns, int* err, cudaStream_t st);
 extern "C" cudaError_t kie_pf_pack_e4m3(const uint8_t* codes, int n, int K, int row0, __half* dst, cudaStream_t st);
 extern "C" cudaError_t kie_pf_pack_fp4(const uint8_t* codes, const uint8_t* bscales, int n, int K, int row0, __half* dst,
                                        cudaStream_t st);
@@ -44,10 +44,11 @@ extern "C" cudaError_t kie_pf_split(const float* src, int ld, int T, int T_pad, 
                                     cudaStream_t st);
 extern "C" cudaError_t kie_pf_swiglu_split(const float* C, int ldc, int T, int T_pad, int F, __half* hi, __half* lo,
                                            cudaStream_t st);
-extern "C" cudaError_t kie_pf_residual(float* x, const float* C, int ldc, int T, int d, cudaStream_t st);
-extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0, int H, int hd, const float* inv_freq,
-                                       int kvfmt, uint8_t* kc, uint8_t* vc, int layer, int max_ctx, float* Q,
+extern "C" cudaError_t kie_pf_residual(float* x, const float* C, int ldc, int T, int d, int ns, size_t c_stride,
                                        cudaStream_t st);
+extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0, int H, int hd, const float* inv_freq,
+                                       int kvfmt, uint8_t* kc, uint8_t* vc, int layer, int max_ctx, float* Q, int ns,
+                                       size_t c_stride, cudaStream_t st);
 extern "C" cudaError_t kie_pf_attention(const float* Q, const uint8_t* kc, const uint8_t* vc, int layer, int H,
                                         int hd, int kvfmt, int max_ctx, int pos0, int T, float scale, float* O,
                                         uint64_t timeout_ns, int* err, cudaStream_t st);
@@ -115,6 +116,7 @@ struct Layout {  // byte offsets into the workspace
     int pf_tc = 0;                    // prompt rows per prefill chunk (a multiple of 128)
     size_t pf_w, pf_layer_elems, pf_qkv, pf_o, pf_gu, pf_d, pf_lm;   // element offsets within a layer / of Wlm
     size_t pf_x, pf_ahi, pf_alo, pf_c, pf_q, pf_att, pf_err;
+    size_t pf_c_elems = 0;            // floats in pf_c
     size_t pf_sc, pf_sc_layer;        // FP8: output-column scales (floats) per layer [QKV | O | GU | D], then Wlm
     size_t total;
     int nseg;
@@ -383,6 +385,7 @@ void compute_layout(const kie_config& c, const Plan& pl, Layout& L) {
         L.pf_ahi = take(size_t(L.pf_tc) * kmax * 2);
         L.pf_alo = take(size_t(L.pf_tc) * kmax * 2);
         L.pf_c = take(nmax * 4);
+        L.pf_c_elems = nmax;
         L.pf_q = take(size_t(L.pf_tc) * HD * 4);
         L.pf_att = take(size_t(L.pf_tc) * HD * 4);
         L.pf_err = take(16);
@@ -624,6 +627,27 @@ kie_status run_steps(kie_engine* e, int n, int first_tok, const int32_t* d_force
     return KIE_OK;
 }
 
+// Split-K factor of a prefill GEMM with `tiles` 128 x 256 output tiles and KB
+// 64-column K tiles, on G SMs (one CTA each): s CTAs per output tile each take
+// KB / s of the K tiles and store a partial of c_elems floats; the s partials
+// must fit the cap_elems of the output buffer.  Chosen to minimise the
+// modelled time: waves of tiles * s CTAs x K tiles per CTA x the time of one
+// K tile (hi and lo MMAs: about 0.8 us, measured on the 1.8B prompt), plus
+// writing and re-reading each extra partial at about 6 TB/s.  An O or down
+// projection of a 1,024-row chunk has 64 tiles for 152 SMs: split 2 and 3 ways.
+int pf_ksplit(int tiles, int KB, size_t c_elems, size_t cap_elems, int G) {
+    constexpr double kKTileUs = 0.8, kBytesPerUs = 6.0e6;
+    double best = 0.0;
+    int bs = 1;
+    for (int s = 1; s <= 8 && s <= KB; ++s) {
+        if (size_t(s) * c_elems > cap_elems) break;
+        const double waves = double((int64_t(tiles) * s + G - 1) / G);
+        const double t = waves * std::ceil(double(KB) / s) * kKTileUs + double(s - 1) * double(c_elems) * 8.0 / kBytesPerUs;
+        if (s == 1 || t < best) { best = t; bs = s; }
+    }
+    return bs;
+}
+
 // Prompt prefill through the tensor-core path (kie_prefill.cu): chunks of up
 // to pf_tc prompt rows, each through all layers; the last row's logits.
 kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, float* last_logits) {
@@ -660,6 +684,11 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
     for (int c0 = 0; c0 < n; c0 += L.pf_tc) {
         Tn = std::min(L.pf_tc, n - c0);
         const int Tp = (Tn + 127) / 128 * 128, pos = pos_start + c0;
+        // split K where the output tiles alone leave SMs idle (partials Tp x N apart in C)
+        const size_t cap = L.pf_c_elems;
+        const int s_qkv = pf_ksplit((nqkv / 256) * (Tp / 128), d / 64, size_t(Tp) * nqkv, cap, e->G);
+        const int s_o = pf_ksplit((nd / 256) * (Tp / 128), HD / 64, size_t(Tp) * nd, cap, e->G);
+        const int s_d = pf_ksplit((nd / 256) * (Tp / 128), F / 64, size_t(Tp) * nd, cap, e->G);
         KIE_CUDA(e, kie_pf_embed(d_tok + c0, Tn, emb, d, x, st));
         for (int l = 0; l < c.n_layers; ++l) {
             const __half* W = pfw + L.pf_layer_elems * l;
@@ -667,27 +696,29 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
             const float* g1 = norms + size_t(2 * l) * d;
             const float* g2 = g1 + d;
             KIE_CUDA(e, kie_pf_norm_split(x, d, g1, c.rms_eps, Tn, Tp, d, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, colsc(a8, sb), to, err, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_qkv, C, nqkv, Tp, nqkv, d, Tn, colsc(a8, sb), s_qkv,
+                                    size_t(Tp) * nqkv, to, err, st));
             KIE_CUDA(e, kie_pf_qkv_post(C, nqkv, Tn, pos, H, hd, inv_freq, kvf, kc, vc, l,
-                                        c.max_ctx, Q, st));
+                                        c.max_ctx, Q, s_qkv, size_t(Tp) * nqkv, st));
             KIE_CUDA(e, kie_pf_attention(Q, kc, vc, l, H, hd, kvf, c.max_ctx, pos, Tn, scale, O, to, err, st));
             KIE_CUDA(e, kie_pf_split(O, HD, Tn, Tp, HD, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, colsc(a8, sb + 3 * HD), to, err, st));
-            KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_o, C, nd, Tp, nd, HD, Tn, colsc(a8, sb + 3 * HD), s_o,
+                                    size_t(Tp) * nd, to, err, st));
+            KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, s_o, size_t(Tp) * nd, st));
             KIE_CUDA(e, kie_pf_norm_split(x, d, g2, c.rms_eps, Tn, Tp, d, ahi, alo, st));
-            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_gu, C, ngu, Tp, ngu, d, Tn, colsc(f8, sb + 3 * HD + d), to, err,
-                                    st));
+            KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_gu, C, ngu, Tp, ngu, d, Tn, colsc(f8, sb + 3 * HD + d), 1, 0,
+                                    to, err, st));
             KIE_CUDA(e, kie_pf_swiglu_split(C, ngu, Tn, Tp, F, ahi, alo, st));
             KIE_CUDA(e, kie_pf_gemm(ahi, alo, W + L.pf_d, C, nd, Tp, nd, F, Tn,
-                                    colsc(f8, sb + 3 * HD + d + 2 * size_t(F)), to, err, st));
-            KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, st));
+                                    colsc(f8, sb + 3 * HD + d + 2 * size_t(F)), s_d, size_t(Tp) * nd, to, err, st));
+            KIE_CUDA(e, kie_pf_residual(x, C, nd, Tn, d, s_d, size_t(Tp) * nd, st));
         }
     }
     // logits of the last prompt row
     KIE_CUDA(e, kie_pf_norm_split(x + size_t(Tn - 1) * d, d, norms + size_t(2 * c.n_layers) * d, c.rms_eps, 1, 128, d,
                                   ahi, alo, st));
-    KIE_CUDA(e, kie_pf_gemm(ahi, alo, pfw + L.pf_lm, C, nv, 128, nv, d, 1, colsc(a8, L.pf_sc_layer * c.n_layers), to,
-                            err, st));
+    KIE_CUDA(e, kie_pf_gemm(ahi, alo, pfw + L.pf_lm, C, nv, 128, nv, d, 1, colsc(a8, L.pf_sc_layer * c.n_layers), 1, 0,
+                            to, err, st));
     int herr = 0;
     KIE_CUDA(e, cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
     KIE_CUDA(e, cudaStreamSynchronize(st));

@@ -62,20 +62,25 @@ __device__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns
 // C[m, n] = sum_k (Ahi + Alo)[m, k] W[n, k] for one 128 x 256 tile of C.
 // Thread 0 streams the K tiles (3-stage ring), thread 32 issues the MMAs, all
 // four warps then move their 32 TMEM lanes (rows) to C.  Rows >= m_valid are
-// not stored.  Every wait is bounded; a timeout sets *err.
+// not stored.  Split K (gridDim.z = s > 1): CTA z takes the 64-column K tiles
+// [z KB / s, (z+1) KB / s) and stores its partial sum at C + z * c_stride; the
+// next kernel adds the s partials in order.  Every wait is bounded; a timeout
+// sets *err.
 __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __restrict__ Ahi,
                                                              const __half* __restrict__ Alo,
                                                              const __half* __restrict__ W, float* __restrict__ C,
                                                              int ldc, int KB, int m_valid,
                                                              const float* __restrict__ col_scale,
-                                                             uint64_t timeout_ns, int* err) {
+                                                             size_t c_stride, uint64_t timeout_ns, int* err) {
     extern __shared__ __align__(1024) uint8_t sm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + STAGES * STAGE_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* done = empty + STAGES;
     uint32_t* taddr = reinterpret_cast<uint32_t*>(done + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nb = blockIdx.x, mb = blockIdx.y;
+    const int nb = blockIdx.x, mb = blockIdx.y, z = blockIdx.z, ns = gridDim.z;
+    const int kb0 = int((int64_t(z) * KB) / ns), kb1 = int((int64_t(z + 1) * KB) / ns), nkb = kb1 - kb0;
+    C += size_t(z) * c_stride;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         mbar_init(done, 1);
@@ -88,9 +93,9 @@ __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __res
     const uint32_t tacc = *taddr;
     const size_t a_off = size_t(mb) * KB * (BM * BK), w_off = size_t(nb) * KB * (BN * BK);
     if (threadIdx.x == 0) {
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % STAGES;
-            if (kb >= STAGES && !wait_bounded(&empty[s], uint32_t((kb / STAGES) - 1) & 1u, timeout_ns, err)) break;
+        for (int j = 0; j < nkb; ++j) {
+            const int s = j % STAGES, kb = kb0 + j;
+            if (j >= STAGES && !wait_bounded(&empty[s], uint32_t((j / STAGES) - 1) & 1u, timeout_ns, err)) break;
             uint8_t* dst = sm + s * STAGE_BYTES;
             mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
             bulk_g2s_keep(dst, Ahi + a_off + size_t(kb) * (BM * BK), A_BYTES, &full[s]);
@@ -102,15 +107,15 @@ __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __res
         // K-major, N / 8 in bits 17..22, M / 16 in bits 24..28
         const uint32_t idesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % STAGES;
-            if (!wait_bounded(&full[s], uint32_t(kb / STAGES) & 1u, timeout_ns, err)) { ok = false; break; }
+        for (int j = 0; j < nkb; ++j) {
+            const int s = j % STAGES;
+            if (!wait_bounded(&full[s], uint32_t(j / STAGES) & 1u, timeout_ns, err)) { ok = false; break; }
             tc_fence_after();
             const uint8_t* st = sm + s * STAGE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {   // K = 16 per MMA: two core matrices, 256 bytes
                 const uint64_t bd = smem_desc_noswz(st + 2 * A_BYTES + kk * 256, 128, 1024);
-                tc_mma_f16(tacc, smem_desc_noswz(st + kk * 256, 128, 1024), bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                tc_mma_f16(tacc, smem_desc_noswz(st + kk * 256, 128, 1024), bd, idesc, (j | kk) != 0 ? 1u : 0u);
                 tc_mma_f16(tacc, smem_desc_noswz(st + A_BYTES + kk * 256, 128, 1024), bd, idesc, 1u);
             }
             tc_commit(&empty[s]);
@@ -264,10 +269,19 @@ __global__ void kie_pf_swiglu_split_kernel(const float* __restrict__ C, int ldc,
     }
 }
 
+// Element (t, k) of a GEMM output stored as ns split-K partials c_stride apart,
+// added in partial order.
+__device__ __forceinline__ float c_sum(const float* C, size_t at, int ns, size_t c_stride) {
+    float v = C[at];
+    for (int z = 1; z < ns; ++z) v += C[size_t(z) * c_stride + at];
+    return v;
+}
+
 // x[t, :] += C[t, :d]
-__global__ void kie_pf_residual_kernel(float* __restrict__ x, const float* __restrict__ C, int ldc, int d) {
+__global__ void kie_pf_residual_kernel(float* __restrict__ x, const float* __restrict__ C, int ldc, int d, int ns,
+                                       size_t c_stride) {
     const int t = blockIdx.x;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) x[size_t(t) * d + k] += C[size_t(t) * ldc + k];
+    for (int k = threadIdx.x; k < d; k += blockDim.x) x[size_t(t) * d + k] += c_sum(C, size_t(t) * ldc + k, ns, c_stride);
 }
 
 // Rotate q and k of row t (position pos0 + t) by RoPE (half-split pairs), store
@@ -275,19 +289,21 @@ __global__ void kie_pf_residual_kernel(float* __restrict__ x, const float* __res
 // E5M2 from that fp16), and q (fp32) into Q[t][H*hd].
 __global__ void kie_pf_qkv_post_kernel(const float* __restrict__ C, int ldc, int pos0, int H, int hd,
                                        const float* __restrict__ inv_freq, int kvfmt, uint8_t* __restrict__ kc,
-                                       uint8_t* __restrict__ vc, int layer, int max_ctx, float* __restrict__ Q) {
+                                       uint8_t* __restrict__ vc, int layer, int max_ctx, float* __restrict__ Q, int ns,
+                                       size_t c_stride) {
     const int t = blockIdx.x, pos = pos0 + t, hh = hd / 2, HD = H * hd;
-    const float* row = C + size_t(t) * ldc;
+    const size_t row = size_t(t) * ldc;
     for (int u = threadIdx.x; u < H * hh; u += blockDim.x) {
         const int h = u / hh, i = u % hh;
         float sn, cs;
         sincosf(float(pos) * inv_freq[i], &sn, &cs);
         const int e0 = h * hd + i;
-        const float qa = row[e0], qb = row[e0 + hh];
+        const float qa = c_sum(C, row + e0, ns, c_stride), qb = c_sum(C, row + e0 + hh, ns, c_stride);
         Q[size_t(t) * HD + e0] = qa * cs - qb * sn;
         Q[size_t(t) * HD + e0 + hh] = qb * cs + qa * sn;
-        const float ka = row[HD + e0], kb = row[HD + e0 + hh];
-        const float kv[4] = {ka * cs - kb * sn, kb * cs + ka * sn, row[2 * HD + e0], row[2 * HD + e0 + hh]};
+        const float ka = c_sum(C, row + HD + e0, ns, c_stride), kb = c_sum(C, row + HD + e0 + hh, ns, c_stride);
+        const float kv[4] = {ka * cs - kb * sn, kb * cs + ka * sn, c_sum(C, row + 2 * HD + e0, ns, c_stride),
+                             c_sum(C, row + 2 * HD + e0 + hh, ns, c_stride)};
         const size_t base = ((size_t(layer) * H + h) * max_ctx + pos) * hd + i;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -569,12 +585,13 @@ cudaError_t launch_attention(const float* Q, const uint8_t* kc, const uint8_t* v
 extern "C" size_t kie_pf_tile_elems(int rows_pad, int K) { return size_t(rows_pad) * K; }
 
 extern "C" cudaError_t kie_pf_gemm(const __half* Ahi, const __half* Alo, const __half* W, float* C, int ldc,
-                                   int M_pad, int N_pad, int K, int m_valid, const float* col_scale,
-                                   uint64_t timeout_ns, int* err, cudaStream_t st) {
+                                   int M_pad, int N_pad, int K, int m_valid, const float* col_scale, int ksplit,
+                                   size_t c_stride, uint64_t timeout_ns, int* err, cudaStream_t st) {
+    if (ksplit < 1 || ksplit > K / BK) return cudaErrorInvalidValue;
     cudaError_t r = cudaFuncSetAttribute(kie_pf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(GEMM_SMEM));
     if (r != cudaSuccess) return r;
-    kie_pf_gemm_kernel<<<dim3(N_pad / BN, M_pad / BM), 128, GEMM_SMEM, st>>>(Ahi, Alo, W, C, ldc, K / BK, m_valid,
-                                                                            col_scale, timeout_ns, err);
+    kie_pf_gemm_kernel<<<dim3(N_pad / BN, M_pad / BM, ksplit), 128, GEMM_SMEM, st>>>(
+        Ahi, Alo, W, C, ldc, K / BK, m_valid, col_scale, c_stride, timeout_ns, err);
     return cudaGetLastError();
 }
 
@@ -624,15 +641,17 @@ extern "C" cudaError_t kie_pf_swiglu_split(const float* C, int ldc, int T, int T
     return cudaGetLastError();
 }
 
-extern "C" cudaError_t kie_pf_residual(float* x, const float* C, int ldc, int T, int d, cudaStream_t st) {
-    kie_pf_residual_kernel<<<T, 256, 0, st>>>(x, C, ldc, d);
+extern "C" cudaError_t kie_pf_residual(float* x, const float* C, int ldc, int T, int d, int ns, size_t c_stride,
+                                       cudaStream_t st) {
+    kie_pf_residual_kernel<<<T, 256, 0, st>>>(x, C, ldc, d, ns, c_stride);
     return cudaGetLastError();
 }
 
 extern "C" cudaError_t kie_pf_qkv_post(const float* C, int ldc, int T, int pos0, int H, int hd, const float* inv_freq,
-                                       int kvfmt, uint8_t* kc, uint8_t* vc, int layer, int max_ctx, float* Q,
-                                       cudaStream_t st) {
-    kie_pf_qkv_post_kernel<<<T, 256, 0, st>>>(C, ldc, pos0, H, hd, inv_freq, kvfmt, kc, vc, layer, max_ctx, Q);
+                                       int kvfmt, uint8_t* kc, uint8_t* vc, int layer, int max_ctx, float* Q, int ns,
+                                       size_t c_stride, cudaStream_t st) {
+    kie_pf_qkv_post_kernel<<<T, 256, 0, st>>>(C, ldc, pos0, H, hd, inv_freq, kvfmt, kc, vc, layer, max_ctx, Q, ns,
+                                              c_stride);
     return cudaGetLastError();
 }
 
