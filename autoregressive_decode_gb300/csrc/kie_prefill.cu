@@ -200,10 +200,33 @@ __global__ void kie_pf_pack_fp4_kernel(const uint8_t* __restrict__ codes, const 
     }
 }
 
-__device__ __forceinline__ void put_split(__half* hi, __half* lo, size_t idx, float v) {
-    const __half h = __float2half_rn(v);
-    hi[idx] = h;
-    lo[idx] = __float2half_rn(v - __half2float(h));
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// 8 fp32 values as fp16 hi (into *hi) and lo = fp16(v - hi) (into *lo)
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 hh = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        const float2 f = __half22float2(hh);
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[i] = pack_half2(v[2 * i] - f.x, v[2 * i + 1] - f.y);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// Columns [k8, k8 + 8) of row t (8-aligned: 16 contiguous bytes of a tile) as hi / lo.
+__device__ __forceinline__ void put_split8(__half* hi, __half* lo, size_t idx, const float* v) {
+    uint4 h, l;
+    split8(v, h, l);
+    *reinterpret_cast<uint4*>(hi + idx) = h;
+    *reinterpret_cast<uint4*>(lo + idx) = l;
+}
+__device__ __forceinline__ void load8(const float* p, float* v) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 __device__ __forceinline__ float block_sum256(float v, float* red) {
@@ -226,46 +249,62 @@ __global__ void kie_pf_embed_kernel(const int32_t* __restrict__ tokens, const ui
 }
 
 // Rows [0, T) of x (row stride ld): u = x / sqrt(mean(x^2) + eps) * g split into
-// hi / lo tiles of 128 rows; rows [T, T_pad) are written as zeros.  256 threads per row.
+// hi / lo tiles of 128 rows; rows [T, T_pad) are written as zeros.  256 threads
+// per row, 8 consecutive columns a thread at a time (16-byte tile stores).
 __global__ void kie_pf_norm_split_kernel(const float* __restrict__ x, int ld, const float* __restrict__ g, float eps,
                                          int T, int d, __half* __restrict__ hi, __half* __restrict__ lo) {
     __shared__ float red[8];
     const int t = blockIdx.x, KB = d / 64;
     if (t >= T) {
-        for (int k = threadIdx.x; k < d; k += blockDim.x) {
-            const size_t idx = tile_idx(t, k, BM, KB);
-            hi[idx] = __float2half_rn(0.f);
-            lo[idx] = __float2half_rn(0.f);
-        }
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k8 = 8 * threadIdx.x; k8 < d; k8 += 8 * blockDim.x) put_split8(hi, lo, tile_idx(t, k8, BM, KB), z);
         return;
     }
     const float* xr = x + size_t(t) * ld;
     float ss = 0.f;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) ss += xr[k] * xr[k];
+    for (int k8 = 8 * threadIdx.x; k8 < d; k8 += 8 * blockDim.x) {
+        float v[8];
+        load8(xr + k8, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
+    }
     ss = block_sum256(ss, red);
     const float r = sqrtf(ss / float(d) + eps);
-    for (int k = threadIdx.x; k < d; k += blockDim.x) put_split(hi, lo, tile_idx(t, k, BM, KB), xr[k] / r * g[k]);
+    for (int k8 = 8 * threadIdx.x; k8 < d; k8 += 8 * blockDim.x) {
+        float v[8], gv[8];
+        load8(xr + k8, v);
+        load8(g + k8, gv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = v[e] / r * gv[e];
+        put_split8(hi, lo, tile_idx(t, k8, BM, KB), v);
+    }
 }
 
 // Rows [0, T) of src (row stride ld, K columns) split into hi / lo tiles; rows [T, T_pad) zero.
 __global__ void kie_pf_split_kernel(const float* __restrict__ src, int ld, int T, int K, __half* __restrict__ hi,
                                     __half* __restrict__ lo) {
     const int t = blockIdx.x, KB = K / 64;
-    for (int k = threadIdx.x; k < K; k += blockDim.x)
-        put_split(hi, lo, tile_idx(t, k, BM, KB), t < T ? src[size_t(t) * ld + k] : 0.f);
+    for (int k8 = 8 * threadIdx.x; k8 < K; k8 += 8 * blockDim.x) {
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (t < T) load8(src + size_t(t) * ld + k8, v);
+        put_split8(hi, lo, tile_idx(t, k8, BM, KB), v);
+    }
 }
 
 // a = silu(C[:, i]) * C[:, F + i], split into hi / lo tiles; rows [T, T_pad) zero.
 __global__ void kie_pf_swiglu_split_kernel(const float* __restrict__ C, int ldc, int T, int F, __half* __restrict__ hi,
                                            __half* __restrict__ lo) {
     const int t = blockIdx.x, KB = F / 64;
-    for (int i = threadIdx.x; i < F; i += blockDim.x) {
-        float a = 0.f;
+    for (int i8 = 8 * threadIdx.x; i8 < F; i8 += 8 * blockDim.x) {
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (t < T) {
-            const float gt = C[size_t(t) * ldc + i], up = C[size_t(t) * ldc + F + i];
-            a = (gt / (1.f + expf(-gt))) * up;
+            float gt[8], up[8];
+            load8(C + size_t(t) * ldc + i8, gt);
+            load8(C + size_t(t) * ldc + F + i8, up);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] = (gt[e] / (1.f + expf(-gt[e]))) * up[e];
         }
-        put_split(hi, lo, tile_idx(t, i, BM, KB), a);
+        put_split8(hi, lo, tile_idx(t, i8, BM, KB), a);
     }
 }
 
@@ -281,7 +320,16 @@ __device__ __forceinline__ float c_sum(const float* C, size_t at, int ns, size_t
 __global__ void kie_pf_residual_kernel(float* __restrict__ x, const float* __restrict__ C, int ldc, int d, int ns,
                                        size_t c_stride) {
     const int t = blockIdx.x;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) x[size_t(t) * d + k] += c_sum(C, size_t(t) * ldc + k, ns, c_stride);
+    for (int k4 = 4 * threadIdx.x; k4 < d; k4 += 4 * blockDim.x) {
+        float4 v = *reinterpret_cast<const float4*>(C + size_t(t) * ldc + k4);
+        for (int z = 1; z < ns; ++z) {
+            const float4 w = *reinterpret_cast<const float4*>(C + size_t(z) * c_stride + size_t(t) * ldc + k4);
+            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        }
+        float4* xp = reinterpret_cast<float4*>(x + size_t(t) * d + k4);
+        const float4 o = *xp;
+        *xp = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+    }
 }
 
 // Rotate q and k of row t (position pos0 + t) by RoPE (half-split pairs), store
@@ -343,23 +391,6 @@ struct AttnTc {
 
 __device__ __forceinline__ uint32_t kmaj(int row, int k, uint32_t sbo) {
     return uint32_t(row >> 3) * sbo + uint32_t(k >> 3) * 128u + uint32_t(row & 7) * 16u + uint32_t(k & 7) * 2u;
-}
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-    const __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-// 8 fp32 values as fp16 hi (into *hi) and lo = fp16(v - hi) (into *lo)
-__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half2 hh = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-        const float2 f = __half22float2(hh);
-        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
-        l[i] = pack_half2(v[2 * i] - f.x, v[2 * i + 1] - f.y);
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 // 8 stored K or V values (fp16, or E5M2 bytes) of one position as fp16
 template <int KVF>
