@@ -627,14 +627,15 @@ kie_status run_steps(kie_engine* e, int n, int first_tok, const int32_t* d_force
     return KIE_OK;
 }
 
-// Split-K factor of a prefill GEMM with `tiles` 128 x 256 output tiles and KB
-// 64-column K tiles, on G SMs (one CTA each): s CTAs per output tile each take
-// KB / s of the K tiles and store a partial of c_elems floats; the s partials
-// must fit the cap_elems of the output buffer.  Chosen to minimise the
-// modelled time: waves of tiles * s CTAs x K tiles per CTA x the time of one
-// K tile (hi and lo MMAs: about 0.8 us, measured on the 1.8B prompt), plus
-// writing and re-reading each extra partial at about 6 TB/s.  An O or down
-// projection of a 1,024-row chunk has 64 tiles for 152 SMs: split 2 and 3 ways.
+// Split-K factor of a prefill GEMM with `tiles` output tiles (128 rows x
+// KIE_PF_BN columns) and KB 64-column K tiles, on G resident CTA slots: s CTAs
+// per output tile each take KB / s of the K tiles and store a partial of
+// c_elems floats; the s partials must fit the cap_elems of the output buffer.
+// Chosen to minimise the modelled time: waves of tiles * s CTAs x K tiles per
+// CTA x the time of one K tile on a CTA slot (hi and lo MMAs: about 0.8 us,
+// measured on the 1.8B prompt), plus writing and re-reading each extra
+// partial at about 6 TB/s.  The O and down projections of a 1,024-row chunk
+// have few output tiles for the GPU's slots and are split.
 int pf_ksplit(int tiles, int KB, size_t c_elems, size_t cap_elems, int G) {
     constexpr double kKTileUs = 0.8, kBytesPerUs = 6.0e6;
     double best = 0.0;
@@ -686,9 +687,10 @@ kie_status prefill_tensor_cores(kie_engine* e, const int32_t* tokens, int n, flo
         const int Tp = (Tn + 127) / 128 * 128, pos = pos_start + c0;
         // split K where the output tiles alone leave SMs idle (partials Tp x N apart in C)
         const size_t cap = L.pf_c_elems;
-        const int s_qkv = pf_ksplit((nqkv / 256) * (Tp / 128), d / 64, size_t(Tp) * nqkv, cap, e->G);
-        const int s_o = pf_ksplit((nd / 256) * (Tp / 128), HD / 64, size_t(Tp) * nd, cap, e->G);
-        const int s_d = pf_ksplit((nd / 256) * (Tp / 128), F / 64, size_t(Tp) * nd, cap, e->G);
+        const int slots = e->G * (KIE_PF_BN == 128 ? 2 : 1);   // GEMM CTAs resident at once
+        const int s_qkv = pf_ksplit((nqkv / KIE_PF_BN) * (Tp / 128), d / 64, size_t(Tp) * nqkv, cap, slots);
+        const int s_o = pf_ksplit((nd / KIE_PF_BN) * (Tp / 128), HD / 64, size_t(Tp) * nd, cap, slots);
+        const int s_d = pf_ksplit((nd / KIE_PF_BN) * (Tp / 128), F / 64, size_t(Tp) * nd, cap, slots);
         KIE_CUDA(e, kie_pf_embed(d_tok + c0, Tn, emb, d, x, st));
         for (int l = 0; l < c.n_layers; ++l) {
             const __half* W = pfw + L.pf_layer_elems * l;

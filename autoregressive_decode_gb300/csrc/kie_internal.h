@@ -41,6 +41,11 @@
 #define KIE_SLOT_BYTES 16384     // slot capacity (KIE_R rows x KIE_KC_F16 fp16); 8 KB slots measured slower
 #endif
 #define KIE_MAX_SLOTS 16
+// prefill GEMM output tile columns: 256 (one CTA per SM) or 128 (two CTAs per
+// SM; measured slower, 1.8B 2,048-token prompt 25.0 vs 23.4 ms)
+#ifndef KIE_PF_BN
+#define KIE_PF_BN 256
+#endif
 #ifndef KIE_REPL
 #define KIE_REPL 2               // copies of the activations x, a, o that CTAs exchange (readers poll copy cta % KIE_REPL)
 #endif

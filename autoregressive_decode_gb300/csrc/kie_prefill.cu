@@ -39,9 +39,17 @@ using namespace kie;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
+// Output tiles of BM x BN.  Weights are packed in tiles of WT = 256 rows; a
+// 128-column output tile reads one half of a weight tile (its rows 0-127 or
+// 128-255 are 16 KB apart in the canonical layout).  BN = 256 (the default)
+// runs one CTA per SM with 3 stages of 64 KB; BN = 128 two CTAs per SM with 2
+// stages of 48 KB each, overlapping one CTA's epilogue with the other's MMAs,
+// and measured slower.
+constexpr int BM = 128, BN = KIE_PF_BN, BK = 64, WT = 256;
+constexpr int STAGES = BN == 256 ? 3 : 2, GEMM_CTAS_PER_SM = BN == 256 ? 1 : 2;
+static_assert(BN == 128 || BN == 256, "output tile width");
 constexpr uint32_t A_BYTES = BM * BK * 2;                 // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;                 // 32 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;                 // 16 or 32 KB
 constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + B_BYTES;   // A hi, A lo, B
 constexpr uint32_t GEMM_SMEM = STAGES * STAGE_BYTES + 256;
 
@@ -66,7 +74,7 @@ __device__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns
 // [z KB / s, (z+1) KB / s) and stores its partial sum at C + z * c_stride; the
 // next kernel adds the s partials in order.  Every wait is bounded; a timeout
 // sets *err.
-__global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __restrict__ Ahi,
+__global__ void __launch_bounds__(128, GEMM_CTAS_PER_SM) kie_pf_gemm_kernel(const __half* __restrict__ Ahi,
                                                              const __half* __restrict__ Alo,
                                                              const __half* __restrict__ W, float* __restrict__ C,
                                                              int ldc, int KB, int m_valid,
@@ -86,12 +94,13 @@ __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __res
         mbar_init(done, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(taddr, BN);   // 128 lanes x 256 fp32 columns
+    if (warp == 0) tmem_alloc(taddr, BN);   // 128 lanes x BN fp32 columns
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tacc = *taddr;
-    const size_t a_off = size_t(mb) * KB * (BM * BK), w_off = size_t(nb) * KB * (BN * BK);
+    const size_t a_off = size_t(mb) * KB * (BM * BK);
+    const size_t w_off = size_t(nb * BN / WT) * KB * (WT * BK) + size_t((nb * BN) % WT) * BK;
     if (threadIdx.x == 0) {
         for (int j = 0; j < nkb; ++j) {
             const int s = j % STAGES, kb = kb0 + j;
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_gemm_kernel(const __half* __res
             mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
             bulk_g2s_keep(dst, Ahi + a_off + size_t(kb) * (BM * BK), A_BYTES, &full[s]);
             bulk_g2s_keep(dst + A_BYTES, Alo + a_off + size_t(kb) * (BM * BK), A_BYTES, &full[s]);
-            bulk_g2s_keep(dst + 2 * A_BYTES, W + w_off + size_t(kb) * (BN * BK), B_BYTES, &full[s]);
+            bulk_g2s_keep(dst + 2 * A_BYTES, W + w_off + size_t(kb) * (WT * BK), B_BYTES, &full[s]);
         }
     } else if (threadIdx.x == 32) {
         // kind::f16 instruction descriptor: fp32 D (bit 4), fp16 A and B, both
@@ -155,7 +164,7 @@ __global__ void kie_pf_pack_kernel(const __half* __restrict__ src, int n, int K,
     const int KB = K / 64, g8 = K / 8;
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < size_t(n) * g8; i += size_t(gridDim.x) * blockDim.x) {
         const int r = int(i / g8), k = int(i % g8) * 8;
-        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) =
+        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, WT, KB)) =
             *reinterpret_cast<const uint4*>(src + size_t(r) * K + k);
     }
 }
@@ -173,7 +182,7 @@ __global__ void kie_pf_pack_e4m3_kernel(const uint8_t* __restrict__ src, int n, 
         __align__(16) __half h[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(f[j]);   // exact: E4M3 values are fp16 values
-        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) = *reinterpret_cast<const uint4*>(h);
+        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, WT, KB)) = *reinterpret_cast<const uint4*>(h);
     }
 }
 
@@ -196,7 +205,7 @@ __global__ void kie_pf_pack_fp4_kernel(const uint8_t* __restrict__ codes, const 
             h[2 * j] = __float2half_rn(v.x * bs[0]);       // exact (see above)
             h[2 * j + 1] = __float2half_rn(v.y * bs[0]);
         }
-        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, BN, KB)) = *reinterpret_cast<const uint4*>(h);
+        *reinterpret_cast<uint4*>(dst + tile_idx(row0 + r, k, WT, KB)) = *reinterpret_cast<const uint4*>(h);
     }
 }
 
