@@ -83,12 +83,6 @@ __device__ __forceinline__ uint4 frag_quad(float2 a, float2 c) {
                       *reinterpret_cast<const uint32_t*>(&hc), *reinterpret_cast<const uint32_t*>(&lc));
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
 __device__ __forceinline__ float2 ld_relaxed_f2(const float* p) {
     float2 v;
     asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));

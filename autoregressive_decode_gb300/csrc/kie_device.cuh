@@ -218,6 +218,19 @@ __device__ __forceinline__ int32_t ld_volatile_i32(const int32_t* p) {
     return *reinterpret_cast<const volatile int32_t*>(p);
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all of this thread's.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+// The same with the source read only when `valid` (zeros otherwise).
+__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(smem_u32(smem)), "l"(gmem), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Named barrier among the consumer warps only (the producer warp never joins).
 __device__ __forceinline__ void consumer_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");

@@ -467,6 +467,18 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     int committed = 0;                                     // O commits issued (bar[1] phases to retire)
+    // fp16 cache: K tiles land by asynchronous copies straight into Ks, the next
+    // one issued as soon as the tile's S = Q K^T has read Ks, so its latency
+    // passes during the softmax and O += P V (E5M2 goes through registers)
+    auto k_async = [&](int k0) {
+        for (int i = tid; i < 128 * (HD / 8); i += 128) {
+            const int key = i / (HD / 8), db = i % (HD / 8), j = k0 + key;
+            const bool valid = j <= last && j < max_ctx;
+            const uint8_t* src = kc + ((head_base + (valid ? j : 0)) * HD + db * 8) * 2;
+            cp_async16_zfill(Ks + kmaj(key, db * 8, C::SBO_D), src, valid);
+        }
+    };
+    if (KVF == KV_F16) k_async(0);
     for (int kt = 0; kt < ntile && ok; ++kt) {
         const int k0 = kt * 128;
         // the previous tile's O += P V has read Vt, Ph, Pl (every decision below is
@@ -484,14 +496,16 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
                 const int j = k0 + kb * 8 + u;
                 if (j <= last && j < max_ctx) {
                     const size_t at = (head_base + j) * HD + db * 8;
-                    kr[u] = load8_f16<KVF>(kc, at);
+                    if (KVF != KV_F16) kr[u] = load8_f16<KVF>(kc, at);
                     vr[u] = load8_f16<KVF>(vc, at);
                 } else {
                     kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
+            if (KVF != KV_F16) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(Ks + kmaj(kb * 8 + u, db * 8, C::SBO_D)) = kr[u];
+                for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(Ks + kmaj(kb * 8 + u, db * 8, C::SBO_D)) = kr[u];
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {   // dim db*8 + e over the 8 keys
                 const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
@@ -503,6 +517,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
                 *reinterpret_cast<uint4*>(Vt + kmaj(db * 8 + e, kb * 8, C::SBO_K)) = make_uint4(w0, w1, w2, w3);
             }
         }
+        if (KVF == KV_F16) cp_async_wait_all();   // this thread's copies of the K tile have landed
         fence_proxy_async_shared();
         __syncthreads();
         if (tid == 0) {
@@ -521,6 +536,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
             break;
         }
         tc_fence_after();
+        if (KVF == KV_F16 && kt + 1 < ntile) k_async(k0 + 128);   // S has read Ks
         // this row's scores: the tile's maximum, then P = exp(S - m) as fp16 hi + lo
         float mt = -INFINITY;
 #pragma unroll
@@ -582,6 +598,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
         __syncwarp();
         committed = kt + 1;
     }
+    if (KVF == KV_F16) cp_async_wait_all();   // no copy of a K tile is left in flight (error paths)
     // every issued O update has landed (also on the error path, bounded), then O / l
     const bool done = __syncthreads_and(committed > 0 &&
                                         wait_bounded(&bar[1], uint32_t(committed - 1) & 1u, timeout_ns, err));
