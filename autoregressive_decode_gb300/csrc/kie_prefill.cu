@@ -343,33 +343,67 @@ __global__ void kie_pf_residual_kernel(float* __restrict__ x, const float* __res
 
 // Rotate q and k of row t (position pos0 + t) by RoPE (half-split pairs), store
 // k and v into the cache in its storage format (fp16 round to nearest even;
-// E5M2 from that fp16), and q (fp32) into Q[t][H*hd].
+// E5M2 from that fp16), and q (fp32) into Q[t][H*hd].  A thread takes 4
+// consecutive pair indices i (hd / 2 is a multiple of 4): 16-byte loads of the
+// GEMM's partials and of q, 8- or 4-byte cache stores.
+__device__ __forceinline__ float4 c_sum4(const float* C, size_t at, int ns, size_t c_stride) {
+    float4 v = *reinterpret_cast<const float4*>(C + at);
+    for (int z = 1; z < ns; ++z) {
+        const float4 w = *reinterpret_cast<const float4*>(C + size_t(z) * c_stride + at);
+        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+    }
+    return v;
+}
+__device__ __forceinline__ void store4(uint8_t* cache, size_t at, int kvfmt, const float* v) {
+    __half h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __float2half_rn(v[e]);
+    if (kvfmt == KV_F16) {
+        uint2 w;
+        w.x = uint32_t(__half_as_ushort(h[0])) | (uint32_t(__half_as_ushort(h[1])) << 16);
+        w.y = uint32_t(__half_as_ushort(h[2])) | (uint32_t(__half_as_ushort(h[3])) << 16);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(cache) + at) = w;
+    } else {
+        uint32_t w = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w |= (uint32_t(f16x2_to_e5m2x2(h[e], h[e])) & 0xFFu) << (8 * e);
+        *reinterpret_cast<uint32_t*>(cache + at) = w;
+    }
+}
 __global__ void kie_pf_qkv_post_kernel(const float* __restrict__ C, int ldc, int pos0, int H, int hd,
                                        const float* __restrict__ inv_freq, int kvfmt, uint8_t* __restrict__ kc,
                                        uint8_t* __restrict__ vc, int layer, int max_ctx, float* __restrict__ Q, int ns,
                                        size_t c_stride) {
     const int t = blockIdx.x, pos = pos0 + t, hh = hd / 2, HD = H * hd;
     const size_t row = size_t(t) * ldc;
-    for (int u = threadIdx.x; u < H * hh; u += blockDim.x) {
-        const int h = u / hh, i = u % hh;
-        float sn, cs;
-        sincosf(float(pos) * inv_freq[i], &sn, &cs);
-        const int e0 = h * hd + i;
-        const float qa = c_sum(C, row + e0, ns, c_stride), qb = c_sum(C, row + e0 + hh, ns, c_stride);
-        Q[size_t(t) * HD + e0] = qa * cs - qb * sn;
-        Q[size_t(t) * HD + e0 + hh] = qb * cs + qa * sn;
-        const float ka = c_sum(C, row + HD + e0, ns, c_stride), kb = c_sum(C, row + HD + e0 + hh, ns, c_stride);
-        const float kv[4] = {ka * cs - kb * sn, kb * cs + ka * sn, c_sum(C, row + 2 * HD + e0, ns, c_stride),
-                             c_sum(C, row + 2 * HD + e0 + hh, ns, c_stride)};
-        const size_t base = ((size_t(layer) * H + h) * max_ctx + pos) * hd + i;
+    for (int u4 = threadIdx.x; u4 < H * hh / 4; u4 += blockDim.x) {
+        const int u = 4 * u4, h = u / hh, i = u % hh;
+        float sn[4], cs[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint8_t* cache = j < 2 ? kc : vc;
-            const size_t at = base + ((j & 1) ? hh : 0);
-            const __half hv = __float2half_rn(kv[j]);
-            if (kvfmt == KV_F16) reinterpret_cast<__half*>(cache)[at] = hv;
-            else cache[at] = uint8_t(f16x2_to_e5m2x2(hv, hv) & 0xFFu);
+        for (int e = 0; e < 4; ++e) sincosf(float(pos) * inv_freq[i + e], &sn[e], &cs[e]);
+        const int e0 = h * hd + i;
+        const float4 qa4 = c_sum4(C, row + e0, ns, c_stride), qb4 = c_sum4(C, row + e0 + hh, ns, c_stride);
+        const float4 ka4 = c_sum4(C, row + HD + e0, ns, c_stride), kb4 = c_sum4(C, row + HD + e0 + hh, ns, c_stride);
+        const float4 va4 = c_sum4(C, row + 2 * HD + e0, ns, c_stride);
+        const float4 vb4 = c_sum4(C, row + 2 * HD + e0 + hh, ns, c_stride);
+        const float qa[4] = {qa4.x, qa4.y, qa4.z, qa4.w}, qb[4] = {qb4.x, qb4.y, qb4.z, qb4.w};
+        const float ka[4] = {ka4.x, ka4.y, ka4.z, ka4.w}, kb[4] = {kb4.x, kb4.y, kb4.z, kb4.w};
+        float q0[4], q1[4], k0[4], k1[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            q0[e] = qa[e] * cs[e] - qb[e] * sn[e];
+            q1[e] = qb[e] * cs[e] + qa[e] * sn[e];
+            k0[e] = ka[e] * cs[e] - kb[e] * sn[e];
+            k1[e] = kb[e] * cs[e] + ka[e] * sn[e];
         }
+        *reinterpret_cast<float4*>(Q + size_t(t) * HD + e0) = make_float4(q0[0], q0[1], q0[2], q0[3]);
+        *reinterpret_cast<float4*>(Q + size_t(t) * HD + e0 + hh) = make_float4(q1[0], q1[1], q1[2], q1[3]);
+        const size_t base = ((size_t(layer) * H + h) * max_ctx + pos) * hd + i;
+        const float v0[4] = {va4.x, va4.y, va4.z, va4.w}, v1[4] = {vb4.x, vb4.y, vb4.z, vb4.w};
+        store4(kc, base, kvfmt, k0);
+        store4(kc, base + hh, kvfmt, k1);
+        store4(vc, base, kvfmt, v0);
+        store4(vc, base + hh, kvfmt, v1);
     }
 }
 
@@ -571,7 +605,9 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
         }
         l = l * cf + ps;
         m = mn;
-        if (kt > 0) {   // O row *= exp(m_old - m_new) before this tile's P V is added
+        // O row *= exp(m_old - m_new) before this tile's P V is added; a warp whose
+        // rows all kept their maximum (factor exactly 1) skips the TMEM round trip
+        if (kt > 0 && __any_sync(0xffffffffu, cf != 1.f)) {
 #pragma unroll
             for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t ov[32];
