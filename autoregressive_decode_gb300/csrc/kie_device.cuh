@@ -230,6 +230,11 @@ __device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, b
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
+// Close the current group of this thread's asynchronous copies; wait until at
+// most N of its groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // Named barrier among the consumer warps only (the producer warp never joins).
 __device__ __forceinline__ void consumer_sync(int nthreads) {

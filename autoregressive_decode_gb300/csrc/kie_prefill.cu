@@ -423,6 +423,17 @@ __global__ void kie_pf_qkv_post_kernel(const float* __restrict__ C, int ldc, int
 //                 keys), transposed 8 x 8 at a time while the tile is staged.
 // All operand tiles use the canonical no-swizzle K-major layout: element
 // (row, k) at (row/8)*SBO + (k/8)*128 + (row%8)*16 + (k%8)*2.
+// V tile layout: 0 (default) = V^T K-major, transposed 8 x 8 through registers
+// while staged; 1 = V as stored (keys x dims, dims contiguous) in the MN-major
+// canonical layout, fp16 copied asynchronously like K, the MMA's B operand
+// marked MN-major.  For the MN-major operand the descriptor keeps the roles of
+// its two byte offsets: the leading one steps along K (here the keys: 8 keys,
+// SBO_D bytes), the stride one along N (the dims: 8 dims, 128 bytes); read the
+// other way round the prefill parity tests fail.  Both are parity-green; 1 was
+// not faster (1.8B 2,048-token prompt 22.9 ms either way).
+#ifndef KIE_PF_VMN
+#define KIE_PF_VMN 0
+#endif
 template <int HD>
 struct AttnTc {
     static constexpr uint32_t SBO_D = (HD / 8) * 128;   // Q and K tiles: K = head_dim
@@ -432,6 +443,11 @@ struct AttnTc {
     static constexpr uint32_t SMEM = 2 * Q_BYTES + K_BYTES + V_BYTES + 2 * P_BYTES + 64;
 };
 
+// MN-major V tile: element (key, dim) in 8-key x 8-dim core matrices of 128 bytes,
+// 128 bytes apart along the dims and sbo_k apart along the keys.
+__device__ __forceinline__ uint32_t vmn(int key, int dim, uint32_t sbo_k) {
+    return uint32_t(dim >> 3) * 128u + uint32_t(key >> 3) * sbo_k + uint32_t(key & 7) * 16u + uint32_t(dim & 7) * 2u;
+}
 __device__ __forceinline__ uint32_t kmaj(int row, int k, uint32_t sbo) {
     return uint32_t(row >> 3) * sbo + uint32_t(k >> 3) * 128u + uint32_t(row & 7) * 16u + uint32_t(k & 7) * 2u;
 }
@@ -497,7 +513,9 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
     const int ntile = last / 128 + 1;
     const size_t head_base = (size_t(layer) * H + h) * max_ctx;
     const uint32_t idesc_s = (1u << 4) | (uint32_t(128 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
-    const uint32_t idesc_o = (1u << 4) | (uint32_t(HD >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    // B = V: K-major V^T, or (KIE_PF_VMN) MN-major V (transpose-B bit 16)
+    const uint32_t idesc_o = (1u << 4) | (KIE_PF_VMN ? (1u << 16) : 0u) | (uint32_t(HD >> 3) << 17) |
+                             (uint32_t(128 >> 4) << 24);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     int committed = 0;                                     // O commits issued (bar[1] phases to retire)
@@ -512,7 +530,15 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
             cp_async16_zfill(Ks + kmaj(key, db * 8, C::SBO_D), src, valid);
         }
     };
-    if (KVF == KV_F16) k_async(0);
+    auto v_async = [&](int k0) {   // MN-major V tile (KIE_PF_VMN), fp16 cache
+        for (int i = tid; i < 128 * (HD / 8); i += 128) {
+            const int key = i / (HD / 8), db = i % (HD / 8), j = k0 + key;
+            const bool valid = j <= last && j < max_ctx;
+            const uint8_t* src = vc + ((head_base + (valid ? j : 0)) * HD + db * 8) * 2;
+            cp_async16_zfill(Vt + vmn(key, db * 8, C::SBO_D), src, valid);
+        }
+    };
+    if (KVF == KV_F16) { k_async(0); cp_async_commit(); }
     for (int kt = 0; kt < ntile && ok; ++kt) {
         const int k0 = kt * 128;
         // the previous tile's O += P V has read Vt, Ph, Pl (every decision below is
@@ -521,37 +547,57 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
             ok = false;
             break;
         }
-        // K tile (rows = keys) and V^T tile (rows = dims): 8 keys x 8 dims an item, dims fastest
-        for (int i = tid; i < 16 * (HD / 8); i += 128) {
-            const int db = i % (HD / 8), kb = i / (HD / 8);
-            uint4 kr[8], vr[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = k0 + kb * 8 + u;
-                if (j <= last && j < max_ctx) {
-                    const size_t at = (head_base + j) * HD + db * 8;
-                    if (KVF != KV_F16) kr[u] = load8_f16<KVF>(kc, at);
-                    vr[u] = load8_f16<KVF>(vc, at);
-                } else {
-                    kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (KIE_PF_VMN) {
+            if (KVF == KV_F16) {   // V lands during S = Q K^T and the softmax
+                v_async(k0);
+                cp_async_commit();
+            } else {   // E5M2: K and V expanded to fp16 through registers, no transposition
+                for (int i = tid; i < 128 * (HD / 8); i += 128) {
+                    const int key = i / (HD / 8), db = i % (HD / 8), j = k0 + key;
+                    uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
+                    if (j <= last && j < max_ctx) {
+                        const size_t at = (head_base + j) * HD + db * 8;
+                        kr = load8_f16<KVF>(kc, at);
+                        vr = load8_f16<KVF>(vc, at);
+                    }
+                    *reinterpret_cast<uint4*>(Ks + kmaj(key, db * 8, C::SBO_D)) = kr;
+                    *reinterpret_cast<uint4*>(Vt + vmn(key, db * 8, C::SBO_D)) = vr;
                 }
             }
-            if (KVF != KV_F16) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(Ks + kmaj(kb * 8 + u, db * 8, C::SBO_D)) = kr[u];
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {   // dim db*8 + e over the 8 keys
-                const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-                const int wi = e >> 1;
-                const uint32_t w0 = __byte_perm((&vr[0].x)[wi], (&vr[1].x)[wi], sel);
-                const uint32_t w1 = __byte_perm((&vr[2].x)[wi], (&vr[3].x)[wi], sel);
-                const uint32_t w2 = __byte_perm((&vr[4].x)[wi], (&vr[5].x)[wi], sel);
-                const uint32_t w3 = __byte_perm((&vr[6].x)[wi], (&vr[7].x)[wi], sel);
-                *reinterpret_cast<uint4*>(Vt + kmaj(db * 8 + e, kb * 8, C::SBO_K)) = make_uint4(w0, w1, w2, w3);
+        } else {
+            // K tile (rows = keys) and V^T tile (rows = dims): 8 keys x 8 dims an item, dims fastest
+            for (int i = tid; i < 16 * (HD / 8); i += 128) {
+                const int db = i % (HD / 8), kb = i / (HD / 8);
+                uint4 kr[8], vr[8];
+    #pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = k0 + kb * 8 + u;
+                    if (j <= last && j < max_ctx) {
+                        const size_t at = (head_base + j) * HD + db * 8;
+                        if (KVF != KV_F16) kr[u] = load8_f16<KVF>(kc, at);
+                        vr[u] = load8_f16<KVF>(vc, at);
+                    } else {
+                        kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                if (KVF != KV_F16) {
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(Ks + kmaj(kb * 8 + u, db * 8, C::SBO_D)) = kr[u];
+                }
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) {   // dim db*8 + e over the 8 keys
+                    const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+                    const int wi = e >> 1;
+                    const uint32_t w0 = __byte_perm((&vr[0].x)[wi], (&vr[1].x)[wi], sel);
+                    const uint32_t w1 = __byte_perm((&vr[2].x)[wi], (&vr[3].x)[wi], sel);
+                    const uint32_t w2 = __byte_perm((&vr[4].x)[wi], (&vr[5].x)[wi], sel);
+                    const uint32_t w3 = __byte_perm((&vr[6].x)[wi], (&vr[7].x)[wi], sel);
+                    *reinterpret_cast<uint4*>(Vt + kmaj(db * 8 + e, kb * 8, C::SBO_K)) = make_uint4(w0, w1, w2, w3);
+                }
             }
         }
-        if (KVF == KV_F16) cp_async_wait_all();   // this thread's copies of the K tile have landed
+        // this thread's copies of the K tile have landed (V's may still be in flight)
+        if (KVF == KV_F16) { if (KIE_PF_VMN) cp_async_wait_group<1>(); else cp_async_wait_group<0>(); }
         fence_proxy_async_shared();
         __syncthreads();
         if (tid == 0) {
@@ -570,7 +616,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
             break;
         }
         tc_fence_after();
-        if (KVF == KV_F16 && kt + 1 < ntile) k_async(k0 + 128);   // S has read Ks
+        if (KVF == KV_F16 && kt + 1 < ntile) { k_async(k0 + 128); cp_async_commit(); }   // S has read Ks
         // this row's scores: the tile's maximum, then P = exp(S - m) as fp16 hi + lo
         float mt = -INFINITY;
 #pragma unroll
@@ -617,6 +663,9 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
                 tmem_st_32x32b_x32(tO + lane_off + uint32_t(c0), ov);
             }
         }
+        if (KIE_PF_VMN && KVF == KV_F16) {   // this thread's copies of the V tile have landed
+            if (kt + 1 < ntile) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
+        }
         tc_fence_before();
         fence_proxy_async_shared();
         __syncthreads();
@@ -624,7 +673,8 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk) {
-                const uint64_t bd = smem_desc_noswz(Vt + kk * 256, 128, C::SBO_K);
+                const uint64_t bd = KIE_PF_VMN ? smem_desc_noswz(Vt + kk * 2 * C::SBO_D, C::SBO_D, 128)
+                                               : smem_desc_noswz(Vt + kk * 256, 128, C::SBO_K);
                 tc_mma_f16(tO, smem_desc_noswz(Ph + kk * 256, 128, C::SBO_K), bd, idesc_o,
                            (kt > 0 || kk > 0) ? 1u : 0u);
                 tc_mma_f16(tO, smem_desc_noswz(Pl + kk * 256, 128, C::SBO_K), bd, idesc_o, 1u);
@@ -634,7 +684,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
         __syncwarp();
         committed = kt + 1;
     }
-    if (KVF == KV_F16) cp_async_wait_all();   // no copy of a K tile is left in flight (error paths)
+    if (KVF == KV_F16) cp_async_wait_group<0>();   // no copy of a K or V tile is left in flight (error paths)
     // every issued O update has landed (also on the error path, bounded), then O / l
     const bool done = __syncthreads_and(committed > 0 &&
                                         wait_bounded(&bar[1], uint32_t(committed - 1) & 1u, timeout_ns, err));
