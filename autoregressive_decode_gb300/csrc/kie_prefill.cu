@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
             for (int i = tid; i < 16 * (HD / 8); i += 128) {
                 const int db = i % (HD / 8), kb = i / (HD / 8);
                 uint4 kr[8], vr[8];
-    #pragma unroll
+#pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int j = k0 + kb * 8 + u;
                     if (j <= last && j < max_ctx) {
@@ -581,10 +581,10 @@ __global__ void __launch_bounds__(128, 1) kie_pf_attn_tc_kernel(const float* __r
                     }
                 }
                 if (KVF != KV_F16) {
-    #pragma unroll
+#pragma unroll
                     for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(Ks + kmaj(kb * 8 + u, db * 8, C::SBO_D)) = kr[u];
                 }
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 8; ++e) {   // dim db*8 + e over the 8 keys
                     const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
                     const int wi = e >> 1;
