@@ -156,6 +156,25 @@ def test_scaled_e5m2_recalibration_hand_example():
     assert c.k[0][0, 512, 0] == np.float32(1.0) or abs(c.k[0][0, 512, 0] - 1.0) <= 0.125
 
 
+def test_scaled_e5m2_codec_closed_forms():
+    """The scaled codec on values E5M2 holds exactly: 1.0 at scale 0.5 is stored as
+    2.0 (code 0x40: sign 0, exponent 16, mantissa 0) and reads back as 1.0; -3.0
+    at scale 0.25 is -12.0 (0xCA) and reads back as -3.0.  The next slice's scale
+    maps the largest stored magnitude (in units of the previous scale) to 127:
+    127 at scale 1 gives 1; a slice of zeros, or a non-finite maximum, keeps the
+    previous scale."""
+    c = O.e5m2s_quantize(np.array([1.0, -3.0], np.float16), np.float32(0.5))
+    assert c[0] == 0x40
+    c2 = O.e5m2s_quantize(np.array([-3.0], np.float16), np.float32(0.25))
+    assert c2[0] == 0xCA
+    assert O.e5m2s_dequantize(c[:1], np.float32(0.5))[0] == np.float32(1.0)
+    assert O.e5m2s_dequantize(c2, np.float32(0.25))[0] == np.float32(-3.0)
+    assert O.e5m2s_next_scale(127.0, np.float32(1.0)) == np.float32(1.0)
+    assert O.e5m2s_next_scale(254.0, np.float32(0.5)) == np.float32(1.0)
+    assert O.e5m2s_next_scale(0.0, np.float32(0.0039)) == np.float32(0.0039)
+    assert O.e5m2s_next_scale(float("inf"), np.float32(0.0042)) == np.float32(0.0042)
+
+
 def test_scaled_e5m2_round_trip_and_headroom():
     """Three slices whose magnitudes grow 4x per slice: every value reads back
     within E5M2's half step (2^-3 relative) of its fp16 value, and no code
@@ -424,6 +443,20 @@ def test_softmax_invariants():
     np.testing.assert_allclose(a.sum(-1), 1.0, rtol=1e-6)
     np.testing.assert_allclose(O.softmax(s + 17.0), a, rtol=1e-5, atol=1e-7)
     np.testing.assert_allclose(O.softmax(np.array([0.0, math.log(3.0)], np.float32)), [0.25, 0.75], rtol=1e-6)
+
+
+def test_silu_closed_forms():
+    """silu(z) = z * sigmoid(z) (the SwiGLU gate): silu(0) = 0, silu(1) = e / (1 + e),
+    silu(ln 3) = (3/4) ln 3, the odd-part identity silu(z) - silu(-z) = z, and the
+    asymptotes silu(z) -> z (z >> 0) and -> 0 (z << 0).  A flipped exponent sign or
+    a dropped factor fails the first three."""
+    assert O.silu(np.float32(0.0)) == 0.0
+    np.testing.assert_allclose(O.silu(np.float32(1.0)), math.e / (1.0 + math.e), rtol=1e-6)
+    np.testing.assert_allclose(O.silu(np.float32(math.log(3.0))), 0.75 * math.log(3.0), rtol=1e-6)
+    z = S.normal_f32(9, 0, (4096,), 3.0)
+    np.testing.assert_allclose(O.silu(z) - O.silu(-z), z, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(O.silu(np.float32(40.0)), 40.0, rtol=1e-7)
+    assert abs(float(O.silu(np.float32(-40.0)))) < 1e-15
 
 
 def test_attention_single_key_and_equal_keys():
